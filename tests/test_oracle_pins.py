@@ -1,0 +1,248 @@
+"""Pins of the float64 oracle to things other than itself (CPU only).
+
+No page prints a worked numeric example, so the oracle is pinned by:
+  * brute-force enumeration of every alignment (oracle/brute.py, autograd
+    for the gradient) on tiny lattices, fused and non-fused, clamp and every
+    reduction, float32 and float16 rows;
+  * closed forms: T=1,U=0 (loss = -log_softmax(h)[blank]); U=0 (blanks
+    only); T=1 (all labels then the terminal blank); constant logits
+    (combinatorial loss, occupancies and gradient) incl. the stored fixture
+    tests/golden/uniform_logits.json;
+  * invariants: loss from alpha == loss from beta, per-anti-diagonal
+    occupancy sums to 1, zero gradient row sums with fused log-softmax,
+    each frame crossed by exactly one blank and each label emitted once;
+  * central finite differences of the oracle's own loss.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy.special import log_softmax, logsumexp
+
+import oracle
+from oracle import brute
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rand_case(rng, B, Tmax, Umax, V, dtype=np.float32, sigma=1.0, blank=None, fused=True):
+    T = rng.integers(1, Tmax + 1, size=B).astype(np.int32)
+    U = rng.integers(0, Umax + 1, size=B).astype(np.int32)
+    if blank is None:
+        blank = int(rng.integers(-V, V))
+    bl = blank + V if blank < 0 else blank
+    S = max(1, int(U.max()))
+    y = rng.integers(0, V - 1, size=(B, S))
+    y = np.where(y >= bl, y + 1, y).astype(np.int32)
+    rows = int((T.astype(np.int64) * (U + 1)).sum())
+    x = rng.normal(0.0, sigma, size=(rows, V))
+    if not fused:
+        x = log_softmax(x, axis=1)
+    return x.astype(dtype), y, T, U, blank
+
+
+@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("fused", [True, False])
+def test_brute_force_loss_and_grad(seed, fused):
+    rng = np.random.default_rng(100 + seed)
+    V = int(rng.integers(2, 7))
+    x, y, T, U, blank = rand_case(rng, B=3, Tmax=4, Umax=4, V=V, fused=fused,
+                                  dtype=np.float16 if seed % 3 == 0 else np.float32)
+    clamp = [-1.0, 0.0, 0.05, 0.3][seed % 4]
+    red = ["none", "sum", "mean"][seed % 3]
+    got = oracle.rnnt_loss(x, y, T, U, blank=blank, clamp=clamp, reduction=red,
+                           fused_log_softmax=fused)
+    want_l, want_red, want_g = brute.rnnt_loss(x.astype(np.float64), y, T, U, blank=blank,
+                                               clamp=clamp, reduction=red,
+                                               fused_log_softmax=fused)
+    np.testing.assert_allclose(got.losses, want_l, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(got.losses_beta, want_l, rtol=1e-12, atol=1e-12)
+    assert got.reduced == pytest.approx(want_red, rel=1e-12, abs=1e-12)
+    np.testing.assert_allclose(got.grad, want_g, rtol=1e-10, atol=1e-12)
+
+
+def test_brute_force_enumerates_binomial_paths():
+    for T in range(1, 6):
+        for U in range(0, 5):
+            assert sum(1 for _ in brute.alignments(T, U)) == math.comb(T - 1 + U, U)
+
+
+@pytest.mark.parametrize("V,blank", [(5, -1), (7, 0), (3, 1)])
+def test_closed_form_single_node(V, blank):
+    rng = np.random.default_rng(V)
+    h = rng.normal(0, 2.0, size=(1, V))
+    fw = oracle.sample_forward(h, 1, 0, [], blank, True)
+    bl = blank + V if blank < 0 else blank
+    assert fw.loss_alpha == pytest.approx(-(h[0, bl] - logsumexp(h[0])), abs=1e-13)
+    assert fw.loss_beta == pytest.approx(fw.loss_alpha, abs=1e-13)
+
+
+def test_closed_form_blanks_only():
+    rng = np.random.default_rng(1)
+    T, V = 23, 9
+    h = rng.normal(0, 1.5, size=(T, V))
+    fw = oracle.sample_forward(h, T, 0, [], 4, True)
+    assert fw.loss_alpha == pytest.approx(-log_softmax(h, axis=1)[:, 4].sum(), rel=1e-13)
+
+
+def test_closed_form_single_frame():
+    rng = np.random.default_rng(2)
+    U, V = 6, 10
+    y = [3, 1, 1, 8, 2, 5]
+    h = rng.normal(0, 1.5, size=(U + 1, V))
+    lp = log_softmax(h, axis=1)
+    want = -(sum(lp[u, y[u]] for u in range(U)) + lp[U, 0])
+    fw = oracle.sample_forward(h, 1, U, y, 0, True)
+    assert fw.loss_alpha == pytest.approx(want, rel=1e-13)
+
+
+def log_binom(n, k):
+    return math.lgamma(n + 1) - math.lgamma(k + 1) - math.lgamma(n - k + 1)
+
+
+def uniform_grad(T, U, V, y, blank, fused=True):
+    """Closed-form gradient for constant logits (every p = 1/V).
+
+    Occupancy of node (t,u) = C(t+u,u) C(T-1-t+U-u, U-u) / C(T-1+U, U); the
+    blank arc out of it is taken by C(t+u,u) C(T-2-t+U-u, U-u) of those
+    alignments (all of them at the terminal node), the label arc by
+    C(t+u,u) C(T-1-t+U-u-1, U-u-1).
+    """
+    W = U + 1
+    tot = log_binom(T - 1 + U, U)
+    g = np.zeros((T * W, V))
+    for t in range(T):
+        for u in range(W):
+            before = log_binom(t + u, u)
+            occ = math.exp(before + log_binom(T - 1 - t + U - u, U - u) - tot)
+            if t < T - 1:
+                eb = math.exp(before + log_binom(T - 2 - t + U - u, U - u) - tot)
+            else:
+                eb = occ if u == U else 0.0
+            ey = math.exp(before + log_binom(T - 1 - t + U - u - 1, U - u - 1) - tot) \
+                if u < U else 0.0
+            r = t * W + u
+            if fused:
+                g[r, :] = occ / V
+            g[r, blank] -= eb
+            if u < U:
+                g[r, y[u]] -= ey
+    return g
+
+
+@pytest.mark.parametrize("T,U,V,blank", [(1, 0, 4, 0), (5, 3, 6, 5), (40, 12, 16, 0),
+                                         (120, 30, 8, 7)])
+def test_closed_form_uniform_logits(T, U, V, blank):
+    rng = np.random.default_rng(T * 31 + U)
+    y = rng.integers(0, V - 1, size=max(U, 1))
+    y = np.where(y >= blank, y + 1, y).astype(np.int32)
+    h = np.full((T * (U + 1), V), 0.37)
+    fw = oracle.sample_forward(h, T, U, y, blank, True)
+    want = (T + U) * math.log(V) - log_binom(T - 1 + U, U)
+    assert fw.loss_alpha == pytest.approx(want, rel=1e-12, abs=1e-12)
+    g = oracle.sample_grad(h, fw, y, blank, True, -1.0, 1.0)
+    np.testing.assert_allclose(g, uniform_grad(T, U, V, y, blank), rtol=1e-9, atol=1e-13)
+    # Same lattice given as log-probabilities (in-kernel log-softmax off).
+    lp = np.full_like(h, -math.log(V))
+    fwn = oracle.sample_forward(lp, T, U, y, blank, False)
+    assert fwn.loss_alpha == pytest.approx(want, rel=1e-12, abs=1e-12)
+    gn = oracle.sample_grad(lp, fwn, y, blank, False, -1.0, 1.0)
+    np.testing.assert_allclose(gn, uniform_grad(T, U, V, y, blank, fused=False), rtol=1e-9,
+                               atol=1e-13)
+
+
+def test_golden_uniform_fixture():
+    with open(os.path.join(GOLDEN, "uniform_logits.json")) as f:
+        fx = json.load(f)
+    for case in fx["cases"]:
+        V = case["V"]
+        for T, U, want in zip(case["T"], case["U"], case["losses"]):
+            y = np.arange(U, dtype=np.int32) % (V - 1)  # blank = V-1 never used as a label
+            h = np.zeros((T * (U + 1), V), dtype=np.float32)
+            fw = oracle.sample_forward(h, T, U, y, -1, True)
+            assert fw.loss_alpha == pytest.approx(want, rel=1e-11), case["name"]
+            assert fw.loss_beta == pytest.approx(want, rel=1e-11), case["name"]
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_invariants_random(fused):
+    rng = np.random.default_rng(5 if fused else 6)
+    T, U, V, blank = 60, 17, 12, 0
+    y = rng.integers(1, V, size=U).astype(np.int32)
+    h = rng.normal(0, 2.0, size=(T * (U + 1), V))
+    if not fused:
+        h = log_softmax(h, axis=1)
+    fw = oracle.sample_forward(h, T, U, y, blank, fused)
+    assert fw.loss_alpha == pytest.approx(fw.loss_beta, rel=1e-12)
+    W = U + 1
+    a = fw.alpha.reshape(T, W)
+    b = fw.beta.reshape(T, W)
+    for d in range(T + U):
+        cells = [(t, d - t) for t in range(max(0, d - U), min(T - 1, d) + 1)]
+        occ = sum(math.exp(a[t, u] + b[t, u] - fw.ll) for t, u in cells)
+        assert occ == pytest.approx(1.0, abs=1e-10)
+    g = oracle.sample_grad(h, fw, y, blank, fused, -1.0, 1.0)
+    if fused:
+        np.testing.assert_allclose(g.sum(axis=1), 0.0, atol=1e-12)
+    else:
+        gb = g[:, blank].reshape(T, W)
+        np.testing.assert_allclose(gb.sum(axis=1), -1.0, atol=1e-10)
+        gy = np.array([[g[t * W + u, y[u]] for u in range(U)] for t in range(T)])
+        np.testing.assert_allclose(gy.sum(axis=0), -1.0, atol=1e-10)
+        mask = np.ones_like(g, dtype=bool)
+        mask[:, blank] = False
+        for t in range(T):
+            for u in range(U):
+                mask[t * W + u, y[u]] = False
+        assert np.all(g[mask] == 0.0)
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_central_finite_differences(fused):
+    rng = np.random.default_rng(9 if fused else 10)
+    T, U, V, blank = 5, 3, 5, 2
+    y = np.array([0, 4, 1], dtype=np.int32)
+    h = rng.normal(0, 1.0, size=(T * (U + 1), V))
+    if not fused:
+        h = log_softmax(h, axis=1)
+    fw = oracle.sample_forward(h, T, U, y, blank, fused)
+    g = oracle.sample_grad(h, fw, y, blank, fused, -1.0, 1.0)
+    eps = 1e-6
+    fd = np.zeros_like(h)
+    for i in range(h.shape[0]):
+        for k in range(V):
+            hp = h.copy()
+            hp[i, k] += eps
+            hm = h.copy()
+            hm[i, k] -= eps
+            lp_ = oracle.sample_forward(hp, T, U, y, blank, fused).loss_alpha
+            lm_ = oracle.sample_forward(hm, T, U, y, blank, fused).loss_alpha
+            fd[i, k] = (lp_ - lm_) / (2 * eps)
+    np.testing.assert_allclose(g, fd, atol=2e-8)
+
+
+def test_offsets_exact():
+    T = np.array([8, 6, 1, 1000], dtype=np.int32)
+    U = np.array([3, 2, 0, 299], dtype=np.int32)
+    np.testing.assert_array_equal(oracle.offsets(T, U), [0, 32, 50, 51, 300051])
+
+
+def test_grad_rows_slice_matches_full():
+    rng = np.random.default_rng(3)
+    T, U, V = 9, 4, 7
+    y = np.array([1, 2, 3, 4], dtype=np.int32)
+    h = rng.normal(size=(T * (U + 1), V)).astype(np.float32)
+    fw = oracle.sample_forward(h, T, U, y, 0, True)
+    full = oracle.sample_grad(h, fw, y, 0, True, 0.2, 0.5)
+    part = oracle.sample_grad(h, fw, y, 0, True, 0.2, 0.5, 11, 29)
+    np.testing.assert_array_equal(full[11:29], part)
+
+
+def test_rejects_bad_arguments():
+    h = np.zeros((4, 3))
+    with pytest.raises(ValueError):
+        oracle.sample_forward(h, 0, 3, [0, 1, 0], 2, True)
+    with pytest.raises(ValueError):
+        oracle.rnnt_loss(h.astype(np.float32), [[0]], [2], [2], blank=2)
