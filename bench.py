@@ -1,0 +1,389 @@
+#!/usr/bin/env python3
+"""Benchmark: fused RNN-T loss + gradient on GB300, logit elements per second.
+
+One step = one ``rnnt_loss_fused`` call (offsets/schedule, row pass, alpha/beta
+DP, gradient pass, loss check) over the whole BPE-ASR workload: B=16,
+T_b ~ U[300, 500], U_b ~ U[50, 100], V=1024, float16 logits ~ N(0, 1.5),
+blank=-1, no clamp, in-kernel log-softmax, reduction "sum" (about 4.9e8
+logit elements, 1 GB).  Inputs are resident in HBM before timing; L2 is
+flushed (512 MiB write) between timed steps and the inputs alone exceed L2.
+
+Prints one JSON line.  ``value`` = logit elements/s over all ranks
+(weak scaling: each rank runs its own copy of the workload, no collective on
+the data path); ``roofline`` describes the dominant kernel against the
+measured HBM copy bandwidth; ``e2e`` times the public Python API with the
+step's inputs copied from pinned host memory and the loss copied back;
+``cpu_baseline`` times the float64 oracle on the host cores on a bounded
+sub-batch.  ``--impl reference`` times that oracle alone (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "RNN-T loss+grad logit elements/s (fwd+bwd, 1 GB300); % of HBM roofline"
+UNIT = "logit elements/s"
+FALLBACK_HBM_GBS = 6800.0
+STAGES = ("prepare", "row_pass", "alpha_beta_dp", "grad_pass", "finalize")
+KERNEL_FILE = os.path.join(ROOT, "rnnt_loss_gb300", "csrc", "rnnt_gb300.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+
+
+def dist_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_FILE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches this kernel source."""
+    try:
+        lines = open(TRAFFIC_FILE).read().splitlines()
+    except OSError:
+        return None
+    kv = dict(l.split("=", 1) for l in lines if "=" in l and not l.startswith("#"))
+    if kv.get("source_sha256_16") != kernel_source_hash() or kv.get("workload") != workload:
+        return None
+    v = kv.get(f"{kernel}.dram_bytes_per_launch")
+    return float(v) if v else None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_sample_run(wl, n_samples: int):
+    """Float64 oracle loss+grad over the first n_samples samples; returns (elements, seconds)."""
+    import numpy as np
+    import oracle
+    n = min(n_samples, wl.cfg.B)
+    r1 = int(wl.offsets[n])
+    x = wl.logits[:r1].cpu().numpy()
+    t0 = time.perf_counter()
+    oracle.rnnt_loss(x, wl.targets[:n], wl.T[:n], wl.U[:n], blank=wl.cfg.blank,
+                     clamp=wl.cfg.clamp, reduction=wl.cfg.reduction,
+                     fused_log_softmax=wl.cfg.fused)
+    dt = time.perf_counter() - t0
+    del x
+    _ = np  # numpy is the oracle's array type
+    return r1 * wl.cfg.V, dt
+
+
+def cpu_baseline(wl, budget_s: float = 20.0):
+    import oracle
+    cores = oracle.num_threads()
+    n = max(1, min(wl.cfg.B, cores))
+    el, dt = oracle_sample_run(wl, n)
+    total_el, total_t, reps = el, dt, 1
+    while total_t + dt < budget_s and reps < 10:
+        e2, t2 = oracle_sample_run(wl, n)
+        total_el += e2
+        total_t += t2
+        reps += 1
+    return {"value": total_el / total_t, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"first {n} of {wl.cfg.B} samples ({el} logit elements) x {reps} runs, "
+                      f"float64 loss+grad, OpenMP over samples, {total_t:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    from rnnt_loss_gb300 import workloads as W
+    oracle.build()
+    wl = W.make(args.workload, "cpu")
+    cores = oracle.num_threads()
+    n = max(1, min(wl.cfg.B, args.ref_samples or cores))
+    for _ in range(args.warmup):
+        oracle_sample_run(wl, n)
+    times, el = [], 0
+    for _ in range(args.steps):
+        el, dt = oracle_sample_run(wl, n)
+        times.append(dt)
+    ms = 1e3 * statistics.mean(times)
+    value = el / (ms / 1e3)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(wl, args, l2="host run"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"first {n} of {wl.cfg.B} samples per step ({el} logit "
+                                   f"elements), float64 loss+grad"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl, args, l2):
+    c = wl.cfg
+    return {"workload": c.name, "B": c.B, "V": c.V, "rows": wl.rows, "elements": wl.elements,
+            "logit_dtype": c.dtype, "T_range": list(c.T_range), "U_range": list(c.U_range),
+            "blank": c.blank, "clamp": c.clamp, "fused_log_softmax": c.fused,
+            "reduction": c.reduction, "seed": c.seed, "l2": l2,
+            "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from rnnt_loss_gb300 import _native as N
+    from rnnt_loss_gb300 import build as B
+    from rnnt_loss_gb300 import workloads as W
+    from rnnt_loss_gb300.functional import _DT, rnnt_loss_forward
+
+    B.build()
+    N.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    wl = W.make(args.workload, dev)
+    cfg = wl.cfg
+    rows, V = wl.rows, cfg.V
+    dt = _DT[wl.logits.dtype]
+    esize = wl.logits.element_size()
+    targets = torch.as_tensor(wl.targets, device=dev)
+    Tl = torch.as_tensor(wl.T, device=dev)
+    Ul = torch.as_tensor(wl.U, device=dev)
+    nbytes = N.rnnt_workspace_size(cfg.B, rows, V, dt)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    loss = torch.empty(cfg.B, dtype=torch.float32, device=dev)
+    red = torch.empty((), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    grad = torch.empty_like(wl.logits)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    red_code = N.REDUCTIONS[cfg.reduction]
+
+    def make_events():
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        for e in ev:
+            e.record(stream)
+        return ev
+
+    def step(ev):
+        rc = N.rnnt_loss_fused_staged(
+            wl.logits.data_ptr(), dt, rows, V, targets.data_ptr(), targets.shape[1],
+            Tl.data_ptr(), Ul.data_ptr(), cfg.B, cfg.blank, cfg.clamp, cfg.fused, red_code,
+            loss.data_ptr(), red.data_ptr(), grad.data_ptr(), ws.data_ptr(), nbytes,
+            status.data_ptr(), stream.cuda_stream, [e.cuda_event for e in ev])
+        if rc != N.RNNT_OK:
+            raise N.RNNTError(rc, "rnnt_loss_fused_staged")
+
+    warm_ev = make_events()
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step(warm_ev)
+    torch.cuda.synchronize()
+    if int(status.item()) != N.RNNT_OK:
+        raise N.RNNTError(int(status.item()), "bench warm-up")
+
+    evs = [make_events() for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()
+        step(evs[k])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+
+    step_ms = [ev[0].elapsed_time(ev[5]) for ev in evs]
+    stage_ms = {s: statistics.mean(ev[i].elapsed_time(ev[i + 1]) for ev in evs)
+                for i, s in enumerate(STAGES)}
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * wl.elements / (ms / 1e3)
+
+    peak, peak_kind = load_peak()
+    step_bytes = 2 * wl.elements * esize   # algorithmic: one logit read + one grad write
+    kernel_bytes = {"row_pass": wl.elements * esize if cfg.fused else 2 * rows * esize,
+                    "grad_pass": 2 * wl.elements * esize if cfg.fused
+                    else wl.elements * esize + 2 * rows * esize}
+    dom = max(("row_pass", "alpha_beta_dp", "grad_pass"), key=lambda s: stage_ms[s])
+    if dom == "alpha_beta_dp":
+        roof = {"bound": "latency", "kernel": dom, "achieved": None, "peak": None,
+                "unit": "GB/s", "frac": None, "traffic": None,
+                "note": "the DP is bound by T+U dependent anti-diagonal steps"}
+    else:
+        ach = kernel_bytes[dom] / (stage_ms[dom] / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak, "unit": "GB/s",
+                "frac": ach / peak, "peak_kind": f"{peak_kind} (hbm_gbs, copy bandwidth)",
+                "algorithmic_bytes_per_launch": kernel_bytes[dom],
+                "traffic": recorded_traffic(dom, cfg.name)}
+    step_ach = step_bytes / (ms / 1e3) / 1e9
+
+    # End to end through the public API: pinned host inputs -> device, loss -> host.
+    h_logits = wl.logits.cpu().pin_memory()
+    h_targets = targets.cpu().pin_memory()
+    h_T, h_U = Tl.cpu().pin_memory(), Ul.cpu().pin_memory()
+    d_logits = torch.empty_like(wl.logits)
+    d_targets, d_T, d_U = torch.empty_like(targets), torch.empty_like(Tl), torch.empty_like(Ul)
+    h_loss = torch.empty(cfg.B, dtype=torch.float32).pin_memory()
+    h_red = torch.empty((), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        d_logits.copy_(h_logits, non_blocking=True)
+        d_targets.copy_(h_targets, non_blocking=True)
+        d_T.copy_(h_T, non_blocking=True)
+        d_U.copy_(h_U, non_blocking=True)
+        l, r, g, _ = rnnt_loss_forward(d_logits, d_targets, d_T, d_U, cfg.blank, cfg.clamp,
+                                       cfg.reduction, cfg.fused, check=False)
+        h_loss.copy_(l, non_blocking=True)
+        h_red.copy_(r, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(max(3, min(args.steps, 10))):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    e2e_t = statistics.mean(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_t], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_t = float(t.item())
+    h2d = (h_logits.numel() * h_logits.element_size() + h_targets.numel() * 4
+           + h_T.numel() * 4 + h_U.numel() * 4)
+    d2h = h_loss.numel() * 4 + 4
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "storage_dtype": cfg.dtype,
+        "data": "synthetic (seeded; shapes and value distribution of the BPE-ASR workload)",
+        "config": config_of(wl, args, l2="flushed between steps (512 MiB write); "
+                                         "inputs 1 GB > L2"),
+        "roofline": roof,
+        "step_roofline": {"bound": "hbm", "achieved": step_ach, "peak": peak, "unit": "GB/s",
+                          "frac": step_ach / peak,
+                          "algorithmic_bytes": step_bytes,
+                          "note": "whole call: one logit read + one grad write per element"},
+        "stages_ms": stage_ms,
+        "e2e": {"value": world * wl.elements / (e2e_t / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_t},
+        "gpu_launches": 5 * args.steps,
+        "clocks": clk,
+        "wall_ms_timed_region": wall * 1e3,
+        "kernel_source_sha256_16": kernel_source_hash(),
+    }
+    del h_logits, d_logits
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--workload", default="bpe_asr")
+    ap.add_argument("--ref-samples", type=int, default=0,
+                    help="samples per reference step (default: host core count)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    rank, world, local_rank = dist_info()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,172 @@
+/*
+ * rnnt_gb300.h -- C ABI of the fused RNN-T (transducer) loss for GB300 (sm_103a).
+ *
+ * One call computes, for a batch of B utterances, the per-sample RNN-T loss
+ * (negative log-likelihood summed over every alignment) and, optionally, its
+ * gradient with respect to the joiner logits, with the semantics of
+ * torchaudio.functional.rnnt_loss.  The operation and its arguments are the
+ * ones of the rnnt-loss-ascend README ("optimized_transducer"):
+ *   - section 参数说明 (parameter table): compact 2D logits, int32 targets and
+ *     lengths, blank, clamp, fused_log_softmax, per-sample loss, grad with
+ *     the shape of the logits;
+ *   - section 约束说明 (constraints): float32/float16 logits, blank in
+ *     [-V, V-1] with -1 meaning V-1, sum of T_b*(U_b+1) equal to the number
+ *     of logit rows, clamp <= 0 meaning no clipping;
+ *   - section 架构设计 (architecture): a two-phase interface, workspace size
+ *     first, then the fused launch;
+ *   - section 核心梯度融合公式 / 精度保证: the gradient formula and the check that
+ *     the alpha-side and beta-side losses agree.
+ * Status codes follow the RNNTStatus convention of the ESPnet GPURNNT docs
+ * (cost_and_grad returns success or RNNT_STATUS_INVALID_VALUE).
+ *
+ * Memory and streams: every pointer argument named "device" must point to
+ * memory the current CUDA device can access.  The library allocates nothing
+ * and keeps no state between calls other than per-device kernel attributes;
+ * all work is enqueued on `stream` and the host never synchronises.
+ */
+#ifndef RNNT_GB300_H
+#define RNNT_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *rnnt_stream_t;
+
+typedef enum {
+    RNNT_OK = 0,
+    RNNT_INVALID_VALUE = 1,       /* bad argument (host) or bad lengths/targets (device) */
+    RNNT_WORKSPACE_TOO_SMALL = 2, /* workspace_bytes below rnnt_workspace_size()         */
+    RNNT_LAUNCH_FAILED = 3,       /* a kernel launch returned a CUDA error               */
+    RNNT_LOSS_MISMATCH = 4,       /* alpha-side and beta-side losses disagree (or NaN)   */
+    RNNT_TIMEOUT = 5              /* reserved: a bounded device wait gave up             */
+} rnnt_status_t;
+
+typedef enum { RNNT_F32 = 0, RNNT_F16 = 1 } rnnt_dtype_t;
+
+typedef enum { RNNT_RED_NONE = 0, RNNT_RED_SUM = 1, RNNT_RED_MEAN = 2 } rnnt_reduction_t;
+
+/* Largest supported target length (U_b <= RNNT_MAX_TARGET_LENGTH, so a lattice
+ * is at most 1024 nodes wide). */
+#define RNNT_MAX_TARGET_LENGTH 1023
+
+/*
+ * rnnt_workspace_size -- bytes of device scratch rnnt_loss_fused needs.
+ * README 架构设计, first phase of the two-phase interface.
+ *   B     number of samples (>= 1)
+ *   rows  number of logit rows, sum over b of T_b*(U_b+1) (>= 1)
+ *   V     vocabulary size including blank (>= 1)
+ *   dt    logit element type
+ *   bytes out: required size; about 44 bytes per logit row plus O(B).
+ * Returns RNNT_INVALID_VALUE for a NULL `bytes` or out-of-range sizes.
+ */
+rnnt_status_t rnnt_workspace_size(int32_t B, int64_t rows, int32_t V, rnnt_dtype_t dt,
+                                  size_t *bytes);
+
+/*
+ * rnnt_loss_fused -- loss and gradient of a batch in one call (README 架构设计,
+ * second phase; 参数说明 for the arguments).
+ *
+ *   logits            device, (rows, V) row-major contiguous, dt.  Sample b owns
+ *                     rows [off_b, off_b + T_b*(U_b+1)), off_b = sum_{i<b}
+ *                     T_i*(U_i+1); inside a sample, row t*(U_b+1)+u holds the
+ *                     joiner output for frame t after u emitted labels.
+ *                     Must be 16-byte aligned.  Raw logits when
+ *                     fused_log_softmax != 0, log-probabilities otherwise.
+ *   targets           device int32, (B, targets_stride) row-major; row b holds
+ *                     the U_b labels of sample b followed by ignored padding.
+ *                     Labels must lie in [0, V) and differ from blank.
+ *   targets_stride    1 <= targets_stride <= RNNT_MAX_TARGET_LENGTH, and
+ *                     >= max_b U_b.
+ *   logit_lengths     device int32 [B], T_b >= 1.
+ *   target_lengths    device int32 [B], 0 <= U_b <= targets_stride.
+ *   B                 batch size >= 1.
+ *   blank             in [-V, V-1]; a negative value counts from the end.
+ *   clamp             > 0 clips every gradient element to [-clamp, clamp]
+ *                     before the reduction scale; <= 0 disables clipping.
+ *   fused_log_softmax nonzero: the kernel applies log-softmax to each row.
+ *   reduction         NONE / SUM / MEAN (mean over the batch).  It sets the
+ *                     gradient scale (1/B for MEAN, else 1) and loss_reduced.
+ *   loss              device float [B], required: per-sample loss.
+ *   loss_reduced      device float [1] or NULL: sum (SUM, NONE) or mean (MEAN).
+ *   grad              device (rows, V) in dt, or NULL for loss only.  It may
+ *                     equal `logits` (the gradient then overwrites the
+ *                     logits in place) but must not partly overlap it.  Must
+ *                     be 16-byte aligned.
+ *   workspace         device scratch of at least rnnt_workspace_size() bytes,
+ *                     256-byte aligned, owned by the caller; it may be reused
+ *                     by later calls on the same stream once this one is
+ *                     enqueued (contents are rewritten every call).
+ *   status_dev        device int32 [1] or NULL.  Receives RNNT_OK,
+ *                     RNNT_INVALID_VALUE (device-detected: a T_b < 1, a U_b
+ *                     out of range, a label out of range or equal to blank,
+ *                     or rows != sum T_b*(U_b+1)) or RNNT_LOSS_MISMATCH
+ *                     (alpha/beta losses differ by more than
+ *                     1e-3*max(1,|loss|), or a loss is not finite).  When it
+ *                     is not RNNT_OK, loss/grad contents are unspecified.
+ *   stream            CUDA stream all kernels are enqueued on.
+ *
+ * Host-side return value: RNNT_INVALID_VALUE for NULL required pointers, bad
+ * sizes/enums/blank, misaligned or partly overlapping buffers;
+ * RNNT_WORKSPACE_TOO_SMALL; RNNT_LAUNCH_FAILED if a launch fails.  Nothing is
+ * enqueued when a host-side check fails.
+ */
+rnnt_status_t rnnt_loss_fused(const void *logits, rnnt_dtype_t dt, int64_t rows, int32_t V,
+                              const int32_t *targets, int32_t targets_stride,
+                              const int32_t *logit_lengths, const int32_t *target_lengths,
+                              int32_t B, int32_t blank, float clamp, int32_t fused_log_softmax,
+                              rnnt_reduction_t reduction, float *loss, float *loss_reduced,
+                              void *grad, void *workspace, size_t workspace_bytes,
+                              int32_t *status_dev, rnnt_stream_t stream);
+
+/*
+ * rnnt_loss_fused_staged -- rnnt_loss_fused with stage timing (tracing aid).
+ * Same arguments, plus stage_events: NULL, or an array of 6 cudaEvent_t
+ * handles (entries may be NULL) that the call records on `stream` at its
+ * stage boundaries: [0] start, [1] after offsets/schedule, [2] after the
+ * row pass, [3] after the alpha/beta DP, [4] after the gradient pass,
+ * [5] after the loss check/reduction.  The caller creates and owns the events.
+ */
+rnnt_status_t rnnt_loss_fused_staged(const void *logits, rnnt_dtype_t dt, int64_t rows, int32_t V,
+                                     const int32_t *targets, int32_t targets_stride,
+                                     const int32_t *logit_lengths, const int32_t *target_lengths,
+                                     int32_t B, int32_t blank, float clamp,
+                                     int32_t fused_log_softmax, rnnt_reduction_t reduction,
+                                     float *loss, float *loss_reduced, void *grad, void *workspace,
+                                     size_t workspace_bytes, int32_t *status_dev,
+                                     rnnt_stream_t stream, void *const *stage_events);
+
+/*
+ * rnnt_grad_scale -- multiply a gradient produced by rnnt_loss_fused by the
+ * upstream gradient of the loss (the autograd backward step the README's
+ * Python layer performs, section 架构设计 "Python 层").
+ *   grad, dt, rows, V   the gradient buffer of a previous rnnt_loss_fused call
+ *   B                   batch size of that call
+ *   workspace           the workspace of that call, unmodified since (its
+ *                       row offsets map rows to samples)
+ *   factors             device float: factors[0] for the whole gradient
+ *                       (per_sample == 0) or factors[b] for sample b's rows
+ *                       (per_sample != 0).  Rows whose factor is exactly 1
+ *                       are left untouched (no memory traffic).
+ * Returns RNNT_INVALID_VALUE / RNNT_WORKSPACE_TOO_SMALL / RNNT_LAUNCH_FAILED
+ * as rnnt_loss_fused does.
+ */
+rnnt_status_t rnnt_grad_scale(void *grad, rnnt_dtype_t dt, int64_t rows, int32_t V, int32_t B,
+                              const void *workspace, size_t workspace_bytes,
+                              const float *factors, int32_t per_sample, rnnt_stream_t stream);
+
+/* Static English description of a status code. */
+const char *rnnt_status_string(rnnt_status_t status);
+
+/* ABI version of this header (major * 100 + minor). */
+int32_t rnnt_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RNNT_GB300_H */

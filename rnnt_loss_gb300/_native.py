@@ -1,0 +1,104 @@
+"""ctypes binding of librnnt_gb300.so (include/rnnt_gb300.h); argument marshalling only.
+
+The function names mirror the C ABI.  The library is loaded lazily; if it is
+missing the call raises (build it with ``python -m rnnt_loss_gb300.build`` or
+``__graft_entry__.build()``).  Nothing here computes any part of the loss.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "librnnt_gb300.so")
+
+RNNT_OK, RNNT_INVALID_VALUE, RNNT_WORKSPACE_TOO_SMALL = 0, 1, 2
+RNNT_LAUNCH_FAILED, RNNT_LOSS_MISMATCH, RNNT_TIMEOUT = 3, 4, 5
+RNNT_F32, RNNT_F16 = 0, 1
+REDUCTIONS = {"none": 0, "sum": 1, "mean": 2}
+MAX_TARGET_LENGTH = 1023
+
+# Every symbol include/rnnt_gb300.h declares.
+EXPORTS = ("rnnt_workspace_size", "rnnt_loss_fused", "rnnt_loss_fused_staged", "rnnt_grad_scale",
+           "rnnt_status_string", "rnnt_abi_version")
+
+_lib = None
+
+
+class RNNTError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__(f"{where}: {status_string(code)} (status {code})")
+
+
+def load() -> ctypes.CDLL:
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} not found: the CUDA library is required (there is no fallback); "
+            "build it with `python -m rnnt_loss_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                            ctypes.c_size_t)
+    lib.rnnt_workspace_size.argtypes = [i32, i64, i32, i32, ctypes.POINTER(sz)]
+    lib.rnnt_workspace_size.restype = i32
+    lib.rnnt_loss_fused.argtypes = [P, i32, i64, i32, P, i32, P, P, i32, i32, f32, i32, i32,
+                                    P, P, P, P, sz, P, P]
+    lib.rnnt_loss_fused.restype = i32
+    lib.rnnt_loss_fused_staged.argtypes = lib.rnnt_loss_fused.argtypes + [P]
+    lib.rnnt_loss_fused_staged.restype = i32
+    lib.rnnt_grad_scale.argtypes = [P, i32, i64, i32, i32, P, sz, P, i32, P]
+    lib.rnnt_grad_scale.restype = i32
+    lib.rnnt_status_string.argtypes = [i32]
+    lib.rnnt_status_string.restype = ctypes.c_char_p
+    lib.rnnt_abi_version.argtypes = []
+    lib.rnnt_abi_version.restype = i32
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load().rnnt_status_string(int(code)).decode()
+
+
+def abi_version() -> int:
+    return int(load().rnnt_abi_version())
+
+
+def rnnt_workspace_size(B: int, rows: int, V: int, dt: int) -> int:
+    out = ctypes.c_size_t(0)
+    rc = load().rnnt_workspace_size(B, rows, V, dt, ctypes.byref(out))
+    if rc != RNNT_OK:
+        raise RNNTError(rc, "rnnt_workspace_size")
+    return int(out.value)
+
+
+def rnnt_loss_fused(logits, dt, rows, V, targets, targets_stride, logit_lengths, target_lengths,
+                    B, blank, clamp, fused_log_softmax, reduction, loss, loss_reduced, grad,
+                    workspace, workspace_bytes, status_dev, stream) -> int:
+    """Raw call; pointer arguments are integers (device addresses) or None."""
+    return int(load().rnnt_loss_fused(logits, dt, rows, V, targets, targets_stride,
+                                      logit_lengths, target_lengths, B, blank, float(clamp),
+                                      int(fused_log_softmax), reduction, loss, loss_reduced, grad,
+                                      workspace, workspace_bytes, status_dev, stream))
+
+
+def rnnt_loss_fused_staged(logits, dt, rows, V, targets, targets_stride, logit_lengths,
+                           target_lengths, B, blank, clamp, fused_log_softmax, reduction, loss,
+                           loss_reduced, grad, workspace, workspace_bytes, status_dev, stream,
+                           stage_events) -> int:
+    """rnnt_loss_fused recording 6 caller-owned CUDA events (raw handles) at stage boundaries."""
+    arr = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(e) if e else None for e in stage_events])
+    return int(load().rnnt_loss_fused_staged(logits, dt, rows, V, targets, targets_stride,
+                                             logit_lengths, target_lengths, B, blank,
+                                             float(clamp), int(fused_log_softmax), reduction,
+                                             loss, loss_reduced, grad, workspace,
+                                             workspace_bytes, status_dev, stream, arr))
+
+
+def rnnt_grad_scale(grad, dt, rows, V, B, workspace, workspace_bytes, factors, per_sample,
+                    stream) -> int:
+    return int(load().rnnt_grad_scale(grad, dt, rows, V, B, workspace, workspace_bytes, factors,
+                                      int(per_sample), stream))

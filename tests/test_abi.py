@@ -1,0 +1,95 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and rejects bad host-side arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from rnnt_loss_gb300 import _native as N
+from rnnt_loss_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return N.load()
+
+
+def declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for fn in os.listdir(inc):
+        if fn.endswith(".h"):
+            src = open(os.path.join(inc, fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(rnnt_[a-z_0-9]+)\s*\(", src))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert names, "no declarations found"
+    assert names == set(N.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert N.status_string(code)
+    assert N.abi_version() == 100
+
+
+def test_workspace_size(lib):
+    small = N.rnnt_workspace_size(2, 50, 16, N.RNNT_F32)
+    big = N.rnnt_workspace_size(2, 5000, 16, N.RNNT_F32)
+    assert small > 0 and big > small
+    per_row = (N.rnnt_workspace_size(4, 2_000_000, 8, N.RNNT_F16)
+               - N.rnnt_workspace_size(4, 1_000_000, 8, N.RNNT_F16)) / 1_000_000
+    assert 40 <= per_row <= 48
+    with pytest.raises(N.RNNTError):
+        N.rnnt_workspace_size(0, 50, 16, N.RNNT_F32)
+    with pytest.raises(N.RNNTError):
+        N.rnnt_workspace_size(2, 50, 16, 7)
+
+
+def _call(**kw):
+    args = dict(logits=4096, dt=N.RNNT_F32, rows=50, V=16, targets=8192, targets_stride=3,
+                logit_lengths=8448, target_lengths=8704, B=2, blank=-1, clamp=-1.0,
+                fused_log_softmax=1, reduction=0, loss=8960, loss_reduced=None, grad=None,
+                workspace=1 << 20, workspace_bytes=1 << 30, status_dev=None, stream=None)
+    args.update(kw)
+    return N.rnnt_loss_fused(**args)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(logits=None), dict(loss=None), dict(workspace=None), dict(targets=None),
+    dict(V=0), dict(B=0), dict(rows=1, B=2), dict(dt=3), dict(blank=16), dict(blank=-17),
+    dict(reduction=5), dict(targets_stride=0), dict(targets_stride=1024),
+    dict(logits=4100), dict(grad=4104), dict(workspace=(1 << 20) + 16),
+    dict(clamp=float("nan")),
+    dict(grad=4096 + 64),          # partly overlaps the logits
+])
+def test_host_validation_rejects(lib, bad):
+    assert _call(**bad) == N.RNNT_INVALID_VALUE
+
+
+def test_workspace_too_small(lib):
+    assert _call(workspace_bytes=1024) == N.RNNT_WORKSPACE_TOO_SMALL
+
+
+def test_grad_scale_host_validation(lib):
+    assert N.rnnt_grad_scale(None, 0, 10, 4, 1, 1 << 20, 1 << 30, 4096, 0, None) \
+        == N.RNNT_INVALID_VALUE
+    assert N.rnnt_grad_scale(4096, 0, 10, 4, 1, 1 << 20, 16, 4096, 0, None) \
+        == N.RNNT_WORKSPACE_TOO_SMALL
+
+
+def test_library_has_no_torch_dependency(lib):
+    # The boundary is plain C: the shared object must not link libtorch/libc10.
+    with open(N.LIB_PATH, "rb") as f:
+        blob = f.read()
+    assert b"libtorch" not in blob and b"libc10" not in blob

@@ -1,0 +1,243 @@
+"""GPU parity: the CUDA path (called through the C ABI) against the float64
+oracle on identical seeded inputs.  Element-wise on every small and medium
+case; at full workload sizes, per-sample losses of all (or sampled) samples,
+sampled gradient rows recomputed by the oracle one by one, and properties that
+hold at any size (zero row sums, alpha/beta agreement via the status word)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from rnnt_loss_gb300 import workloads as W
+from rnnt_loss_gb300 import _native as N
+from rnnt_loss_gb300.functional import rnnt_loss, rnnt_loss_forward
+
+from parity_util import (TOL, assert_grad_close, assert_loss_close, gpu_run, oracle_full,
+                         sampled_rows, to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+def full_compare(wl, **over):
+    loss, red, grad = gpu_run(wl, **over)
+    ref = oracle_full(wl, **over)
+    dt = wl.cfg.dtype
+    assert_loss_close(to_np(loss), ref.losses, dt)
+    red_name = over.get("reduction", wl.cfg.reduction)
+    if red_name != "none":
+        assert_loss_close([float(red)], [ref.reduced], dt)
+    assert_grad_close(to_np(grad.float()), ref.grad, dt)
+    return loss, grad, ref
+
+
+# ------------------------------------------------------------------ workloads
+def test_tiny_elementwise():
+    full_compare(W.make("tiny", "cuda"))
+
+
+def test_char_asr_elementwise():
+    full_compare(W.make("char_asr", "cuda"))
+
+
+@pytest.mark.parametrize("red", ["none", "sum", "mean"])
+def test_char_asr_reductions(red):
+    full_compare(W.make("char_asr", "cuda"), reduction=red, clamp=-1.0)
+
+
+def sampled_compare(wl, per_sample, samples=None, seed=0):
+    """Losses of `samples` and sampled gradient rows against the oracle, per sample."""
+    cfg = wl.cfg
+    loss, red, grad = gpu_run(wl)
+    gl = to_np(loss)
+    scale = 1.0 / cfg.B if cfg.reduction == "mean" else 1.0
+    rows = sampled_rows(wl, per_sample, seed)
+    samples = range(cfg.B) if samples is None else samples
+    for b in samples:
+        sl = wl.sample_rows(b)
+        x = to_np(wl.logits[sl])
+        T, U = int(wl.T[b]), int(wl.U[b])
+        fw = oracle.sample_forward(x, T, U, wl.targets[b], cfg.blank, cfg.fused)
+        assert_loss_close([gl[b]], [fw.loss_alpha], cfg.dtype)
+        ids = rows[b]
+        gsel = to_np(grad[sl][torch.as_tensor(ids, device=grad.device)].float())
+        for k, r in enumerate(ids):
+            want = oracle.sample_grad(x, fw, wl.targets[b], cfg.blank, cfg.fused, cfg.clamp,
+                                      scale, int(r), int(r) + 1)
+            assert_grad_close(gsel[k:k + 1], want, cfg.dtype, f"sample {b} row {r}")
+    return loss, red, grad
+
+
+def test_bpe_asr_full_size():
+    wl = W.make("bpe_asr", "cuda")
+    loss, red, grad = sampled_compare(wl, per_sample=48)
+    # Row sums of the fused, unclamped gradient vanish at any size.
+    s = grad.float().sum(dim=1)
+    assert float(s.abs().max()) < 0.05
+    assert abs(float(red) - float(loss.double().sum())) <= 1e-5 * abs(float(red))
+
+
+def test_skewed_full_size():
+    wl = W.make("skewed", "cuda")
+    sampled_compare(wl, per_sample=40)
+
+
+@pytest.mark.slow
+def test_large_vocab_full_size():
+    wl = W.make("large_vocab", "cuda")
+    order = np.argsort(wl.T.astype(np.int64) * (wl.U + 1))
+    loss, red, grad = sampled_compare(wl, per_sample=24, samples=[int(order[0]), int(order[1])])
+    s = grad.sum(dim=1)
+    assert float(s.abs().max()) < 1e-5
+
+
+# ------------------------------------------------------------------ edge cases
+def make(B, T, U, V, **kw):
+    return W.custom(B, T, U, V, device="cuda", **kw)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("fused", [True, False])
+def test_random_many_tiles(dtype, fused):
+    rng = np.random.default_rng(11 if fused else 12)
+    B = 9
+    T = rng.integers(1, 70, size=B)
+    U = rng.integers(0, 45, size=B)
+    wl = make(B, T, U, 37, dtype=dtype, sigma=1.7, blank=5, clamp=-1.0, fused=fused,
+              reduction="sum", seed=3)
+    full_compare(wl)
+
+
+@pytest.mark.parametrize("V", [1, 2, 7, 8, 29, 64, 1001])
+def test_vocab_sizes(V):
+    U = [0, 0] if V == 1 else [3, 1]
+    wl = make(2, [5, 9], U, V, dtype="f32", blank=-1, reduction="none")
+    full_compare(wl)
+
+
+@pytest.mark.parametrize("U", [30, 31, 32, 33, 63, 64, 65, 127, 128, 129, 300, 520])
+def test_lattice_widths(U):
+    wl = make(2, [40, 3], [U, U // 2], 12, dtype="f32", blank=0, reduction="mean")
+    full_compare(wl)
+
+
+def test_degenerate_lattices():
+    # T=1 and U=0 in every combination, incl. the single-node lattice.
+    wl = make(5, [1, 1, 7, 1, 13], [0, 6, 0, 1, 0], 9, dtype="f32", blank=3, reduction="sum")
+    full_compare(wl)
+
+
+def test_single_node_closed_form():
+    wl = make(1, [1], [0], 6, dtype="f32", blank=-1, reduction="none")
+    loss, _, grad = gpu_run(wl)
+    h = to_np(wl.logits).astype(np.float64)[0]
+    lse = np.log(np.exp(h - h.max()).sum()) + h.max()
+    assert float(loss[0]) == pytest.approx(-(h[-1] - lse), rel=1e-6)
+
+
+@pytest.mark.parametrize("blank", [0, 4, 10, -11, -1])
+def test_blank_positions(blank):
+    wl = make(3, [12, 4, 20], [5, 2, 9], 11, dtype="f32", blank=blank, reduction="mean",
+              clamp=0.05)
+    full_compare(wl)
+
+
+def test_long_targets_j32():
+    wl = make(2, [30, 25], [700, 1000], 16, dtype="f32", blank=0, reduction="sum")
+    full_compare(wl)
+
+
+def test_large_batch_many_small_samples():
+    rng = np.random.default_rng(4)
+    B = 1500
+    wl = make(B, rng.integers(1, 6, size=B), rng.integers(0, 4, size=B), 9, dtype="f16",
+              blank=0, reduction="mean")
+    full_compare(wl)
+
+
+def test_inplace_gradient_matches():
+    wl = make(3, [30, 17, 9], [8, 12, 0], 64, dtype="f16", blank=-1, reduction="sum")
+    _, _, g_sep = gpu_run(wl)
+    _, _, g_inp = gpu_run(wl, inplace=True)
+    assert torch.equal(g_sep, g_inp)
+
+
+def test_loss_only_matches():
+    wl = make(3, [30, 17, 9], [8, 12, 0], 64, dtype="f32", blank=-1, reduction="sum")
+    l1, r1, _ = gpu_run(wl)
+    l2, r2, g2 = gpu_run(wl, want_grad=False)
+    assert g2 is None
+    assert torch.equal(l1, l2) and torch.equal(r1, r2)
+
+
+def test_deterministic():
+    wl = W.make("char_asr", "cuda")
+    a = gpu_run(wl)
+    b = gpu_run(wl)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_uniform_logits_closed_form_at_bpe_shape():
+    # Constant logits: loss = (T+U) log V - log C(T-1+U, U) at a BPE-sized lattice.
+    import math
+    T, U, V = 400, 75, 1024
+    wl = make(1, [T], [U], V, dtype="f16", blank=-1, reduction="none")
+    wl.logits.zero_()
+    loss, _, _ = gpu_run(wl)
+    lb = math.lgamma(T + U) - math.lgamma(U + 1) - math.lgamma(T)
+    assert float(loss[0]) == pytest.approx((T + U) * math.log(V) - lb, rel=1e-5)
+
+
+# ------------------------------------------------------------------ errors
+def _status_of(wl, **over):
+    cfg = wl.cfg
+    with pytest.raises((ValueError, N.RNNTError)) as e:
+        rnnt_loss_forward(wl.logits, torch.as_tensor(over.get("targets", wl.targets), device="cuda"),
+                          torch.as_tensor(over.get("T", wl.T), device="cuda"),
+                          torch.as_tensor(over.get("U", wl.U), device="cuda"), cfg.blank,
+                          cfg.clamp, cfg.reduction, cfg.fused)
+    return e.value
+
+
+def test_device_detects_bad_inputs():
+    wl = make(2, [5, 4], [2, 3], 7, dtype="f32", blank=0, reduction="sum")
+    bad = wl.targets.copy()
+    bad[1, 0] = 0  # label equal to blank
+    assert isinstance(_status_of(wl, targets=bad), ValueError)
+    bad = wl.targets.copy()
+    bad[0, 1] = 7  # label out of range
+    assert isinstance(_status_of(wl, targets=bad), ValueError)
+    assert isinstance(_status_of(wl, T=np.array([5, 5], dtype=np.int32)), ValueError)  # rows
+    assert isinstance(_status_of(wl, T=np.array([0, 4], dtype=np.int32)), ValueError)
+    # The workspace is reusable after an error: a valid call still succeeds.
+    full_compare(wl)
+
+
+def test_non_finite_input_reports_mismatch():
+    wl = make(2, [5, 4], [2, 3], 7, dtype="f32", blank=0, reduction="sum")
+    wl.logits[3, 2] = float("nan")
+    e = _status_of(wl)
+    assert isinstance(e, N.RNNTError) and e.code == N.RNNT_LOSS_MISMATCH
+
+
+# ------------------------------------------------------------------ autograd
+@pytest.mark.parametrize("red", ["none", "sum", "mean"])
+def test_autograd_backward_scales(red):
+    wl = make(3, [20, 11, 6], [4, 9, 2], 33, dtype="f32", blank=-1, reduction=red, clamp=-1.0)
+    x = wl.logits.clone().requires_grad_(True)
+    y = torch.as_tensor(wl.targets, device="cuda")
+    Tl = torch.as_tensor(wl.T, device="cuda")
+    Ul = torch.as_tensor(wl.U, device="cuda")
+    out = rnnt_loss(x, y, Tl, Ul, blank=-1, reduction=red)
+    w = torch.tensor([0.5, -2.0, 3.0], device="cuda") if red == "none" else torch.tensor(
+        1.7, device="cuda")
+    (out * w).sum().backward()
+    ref = oracle_full(wl, reduction=red)
+    want = ref.grad.copy()
+    if red == "none":
+        for b in range(3):
+            sl = wl.sample_rows(b)
+            want[sl] *= float(w[b])
+    else:
+        want *= float(w)
+    assert_grad_close(to_np(x.grad), want, "f32")
