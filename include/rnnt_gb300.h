@@ -61,7 +61,7 @@ typedef enum { RNNT_RED_NONE = 0, RNNT_RED_SUM = 1, RNNT_RED_MEAN = 2 } rnnt_red
  *   rows  number of logit rows, sum over b of T_b*(U_b+1) (>= 1)
  *   V     vocabulary size including blank (>= 1)
  *   dt    logit element type
- *   bytes out: required size; about 44 bytes per logit row plus O(B).
+ *   bytes out: required size; about 52 bytes per logit row plus O(B).
  * Returns RNNT_INVALID_VALUE for a NULL `bytes` or out-of-range sizes.
  */
 rnnt_status_t rnnt_workspace_size(int32_t B, int64_t rows, int32_t V, rnnt_dtype_t dt,

@@ -6,28 +6,32 @@
 //               Replaces the host-side largest-task-first balancer of the
 //               rnnt-loss-ascend README (架构设计 "Host 侧").
 //   k_row_*     one pass over the logits: per row the log-softmax denominator
-//               (single-pass max/sum, warp-shuffle reduction) and the blank /
-//               target log-probs, scattered into an anti-diagonal-packed
-//               layout for the DP (README 对角线遍历 α/β).  With the in-kernel
-//               log-softmax off only the two needed elements are read.
-//   k_dp        one CTA of two warps per sample: warp 0 runs the alpha
-//               recursion over anti-diagonals d = 0..T+U-1, warp 1 the beta
-//               recursion from the end; they meet at the middle diagonal,
-//               swap frame offsets, and each then finishes its sweep while
-//               combining alpha and beta of the half the other warp computed
-//               into per-row gradient coefficients (README 核心梯度融合公式).
-//   k_grad_*    one read + one write of the logits: grad_k =
-//               p_k*occ - [k=blank]*post_blank - [k=y]*post_label, clip,
-//               reduction scale, store in the input dtype (may alias logits).
+//               (max, then sum of exponentials, group-shuffle reductions) and
+//               the blank / target transition probabilities, scattered into
+//               an anti-diagonal-packed layout for the DP (README 对角线遍历
+//               α/β).  With the in-kernel log-softmax off only the two needed
+//               elements of a row are read.
+//   k_dp        one CTA of two warps per sample: warp 0 runs the forward
+//               (alpha) recursion over anti-diagonals d = 0..T+U-1, warp 1
+//               the backward (beta) recursion from the end; a lattice column
+//               per lane, the neighbouring column's value by warp shuffle.
+//   k_combine   per row: occupancy and the blank/label arc posteriors from
+//               alpha, beta and P(y|x) (README 核心梯度融合公式).
+//   k_grad      one read + one write of the logits: grad_k = p_k*occ -
+//               [k=blank]*post_blank - [k=y]*post_label, clip, reduction
+//               scale, store in the input dtype (may alias the logits).
 //               Rows whose occupancy is too small to change any output value
 //               are written as zeros without reading the logits.
 //   k_finalize  1 CTA: alpha/beta loss cross-check (README 精度保证 "双 loss
 //               互校验"), deterministic reduction, status word.
 //
-// Numerics: log-domain, base 2.  The DP keeps each anti-diagonal in a frame
-// with an integer offset (a power-of-two scale in the probability domain), so
-// fp32 values stay O(10) while the exact frame offsets carry the magnitude
-// of the accumulated log-probability.
+// Numerics.  The DP runs in the probability domain on extended-range
+// numbers m * 2^e (m in [1,2) as float, e as int32): a product is one
+// float multiply and an integer add, a sum aligns the exponents exactly and
+// does one fused multiply-add.  Every step therefore rounds only with
+// round-to-nearest multiplies/adds and nothing underflows, which is the
+// same protection the README's log-domain recursion ("全程在 log 域") is
+// after, without evaluating a transcendental function per lattice node.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -37,20 +41,25 @@
 
 namespace {
 
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr double kLn2 = 0.69314718055994530942;
+constexpr float kLog2e = 1.4426950216293335f;     // float(log2 e)
+constexpr float kLog2eLo = 1.925962989e-8f;        // log2 e - kLog2e
+constexpr float kLn2 = 0.6931471824645996f;
+constexpr float kSqrt2 = 1.4142135381698608f;
+constexpr double kLn2d = 0.69314718055994530942;
 constexpr int kMaxW = RNNT_MAX_TARGET_LENGTH + 1;
+constexpr int kZeroExp = -(1 << 29);               // exponent of an extended-range zero
 
 enum : int {
     ERR_LENGTH = 1,
     ERR_ROWS = 2,
     ERR_TARGET = 4,
     ERR_MISMATCH = 8,
+    ERR_NONFINITE = 16,
 };
 
 // ---------------------------------------------------------------- workspace
 struct Layout {
-    size_t err, off, order, lossa, lossb, delta, lse2, lpb, lpy, va, vb, oa, qb, info, total;
+    size_t err, off, order, lossa, lossb, pm, pe, lse2, edge, alpha, beta, info, total;
 };
 
 __host__ __device__ inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -64,14 +73,12 @@ __host__ __device__ inline Layout ws_layout(int B, int64_t rows) {
     L.order = p; p = al256(p + sizeof(int32_t) * (size_t)B);
     L.lossa = p; p = al256(p + sizeof(double) * (size_t)B);
     L.lossb = p; p = al256(p + sizeof(double) * (size_t)B);
-    L.delta = p; p = al256(p + sizeof(float) * (size_t)B);
+    L.pm = p;    p = al256(p + sizeof(float) * (size_t)B);
+    L.pe = p;    p = al256(p + sizeof(int32_t) * (size_t)B);
     L.lse2 = p;  p = al256(p + sizeof(float) * R);
-    L.lpb = p;   p = al256(p + sizeof(float) * R);
-    L.lpy = p;   p = al256(p + sizeof(float) * R);
-    L.va = p;    p = al256(p + sizeof(float) * R);
-    L.vb = p;    p = al256(p + sizeof(float) * R);
-    L.oa = p;    p = al256(p + sizeof(int32_t) * R);
-    L.qb = p;    p = al256(p + sizeof(int32_t) * R);
+    L.edge = p;  p = al256(p + sizeof(int4) * R);
+    L.alpha = p; p = al256(p + sizeof(int2) * R);
+    L.beta = p;  p = al256(p + sizeof(int2) * R);
     L.info = p;  p = al256(p + sizeof(float4) * R);
     L.total = p;
     return L;
@@ -94,8 +101,7 @@ struct Params {
     float skip2;      // log2-occupancy below which a gradient row is exactly zero
     int fused;
     int red;
-    int want_grad;
-    int ring_floats;  // per-warp DP ring size (floats)
+    int ring_int4;    // per-warp DP ring size (int4 records)
     float* loss;
     float* loss_red;
     int32_t* status;
@@ -105,15 +111,13 @@ struct Params {
     int32_t* order;
     double* lossa;
     double* lossb;
-    float* delta;
-    float* lse2;
-    float* lpb;
-    float* lpy;
-    float* va;
-    float* vb;
-    int32_t* oa;
-    int32_t* qb;
-    float4* info;
+    float* pm;        // P(y|x) of each sample, extended range
+    int32_t* pe;
+    float* lse2;      // per row (row order): log2 sum_k 2^(h_k log2 e)
+    int4* edge;       // per node (diagonal-packed): {p_blank.m, p_blank.e, p_label.m, p_label.e}
+    int2* alpha;      // per node (diagonal-packed): {m, e}
+    int2* beta;
+    float4* info;     // per row: {log2 occ - lse2, log2 occ, post_blank, post_label}
 };
 
 // ---------------------------------------------------------------- helpers
@@ -127,18 +131,17 @@ __device__ __forceinline__ float lg2(float x) {
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-// log2(2^a + 2^b); -inf absorbing, NaN-free when both are -inf.
-__device__ __forceinline__ float lae2(float a, float b) {
-    float mx = fmaxf(a, b), mn = fminf(a, b);
-    float dd = fmaxf(mn - mx, -126.0f);
-    return mx + lg2(1.0f + ex2(dd));
-}
 
 // Number of lattice nodes (t,u), 0<=t<T, 0<=u<W, with t+u < d: first packed
 // index of anti-diagonal d (inclusion-exclusion over the rectangle).
 __device__ __forceinline__ int64_t tri(int64_t n) { return n > 0 ? n * (n + 1) / 2 : 0; }
 __device__ __forceinline__ int64_t diag_start(int d, int T, int W) {
     return tri(d) - tri((int64_t)d - T) - tri((int64_t)d - W) + tri((int64_t)d - T - W);
+}
+// Packed index of node (t,u) relative to its sample's first row.
+__device__ __forceinline__ int64_t node_index(int t, int u, int T, int U) {
+    const int d = t + u;
+    return diag_start(d, T, U + 1) + (t - max(0, d - U));
 }
 
 __device__ __forceinline__ int find_sample(const int64_t* off, int B, int64_t r) {
@@ -148,6 +151,79 @@ __device__ __forceinline__ int find_sample(const int64_t* off, int B, int64_t r)
         if (__ldg(off + mid) <= r) lo = mid; else hi = mid;
     }
     return lo;
+}
+// Rows are visited in increasing order; step to r's sample, searching only on a change.
+__device__ __forceinline__ int advance_sample(const int64_t* off, int B, int b, int64_t r) {
+    return (__ldg(off + b + 1) <= r) ? find_sample(off, B, r) : b;
+}
+
+// ------------------------------------------------ extended-range arithmetic
+// 2^f for f in [0,1) as sqrt(2) * exp(g), g = (f - 1/2) ln 2, |g| <= 0.347,
+// with the Taylor series of exp truncated after g^9 (remainder < 3e-10).
+__device__ __forceinline__ float exp_taylor(float g) {
+    float q = 1.0f / 362880.0f;
+    q = fmaf(q, g, 1.0f / 40320.0f);
+    q = fmaf(q, g, 1.0f / 5040.0f);
+    q = fmaf(q, g, 1.0f / 720.0f);
+    q = fmaf(q, g, 1.0f / 120.0f);
+    q = fmaf(q, g, 1.0f / 24.0f);
+    q = fmaf(q, g, 1.0f / 6.0f);
+    q = fmaf(q, g, 0.5f);
+    q = fmaf(q, g, 1.0f);
+    return fmaf(q, g, 1.0f);
+}
+
+// Renormalise m * 2^e to m in [1,2) (m > 0 finite), or leave a zero alone.
+__device__ __forceinline__ void xf_norm(float& m, int& e) {
+    const int bits = __float_as_int(m);
+    const int ex = (m != 0.0f) ? (bits >> 23) - 127 : 0;
+    m = __int_as_float(bits - (ex << 23));
+    e += ex;
+}
+
+// 2^(xh + xl) as m * 2^e, m in [1,2); xl is a small correction (|xl| < 1e-3).
+__device__ __forceinline__ void xf_exp2(float xh, float xl, float& m, int& e) {
+    if (!(xh > -1.0e8f)) {   // -inf (a zero probability) and anything below 2^-1e8
+        m = 0.0f;
+        e = kZeroExp;
+        return;
+    }
+    const float n = floorf(fminf(xh, 1.0e8f));
+    const float f = xh - n;                      // exact, in [0, 1)
+    m = exp_taylor(fmaf(f - 0.5f, kLn2, xl * kLn2)) * kSqrt2;
+    e = (int)n;
+    xf_norm(m, e);
+}
+
+// p = 2^((h - M) log2 e) / s with the exponent carried in two floats.
+__device__ __forceinline__ void xf_prob(float h, float M, float s, float& m, int& e) {
+    const float d = h - M;                       // TwoSum(h, -M)
+    const float bb = d - h;
+    const float derr = (h - (d - bb)) + (-M - bb);
+    const float xh = d * kLog2e;
+    const float xl = fmaf(d, kLog2e, -xh) + fmaf(derr, kLog2e, d * kLog2eLo);
+    xf_exp2(xh, xl, m, e);
+    if (m != 0.0f) {
+        m = m / s;
+        xf_norm(m, e);
+    }
+}
+
+__device__ __forceinline__ void xf_mul(float am, int ae, float pm, int pe, float& m, int& e) {
+    m = am * pm;
+    e = max(ae + pe, kZeroExp);
+}
+
+// (m1 2^e1) + (m2 2^e2): exact alignment by the exponent difference, one FMA.
+__device__ __forceinline__ void xf_add(float m1, int e1, float m2, int e2, float& m, int& e) {
+    const bool first = e1 >= e2;
+    const float big = first ? m1 : m2, small = first ? m2 : m1;
+    const int E = first ? e1 : e2;
+    const int k = first ? e2 - e1 : e1 - e2;                   // <= 0
+    const float sc = __int_as_float(max(k + 127, 0) << 23);    // 2^k (0 below 2^-126)
+    m = fmaf(small, sc, big);
+    e = E;
+    xf_norm(m, e);
 }
 
 template <typename Tin> struct Elt;
@@ -201,6 +277,19 @@ __device__ __forceinline__ unsigned group_mask() {
     }
 }
 
+template <int G>
+__device__ __forceinline__ float group_max(float v, unsigned gm) {
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(gm, v, o, G));
+    return v;
+}
+template <int G>
+__device__ __forceinline__ float group_sum(float v, unsigned gm) {
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(gm, v, o, G);
+    return v;
+}
+
 // ---------------------------------------------------------------- k_prepare
 __global__ void __launch_bounds__(1024) k_prepare(Params p) {
     __shared__ int64_t wsum[32];
@@ -245,7 +334,7 @@ __global__ void __launch_bounds__(1024) k_prepare(Params p) {
         p.off[p.B] = carry;
         if (carry != p.rows) atomicOr(&errs, ERR_ROWS);
     }
-    // Labels: in range, not blank (warp-transducer blog 5.2).
+    // Labels: in range and not blank (warp-transducer blog 5.2).
     const int64_t nt = (int64_t)p.B * p.S;
     for (int64_t i = tid; i < nt; i += blockDim.x) {
         const int b = (int)(i / p.S), u = (int)(i % p.S);
@@ -255,7 +344,7 @@ __global__ void __launch_bounds__(1024) k_prepare(Params p) {
             if (y < 0 || y >= p.V || y == p.blank) atomicOr(&errs, ERR_TARGET);
         }
     }
-    // Largest DP first: key (T+U, area), ties by index.  O(B^2) rank sort.
+    // Longest DP first: key (T+U, area), ties by index.  O(B^2) rank sort.
     for (int b = tid; b < p.B; b += blockDim.x) {
         if (p.B > 8192) { p.order[b] = b; continue; }
         const int Tb = p.Tl[b], Ub = p.Ul[b];
@@ -273,33 +362,105 @@ __global__ void __launch_bounds__(1024) k_prepare(Params p) {
 }
 
 // ---------------------------------------------------------------- row pass
-// Writes, at the packed index of node (t,u):
-//   lse2 = log2 sum_k 2^(h_k log2e)     (0 with the in-kernel softmax off)
-//   lpb  = log2 P(blank|t,u), -inf at t=T-1, u<U (no blank leaves the last frame
-//          before every label is out)
-//   lpy  = log2 P(y_{u+1}|t,u), -inf at u=U
-__device__ __forceinline__ void row_store(const Params& p, int b, int64_t r, float lse2v,
-                                          float hb, float hy) {
+// Row epilogue (one lane): log2 of the softmax denominator in row order, and
+// the node's two transition probabilities at its packed index.  A blank from
+// the last frame before every label is out, and a label at u = U, have
+// probability 0 (the lattice has no such arc).
+template <typename Tin>
+__device__ __forceinline__ void row_epilogue(const Params& p, const Tin* row, int b, int64_t r,
+                                             float M, float s) {
+    using E = Elt<Tin>;
     const int T = __ldg(p.Tl + b), U = __ldg(p.Ul + b), W = U + 1;
     const int64_t o = __ldg(p.off + b);
-    const int64_t rr = r - o;
-    const int t = (int)(rr / W), u = (int)(rr - (int64_t)t * W);
-    const int d = t + u;
-    const int64_t idx = o + diag_start(d, T, W) + (t - max(0, d - U));
-    p.lse2[idx] = lse2v;
-    p.lpb[idx] = (t == T - 1 && u < U) ? -INFINITY : hb * kLog2e - lse2v;
-    p.lpy[idx] = (u < U) ? hy * kLog2e - lse2v : -INFINITY;
+    const unsigned rr = (unsigned)(r - o);
+    const int t = (int)(rr / (unsigned)W), u = (int)(rr - (unsigned)t * W);
+    const float hb = E::get(row, p.blank);
+    const float hy = (u < U) ? E::get(row, __ldg(p.targets + (int64_t)b * p.S + u)) : 0.0f;
+    if (p.fused) {
+        const float lse2v = fmaf(M, kLog2e, lg2(s));
+        p.lse2[r] = lse2v;
+        if (!(lse2v < INFINITY)) atomicOr(p.err, ERR_NONFINITE);   // NaN or +inf logits
+    } else {
+        p.lse2[r] = 0.0f;
+        if (!(hb < INFINITY) || !(hy < INFINITY)) atomicOr(p.err, ERR_NONFINITE);
+    }
+    float bm = 0.0f, ym = 0.0f;
+    int be = kZeroExp, ye = kZeroExp;
+    if (!(t == T - 1 && u < U)) xf_prob(hb, M, s, bm, be);
+    if (u < U) xf_prob(hy, M, s, ym, ye);
+    p.edge[o + node_index(t, u, T, U)] =
+        make_int4(__float_as_int(bm), be, __float_as_int(ym), ye);
 }
 
-__device__ __forceinline__ int row_label(const Params& p, int b, int64_t r) {
-    const int U = __ldg(p.Ul + b), W = U + 1;
-    const int64_t rr = r - __ldg(p.off + b);
-    const int u = (int)(rr % W);
-    return (u < U) ? __ldg(p.targets + (int64_t)b * p.S + u) : -1;
+// Row held in registers: NV 16-byte vectors per lane, G lanes per row; the
+// next row's vectors are loaded before the current one is reduced.
+template <typename Tin, int G, int NV>
+__global__ void __launch_bounds__(256) k_row_regs(Params p) {
+    if (*p.err) return;
+    using E = Elt<Tin>;
+    constexpr int EPV = E::kPerVec;
+    const Tin* X = static_cast<const Tin*>(p.logits);
+    const int V = p.V, nvec = V / EPV;
+    const int lane = threadIdx.x & (G - 1);
+    const unsigned gm = group_mask<G>();
+    const int64_t ng = (int64_t)gridDim.x * (blockDim.x / G);
+    int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
+    if (r >= p.rows) return;
+    int b = find_sample(p.off, p.B, r);
+    uint4 cur[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int vi = lane + k * G;
+        if (vi < nvec) cur[k] = __ldg(reinterpret_cast<const uint4*>(X + r * (int64_t)V) + vi);
+    }
+    for (;;) {
+        const int64_t rn = r + ng;
+        uint4 nxt[NV];
+        if (rn < p.rows) {
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const int vi = lane + k * G;
+                if (vi < nvec)
+                    nxt[k] = __ldg(reinterpret_cast<const uint4*>(X + rn * (int64_t)V) + vi);
+            }
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            if (lane + k * G < nvec) {
+                float x[EPV];
+                E::unpack(cur[k], x);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) M = fmaxf(M, x[e]);
+            }
+        }
+        M = group_max<G>(M, gm);
+        float s = 0.0f;
+        if (M != -INFINITY) {
+            const float ML = M * kLog2e;
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                if (lane + k * G < nvec) {
+                    float x[EPV];
+                    E::unpack(cur[k], x);
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) s += ex2(fmaf(x[e], kLog2e, -ML));
+                }
+            }
+        }
+        s = group_sum<G>(s, gm);
+        if (lane == 0) row_epilogue<Tin>(p, X + r * (int64_t)V, b, r, M, s);
+        if (rn >= p.rows) break;
+        r = rn;
+        b = advance_sample(p.off, p.B, b, r);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) cur[k] = nxt[k];
+    }
 }
 
+// Long rows (or rows not 16-byte aligned): streaming max/sum with rescale.
 template <typename Tin, int G, bool VEC>
-__global__ void __launch_bounds__(256) k_row_fused(Params p) {
+__global__ void __launch_bounds__(256) k_row_stream(Params p) {
     if (*p.err) return;
     using E = Elt<Tin>;
     const Tin* X = static_cast<const Tin*>(p.logits);
@@ -307,7 +468,10 @@ __global__ void __launch_bounds__(256) k_row_fused(Params p) {
     const int lane = threadIdx.x & (G - 1);
     const unsigned gm = group_mask<G>();
     const int64_t ng = (int64_t)gridDim.x * (blockDim.x / G);
-    for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G; r < p.rows; r += ng) {
+    int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
+    int b = (r < p.rows) ? find_sample(p.off, p.B, r) : 0;
+    for (; r < p.rows; r += ng) {
+        b = advance_sample(p.off, p.B, b, r);
         const Tin* row = X + r * (int64_t)V;
         float m = -INFINITY, s = 0.0f;
         if (VEC) {
@@ -360,22 +524,10 @@ __global__ void __launch_bounds__(256) k_row_fused(Params p) {
                 }
             }
         }
-#pragma unroll
-        for (int o = G / 2; o > 0; o >>= 1) {
-            const float om = __shfl_xor_sync(gm, m, o, G);
-            const float os = __shfl_xor_sync(gm, s, o, G);
-            const float nm = fmaxf(m, om);
-            if (nm != -INFINITY) s = s * ex2((m - nm) * kLog2e) + os * ex2((om - nm) * kLog2e);
-            m = nm;
-        }
-        if (lane == 0) {
-            const float lse2v = m * kLog2e + lg2(s);
-            const int b = find_sample(p.off, p.B, r);
-            const int y = row_label(p, b, r);
-            const float hb = E::get(row, p.blank);
-            const float hy = (y >= 0) ? E::get(row, y) : 0.0f;
-            row_store(p, b, r, lse2v, hb, hy);
-        }
+        const float M = group_max<G>(m, gm);
+        s = (M == -INFINITY) ? 0.0f : s * ex2((m - M) * kLog2e);
+        s = group_sum<G>(s, gm);
+        if (lane == 0) row_epilogue<Tin>(p, row, b, r, M, s);
     }
 }
 
@@ -383,389 +535,260 @@ __global__ void __launch_bounds__(256) k_row_fused(Params p) {
 template <typename Tin>
 __global__ void __launch_bounds__(256) k_row_gather(Params p) {
     if (*p.err) return;
-    using E = Elt<Tin>;
     const Tin* X = static_cast<const Tin*>(p.logits);
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < p.rows; r += stride) {
-        const Tin* row = X + r * (int64_t)p.V;
-        const int b = find_sample(p.off, p.B, r);
-        const int y = row_label(p, b, r);
-        const float hb = E::get(row, p.blank);
-        const float hy = (y >= 0) ? E::get(row, y) : 0.0f;
-        row_store(p, b, r, 0.0f, hb, hy);
+    int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    int b = (r < p.rows) ? find_sample(p.off, p.B, r) : 0;
+    for (; r < p.rows; r += stride) {
+        b = advance_sample(p.off, p.B, b, r);
+        row_epilogue<Tin>(p, X + r * (int64_t)p.V, b, r, 0.0f, 1.0f);
     }
 }
 
 // ---------------------------------------------------------------- DP
-// Per-warp ring of prefetched anti-diagonal data in shared memory.  Slot
-// layout (floats): [lpb J*32][lpy J*32][lse2 J*32][v_other J*32][frame 32];
-// column u = lane + 32*j.  Ring depth R, prefetch distance R-2.
+// Per-warp ring of prefetched anti-diagonal edge records in shared memory:
+// slot = J*32 int4 (column u = lane + 32*j); depth R, prefetch distance R-2.
 template <int J> struct Ring;
 template <> struct Ring<1> { static constexpr int R = 32; };
 template <> struct Ring<2> { static constexpr int R = 32; };
-template <> struct Ring<4> { static constexpr int R = 16; };
-template <> struct Ring<8> { static constexpr int R = 8; };
-template <> struct Ring<16> { static constexpr int R = 6; };
+template <> struct Ring<4> { static constexpr int R = 24; };
+template <> struct Ring<8> { static constexpr int R = 12; };
+template <> struct Ring<16> { static constexpr int R = 7; };
 template <> struct Ring<32> { static constexpr int R = 4; };
 
-__host__ __device__ constexpr int ring_slot_floats(int J) { return (4 * J + 1) * 32; }
-
-__device__ __forceinline__ void cp4(void* smem, const void* gmem) {
+__device__ __forceinline__ void cp16(void* smem, const void* gmem) {
     const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(sa), "l"(gmem) : "memory");
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem) : "memory");
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
-__device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 struct Samp {
-    int b, T, U, W, D, dm;
+    int b, T, U, W, D;
     int64_t off;
 };
 
-// Queue the loads of anti-diagonal d into its ring slot: edge log-weights
-// always, and (when `comb`) lse2, the other direction's values and frame.
+__device__ __forceinline__ bool on_lattice(const Samp& c, int d, int u) {
+    const int t = d - u;
+    return u <= c.U && t >= 0 && t < c.T;
+}
+// Global packed index of the node on diagonal d in column u: base(d) - u.
+__device__ __forceinline__ int64_t diag_base(const Samp& c, int d) {
+    return c.off + diag_start(d, c.T, c.W) - max(0, d - c.U) + d;
+}
+
 template <int J>
-__device__ __forceinline__ void ring_issue(const Samp& c, float* ring, int d, bool comb,
-                                           const float* lpb, const float* lpy, const float* lse2,
-                                           const float* vo, const int32_t* fo, int lane) {
-    constexpr int R = Ring<J>::R, SL = ring_slot_floats(J);
+__device__ __forceinline__ void ring_issue(const Params& p, const Samp& c, int4* ring, int d,
+                                           int lane) {
+    constexpr int R = Ring<J>::R;
     if (d >= 0 && d < c.D) {
-        float* sl = ring + (d % R) * SL;
-        const int64_t base = c.off + diag_start(d, c.T, c.W) - max(0, d - c.U) + d;
+        int4* sl = ring + (d % R) * (J * 32);
+        const int64_t base = diag_base(c, d);
 #pragma unroll
         for (int j = 0; j < J; ++j) {
-            const int u = lane + 32 * j, t = d - u;
-            float* e = sl + j * 32 + lane;
-            if (u <= c.U && t >= 0 && t < c.T) {
-                const int64_t g = base - u;
-                cp4(e, lpb + g);
-                cp4(e + J * 32, lpy + g);
-                if (comb) {
-                    cp4(e + 2 * J * 32, lse2 + g);
-                    cp4(e + 3 * J * 32, vo + g);
-                }
-            } else {
-                e[0] = -INFINITY;
-                e[J * 32] = -INFINITY;
-                if (comb) {
-                    e[2 * J * 32] = 0.0f;
-                    e[3 * J * 32] = -INFINITY;
-                }
-            }
+            const int u = lane + 32 * j;
+            if (on_lattice(c, d, u)) cp16(sl + j * 32 + lane, p.edge + (base - u));
+            else sl[j * 32 + lane] = make_int4(0, kZeroExp, 0, kZeroExp);
         }
-        if (comb) cp4(sl + 4 * J * 32 + lane, fo + c.off + d);
     }
 }
 
 template <int J>
-__device__ __forceinline__ float warp_max_valid(const float* v, int d, const Samp& c, int lane) {
-    float m = -INFINITY;
+__device__ __forceinline__ void store_diag(const Samp& c, int2* out, int d, const float* m,
+                                           const int* e, int lane) {
+    const int64_t base = diag_base(c, d);
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-        const int u = lane + 32 * j, t = d - u;
-        if (u <= c.U && t >= 0 && t < c.T) m = fmaxf(m, v[j]);
+        const int u = lane + 32 * j;
+        if (on_lattice(c, d, u)) out[base - u] = make_int2(__float_as_int(m[j]), e[j]);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    return m;
 }
 
-// Gradient coefficients of node (t,u) on anti-diagonal e (all log2, relative
-// to the sample's reference frame C; the per-sample correction C - ll is
-// added by the gradient pass):
-//   x: log2(occupancy) - lse2    y: log2(occupancy)
-//   z: log2(posterior of the blank arc)   w: log2(posterior of the label arc)
-__device__ __forceinline__ void put_info(const Params& p, const Samp& c, int t, int u, float va,
-                                         float vbe, float lpb, float lpy, float lse2v,
-                                         float vb_blank, float vb_label, float KA, float KB) {
-    const float lc = va + vbe + KA;
-    float eb;
-    if (t < c.T - 1) eb = va + lpb + vb_blank + KB;
-    else eb = (u == c.U) ? lc : -INFINITY;
-    const float ey = (u < c.U) ? va + lpy + vb_label + KB : -INFINITY;
-    p.info[c.off + (int64_t)t * c.W + u] = make_float4(lc - lse2v, lc, eb, ey);
-}
-
+// Forward variable: alpha(t,u) = alpha(t-1,u) p_blank(t-1,u) + alpha(t,u-1) p_label(t,u-1).
 template <int J>
-__device__ void dp_alpha(const Params& p, const Samp& c, float* ring, int* xch) {
-    constexpr int R = Ring<J>::R, PF = R - 2, SL = ring_slot_floats(J);
+__device__ void dp_alpha(const Params& p, const Samp& c, int4* ring) {
+    constexpr int R = Ring<J>::R, PF = R - 2;
     const int lane = threadIdx.x & 31;
-    float v[J];
+    float am[J];
+    int ae[J];
 #pragma unroll
-    for (int j = 0; j < J; ++j) v[j] = (lane + 32 * j == 0) ? 0.0f : -INFINITY;
-    if (lane == 0) {
-        p.va[c.off] = 0.0f;
-        p.oa[c.off] = 0;
+    for (int j = 0; j < J; ++j) {
+        const bool origin = lane + 32 * j == 0;
+        am[j] = origin ? 1.0f : 0.0f;
+        ae[j] = origin ? 0 : kZeroExp;
     }
+    store_diag<J>(c, p.alpha, 0, am, ae, lane);
     for (int k = 0; k <= PF; ++k) {
-        ring_issue<J>(c, ring, k, false, p.lpb, p.lpy, p.lse2, p.vb, p.qb, lane);
+        ring_issue<J>(p, c, ring, k, lane);
         cp_commit();
     }
-    // Integer frame offsets (log2 units) of diagonals d-1..d-4 and the warp
-    // maxima of v on d-2..d-4 (each in its own frame).  The frame of d is
-    // extrapolated from the maxima of d-3 and d-4, whose reductions have two
-    // iterations to complete, so they stay off the recursion's critical path.
-    int O = 0, Oh2 = 0, Oh3 = 0, Oh4 = 0;
-    float mA = -INFINITY, mB = -INFINITY, mC = -INFINITY;
-    bool synced = false;
-    int C = 0;
-    const bool comb_on = p.want_grad != 0;
-
-    for (int d = 1; d <= c.D; ++d) {
-        if (d == c.dm + 1) {
-            // Midpoint: swap frame offsets, then fetch what the combine needs.
-            if (lane == 0) xch[0] = O;
-            asm volatile("bar.sync 1, 64;\n" ::: "memory");
-            C = xch[0] + xch[1];
-            synced = true;
-            if (comb_on) {
-                for (int e = c.dm + 1; e <= min(c.dm + PF, c.D - 1); ++e) {
-                    float* sl = ring + (e % R) * SL;
-                    const int64_t base = c.off + diag_start(e, c.T, c.W) - max(0, e - c.U) + e;
-#pragma unroll
-                    for (int j = 0; j < J; ++j) {
-                        const int u = lane + 32 * j, t = e - u;
-                        float* q = sl + j * 32 + lane;
-                        if (u <= c.U && t >= 0 && t < c.T) {
-                            cp4(q + 2 * J * 32, p.lse2 + base - u);
-                            cp4(q + 3 * J * 32, p.vb + base - u);
-                        } else {
-                            q[2 * J * 32] = 0.0f;
-                            q[3 * J * 32] = -INFINITY;
-                        }
-                    }
-                    cp4(sl + 4 * J * 32 + lane, p.qb + c.off + e);
-                }
-                cp_commit();
-                cp_wait_all();
-            }
-        }
-        if (d == c.D) break;
-        ring_issue<J>(c, ring, d + PF, synced && comb_on, p.lpb, p.lpy, p.lse2, p.vb, p.qb, lane);
-        cp_commit();
-        cp_wait<PF>();
-        __syncwarp();
-        const float* sp = ring + ((d - 1) % R) * SL;
-        const float* sc = ring + (d % R) * SL;
-
-        int Onew = O;
-        if (fabsf(mB) < 1e6f && fabsf(mC) < 1e6f) {
-            const int a3 = Oh3 + (int)rintf(mB), a4 = Oh4 + (int)rintf(mC);
-            Onew = a3 + 3 * (a3 - a4);
-        }
-        const int sig = Onew - O;
-        const float sh = (float)sig;
-        float ob[J], oy[J], yy[J], nv[J];
-#pragma unroll
-        for (int j = 0; j < J; ++j) {
-            ob[j] = v[j] + (sp[j * 32 + lane] - sh);
-            oy[j] = v[j] + (sp[(J + j) * 32 + lane] - sh);
-        }
-#pragma unroll
-        for (int j = 0; j < J; ++j) yy[j] = __shfl_sync(0xffffffffu, oy[j], (lane + 31) & 31);
-#pragma unroll
-        for (int j = 0; j < J; ++j) {
-            const float nb = lane ? yy[j] : (j ? yy[j - 1] : -INFINITY);
-            nv[j] = lae2(ob[j], nb);
-        }
-        // Lagged frame choice: the max of diagonal d-1 drives the shift at d+1.
-        const float m_prev = warp_max_valid<J>(v, d - 1, c, lane);
-
-        if (synced && comb_on && d - 1 > c.dm) {
-            const int e = d - 1;
-            const int Qe = __float_as_int(sp[4 * J * 32 + lane]);
-            const int Qn = __float_as_int(sc[4 * J * 32 + lane]);
-            const float KA = (float)(O + Qe - C), KB = (float)(O + Qn - C);
-            float nbv[J];
-#pragma unroll
-            for (int j = 0; j < J; ++j)
-                nbv[j] = __shfl_sync(0xffffffffu, sc[(3 * J + j) * 32 + lane], (lane + 1) & 31);
-#pragma unroll
-            for (int j = 0; j < J; ++j) {
-                const int u = lane + 32 * j, t = e - u;
-                if (u <= c.U && t >= 0 && t < c.T) {
-                    const float lab = (lane < 31) ? nbv[j] : (j + 1 < J ? nbv[j + 1] : -INFINITY);
-                    put_info(p, c, t, u, v[j], sp[(3 * J + j) * 32 + lane], sp[j * 32 + lane],
-                             sp[(J + j) * 32 + lane], sp[(2 * J + j) * 32 + lane],
-                             sc[(3 * J + j) * 32 + lane], lab, KA, KB);
-                }
-            }
-        }
-        // Commit diagonal d.
-        Oh4 = Oh3;
-        Oh3 = Oh2;
-        Oh2 = O;
-        O = Onew;
-        {
-            const int64_t base = c.off + diag_start(d, c.T, c.W) - max(0, d - c.U) + d;
-#pragma unroll
-            for (int j = 0; j < J; ++j) {
-                const int u = lane + 32 * j, t = d - u;
-                v[j] = nv[j];
-                if (u <= c.U && t >= 0 && t < c.T) p.va[base - u] = nv[j];
-            }
-            if (lane == 0) p.oa[c.off + d] = O;
-        }
-        mC = mB;
-        mB = mA;
-        mA = m_prev;
-    }
-    // Last diagonal D-1 holds only the terminal node (T-1, U).
-    const int e = c.D - 1;
-    const float* sp = ring + (e % R) * SL;
-    const int jU = c.U >> 5, lU = c.U & 31;
-    float vU = -INFINITY, lpbU = -INFINITY, vbU = -INFINITY, lseU = 0.0f;
-#pragma unroll
-    for (int j = 0; j < J; ++j)
-        if (j == jU) {
-            vU = v[j];
-            lpbU = sp[j * 32 + lane];
-            vbU = sp[(3 * J + j) * 32 + lane];
-            lseU = sp[(2 * J + j) * 32 + lane];
-        }
-    if (lane == lU) {
-        if (comb_on && e > c.dm) {
-            const int Qe = __float_as_int(sp[4 * J * 32 + lane]);
-            put_info(p, c, c.T - 1, c.U, vU, vbU, lpbU, -INFINITY, lseU, 0.0f, -INFINITY,
-                     (float)(O + Qe - C), (float)(O - C));
-        }
-        const double ll2 = (double)O + (double)vU + (double)lpbU;
-        p.lossa[c.b] = -ll2 * kLn2;
-        p.loss[c.b] = (float)(-ll2 * kLn2);
-        p.delta[c.b] = (float)((double)C - ll2);
-    }
-}
-
-template <int J>
-__device__ void dp_beta(const Params& p, const Samp& c, float* ring, int* xch) {
-    constexpr int R = Ring<J>::R, PF = R - 2, SL = ring_slot_floats(J);
-    const int lane = threadIdx.x & 31;
-    float v[J];   // beta of diagonal d+1 (virtual diagonal D: 0 at column U)
-#pragma unroll
-    for (int j = 0; j < J; ++j) v[j] = (lane + 32 * j == c.U) ? 0.0f : -INFINITY;
-    for (int k = 0; k <= PF; ++k) {
-        ring_issue<J>(c, ring, c.D - 1 - k, false, p.lpb, p.lpy, p.lse2, p.va, p.oa, lane);
-        cp_commit();
-    }
-    int Q = 0, Qh2 = 0, Qh3 = 0, Qh4 = 0;   // frames of d+1..d+4 (mirror of dp_alpha)
-    float mA = -INFINITY, mB = -INFINITY, mC = -INFINITY;
-    bool synced = false;
-    int C = 0;
-    const bool comb_on = p.want_grad != 0;
-
-    for (int d = c.D - 1; d >= 0; --d) {
-        if (d == c.dm) {
-            if (lane == 0) xch[1] = Q;   // frame of diagonal dm+1
-            asm volatile("bar.sync 1, 64;\n" ::: "memory");
-            C = xch[0] + xch[1];
-            synced = true;
-            if (comb_on) {
-                for (int e = c.dm; e >= max(0, c.dm - PF); --e) {
-                    float* sl = ring + (e % R) * SL;
-                    const int64_t base = c.off + diag_start(e, c.T, c.W) - max(0, e - c.U) + e;
-#pragma unroll
-                    for (int j = 0; j < J; ++j) {
-                        const int u = lane + 32 * j, t = e - u;
-                        float* q = sl + j * 32 + lane;
-                        if (u <= c.U && t >= 0 && t < c.T) {
-                            cp4(q + 2 * J * 32, p.lse2 + base - u);
-                            cp4(q + 3 * J * 32, p.va + base - u);
-                        } else {
-                            q[2 * J * 32] = 0.0f;
-                            q[3 * J * 32] = -INFINITY;
-                        }
-                    }
-                    cp4(sl + 4 * J * 32 + lane, p.oa + c.off + e);
-                }
-                cp_commit();
-                cp_wait_all();
-            }
-        }
-        ring_issue<J>(c, ring, d - PF - 1, synced && comb_on, p.lpb, p.lpy, p.lse2, p.va, p.oa,
-                      lane);
+    for (int d = 1; d < c.D; ++d) {
+        ring_issue<J>(p, c, ring, d + PF, lane);
         cp_commit();
         cp_wait<PF + 1>();
-        __syncwarp();
-        const float* sd = ring + (d % R) * SL;
-
-        int Qnew = Q;
-        if (fabsf(mB) < 1e6f && fabsf(mC) < 1e6f) {
-            const int b3 = Qh3 + (int)rintf(mB), b4 = Qh4 + (int)rintf(mC);
-            Qnew = b3 + 3 * (b3 - b4);
-        }
-        const int tau = Qnew - Q;
-        const float sh = (float)tau;
-        float nbv[J], nv[J], lab[J];
-#pragma unroll
-        for (int j = 0; j < J; ++j) nbv[j] = __shfl_sync(0xffffffffu, v[j], (lane + 1) & 31);
+        const int4* sp = ring + ((d - 1) % R) * (J * 32);
+        float bm[J], ym[J];
+        int be[J], ye[J];
 #pragma unroll
         for (int j = 0; j < J; ++j) {
-            lab[j] = (lane < 31) ? nbv[j] : (j + 1 < J ? nbv[j + 1] : -INFINITY);
-            nv[j] = lae2(v[j] + (sd[j * 32 + lane] - sh), lab[j] + (sd[(J + j) * 32 + lane] - sh));
+            const int4 ed = sp[j * 32 + lane];
+            xf_mul(am[j], ae[j], __int_as_float(ed.x), ed.y, bm[j], be[j]);
+            xf_mul(am[j], ae[j], __int_as_float(ed.z), ed.w, ym[j], ye[j]);
         }
-        const float m_next = warp_max_valid<J>(v, d + 1, c, lane);
-        const int Qn = Q;   // frame of d+1
-        Qh4 = Qh3;
-        Qh3 = Qh2;
-        Qh2 = Q;
-        Q = Qnew;           // frame of d
-
-        if (synced && comb_on) {
-            const int Oe = __float_as_int(sd[4 * J * 32 + lane]);
-            const float KA = (float)(Oe + Q - C), KB = (float)(Oe + Qn - C);
+        float sm[J];
+        int se[J];
 #pragma unroll
-            for (int j = 0; j < J; ++j) {
-                const int u = lane + 32 * j, t = d - u;
-                if (u <= c.U && t >= 0 && t < c.T)
-                    put_info(p, c, t, u, sd[(3 * J + j) * 32 + lane], nv[j], sd[j * 32 + lane],
-                             sd[(J + j) * 32 + lane], sd[(2 * J + j) * 32 + lane], v[j], lab[j],
-                             KA, KB);
-            }
+        for (int j = 0; j < J; ++j) {
+            sm[j] = __shfl_sync(0xffffffffu, ym[j], (lane + 31) & 31);
+            se[j] = __shfl_sync(0xffffffffu, ye[j], (lane + 31) & 31);
         }
-        {
-            const int64_t base = c.off + diag_start(d, c.T, c.W) - max(0, d - c.U) + d;
 #pragma unroll
-            for (int j = 0; j < J; ++j) {
-                const int u = lane + 32 * j, t = d - u;
-                v[j] = nv[j];
-                if (u <= c.U && t >= 0 && t < c.T) p.vb[base - u] = nv[j];
-            }
-            if (lane == 0) p.qb[c.off + d] = Q;
+        for (int j = 0; j < J; ++j) {
+            const float nm = lane ? sm[j] : (j ? sm[j - 1] : 0.0f);
+            const int ne = lane ? se[j] : (j ? se[j - 1] : kZeroExp);
+            xf_add(bm[j], be[j], nm, ne, am[j], ae[j]);
         }
-        mC = mB;
-        mB = mA;
-        mA = m_next;
+        store_diag<J>(c, p.alpha, d, am, ae, lane);
     }
-    if (lane == 0) p.lossb[c.b] = -((double)Q + (double)v[0]) * kLn2;
+    // P(y|x) = alpha(T-1,U) p_blank(T-1,U): the terminal blank.
+    cp_wait<0>();
+    const int e = c.D - 1, jU = c.U >> 5;
+    const int4* sp = ring + (e % R) * (J * 32);
+    if (lane == (c.U & 31)) {
+        float m = 0.0f;
+        int x = kZeroExp;
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+            if (j == jU) {
+                const int4 ed = sp[j * 32 + lane];
+                xf_mul(am[j], ae[j], __int_as_float(ed.x), ed.y, m, x);
+            }
+        xf_norm(m, x);
+        p.pm[c.b] = m;
+        p.pe[c.b] = x;
+        const double ll2 = (double)x + log2((double)m);
+        p.lossa[c.b] = -ll2 * kLn2d;
+        p.loss[c.b] = (float)(-ll2 * kLn2d);
+    }
+}
+
+// Backward variable: beta(t,u) = beta(t+1,u) p_blank(t,u) + beta(t,u+1) p_label(t,u),
+// started from a virtual node after the terminal blank with beta = 1.
+template <int J>
+__device__ void dp_beta(const Params& p, const Samp& c, int4* ring) {
+    constexpr int R = Ring<J>::R, PF = R - 2;
+    const int lane = threadIdx.x & 31;
+    float vm[J];
+    int ve[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const bool top = lane + 32 * j == c.U;
+        vm[j] = top ? 1.0f : 0.0f;
+        ve[j] = top ? 0 : kZeroExp;
+    }
+    for (int k = 0; k <= PF; ++k) {
+        ring_issue<J>(p, c, ring, c.D - 1 - k, lane);
+        cp_commit();
+    }
+    for (int d = c.D - 1; d >= 0; --d) {
+        ring_issue<J>(p, c, ring, d - PF - 1, lane);
+        cp_commit();
+        cp_wait<PF + 1>();
+        const int4* sd = ring + (d % R) * (J * 32);
+        float sm[J];
+        int se[J];
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            sm[j] = __shfl_sync(0xffffffffu, vm[j], (lane + 1) & 31);
+            se[j] = __shfl_sync(0xffffffffu, ve[j], (lane + 1) & 31);
+        }
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const int4 ed = sd[j * 32 + lane];
+            const float nm = (lane < 31) ? sm[j] : (j + 1 < J ? sm[j + 1] : 0.0f);
+            const int ne = (lane < 31) ? se[j] : (j + 1 < J ? se[j + 1] : kZeroExp);
+            float bm, ym;
+            int be, ye;
+            xf_mul(vm[j], ve[j], __int_as_float(ed.x), ed.y, bm, be);
+            xf_mul(nm, ne, __int_as_float(ed.z), ed.w, ym, ye);
+            xf_add(bm, be, ym, ye, vm[j], ve[j]);
+        }
+        store_diag<J>(c, p.beta, d, vm, ve, lane);
+    }
+    cp_wait<0>();
+    if (lane == 0) p.lossb[c.b] = -((double)ve[0] + log2((double)vm[0])) * kLn2d;
 }
 
 template <int J>
-__device__ __forceinline__ void dp_run(const Params& p, const Samp& c, float* ring, int* xch) {
-    if (threadIdx.x < 32) dp_alpha<J>(p, c, ring, xch);
-    else dp_beta<J>(p, c, ring + p.ring_floats, xch);
+__device__ __forceinline__ void dp_run(const Params& p, const Samp& c, int4* ring) {
+    if (threadIdx.x < 32) dp_alpha<J>(p, c, ring);
+    else dp_beta<J>(p, c, ring + p.ring_int4);
 }
 
 __global__ void __launch_bounds__(64) k_dp(Params p) {
     if (*p.err) return;
-    extern __shared__ float smem[];
-    __shared__ int xch[2];
+    extern __shared__ int4 smem[];
     Samp c;
     c.b = p.order[blockIdx.x];
     c.T = p.Tl[c.b];
     c.U = p.Ul[c.b];
     c.W = c.U + 1;
     c.D = c.T + c.U;
-    c.dm = (c.D - 1) / 2;
     c.off = p.off[c.b];
     const int J = (c.W + 31) >> 5;
-    if (J <= 1) dp_run<1>(p, c, smem, xch);
-    else if (J <= 2) dp_run<2>(p, c, smem, xch);
-    else if (J <= 4) dp_run<4>(p, c, smem, xch);
-    else if (J <= 8) dp_run<8>(p, c, smem, xch);
-    else if (J <= 16) dp_run<16>(p, c, smem, xch);
-    else dp_run<32>(p, c, smem, xch);
+    if (J <= 1) dp_run<1>(p, c, smem);
+    else if (J <= 2) dp_run<2>(p, c, smem);
+    else if (J <= 4) dp_run<4>(p, c, smem);
+    else if (J <= 8) dp_run<8>(p, c, smem);
+    else if (J <= 16) dp_run<16>(p, c, smem);
+    else dp_run<32>(p, c, smem);
+}
+
+// ---------------------------------------------------------------- combine
+// Per row: occupancy c = alpha beta / P and the arc posteriors
+// alpha p_blank beta(t+1,u) / P and alpha p_label beta(t,u+1) / P.
+__device__ __forceinline__ float xf_to_float(float m, int e) {
+    return (m == 0.0f || e < -200) ? 0.0f : ldexpf(m, min(e, 200));
+}
+
+__global__ void __launch_bounds__(256) k_combine(Params p) {
+    if (*p.err) return;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    int b = (r < p.rows) ? find_sample(p.off, p.B, r) : 0;
+    for (; r < p.rows; r += stride) {
+        b = advance_sample(p.off, p.B, b, r);
+        const int T = __ldg(p.Tl + b), U = __ldg(p.Ul + b), W = U + 1;
+        const int64_t o = __ldg(p.off + b);
+        const unsigned rr = (unsigned)(r - o);
+        const int t = (int)(rr / (unsigned)W), u = (int)(rr - (unsigned)t * W);
+        const int64_t i = o + node_index(t, u, T, U);
+        const int2 A = p.alpha[i], Bt = p.beta[i];
+        const int4 Ed = p.edge[i];
+        const float Pm = __ldg(p.pm + b);
+        const int Pe = __ldg(p.pe + b);
+        const float am = __int_as_float(A.x), bm = __int_as_float(Bt.x);
+        const float inv = 1.0f / Pm;
+        float lc = -INFINITY;
+        if (am != 0.0f && bm != 0.0f) lc = (float)(A.y + Bt.y - Pe) + lg2(am * bm * inv);
+        float eb = 0.0f, ey = 0.0f;
+        if (t < T - 1) {
+            const int2 Bn = p.beta[o + node_index(t + 1, u, T, U)];
+            const float pb = __int_as_float(Ed.x), bn = __int_as_float(Bn.x);
+            if (am != 0.0f && pb != 0.0f && bn != 0.0f)
+                eb = xf_to_float(am * pb * bn * inv, A.y + Ed.y + Bn.y - Pe);
+        } else if (u == U && am != 0.0f && bm != 0.0f) {
+            eb = xf_to_float(am * bm * inv, A.y + Bt.y - Pe);
+        }
+        if (u < U) {
+            const int2 Bn = p.beta[o + node_index(t, u + 1, T, U)];
+            const float py = __int_as_float(Ed.z), bn = __int_as_float(Bn.x);
+            if (am != 0.0f && py != 0.0f && bn != 0.0f)
+                ey = xf_to_float(am * py * bn * inv, A.y + Ed.w + Bn.y - Pe);
+        }
+        p.info[r] = make_float4(lc - p.lse2[r], lc, eb, ey);
+    }
 }
 
 // ---------------------------------------------------------------- grad pass
@@ -779,17 +802,21 @@ __global__ void __launch_bounds__(256) k_grad(Params p) {
     const int lane = threadIdx.x & (G - 1);
     const int64_t ng = (int64_t)gridDim.x * (blockDim.x / G);
     const float cl = p.clamp, sc = p.scale;
-    for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G; r < p.rows; r += ng) {
-        const int b = find_sample(p.off, p.B, r);
-        const int y = row_label(p, b, r);
+    int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
+    int b = (r < p.rows) ? find_sample(p.off, p.B, r) : 0;
+    for (; r < p.rows; r += ng) {
+        b = advance_sample(p.off, p.B, b, r);
+        const int U = __ldg(p.Ul + b), W = U + 1;
+        const unsigned rr = (unsigned)(r - __ldg(p.off + b));
+        const int u = (int)(rr % (unsigned)W);
+        const int y = (u < U) ? __ldg(p.targets + (int64_t)b * p.S + u) : -1;
         const float4 in = p.info[r];
-        const float dl = __ldg(p.delta + b);
         const Tin* row = X + r * (int64_t)V;
         Tin* out = Y + r * (int64_t)V;
-        const bool zero = (in.y + dl) < p.skip2;
-        const float w2 = in.x + dl;
-        const float eb = zero ? 0.0f : ex2(in.z + dl);
-        const float ey = zero ? 0.0f : ex2(in.w + dl);
+        const bool zero = in.y < p.skip2;
+        const float w2 = in.x;
+        const float eb = zero ? 0.0f : in.z;
+        const float ey = zero ? 0.0f : in.w;
         if (VEC) {
             constexpr int EPV = E::kPerVec;
             const int nvec = V / EPV;
@@ -826,7 +853,7 @@ __global__ void __launch_bounds__(256) k_finalize(Params p) {
     const int tid = threadIdx.x;
     if (tid == 0) errs = *p.err;
     __syncthreads();
-    const bool ok_in = errs == 0;
+    const bool ok_in = (errs & (ERR_LENGTH | ERR_ROWS | ERR_TARGET)) == 0;
     double s = 0.0;
     if (ok_in) {
         for (int b = tid; b < p.B; b += blockDim.x) {
@@ -842,10 +869,11 @@ __global__ void __launch_bounds__(256) k_finalize(Params p) {
         __syncthreads();
     }
     if (tid == 0) {
-        if (ok_in && p.loss_red) p.loss_red[0] = (float)(p.red == RNNT_RED_MEAN ? part[0] / p.B : part[0]);
+        if (ok_in && p.loss_red)
+            p.loss_red[0] = (float)(p.red == RNNT_RED_MEAN ? part[0] / p.B : part[0]);
         int st = RNNT_OK;
         if (errs & (ERR_LENGTH | ERR_ROWS | ERR_TARGET)) st = RNNT_INVALID_VALUE;
-        else if (errs & ERR_MISMATCH) st = RNNT_LOSS_MISMATCH;
+        else if (errs & (ERR_MISMATCH | ERR_NONFINITE)) st = RNNT_LOSS_MISMATCH;
         *p.err = errs;
         if (p.status) *p.status = st;
     }
@@ -884,38 +912,52 @@ int num_sms(int dev) {
     return g_num_sms[dev];
 }
 
-int ring_floats_for(int S) {
-    const int W = S + 1;
-    const int Jn = (W + 31) / 32;
-    int best = 0;
+// Per-warp DP ring (int4 records) covering every lattice width up to S+1.
+int ring_int4_for(int S) {
+    const int Jn = (S + 1 + 31) / 32;
     const int Js[6] = {1, 2, 4, 8, 16, 32};
-    const int Rs[6] = {32, 32, 16, 8, 6, 4};
+    const int Rs[6] = {32, 32, 24, 12, 7, 4};
+    int best = 0;
     for (int i = 0; i < 6; ++i) {
-        const int need = Rs[i] * ring_slot_floats(Js[i]);
+        const int need = Rs[i] * Js[i] * 32;
         if (need > best) best = need;
         if (Js[i] >= Jn) break;
     }
     return best;
 }
 
+int grid_for(int64_t work_threads, int sms, int per_sm) {
+    const int64_t blocks = (work_threads + 255) / 256;
+    const int64_t cap = (int64_t)sms * per_sm;
+    return (int)(blocks < 1 ? 1 : (blocks < cap ? blocks : cap));
+}
+
 template <typename Tin>
 void launch_rows(const Params& p, cudaStream_t st, int sms) {
     const int V = p.V;
-    const bool vec = ((size_t)V * sizeof(Tin)) % 16 == 0;
-    const int64_t need_threads = p.rows * 32;
-    int64_t blocks = (need_threads + 255) / 256;
-    const int64_t cap = (int64_t)sms * 8;
-    const int grid = (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
     if (!p.fused) {
-        int64_t gb = (p.rows + 255) / 256;
-        const int g2 = (int)(gb < cap ? (gb > 0 ? gb : 1) : cap);
-        k_row_gather<Tin><<<g2, 256, 0, st>>>(p);
+        k_row_gather<Tin><<<grid_for(p.rows, sms, 8), 256, 0, st>>>(p);
         return;
     }
-#define ROWK(G_)                                                                   \
-    do {                                                                           \
-        if (vec) k_row_fused<Tin, G_, true><<<grid, 256, 0, st>>>(p);              \
-        else k_row_fused<Tin, G_, false><<<grid, 256, 0, st>>>(p);                 \
+    constexpr int EPV = Elt<Tin>::kPerVec;
+    const bool vec = ((size_t)V * sizeof(Tin)) % 16 == 0;
+    const int nvec = V / EPV;
+    const int g = grid_for(p.rows * 32, sms, 8);
+    if (vec && nvec <= 32 * 8) {
+        // Whole row in registers.
+        if (nvec <= 4) k_row_regs<Tin, 4, 1><<<grid_for(p.rows * 4, sms, 8), 256, 0, st>>>(p);
+        else if (nvec <= 16) k_row_regs<Tin, 8, 2><<<grid_for(p.rows * 8, sms, 8), 256, 0, st>>>(p);
+        else if (nvec <= 32) k_row_regs<Tin, 16, 2><<<grid_for(p.rows * 16, sms, 8), 256, 0, st>>>(p);
+        else if (nvec <= 64) k_row_regs<Tin, 32, 2><<<g, 256, 0, st>>>(p);
+        else if (nvec <= 128) k_row_regs<Tin, 32, 4><<<g, 256, 0, st>>>(p);
+        else k_row_regs<Tin, 32, 8><<<g, 256, 0, st>>>(p);
+        return;
+    }
+#define ROWK(G_)                                                                          \
+    do {                                                                                  \
+        const int gg = grid_for(p.rows * G_, sms, 8);                                     \
+        if (vec) k_row_stream<Tin, G_, true><<<gg, 256, 0, st>>>(p);                      \
+        else k_row_stream<Tin, G_, false><<<gg, 256, 0, st>>>(p);                         \
     } while (0)
     if (V >= 512) ROWK(32);
     else if (V >= 128) ROWK(16);
@@ -928,17 +970,15 @@ template <typename Tin>
 void launch_grad(const Params& p, cudaStream_t st, int sms) {
     const int V = p.V;
     const bool vec = ((size_t)V * sizeof(Tin)) % 16 == 0;
-    const int64_t cap = (int64_t)sms * 8;
-    const int64_t blocks = (p.rows * 32 + 255) / 256;
-    const int grid = (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
 #define GRADK(G_)                                                                          \
     do {                                                                                   \
+        const int gg = grid_for(p.rows * G_, sms, 8);                                      \
         if (p.fused) {                                                                     \
-            if (vec) k_grad<Tin, G_, true, true><<<grid, 256, 0, st>>>(p);                 \
-            else k_grad<Tin, G_, false, true><<<grid, 256, 0, st>>>(p);                    \
+            if (vec) k_grad<Tin, G_, true, true><<<gg, 256, 0, st>>>(p);                   \
+            else k_grad<Tin, G_, false, true><<<gg, 256, 0, st>>>(p);                      \
         } else {                                                                           \
-            if (vec) k_grad<Tin, G_, true, false><<<grid, 256, 0, st>>>(p);                \
-            else k_grad<Tin, G_, false, false><<<grid, 256, 0, st>>>(p);                   \
+            if (vec) k_grad<Tin, G_, true, false><<<gg, 256, 0, st>>>(p);                  \
+            else k_grad<Tin, G_, false, false><<<gg, 256, 0, st>>>(p);                     \
         }                                                                                  \
     } while (0)
     if (V >= 512) GRADK(32);
@@ -1007,13 +1047,12 @@ extern "C" rnnt_status_t rnnt_loss_fused_staged(
     p.clamp = clamp > 0.0f ? clamp : INFINITY;
     p.scale = reduction == RNNT_RED_MEAN ? 1.0f / (float)B : 1.0f;
     // A row whose occupancy is below 2^skip2 has every |grad| below half the
-    // smallest subnormal of the output type, so it rounds to zero.
+    // smallest subnormal of the output type, so every element rounds to zero.
     const float zero_at = dt == RNNT_F16 ? -25.5f : -151.0f;
     p.skip2 = zero_at - log2f(p.scale);
     p.fused = fused_log_softmax ? 1 : 0;
     p.red = reduction;
-    p.want_grad = grad != nullptr;
-    p.ring_floats = ring_floats_for(targets_stride);
+    p.ring_int4 = ring_int4_for(targets_stride);
     p.loss = loss;
     p.loss_red = loss_reduced;
     p.status = status_dev;
@@ -1022,17 +1061,15 @@ extern "C" rnnt_status_t rnnt_loss_fused_staged(
     p.order = reinterpret_cast<int32_t*>(w + L.order);
     p.lossa = reinterpret_cast<double*>(w + L.lossa);
     p.lossb = reinterpret_cast<double*>(w + L.lossb);
-    p.delta = reinterpret_cast<float*>(w + L.delta);
+    p.pm = reinterpret_cast<float*>(w + L.pm);
+    p.pe = reinterpret_cast<int32_t*>(w + L.pe);
     p.lse2 = reinterpret_cast<float*>(w + L.lse2);
-    p.lpb = reinterpret_cast<float*>(w + L.lpb);
-    p.lpy = reinterpret_cast<float*>(w + L.lpy);
-    p.va = reinterpret_cast<float*>(w + L.va);
-    p.vb = reinterpret_cast<float*>(w + L.vb);
-    p.oa = reinterpret_cast<int32_t*>(w + L.oa);
-    p.qb = reinterpret_cast<int32_t*>(w + L.qb);
+    p.edge = reinterpret_cast<int4*>(w + L.edge);
+    p.alpha = reinterpret_cast<int2*>(w + L.alpha);
+    p.beta = reinterpret_cast<int2*>(w + L.beta);
     p.info = reinterpret_cast<float4*>(w + L.info);
 
-    const size_t dp_smem = (size_t)p.ring_floats * 2 * sizeof(float);
+    const size_t dp_smem = (size_t)p.ring_int4 * 2 * sizeof(int4);
     if (dev >= 0 && dev < 64 && g_dp_smem_set[dev] < (int)dp_smem) {
         if (cudaFuncSetAttribute(k_dp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dp_smem) !=
             cudaSuccess)
@@ -1051,6 +1088,7 @@ extern "C" rnnt_status_t rnnt_loss_fused_staged(
     else launch_rows<__half>(p, st, sms);
     mark(2);
     k_dp<<<B, 64, dp_smem, st>>>(p);
+    if (grad) k_combine<<<grid_for(rows, sms, 8), 256, 0, st>>>(p);
     mark(3);
     if (grad) {
         if (dt == RNNT_F32) launch_grad<float>(p, st, sms);
@@ -1086,9 +1124,7 @@ extern "C" rnnt_status_t rnnt_grad_scale(void* grad, rnnt_dtype_t dt, int64_t ro
     if (workspace_bytes < L.total) return RNNT_WORKSPACE_TOO_SMALL;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return RNNT_LAUNCH_FAILED;
-    const int64_t cap = (int64_t)num_sms(dev) * 8;
-    const int64_t blocks = (rows * 32 + 255) / 256;
-    const int grid = (int)(blocks < cap ? blocks : cap);
+    const int grid = grid_for(rows * 32, num_sms(dev), 8);
     const int64_t* off = reinterpret_cast<const int64_t*>(static_cast<const char*>(workspace) + L.off);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (dt == RNNT_F32) k_scale<float><<<grid, 256, 0, st>>>(grad, rows, V, B, off, factors, per_sample);
@@ -1102,7 +1138,7 @@ extern "C" const char* rnnt_status_string(rnnt_status_t s) {
         case RNNT_INVALID_VALUE: return "invalid value (arguments, lengths or targets)";
         case RNNT_WORKSPACE_TOO_SMALL: return "workspace too small";
         case RNNT_LAUNCH_FAILED: return "kernel launch failed";
-        case RNNT_LOSS_MISMATCH: return "alpha/beta loss mismatch or non-finite loss";
+        case RNNT_LOSS_MISMATCH: return "alpha/beta loss mismatch or non-finite input";
         case RNNT_TIMEOUT: return "device wait timed out";
     }
     return "unknown status";

@@ -92,6 +92,8 @@ def targets(cfg: Config, U: np.ndarray) -> np.ndarray:
     rng = np.random.default_rng(cfg.seed + 7919)
     blank = cfg.blank + cfg.V if cfg.blank < 0 else cfg.blank
     S = max(1, int(U.max()))
+    if cfg.V == 1:                      # blank is the only class: no labels exist
+        return np.zeros((cfg.B, S), dtype=np.int32)
     y = rng.integers(0, cfg.V - 1, size=(cfg.B, S))
     y = np.where(y >= blank, y + 1, y)
     for b in range(cfg.B):

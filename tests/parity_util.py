@@ -45,7 +45,8 @@ def assert_loss_close(got, want, dtype):
     tol = TOL[dtype]["loss_rel"]
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
-    err = np.abs(got - want) / np.maximum(np.abs(want), 1e-30)
+    # Relative error; below a loss of 1 nat the bound applies as an absolute one.
+    err = np.abs(got - want) / np.maximum(np.abs(want), 1.0)
     assert np.all(err <= tol), f"loss rel err {err.max():.3e} > {tol}"
 
 
