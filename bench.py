@@ -35,7 +35,7 @@ if ROOT not in sys.path:
 METRIC = "RNN-T loss+grad logit elements/s (fwd+bwd, 1 GB300); % of HBM roofline"
 UNIT = "logit elements/s"
 FALLBACK_HBM_GBS = 6800.0
-STAGES = ("prepare", "row_pass", "alpha_beta_dp", "grad_pass", "finalize")
+STAGES = ("prepare", "row_pass", "alpha_beta_dp", "combine", "grad_pass", "finalize")
 KERNEL_FILE = os.path.join(ROOT, "rnnt_loss_gb300", "csrc", "rnnt_gb300.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 
@@ -229,7 +229,7 @@ def run_gpu(args, rank, world, local_rank):
     red_code = N.REDUCTIONS[cfg.reduction]
 
     def make_events():
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
         for e in ev:
             e.record(stream)
         return ev
@@ -269,7 +269,7 @@ def run_gpu(args, rank, world, local_rank):
         dist.barrier()
     clk = clocks.stop()
 
-    step_ms = [ev[0].elapsed_time(ev[5]) for ev in evs]
+    step_ms = [ev[0].elapsed_time(ev[6]) for ev in evs]
     stage_ms = {s: statistics.mean(ev[i].elapsed_time(ev[i + 1]) for ev in evs)
                 for i, s in enumerate(STAGES)}
     ms = statistics.mean(step_ms)
@@ -352,7 +352,7 @@ def run_gpu(args, rank, world, local_rank):
         "stages_ms": stage_ms,
         "e2e": {"value": world * wl.elements / (e2e_t / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_t},
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": 6 * args.steps,
         "clocks": clk,
         "wall_ms_timed_region": wall * 1e3,
         "kernel_source_sha256_16": kernel_source_hash(),

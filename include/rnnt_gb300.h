@@ -125,11 +125,12 @@ rnnt_status_t rnnt_loss_fused(const void *logits, rnnt_dtype_t dt, int64_t rows,
 
 /*
  * rnnt_loss_fused_staged -- rnnt_loss_fused with stage timing (tracing aid).
- * Same arguments, plus stage_events: NULL, or an array of 6 cudaEvent_t
+ * Same arguments, plus stage_events: NULL, or an array of 7 cudaEvent_t
  * handles (entries may be NULL) that the call records on `stream` at its
  * stage boundaries: [0] start, [1] after offsets/schedule, [2] after the
- * row pass, [3] after the alpha/beta DP, [4] after the gradient pass,
- * [5] after the loss check/reduction.  The caller creates and owns the events.
+ * row pass, [3] after the alpha/beta DP, [4] after the per-row gradient
+ * coefficients, [5] after the gradient pass, [6] after the loss
+ * check/reduction.  The caller creates and owns the events.
  */
 rnnt_status_t rnnt_loss_fused_staged(const void *logits, rnnt_dtype_t dt, int64_t rows, int32_t V,
                                      const int32_t *targets, int32_t targets_stride,

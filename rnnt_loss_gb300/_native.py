@@ -89,8 +89,8 @@ def rnnt_loss_fused_staged(logits, dt, rows, V, targets, targets_stride, logit_l
                            target_lengths, B, blank, clamp, fused_log_softmax, reduction, loss,
                            loss_reduced, grad, workspace, workspace_bytes, status_dev, stream,
                            stage_events) -> int:
-    """rnnt_loss_fused recording 6 caller-owned CUDA events (raw handles) at stage boundaries."""
-    arr = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(e) if e else None for e in stage_events])
+    """rnnt_loss_fused recording 7 caller-owned CUDA events (raw handles) at stage boundaries."""
+    arr = (ctypes.c_void_p * 7)(*[ctypes.c_void_p(e) if e else None for e in stage_events])
     return int(load().rnnt_loss_fused_staged(logits, dt, rows, V, targets, targets_stride,
                                              logit_lengths, target_lengths, B, blank,
                                              float(clamp), int(fused_log_softmax), reduction,

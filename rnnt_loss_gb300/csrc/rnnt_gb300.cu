@@ -240,6 +240,10 @@ template <> struct Elt<float> {
     }
     __device__ static float to_f(float v) { return v; }
     __device__ static float from_f(float v) { return v; }
+    __device__ static float vmax(const uint4& q) {
+        return fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)),
+                     fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
+    }
 };
 template <> struct Elt<__half> {
     static constexpr int kPerVec = 8;
@@ -265,6 +269,15 @@ template <> struct Elt<__half> {
     }
     __device__ static float to_f(__half v) { return __half2float(v); }
     __device__ static __half from_f(float v) { return __float2half_rn(v); }
+    // Exact max of 8 halves (packed compares), widened once.
+    __device__ static float vmax(const uint4& q) {
+        const __half2 a = __hmax2(*reinterpret_cast<const __half2*>(&q.x),
+                                  *reinterpret_cast<const __half2*>(&q.y));
+        const __half2 b = __hmax2(*reinterpret_cast<const __half2*>(&q.z),
+                                  *reinterpret_cast<const __half2*>(&q.w));
+        const float2 f = __half22float2(__hmax2(a, b));
+        return fmaxf(f.x, f.y);
+    }
 };
 
 template <int G>
@@ -362,14 +375,20 @@ __global__ void __launch_bounds__(1024) k_prepare(Params p) {
 }
 
 // ---------------------------------------------------------------- row pass
-// Row epilogue (one lane): log2 of the softmax denominator in row order, and
-// the node's two transition probabilities at its packed index.  A blank from
-// the last frame before every label is out, and a label at u = U, have
+// G-lane groups reduce row statistics; every warp owns batches of 32
+// consecutive rows and, once a batch is reduced, finishes it with one row per
+// lane (sample lookup, label, transition probabilities, stores), so the
+// scalar per-row work costs one warp instruction per 32 rows.
+
+// One row per lane: log2 of the softmax denominator in row order, and the
+// node's two transition probabilities at its packed index.  A blank from the
+// last frame before every label is out, and a label at u = U, have
 // probability 0 (the lattice has no such arc).
 template <typename Tin>
-__device__ __forceinline__ void row_epilogue(const Params& p, const Tin* row, int b, int64_t r,
-                                             float M, float s) {
+__device__ __forceinline__ void row_finish(const Params& p, int64_t r, float M, float s) {
     using E = Elt<Tin>;
+    const Tin* row = static_cast<const Tin*>(p.logits) + r * (int64_t)p.V;
+    const int b = find_sample(p.off, p.B, r);
     const int T = __ldg(p.Tl + b), U = __ldg(p.Ul + b), W = U + 1;
     const int64_t o = __ldg(p.off + b);
     const unsigned rr = (unsigned)(r - o);
@@ -392,142 +411,166 @@ __device__ __forceinline__ void row_epilogue(const Params& p, const Tin* row, in
         make_int4(__float_as_int(bm), be, __float_as_int(ym), ye);
 }
 
-// Row held in registers: NV 16-byte vectors per lane, G lanes per row; the
-// next row's vectors are loaded before the current one is reduced.
+// Group results (same in every lane of group g) for row it*NG+g of the batch
+// are handed to the lane with that index.
+template <int G>
+__device__ __forceinline__ void hand_over(int it, int wl, float M, float s, float& myM,
+                                          float& mys) {
+    constexpr int NG = 32 / G;
+    const float vM = __shfl_sync(0xffffffffu, M, (wl % NG) * G);
+    const float vs = __shfl_sync(0xffffffffu, s, (wl % NG) * G);
+    if (wl / NG == it) {
+        myM = vM;
+        mys = vs;
+    }
+}
+
+// Rows held in registers: NV 16-byte vectors per lane, the next row's
+// vectors loaded before the current one is reduced.
 template <typename Tin, int G, int NV>
 __global__ void __launch_bounds__(256) k_row_regs(Params p) {
     if (*p.err) return;
     using E = Elt<Tin>;
-    constexpr int EPV = E::kPerVec;
+    constexpr int EPV = E::kPerVec, NG = 32 / G;
     const Tin* X = static_cast<const Tin*>(p.logits);
     const int V = p.V, nvec = V / EPV;
-    const int lane = threadIdx.x & (G - 1);
+    const int wl = threadIdx.x & 31, lane = wl & (G - 1), grp = wl / G;
     const unsigned gm = group_mask<G>();
-    const int64_t ng = (int64_t)gridDim.x * (blockDim.x / G);
-    int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
-    if (r >= p.rows) return;
-    int b = find_sample(p.off, p.B, r);
-    uint4 cur[NV];
+    const int64_t nbatch = (p.rows + 31) / 32;
+    const int64_t wstride = (int64_t)gridDim.x * (blockDim.x / 32);
+    for (int64_t bt = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32; bt < nbatch;
+         bt += wstride) {
+        const int64_t r0 = bt * 32;
+        const int nrows = (int)min((int64_t)32, p.rows - r0);
+        float myM = 0.0f, mys = 0.0f;
+        uint4 cur[NV];
+        if (grp < nrows) {
+            const uint4* rv = reinterpret_cast<const uint4*>(X + (r0 + grp) * (int64_t)V);
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
-        const int vi = lane + k * G;
-        if (vi < nvec) cur[k] = __ldg(reinterpret_cast<const uint4*>(X + r * (int64_t)V) + vi);
-    }
-    for (;;) {
-        const int64_t rn = r + ng;
-        uint4 nxt[NV];
-        if (rn < p.rows) {
-#pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                const int vi = lane + k * G;
-                if (vi < nvec)
-                    nxt[k] = __ldg(reinterpret_cast<const uint4*>(X + rn * (int64_t)V) + vi);
-            }
+            for (int k = 0; k < NV; ++k)
+                if (lane + k * G < nvec) cur[k] = __ldg(rv + lane + k * G);
         }
-        float M = -INFINITY;
+        for (int it = 0; it < G; ++it) {
+            const int ri = it * NG + grp;
+            uint4 nxt[NV];
+            if (ri + NG < nrows) {
+                const uint4* rv = reinterpret_cast<const uint4*>(X + (r0 + ri + NG) * (int64_t)V);
 #pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            if (lane + k * G < nvec) {
-                float x[EPV];
-                E::unpack(cur[k], x);
-#pragma unroll
-                for (int e = 0; e < EPV; ++e) M = fmaxf(M, x[e]);
+                for (int k = 0; k < NV; ++k)
+                    if (lane + k * G < nvec) nxt[k] = __ldg(rv + lane + k * G);
             }
-        }
-        M = group_max<G>(M, gm);
-        float s = 0.0f;
-        if (M != -INFINITY) {
-            const float ML = M * kLog2e;
+            float M = -INFINITY, s = 0.0f;
+            if (ri < nrows) {
 #pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                if (lane + k * G < nvec) {
-                    float x[EPV];
-                    E::unpack(cur[k], x);
+                for (int k = 0; k < NV; ++k)
+                    if (lane + k * G < nvec) M = fmaxf(M, E::vmax(cur[k]));
+                M = group_max<G>(M, gm);
+                if (M != -INFINITY) {
+                    const float ML = M * kLog2e;
 #pragma unroll
-                    for (int e = 0; e < EPV; ++e) s += ex2(fmaf(x[e], kLog2e, -ML));
+                    for (int k = 0; k < NV; ++k) {
+                        if (lane + k * G < nvec) {
+                            float x[EPV];
+                            E::unpack(cur[k], x);
+#pragma unroll
+                            for (int e = 0; e < EPV; ++e) s += ex2(fmaf(x[e], kLog2e, -ML));
+                        }
+                    }
                 }
+                s = group_sum<G>(s, gm);
             }
-        }
-        s = group_sum<G>(s, gm);
-        if (lane == 0) row_epilogue<Tin>(p, X + r * (int64_t)V, b, r, M, s);
-        if (rn >= p.rows) break;
-        r = rn;
-        b = advance_sample(p.off, p.B, b, r);
+            hand_over<G>(it, wl, M, s, myM, mys);
 #pragma unroll
-        for (int k = 0; k < NV; ++k) cur[k] = nxt[k];
+            for (int k = 0; k < NV; ++k) cur[k] = nxt[k];
+        }
+        if (wl < nrows) row_finish<Tin>(p, r0 + wl, myM, mys);
     }
 }
 
 // Long rows (or rows not 16-byte aligned): streaming max/sum with rescale.
 template <typename Tin, int G, bool VEC>
-__global__ void __launch_bounds__(256) k_row_stream(Params p) {
-    if (*p.err) return;
+__device__ __forceinline__ void row_stats_stream(const Tin* row, int V, int lane, unsigned gm,
+                                                 float& Mo, float& so) {
     using E = Elt<Tin>;
-    const Tin* X = static_cast<const Tin*>(p.logits);
-    const int V = p.V;
-    const int lane = threadIdx.x & (G - 1);
-    const unsigned gm = group_mask<G>();
-    const int64_t ng = (int64_t)gridDim.x * (blockDim.x / G);
-    int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
-    int b = (r < p.rows) ? find_sample(p.off, p.B, r) : 0;
-    for (; r < p.rows; r += ng) {
-        b = advance_sample(p.off, p.B, b, r);
-        const Tin* row = X + r * (int64_t)V;
-        float m = -INFINITY, s = 0.0f;
-        if (VEC) {
-            constexpr int EPV = E::kPerVec, UNR = 4;
-            const uint4* rv = reinterpret_cast<const uint4*>(row);
-            const int nvec = V / EPV;
-            for (int v0 = lane; v0 < nvec; v0 += G * UNR) {
-                float x[UNR * EPV];
+    float m = -INFINITY, s = 0.0f;
+    if (VEC) {
+        constexpr int EPV = E::kPerVec, UNR = 4;
+        const uint4* rv = reinterpret_cast<const uint4*>(row);
+        const int nvec = V / EPV;
+        for (int v0 = lane; v0 < nvec; v0 += G * UNR) {
+            float x[UNR * EPV];
 #pragma unroll
-                for (int k = 0; k < UNR; ++k) {
-                    const int vi = v0 + k * G;
-                    if (vi < nvec) {
-                        E::unpack(__ldg(rv + vi), x + k * EPV);
-                    } else {
+            for (int k = 0; k < UNR; ++k) {
+                const int vi = v0 + k * G;
+                if (vi < nvec) {
+                    E::unpack(__ldg(rv + vi), x + k * EPV);
+                } else {
 #pragma unroll
-                        for (int e = 0; e < EPV; ++e) x[k * EPV + e] = -INFINITY;
-                    }
-                }
-                float cm = x[0];
-#pragma unroll
-                for (int e = 1; e < UNR * EPV; ++e) cm = fmaxf(cm, x[e]);
-                const float nm = fmaxf(m, cm);
-                if (nm != -INFINITY) {
-                    if (nm != m) s *= ex2((m - nm) * kLog2e);
-                    const float nmL = nm * kLog2e;
-#pragma unroll
-                    for (int e = 0; e < UNR * EPV; ++e) s += ex2(fmaf(x[e], kLog2e, -nmL));
-                    m = nm;
+                    for (int e = 0; e < EPV; ++e) x[k * EPV + e] = -INFINITY;
                 }
             }
-        } else {
-            constexpr int UNR = 8;
-            for (int k0 = lane; k0 < V; k0 += G * UNR) {
-                float x[UNR];
+            float cm = x[0];
 #pragma unroll
-                for (int k = 0; k < UNR; ++k) {
-                    const int kk = k0 + k * G;
-                    x[k] = (kk < V) ? E::get(row, kk) : -INFINITY;
-                }
-                float cm = x[0];
+            for (int e = 1; e < UNR * EPV; ++e) cm = fmaxf(cm, x[e]);
+            const float nm = fmaxf(m, cm);
+            if (nm != -INFINITY) {
+                if (nm != m) s *= ex2((m - nm) * kLog2e);
+                const float nmL = nm * kLog2e;
 #pragma unroll
-                for (int e = 1; e < UNR; ++e) cm = fmaxf(cm, x[e]);
-                const float nm = fmaxf(m, cm);
-                if (nm != -INFINITY) {
-                    if (nm != m) s *= ex2((m - nm) * kLog2e);
-                    const float nmL = nm * kLog2e;
-#pragma unroll
-                    for (int e = 0; e < UNR; ++e) s += ex2(fmaf(x[e], kLog2e, -nmL));
-                    m = nm;
-                }
+                for (int e = 0; e < UNR * EPV; ++e) s += ex2(fmaf(x[e], kLog2e, -nmL));
+                m = nm;
             }
         }
-        const float M = group_max<G>(m, gm);
-        s = (M == -INFINITY) ? 0.0f : s * ex2((m - M) * kLog2e);
-        s = group_sum<G>(s, gm);
-        if (lane == 0) row_epilogue<Tin>(p, row, b, r, M, s);
+    } else {
+        constexpr int UNR = 8;
+        for (int k0 = lane; k0 < V; k0 += G * UNR) {
+            float x[UNR];
+#pragma unroll
+            for (int k = 0; k < UNR; ++k) {
+                const int kk = k0 + k * G;
+                x[k] = (kk < V) ? E::get(row, kk) : -INFINITY;
+            }
+            float cm = x[0];
+#pragma unroll
+            for (int e = 1; e < UNR; ++e) cm = fmaxf(cm, x[e]);
+            const float nm = fmaxf(m, cm);
+            if (nm != -INFINITY) {
+                if (nm != m) s *= ex2((m - nm) * kLog2e);
+                const float nmL = nm * kLog2e;
+#pragma unroll
+                for (int e = 0; e < UNR; ++e) s += ex2(fmaf(x[e], kLog2e, -nmL));
+                m = nm;
+            }
+        }
+    }
+    const float M = group_max<G>(m, gm);
+    s = (M == -INFINITY) ? 0.0f : s * ex2((m - M) * kLog2e);
+    Mo = M;
+    so = group_sum<G>(s, gm);
+}
+
+template <typename Tin, int G, bool VEC>
+__global__ void __launch_bounds__(256) k_row_stream(Params p) {
+    if (*p.err) return;
+    constexpr int NG = 32 / G;
+    const Tin* X = static_cast<const Tin*>(p.logits);
+    const int wl = threadIdx.x & 31, lane = wl & (G - 1), grp = wl / G;
+    const unsigned gm = group_mask<G>();
+    const int64_t nbatch = (p.rows + 31) / 32;
+    const int64_t wstride = (int64_t)gridDim.x * (blockDim.x / 32);
+    for (int64_t bt = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32; bt < nbatch;
+         bt += wstride) {
+        const int64_t r0 = bt * 32;
+        const int nrows = (int)min((int64_t)32, p.rows - r0);
+        float myM = 0.0f, mys = 0.0f;
+        for (int it = 0; it < G; ++it) {
+            const int ri = it * NG + grp;
+            float M = -INFINITY, s = 0.0f;
+            if (ri < nrows)
+                row_stats_stream<Tin, G, VEC>(X + (r0 + ri) * (int64_t)p.V, p.V, lane, gm, M, s);
+            hand_over<G>(it, wl, M, s, myM, mys);
+        }
+        if (wl < nrows) row_finish<Tin>(p, r0 + wl, myM, mys);
     }
 }
 
@@ -535,14 +578,9 @@ __global__ void __launch_bounds__(256) k_row_stream(Params p) {
 template <typename Tin>
 __global__ void __launch_bounds__(256) k_row_gather(Params p) {
     if (*p.err) return;
-    const Tin* X = static_cast<const Tin*>(p.logits);
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    int b = (r < p.rows) ? find_sample(p.off, p.B, r) : 0;
-    for (; r < p.rows; r += stride) {
-        b = advance_sample(p.off, p.B, b, r);
-        row_epilogue<Tin>(p, X + r * (int64_t)p.V, b, r, 0.0f, 1.0f);
-    }
+    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < p.rows; r += stride)
+        row_finish<Tin>(p, r, 0.0f, 1.0f);
 }
 
 // ---------------------------------------------------------------- DP
@@ -570,21 +608,37 @@ struct Samp {
 };
 
 __device__ __forceinline__ bool on_lattice(const Samp& c, int d, int u) {
-    const int t = d - u;
-    return u <= c.U && t >= 0 && t < c.T;
-}
-// Global packed index of the node on diagonal d in column u: base(d) - u.
-__device__ __forceinline__ int64_t diag_base(const Samp& c, int d) {
-    return c.off + diag_start(d, c.T, c.W) - max(0, d - c.U) + d;
+    return u <= c.U && (unsigned)(d - u) < (unsigned)c.T;
 }
 
+// Walks the packed start N(d) of anti-diagonal d one step at a time:
+// N(d+1) = N(d) + (nodes on d), nodes on d = min(T-1, d) - max(0, d-U) + 1.
+struct DiagCursor {
+    int d;
+    int64_t n;
+    __device__ __forceinline__ static int64_t count(const Samp& c, int d) {
+        return (d < 0 || d >= c.D) ? 0 : (int64_t)(min(c.T - 1, d) - max(0, d - c.U) + 1);
+    }
+    __device__ __forceinline__ void init(const Samp& c, int d0) {
+        d = d0;
+        n = (d0 <= 0) ? 0 : diag_start(min(d0, c.D), c.T, c.W);
+    }
+    __device__ __forceinline__ void next(const Samp& c) { n += count(c, d); ++d; }
+    __device__ __forceinline__ void prev(const Samp& c) { --d; n -= count(c, d); }
+    // Global packed index of the node in column u is base() - u.
+    __device__ __forceinline__ int64_t base(const Samp& c) const {
+        return c.off + n - max(0, d - c.U) + d;
+    }
+};
+
 template <int J>
-__device__ __forceinline__ void ring_issue(const Params& p, const Samp& c, int4* ring, int d,
-                                           int lane) {
+__device__ __forceinline__ void ring_issue(const Params& p, const Samp& c, int4* ring,
+                                           const DiagCursor& q, int lane) {
     constexpr int R = Ring<J>::R;
+    const int d = q.d;
     if (d >= 0 && d < c.D) {
         int4* sl = ring + (d % R) * (J * 32);
-        const int64_t base = diag_base(c, d);
+        const int64_t base = q.base(c);
 #pragma unroll
         for (int j = 0; j < J; ++j) {
             const int u = lane + 32 * j;
@@ -595,13 +649,13 @@ __device__ __forceinline__ void ring_issue(const Params& p, const Samp& c, int4*
 }
 
 template <int J>
-__device__ __forceinline__ void store_diag(const Samp& c, int2* out, int d, const float* m,
-                                           const int* e, int lane) {
-    const int64_t base = diag_base(c, d);
+__device__ __forceinline__ void store_diag(const Samp& c, int2* out, const DiagCursor& q,
+                                           const float* m, const int* e, int lane) {
+    const int64_t base = q.base(c);
 #pragma unroll
     for (int j = 0; j < J; ++j) {
         const int u = lane + 32 * j;
-        if (on_lattice(c, d, u)) out[base - u] = make_int2(__float_as_int(m[j]), e[j]);
+        if (on_lattice(c, q.d, u)) out[base - u] = make_int2(__float_as_int(m[j]), e[j]);
     }
 }
 
@@ -618,14 +672,19 @@ __device__ void dp_alpha(const Params& p, const Samp& c, int4* ring) {
         am[j] = origin ? 1.0f : 0.0f;
         ae[j] = origin ? 0 : kZeroExp;
     }
-    store_diag<J>(c, p.alpha, 0, am, ae, lane);
+    DiagCursor qs, qi;   // store cursor (diagonal d), issue cursor (diagonal d + PF)
+    qs.init(c, 0);
+    store_diag<J>(c, p.alpha, qs, am, ae, lane);
+    qi.init(c, 0);
     for (int k = 0; k <= PF; ++k) {
-        ring_issue<J>(p, c, ring, k, lane);
+        ring_issue<J>(p, c, ring, qi, lane);
         cp_commit();
+        qi.next(c);
     }
     for (int d = 1; d < c.D; ++d) {
-        ring_issue<J>(p, c, ring, d + PF, lane);
+        ring_issue<J>(p, c, ring, qi, lane);
         cp_commit();
+        qi.next(c);
         cp_wait<PF + 1>();
         const int4* sp = ring + ((d - 1) % R) * (J * 32);
         float bm[J], ym[J];
@@ -649,7 +708,8 @@ __device__ void dp_alpha(const Params& p, const Samp& c, int4* ring) {
             const int ne = lane ? se[j] : (j ? se[j - 1] : kZeroExp);
             xf_add(bm[j], be[j], nm, ne, am[j], ae[j]);
         }
-        store_diag<J>(c, p.alpha, d, am, ae, lane);
+        qs.next(c);
+        store_diag<J>(c, p.alpha, qs, am, ae, lane);
     }
     // P(y|x) = alpha(T-1,U) p_blank(T-1,U): the terminal blank.
     cp_wait<0>();
@@ -687,13 +747,18 @@ __device__ void dp_beta(const Params& p, const Samp& c, int4* ring) {
         vm[j] = top ? 1.0f : 0.0f;
         ve[j] = top ? 0 : kZeroExp;
     }
+    DiagCursor qs, qi;   // store cursor (diagonal d), issue cursor (diagonal d - PF - 1)
+    qi.init(c, c.D - 1);
     for (int k = 0; k <= PF; ++k) {
-        ring_issue<J>(p, c, ring, c.D - 1 - k, lane);
+        ring_issue<J>(p, c, ring, qi, lane);
         cp_commit();
+        if (qi.d > 0) qi.prev(c); else qi.d = -1;
     }
+    qs.init(c, c.D - 1);
     for (int d = c.D - 1; d >= 0; --d) {
-        ring_issue<J>(p, c, ring, d - PF - 1, lane);
+        ring_issue<J>(p, c, ring, qi, lane);
         cp_commit();
+        if (qi.d > 0) qi.prev(c); else qi.d = -1;
         cp_wait<PF + 1>();
         const int4* sd = ring + (d % R) * (J * 32);
         float sm[J];
@@ -714,7 +779,8 @@ __device__ void dp_beta(const Params& p, const Samp& c, int4* ring) {
             xf_mul(nm, ne, __int_as_float(ed.z), ed.w, ym, ye);
             xf_add(bm, be, ym, ye, vm[j], ve[j]);
         }
-        store_diag<J>(c, p.beta, d, vm, ve, lane);
+        store_diag<J>(c, p.beta, qs, vm, ve, lane);
+        if (d > 0) qs.prev(c);
     }
     cp_wait<0>();
     if (lane == 0) p.lossb[c.b] = -((double)ve[0] + log2((double)vm[0])) * kLn2d;
@@ -747,7 +813,10 @@ __global__ void __launch_bounds__(64) k_dp(Params p) {
 
 // ---------------------------------------------------------------- combine
 // Per row: occupancy c = alpha beta / P and the arc posteriors
-// alpha p_blank beta(t+1,u) / P and alpha p_label beta(t,u+1) / P.
+// alpha p_blank beta(t+1,u) / P and alpha p_label beta(t,u+1) / P, folded with
+// the reduction scale into the gradient pass's per-row record
+//   {log2(c scale) - lse2 (or -inf: a row of exact zeros), post_blank scale,
+//    post_label scale, label id (-1 at u = U)}.
 __device__ __forceinline__ float xf_to_float(float m, int e) {
     return (m == 0.0f || e < -200) ? 0.0f : ldexpf(m, min(e, 200));
 }
@@ -755,6 +824,7 @@ __device__ __forceinline__ float xf_to_float(float m, int e) {
 __global__ void __launch_bounds__(256) k_combine(Params p) {
     if (*p.err) return;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const float lsc = log2f(p.scale);
     int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     int b = (r < p.rows) ? find_sample(p.off, p.B, r) : 0;
     for (; r < p.rows; r += stride) {
@@ -772,13 +842,18 @@ __global__ void __launch_bounds__(256) k_combine(Params p) {
         const float inv = 1.0f / Pm;
         float lc = -INFINITY;
         if (am != 0.0f && bm != 0.0f) lc = (float)(A.y + Bt.y - Pe) + lg2(am * bm * inv);
+        const int y = (u < U) ? __ldg(p.targets + (int64_t)b * p.S + u) : -1;
+        if (!(lc >= p.skip2)) {   // every element of this gradient row rounds to zero
+            p.info[r] = make_float4(-INFINITY, 0.0f, 0.0f, __int_as_float(y));
+            continue;
+        }
         float eb = 0.0f, ey = 0.0f;
         if (t < T - 1) {
             const int2 Bn = p.beta[o + node_index(t + 1, u, T, U)];
             const float pb = __int_as_float(Ed.x), bn = __int_as_float(Bn.x);
             if (am != 0.0f && pb != 0.0f && bn != 0.0f)
                 eb = xf_to_float(am * pb * bn * inv, A.y + Ed.y + Bn.y - Pe);
-        } else if (u == U && am != 0.0f && bm != 0.0f) {
+        } else if (u == U) {
             eb = xf_to_float(am * bm * inv, A.y + Bt.y - Pe);
         }
         if (u < U) {
@@ -787,51 +862,63 @@ __global__ void __launch_bounds__(256) k_combine(Params p) {
             if (am != 0.0f && py != 0.0f && bn != 0.0f)
                 ey = xf_to_float(am * py * bn * inv, A.y + Ed.w + Bn.y - Pe);
         }
-        p.info[r] = make_float4(lc - p.lse2[r], lc, eb, ey);
+        p.info[r] = make_float4(lc + lsc - p.lse2[r], eb * p.scale, ey * p.scale,
+                                __int_as_float(y));
     }
 }
 
 // ---------------------------------------------------------------- grad pass
+// grad_k * scale = 2^(h_k log2 e + log2(c scale) - lse2) - [k=blank] post_blank
+// scale - [k=y] post_label scale, clipped to +-clamp*scale (clip-then-scale).
 template <typename Tin, int G, bool VEC, bool FUSED>
 __global__ void __launch_bounds__(256) k_grad(Params p) {
     if (*p.err) return;
     using E = Elt<Tin>;
+    constexpr int EPV = E::kPerVec;
     const Tin* X = static_cast<const Tin*>(p.logits);
     Tin* Y = static_cast<Tin*>(p.grad);
     const int V = p.V;
     const int lane = threadIdx.x & (G - 1);
     const int64_t ng = (int64_t)gridDim.x * (blockDim.x / G);
-    const float cl = p.clamp, sc = p.scale;
-    int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
-    int b = (r < p.rows) ? find_sample(p.off, p.B, r) : 0;
-    for (; r < p.rows; r += ng) {
-        b = advance_sample(p.off, p.B, b, r);
-        const int U = __ldg(p.Ul + b), W = U + 1;
-        const unsigned rr = (unsigned)(r - __ldg(p.off + b));
-        const int u = (int)(rr % (unsigned)W);
-        const int y = (u < U) ? __ldg(p.targets + (int64_t)b * p.S + u) : -1;
+    const float cl = p.clamp * p.scale;
+    const bool clip = p.clamp < INFINITY;
+    const int vb = p.blank / EPV, eb_i = p.blank % EPV;
+    for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G; r < p.rows; r += ng) {
         const float4 in = p.info[r];
+        const bool zero = in.x == -INFINITY;
+        const float w2 = in.x, eb = in.y, ey = in.z;
+        const int y = __float_as_int(in.w);
         const Tin* row = X + r * (int64_t)V;
         Tin* out = Y + r * (int64_t)V;
-        const bool zero = in.y < p.skip2;
-        const float w2 = in.x;
-        const float eb = zero ? 0.0f : in.z;
-        const float ey = zero ? 0.0f : in.w;
         if (VEC) {
-            constexpr int EPV = E::kPerVec;
             const int nvec = V / EPV;
+            const int vy = y >= 0 ? y / EPV : -1, ey_i = y >= 0 ? y % EPV : 0;
             const uint4* rv = reinterpret_cast<const uint4*>(row);
             uint4* ov = reinterpret_cast<uint4*>(out);
             for (int vi = lane; vi < nvec; vi += G) {
-                float x[EPV], g[EPV];
-                if (FUSED && !zero) E::unpack(__ldcs(rv + vi), x);
+                float g[EPV];
+                if (FUSED && !zero) {
+                    float x[EPV];
+                    E::unpack(__ldcs(rv + vi), x);
 #pragma unroll
-                for (int e = 0; e < EPV; ++e) {
-                    const int k = vi * EPV + e;
-                    float gv = (FUSED && !zero) ? ex2(fmaf(x[e], kLog2e, w2)) : 0.0f;
-                    if (k == p.blank) gv -= eb;
-                    if (k == y) gv -= ey;
-                    g[e] = fminf(fmaxf(gv, -cl), cl) * sc;
+                    for (int e = 0; e < EPV; ++e) g[e] = ex2(fmaf(x[e], kLog2e, w2));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) g[e] = 0.0f;
+                }
+                if (vi == vb) {
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e)
+                        if (e == eb_i) g[e] -= eb;
+                }
+                if (vi == vy) {
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e)
+                        if (e == ey_i) g[e] -= ey;
+                }
+                if (clip) {
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) g[e] = fminf(fmaxf(g[e], -cl), cl);
                 }
                 __stcs(ov + vi, E::pack(g));
             }
@@ -840,7 +927,8 @@ __global__ void __launch_bounds__(256) k_grad(Params p) {
                 float gv = (FUSED && !zero) ? ex2(fmaf(E::to_f(row[k]), kLog2e, w2)) : 0.0f;
                 if (k == p.blank) gv -= eb;
                 if (k == y) gv -= ey;
-                out[k] = E::from_f(fminf(fmaxf(gv, -cl), cl) * sc);
+                if (clip) gv = fminf(fmaxf(gv, -cl), cl);
+                out[k] = E::from_f(gv);
             }
         }
     }
@@ -932,32 +1020,55 @@ int grid_for(int64_t work_threads, int sms, int per_sm) {
     return (int)(blocks < 1 ? 1 : (blocks < cap ? blocks : cap));
 }
 
+// Resident 256-thread blocks per SM of a kernel (cached per kernel).
+int occupancy(const void* kernel) {
+    static const void* keys[128];
+    static int vals[128];
+    for (int i = 0; i < 128 && keys[i]; ++i)
+        if (keys[i] == kernel) return vals[i];
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 256, 0) != cudaSuccess || n < 1)
+        n = 1;
+    for (int i = 0; i < 128; ++i)
+        if (!keys[i]) {
+            vals[i] = n;
+            keys[i] = kernel;
+            break;
+        }
+    return n;
+}
+
+// Grid-stride launch: never more blocks than are resident at once.
+template <typename K>
+void launch_gs(K kernel, int64_t work_threads, int sms, cudaStream_t st, const Params& p) {
+    const int g = grid_for(work_threads, sms, occupancy(reinterpret_cast<const void*>(kernel)));
+    kernel<<<g, 256, 0, st>>>(p);
+}
+
 template <typename Tin>
 void launch_rows(const Params& p, cudaStream_t st, int sms) {
     const int V = p.V;
     if (!p.fused) {
-        k_row_gather<Tin><<<grid_for(p.rows, sms, 8), 256, 0, st>>>(p);
+        launch_gs(k_row_gather<Tin>, p.rows, sms, st, p);
         return;
     }
     constexpr int EPV = Elt<Tin>::kPerVec;
     const bool vec = ((size_t)V * sizeof(Tin)) % 16 == 0;
     const int nvec = V / EPV;
-    const int g = grid_for(p.rows * 32, sms, 8);
+    const int64_t wt = (p.rows + 31) / 32 * 32;   // one warp per 32-row batch
     if (vec && nvec <= 32 * 8) {
-        // Whole row in registers.
-        if (nvec <= 4) k_row_regs<Tin, 4, 1><<<grid_for(p.rows * 4, sms, 8), 256, 0, st>>>(p);
-        else if (nvec <= 16) k_row_regs<Tin, 8, 2><<<grid_for(p.rows * 8, sms, 8), 256, 0, st>>>(p);
-        else if (nvec <= 32) k_row_regs<Tin, 16, 2><<<grid_for(p.rows * 16, sms, 8), 256, 0, st>>>(p);
-        else if (nvec <= 64) k_row_regs<Tin, 32, 2><<<g, 256, 0, st>>>(p);
-        else if (nvec <= 128) k_row_regs<Tin, 32, 4><<<g, 256, 0, st>>>(p);
-        else k_row_regs<Tin, 32, 8><<<g, 256, 0, st>>>(p);
+        if (nvec <= 4) launch_gs(k_row_regs<Tin, 4, 1>, wt, sms, st, p);
+        else if (nvec <= 16) launch_gs(k_row_regs<Tin, 8, 2>, wt, sms, st, p);
+        else if (nvec <= 32) launch_gs(k_row_regs<Tin, 16, 2>, wt, sms, st, p);
+        else if (nvec <= 64) launch_gs(k_row_regs<Tin, 32, 2>, wt, sms, st, p);
+        else if (nvec <= 128) launch_gs(k_row_regs<Tin, 32, 4>, wt, sms, st, p);
+        else launch_gs(k_row_regs<Tin, 32, 8>, wt, sms, st, p);
         return;
     }
-#define ROWK(G_)                                                                          \
-    do {                                                                                  \
-        const int gg = grid_for(p.rows * G_, sms, 8);                                     \
-        if (vec) k_row_stream<Tin, G_, true><<<gg, 256, 0, st>>>(p);                      \
-        else k_row_stream<Tin, G_, false><<<gg, 256, 0, st>>>(p);                         \
+#define ROWK(G_)                                                                 \
+    do {                                                                         \
+        if (vec) launch_gs(k_row_stream<Tin, G_, true>, wt, sms, st, p);         \
+        else launch_gs(k_row_stream<Tin, G_, false>, wt, sms, st, p);            \
     } while (0)
     if (V >= 512) ROWK(32);
     else if (V >= 128) ROWK(16);
@@ -970,16 +1081,16 @@ template <typename Tin>
 void launch_grad(const Params& p, cudaStream_t st, int sms) {
     const int V = p.V;
     const bool vec = ((size_t)V * sizeof(Tin)) % 16 == 0;
-#define GRADK(G_)                                                                          \
-    do {                                                                                   \
-        const int gg = grid_for(p.rows * G_, sms, 8);                                      \
-        if (p.fused) {                                                                     \
-            if (vec) k_grad<Tin, G_, true, true><<<gg, 256, 0, st>>>(p);                   \
-            else k_grad<Tin, G_, false, true><<<gg, 256, 0, st>>>(p);                      \
-        } else {                                                                           \
-            if (vec) k_grad<Tin, G_, true, false><<<gg, 256, 0, st>>>(p);                  \
-            else k_grad<Tin, G_, false, false><<<gg, 256, 0, st>>>(p);                     \
-        }                                                                                  \
+#define GRADK(G_)                                                                      \
+    do {                                                                               \
+        const int64_t wt = p.rows * G_;                                                \
+        if (p.fused) {                                                                 \
+            if (vec) launch_gs(k_grad<Tin, G_, true, true>, wt, sms, st, p);           \
+            else launch_gs(k_grad<Tin, G_, false, true>, wt, sms, st, p);              \
+        } else {                                                                       \
+            if (vec) launch_gs(k_grad<Tin, G_, true, false>, wt, sms, st, p);          \
+            else launch_gs(k_grad<Tin, G_, false, false>, wt, sms, st, p);             \
+        }                                                                              \
     } while (0)
     if (V >= 512) GRADK(32);
     else if (V >= 128) GRADK(16);
@@ -1088,15 +1199,16 @@ extern "C" rnnt_status_t rnnt_loss_fused_staged(
     else launch_rows<__half>(p, st, sms);
     mark(2);
     k_dp<<<B, 64, dp_smem, st>>>(p);
-    if (grad) k_combine<<<grid_for(rows, sms, 8), 256, 0, st>>>(p);
     mark(3);
+    if (grad) launch_gs(k_combine, rows, sms, st, p);
+    mark(4);
     if (grad) {
         if (dt == RNNT_F32) launch_grad<float>(p, st, sms);
         else launch_grad<__half>(p, st, sms);
     }
-    mark(4);
-    k_finalize<<<1, 256, 0, st>>>(p);
     mark(5);
+    k_finalize<<<1, 256, 0, st>>>(p);
+    mark(6);
     return cudaGetLastError() == cudaSuccess ? RNNT_OK : RNNT_LAUNCH_FAILED;
 }
 
@@ -1124,7 +1236,7 @@ extern "C" rnnt_status_t rnnt_grad_scale(void* grad, rnnt_dtype_t dt, int64_t ro
     if (workspace_bytes < L.total) return RNNT_WORKSPACE_TOO_SMALL;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return RNNT_LAUNCH_FAILED;
-    const int grid = grid_for(rows * 32, num_sms(dev), 8);
+    const int grid = grid_for(rows * 32, num_sms(dev), 4);
     const int64_t* off = reinterpret_cast<const int64_t*>(static_cast<const char*>(workspace) + L.off);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (dt == RNNT_F32) k_scale<float><<<grid, 256, 0, st>>>(grad, rows, V, B, off, factors, per_sample);
