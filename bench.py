@@ -211,6 +211,8 @@ def run_gpu(args, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
 
     wl = W.make(args.workload, dev)
+    if args.samples:
+        wl = W.subset(wl, args.samples)
     cfg = wl.cfg
     rows, V = wl.rows, cfg.V
     dt = _DT[wl.logits.dtype]
@@ -242,6 +244,18 @@ def run_gpu(args, rank, world, local_rank):
             status.data_ptr(), stream.cuda_stream, [e.cuda_event for e in ev])
         if rc != N.RNNT_OK:
             raise N.RNNTError(rc, "rnnt_loss_fused_staged")
+
+    if args.profile_steps:
+        # Profiling mode (for ncu): run the path a fixed number of times, report nothing.
+        ev = make_events()
+        for _ in range(args.profile_steps):
+            step(ev)
+        torch.cuda.synchronize()
+        if int(status.item()) != N.RNNT_OK:
+            raise N.RNNTError(int(status.item()), "profile run")
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     warm_ev = make_events()
     for _ in range(max(3, args.warmup)):
@@ -377,6 +391,10 @@ def main(argv=None):
     ap.add_argument("--ref-samples", type=int, default=0,
                     help="samples per reference step (default: host core count)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--samples", type=int, default=0,
+                    help="keep only the first N samples of the workload (profiling)")
+    ap.add_argument("--profile-steps", type=int, default=0,
+                    help="run the path N times and exit without timing (for ncu)")
     args = ap.parse_args(argv)
     rank, world, local_rank = dist_info()
     if args.impl == "reference":

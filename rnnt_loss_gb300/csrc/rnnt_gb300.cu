@@ -55,6 +55,7 @@ enum : int {
     ERR_TARGET = 4,
     ERR_MISMATCH = 8,
     ERR_NONFINITE = 16,
+    ERR_TIMEOUT = 32,
 };
 
 // ---------------------------------------------------------------- workspace
@@ -102,6 +103,7 @@ struct Params {
     int fused;
     int red;
     int ring_int4;    // per-warp DP ring size (int4 records)
+    int stage_bytes;  // per-stage shared-memory row buffer of the TMA-staged passes
     float* loss;
     float* loss_red;
     int32_t* status;
@@ -303,6 +305,76 @@ __device__ __forceinline__ float group_sum(float v, unsigned gm) {
     return v;
 }
 
+// ------------------------------------------------ TMA bulk copies + mbarriers
+// Each warp of the streaming passes owns kStages shared-memory row buffers,
+// each with an mbarrier; lane 0 issues one 1-D bulk copy (cp.async.bulk) per
+// row, the warp waits on the barrier's phase parity.  Every wait is bounded.
+constexpr int kStages = 4;
+constexpr int kWaitSpins = 1 << 22;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
+    return (uint32_t)__cvta_generic_to_shared(ptr);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void tma_row_load(void* dst, const void* src, uint32_t bytes,
+                                             uint64_t* bar) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred q;\n mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n"
+        " selp.b32 %0, 1, 0, q;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the copy of phase `parity`; false (error flag raised) on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
+    for (int i = 0; i < kWaitSpins; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    atomicOr(err, ERR_TIMEOUT);
+    return false;
+}
+
+// Rows of one warp's grid-stride sequence of 32-row batches: position k is
+// row (b0 + (k/32)*wstride)*32 + k%32; positions [0, count) are valid rows.
+struct WarpRows {
+    int64_t b0, wstride, count;
+    __device__ __forceinline__ void init(int64_t rows, int64_t warp, int64_t nwarps) {
+        b0 = warp;
+        wstride = nwarps;
+        const int64_t nbatch = (rows + 31) / 32;
+        if (b0 >= nbatch) {
+            count = 0;
+            return;
+        }
+        const int64_t nb = (nbatch - 1 - b0) / wstride + 1;   // batches of this warp
+        const int64_t last = b0 + (nb - 1) * wstride;
+        count = (nb - 1) * 32 + min((int64_t)32, rows - last * 32);
+    }
+    __device__ __forceinline__ int64_t row(int64_t k) const {
+        return (b0 + (k >> 5) * wstride) * 32 + (k & 31);
+    }
+};
+
 // ---------------------------------------------------------------- k_prepare
 __global__ void __launch_bounds__(1024) k_prepare(Params p) {
     __shared__ int64_t wsum[32];
@@ -485,6 +557,81 @@ __global__ void __launch_bounds__(256) k_row_regs(Params p) {
         }
         if (wl < nrows) row_finish<Tin>(p, r0 + wl, myM, mys);
     }
+}
+
+// Rows of up to 32*NV 16-byte vectors staged through shared memory by TMA:
+// a warp streams its row sequence with kStages-1 rows in flight.
+template <typename Tin, int NV>
+__global__ void __launch_bounds__(256) k_row_tma(Params p) {
+    if (*p.err) return;
+    using E = Elt<Tin>;
+    constexpr int EPV = E::kPerVec;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const int nw = blockDim.x >> 5, wid = threadIdx.x >> 5, wl = threadIdx.x & 31;
+    const int sb = p.stage_bytes;
+    unsigned char* buf = smem_raw + (size_t)wid * kStages * sb;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + (size_t)nw * kStages * sb) + wid * kStages;
+    if (wl == 0) {
+#pragma unroll
+        for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const Tin* X = static_cast<const Tin*>(p.logits);
+    const int V = p.V, nvec = V / EPV;
+    const uint32_t rb = (uint32_t)V * sizeof(Tin);
+    WarpRows seq;
+    seq.init(p.rows, (int64_t)blockIdx.x * nw + wid, (int64_t)gridDim.x * nw);
+    if (wl == 0)
+        for (int64_t k = 0; k < min((int64_t)kStages, seq.count); ++k)
+            tma_row_load(buf + (k % kStages) * sb, X + seq.row(k) * (int64_t)V, rb,
+                         &bars[k % kStages]);
+    float myM = 0.0f, mys = 0.0f;
+    int64_t k = 0;
+    for (; k < seq.count; ++k) {
+        const int st = (int)(k % kStages);
+        if (!mbar_wait(&bars[st], (uint32_t)((k / kStages) & 1), p.err)) break;
+        const uint4* rv = reinterpret_cast<const uint4*>(buf + st * sb);
+        uint4 q[NV];
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+            if (wl + 32 * i < nvec) q[i] = rv[wl + 32 * i];
+        __syncwarp();
+        if (wl == 0 && k + kStages < seq.count) {   // refill this stage
+            fence_proxy_async();
+            tma_row_load(buf + st * sb, X + seq.row(k + kStages) * (int64_t)V, rb, &bars[st]);
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+            if (wl + 32 * i < nvec) M = fmaxf(M, E::vmax(q[i]));
+        M = group_max<32>(M, 0xffffffffu);
+        float s = 0.0f;
+        if (M != -INFINITY) {
+            const float ML = M * kLog2e;
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                if (wl + 32 * i < nvec) {
+                    float x[EPV];
+                    E::unpack(q[i], x);
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) s += ex2(fmaf(x[e], kLog2e, -ML));
+                }
+            }
+        }
+        s = group_sum<32>(s, 0xffffffffu);
+        const int it = (int)(k & 31);
+        if (wl == it) {
+            myM = M;
+            mys = s;
+        }
+        if (it == 31 || k == seq.count - 1) {
+            if (wl <= it) row_finish<Tin>(p, seq.row(k - it + wl), myM, mys);
+        }
+    }
+    // After a timeout, wait (bounded) for the copies still in flight before exiting.
+    for (int64_t q = k; q < min(k + kStages, seq.count); ++q)
+        mbar_wait(&bars[q % kStages], (uint32_t)((q / kStages) & 1), p.err);
 }
 
 // Long rows (or rows not 16-byte aligned): streaming max/sum with rescale.
@@ -934,6 +1081,156 @@ __global__ void __launch_bounds__(256) k_grad(Params p) {
     }
 }
 
+// Gradient pass with TMA staging (16-byte aligned rows of <= 32*NV vectors).
+// Each warp walks its 32-row batches; the per-row records of a batch are
+// loaded one per lane (the next batch's one batch ahead), rows of exact zeros
+// are stored without reading the logits, and only the remaining rows are
+// fetched into the warp's stage ring, up to kStages rows ahead.
+template <typename Tin, int NV>
+__global__ void __launch_bounds__(256) k_grad_tma(Params p) {
+    if (*p.err) return;
+    using E = Elt<Tin>;
+    constexpr int EPV = E::kPerVec;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const int nw = blockDim.x >> 5, wid = threadIdx.x >> 5, wl = threadIdx.x & 31;
+    const int sb = p.stage_bytes;
+    unsigned char* buf = smem_raw + (size_t)wid * kStages * sb;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + (size_t)nw * kStages * sb) + wid * kStages;
+    if (wl == 0) {
+#pragma unroll
+        for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const Tin* X = static_cast<const Tin*>(p.logits);
+    Tin* Y = static_cast<Tin*>(p.grad);
+    const int V = p.V, nvec = V / EPV;
+    const uint32_t rb = (uint32_t)V * sizeof(Tin);
+    const float cl = p.clamp * p.scale;
+    const bool clip = p.clamp < INFINITY;
+    const int vb = p.blank / EPV, eb_i = p.blank % EPV;
+    WarpRows seq;
+    seq.init(p.rows, (int64_t)blockIdx.x * nw + wid, (int64_t)gridDim.x * nw);
+    const int64_t nb = (seq.count + 31) / 32;   // batches of this warp
+
+    auto load_info = [&](int64_t j) -> float4 {
+        const int64_t k = j * 32 + wl;
+        return (j < nb && k < seq.count) ? p.info[seq.row(k)]
+                                         : make_float4(-INFINITY, 0.f, 0.f, __int_as_float(-1));
+    };
+    float4 cur = load_info(0), nxt = load_info(1);
+    // Rows still to be fetched, as bit masks over the current and the next batch.
+    uint32_t pend_cur = __ballot_sync(0xffffffffu, cur.x != -INFINITY);
+    uint32_t pend_nxt = 0;
+    bool nxt_known = false;
+    int64_t issued = 0, consumed = 0;
+    int64_t j = 0;   // current batch
+
+    auto issue_more = [&]() {
+        while (issued - consumed < kStages) {
+            if (!pend_cur && !nxt_known && j + 1 < nb) {
+                pend_nxt = __ballot_sync(0xffffffffu, nxt.x != -INFINITY);
+                nxt_known = true;
+            }
+            int64_t row;
+            if (pend_cur) {
+                const int bit = __ffs(pend_cur) - 1;
+                pend_cur &= pend_cur - 1;
+                row = seq.row(j * 32 + bit);
+            } else if (nxt_known && pend_nxt) {
+                const int bit = __ffs(pend_nxt) - 1;
+                pend_nxt &= pend_nxt - 1;
+                row = seq.row((j + 1) * 32 + bit);
+            } else {
+                break;
+            }
+            const int st = (int)(issued % kStages);
+            if (wl == 0) {
+                fence_proxy_async();
+                tma_row_load(buf + st * sb, X + row * (int64_t)V, rb, &bars[st]);
+            }
+            ++issued;
+        }
+    };
+
+    issue_more();
+    bool ok = true;
+    for (; j < nb && ok; ++j) {
+        const int nrows = (int)min((int64_t)32, seq.count - j * 32);
+        for (int it = 0; it < nrows; ++it) {
+            const int64_t r = seq.row(j * 32 + it);
+            const float w2 = __shfl_sync(0xffffffffu, cur.x, it);
+            const float eb = __shfl_sync(0xffffffffu, cur.y, it);
+            const float ey = __shfl_sync(0xffffffffu, cur.z, it);
+            const int y = __shfl_sync(0xffffffffu, __float_as_int(cur.w), it);
+            const int vy = y >= 0 ? y / EPV : -1, ey_i = y >= 0 ? y % EPV : 0;
+            uint4* ov = reinterpret_cast<uint4*>(Y + r * (int64_t)V);
+            const bool zero = w2 == -INFINITY;
+            const uint4* rv = nullptr;
+            int st = 0;
+            if (!zero) {
+                st = (int)(consumed % kStages);
+                if (!mbar_wait(&bars[st], (uint32_t)((consumed / kStages) & 1), p.err)) {
+                    ok = false;
+                    break;
+                }
+                rv = reinterpret_cast<const uint4*>(buf + st * sb);
+            }
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const int vi = wl + 32 * i;
+                if (vi >= nvec) continue;
+                float g[EPV];
+                if (!zero) {
+                    float x[EPV];
+                    E::unpack(rv[vi], x);
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) g[e] = ex2(fmaf(x[e], kLog2e, w2));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) g[e] = 0.0f;
+                }
+                if (vi == vb) {
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e)
+                        if (e == eb_i) g[e] -= eb;
+                }
+                if (vi == vy) {
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e)
+                        if (e == ey_i) g[e] -= ey;
+                }
+                if (clip) {
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) g[e] = fminf(fmaxf(g[e], -cl), cl);
+                }
+                __stcs(ov + vi, E::pack(g));
+            }
+            if (!zero) {
+                __syncwarp();
+                ++consumed;
+                issue_more();
+            }
+        }
+        // Advance to the next batch: its record is already loaded; fetch the one after.
+        cur = nxt;
+        if (!nxt_known) pend_nxt = __ballot_sync(0xffffffffu, cur.x != -INFINITY);
+        pend_cur = pend_nxt;
+        pend_nxt = 0;
+        nxt_known = false;
+        nxt = load_info(j + 2);
+        if (j + 1 < nb) {
+            ++j;
+            issue_more();
+            --j;
+        }
+    }
+    // Drain copies still in flight (only after a timeout) before the CTA exits.
+    if (!ok)
+        for (int64_t k = consumed; k < issued; ++k)
+            mbar_wait(&bars[k % kStages], (uint32_t)((k / kStages) & 1), p.err);
+}
+
 // ---------------------------------------------------------------- finalize
 __global__ void __launch_bounds__(256) k_finalize(Params p) {
     __shared__ double part[256];
@@ -941,7 +1238,7 @@ __global__ void __launch_bounds__(256) k_finalize(Params p) {
     const int tid = threadIdx.x;
     if (tid == 0) errs = *p.err;
     __syncthreads();
-    const bool ok_in = (errs & (ERR_LENGTH | ERR_ROWS | ERR_TARGET)) == 0;
+    const bool ok_in = (errs & (ERR_LENGTH | ERR_ROWS | ERR_TARGET | ERR_TIMEOUT)) == 0;
     double s = 0.0;
     if (ok_in) {
         for (int b = tid; b < p.B; b += blockDim.x) {
@@ -961,6 +1258,7 @@ __global__ void __launch_bounds__(256) k_finalize(Params p) {
             p.loss_red[0] = (float)(p.red == RNNT_RED_MEAN ? part[0] / p.B : part[0]);
         int st = RNNT_OK;
         if (errs & (ERR_LENGTH | ERR_ROWS | ERR_TARGET)) st = RNNT_INVALID_VALUE;
+        else if (errs & ERR_TIMEOUT) st = RNNT_TIMEOUT;
         else if (errs & (ERR_MISMATCH | ERR_NONFINITE)) st = RNNT_LOSS_MISMATCH;
         *p.err = errs;
         if (p.status) *p.status = st;
@@ -1021,17 +1319,23 @@ int grid_for(int64_t work_threads, int sms, int per_sm) {
 }
 
 // Resident 256-thread blocks per SM of a kernel (cached per kernel).
-int occupancy(const void* kernel) {
+int occupancy(const void* kernel, size_t smem) {
     static const void* keys[128];
+    static size_t smems[128];
     static int vals[128];
     for (int i = 0; i < 128 && keys[i]; ++i)
-        if (keys[i] == kernel) return vals[i];
+        if (keys[i] == kernel && smems[i] == smem) return vals[i];
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+        return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 256, 0) != cudaSuccess || n < 1)
-        n = 1;
-    for (int i = 0; i < 128; ++i)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 256, smem) != cudaSuccess || n < 1)
+        n = 0;
+    for (int i = 0; i < 128 && n > 0; ++i)
         if (!keys[i]) {
             vals[i] = n;
+            smems[i] = smem;
             keys[i] = kernel;
             break;
         }
@@ -1040,9 +1344,16 @@ int occupancy(const void* kernel) {
 
 // Grid-stride launch: never more blocks than are resident at once.
 template <typename K>
-void launch_gs(K kernel, int64_t work_threads, int sms, cudaStream_t st, const Params& p) {
-    const int g = grid_for(work_threads, sms, occupancy(reinterpret_cast<const void*>(kernel)));
-    kernel<<<g, 256, 0, st>>>(p);
+void launch_gs(K kernel, int64_t work_threads, int sms, cudaStream_t st, const Params& p,
+               size_t smem = 0) {
+    const int occ = occupancy(reinterpret_cast<const void*>(kernel), smem);
+    const int g = grid_for(work_threads, sms, occ > 0 ? occ : 1);
+    kernel<<<g, 256, smem, st>>>(p);
+}
+
+// Shared memory of the TMA-staged passes: kStages row buffers + barriers per warp.
+size_t tma_smem(const Params& p) {
+    return (size_t)8 * kStages * p.stage_bytes + (size_t)8 * kStages * sizeof(uint64_t);
 }
 
 template <typename Tin>
@@ -1056,6 +1367,13 @@ void launch_rows(const Params& p, cudaStream_t st, int sms) {
     const bool vec = ((size_t)V * sizeof(Tin)) % 16 == 0;
     const int nvec = V / EPV;
     const int64_t wt = (p.rows + 31) / 32 * 32;   // one warp per 32-row batch
+    if (vec && nvec > 32 && nvec <= 32 * 8) {
+        const size_t sm = tma_smem(p);
+        if (nvec <= 64) launch_gs(k_row_tma<Tin, 2>, wt, sms, st, p, sm);
+        else if (nvec <= 128) launch_gs(k_row_tma<Tin, 4>, wt, sms, st, p, sm);
+        else launch_gs(k_row_tma<Tin, 8>, wt, sms, st, p, sm);
+        return;
+    }
     if (vec && nvec <= 32 * 8) {
         if (nvec <= 4) launch_gs(k_row_regs<Tin, 4, 1>, wt, sms, st, p);
         else if (nvec <= 16) launch_gs(k_row_regs<Tin, 8, 2>, wt, sms, st, p);
@@ -1081,6 +1399,15 @@ template <typename Tin>
 void launch_grad(const Params& p, cudaStream_t st, int sms) {
     const int V = p.V;
     const bool vec = ((size_t)V * sizeof(Tin)) % 16 == 0;
+    const int nvec = V / Elt<Tin>::kPerVec;
+    if (p.fused && vec && nvec > 32 && nvec <= 32 * 8) {
+        const size_t sm = tma_smem(p);
+        const int64_t wt = (p.rows + 31) / 32 * 32;
+        if (nvec <= 64) launch_gs(k_grad_tma<Tin, 2>, wt, sms, st, p, sm);
+        else if (nvec <= 128) launch_gs(k_grad_tma<Tin, 4>, wt, sms, st, p, sm);
+        else launch_gs(k_grad_tma<Tin, 8>, wt, sms, st, p, sm);
+        return;
+    }
 #define GRADK(G_)                                                                      \
     do {                                                                               \
         const int64_t wt = p.rows * G_;                                                \
@@ -1164,6 +1491,7 @@ extern "C" rnnt_status_t rnnt_loss_fused_staged(
     p.fused = fused_log_softmax ? 1 : 0;
     p.red = reduction;
     p.ring_int4 = ring_int4_for(targets_stride);
+    p.stage_bytes = (int)(((size_t)V * es + 127) / 128 * 128);
     p.loss = loss;
     p.loss_red = loss_reduced;
     p.status = status_dev;

@@ -149,6 +149,17 @@ def make(name_or_cfg, device="cpu", with_logits: bool = True) -> Workload:
     return Workload(cfg, T, U, y, off, logits)
 
 
+def subset(wl: Workload, n: int) -> Workload:
+    """The first n samples of a workload (same bytes), e.g. for a smaller profiling run."""
+    from dataclasses import replace
+    n = max(1, min(n, wl.cfg.B))
+    cfg = replace(wl.cfg, B=n)
+    r1 = int(wl.offsets[n])
+    return Workload(cfg, wl.T[:n].copy(), wl.U[:n].copy(),
+                    np.ascontiguousarray(wl.targets[:n, :max(1, int(wl.U[:n].max()))]),
+                    wl.offsets[:n + 1].copy(), wl.logits[:r1])
+
+
 def custom(B, T, U, V, dtype="f32", sigma=1.0, blank=-1, clamp=-1.0, fused=True,
            reduction="mean", seed=7, device="cpu") -> Workload:
     """A workload with explicit lengths (tests of edge cases)."""
