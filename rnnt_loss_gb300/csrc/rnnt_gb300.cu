@@ -102,7 +102,6 @@ struct Params {
     float skip2;      // log2-occupancy below which a gradient row is exactly zero
     int fused;
     int red;
-    int ring_int4;    // per-warp DP ring size (int4 records)
     int stage_bytes;  // per-stage shared-memory row buffer of the TMA-staged passes
     float* loss;
     float* loss_red;
@@ -731,15 +730,22 @@ __global__ void __launch_bounds__(256) k_row_gather(Params p) {
 }
 
 // ---------------------------------------------------------------- DP
-// Per-warp ring of prefetched anti-diagonal edge records in shared memory:
-// slot = J*32 int4 (column u = lane + 32*j); depth R, prefetch distance R-2.
+// One CTA of 8 warps per sample: warps 0-3 run the forward recursion, warps
+// 4-7 the backward one.  The W = U+1 lattice columns are split into NWD <= 4
+// contiguous blocks of 32*J columns, one per warp; inside a warp lane l holds
+// columns base + 32*j + l.  The neighbouring column comes from the next lane
+// by shuffle, or, at a block edge, from the neighbouring warp through shared
+// memory with one named barrier per anti-diagonal (barrier 1: alpha, 2: beta).
+// Each warp prefetches its nodes' transition records with cp.async into a
+// ring of R anti-diagonals (prefetch distance R-2).
 template <int J> struct Ring;
-template <> struct Ring<1> { static constexpr int R = 32; };
-template <> struct Ring<2> { static constexpr int R = 32; };
-template <> struct Ring<4> { static constexpr int R = 24; };
-template <> struct Ring<8> { static constexpr int R = 12; };
-template <> struct Ring<16> { static constexpr int R = 7; };
-template <> struct Ring<32> { static constexpr int R = 4; };
+template <> struct Ring<1> { static constexpr int R = 16; };
+template <> struct Ring<2> { static constexpr int R = 12; };
+template <> struct Ring<3> { static constexpr int R = 10; };
+template <> struct Ring<4> { static constexpr int R = 8; };
+template <> struct Ring<6> { static constexpr int R = 6; };
+template <> struct Ring<8> { static constexpr int R = 6; };
+constexpr int kDpWarps = 4;   // warps per direction
 
 __device__ __forceinline__ void cp16(void* smem, const void* gmem) {
     const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
@@ -748,6 +754,9 @@ __device__ __forceinline__ void cp16(void* smem, const void* gmem) {
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
+}
 
 struct Samp {
     int b, T, U, W, D;
@@ -778,9 +787,17 @@ struct DiagCursor {
     }
 };
 
+// Columns of one warp of a direction.
+struct Cols {
+    int u0;    // first column of this warp's block
+    int w;     // warp index within the direction
+    int nwd;   // warps of the direction
+    __device__ __forceinline__ int col(int j, int lane) const { return u0 + 32 * j + lane; }
+};
+
 template <int J>
-__device__ __forceinline__ void ring_issue(const Params& p, const Samp& c, int4* ring,
-                                           const DiagCursor& q, int lane) {
+__device__ __forceinline__ void ring_issue(const Params& p, const Samp& c, const Cols& cc,
+                                           int4* ring, const DiagCursor& q, int lane) {
     constexpr int R = Ring<J>::R;
     const int d = q.d;
     if (d >= 0 && d < c.D) {
@@ -788,7 +805,7 @@ __device__ __forceinline__ void ring_issue(const Params& p, const Samp& c, int4*
         const int64_t base = q.base(c);
 #pragma unroll
         for (int j = 0; j < J; ++j) {
-            const int u = lane + 32 * j;
+            const int u = cc.col(j, lane);
             if (on_lattice(c, d, u)) cp16(sl + j * 32 + lane, p.edge + (base - u));
             else sl[j * 32 + lane] = make_int4(0, kZeroExp, 0, kZeroExp);
         }
@@ -796,40 +813,44 @@ __device__ __forceinline__ void ring_issue(const Params& p, const Samp& c, int4*
 }
 
 template <int J>
-__device__ __forceinline__ void store_diag(const Samp& c, int2* out, const DiagCursor& q,
-                                           const float* m, const int* e, int lane) {
+__device__ __forceinline__ void store_diag(const Samp& c, const Cols& cc, int2* out,
+                                           const DiagCursor& q, const float* m, const int* e,
+                                           int lane) {
     const int64_t base = q.base(c);
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-        const int u = lane + 32 * j;
+        const int u = cc.col(j, lane);
         if (on_lattice(c, q.d, u)) out[base - u] = make_int2(__float_as_int(m[j]), e[j]);
     }
 }
 
 // Forward variable: alpha(t,u) = alpha(t-1,u) p_blank(t-1,u) + alpha(t,u-1) p_label(t,u-1).
+// xch: [2][kDpWarps] (m, e) of the label arc leaving each warp's last column.
 template <int J>
-__device__ void dp_alpha(const Params& p, const Samp& c, int4* ring) {
+__device__ void dp_alpha(const Params& p, const Samp& c, const Cols& cc, int4* ring,
+                         float2* xch) {
     constexpr int R = Ring<J>::R, PF = R - 2;
     const int lane = threadIdx.x & 31;
+    const int nthreads = cc.nwd * 32;
     float am[J];
     int ae[J];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-        const bool origin = lane + 32 * j == 0;
+        const bool origin = cc.col(j, lane) == 0;
         am[j] = origin ? 1.0f : 0.0f;
         ae[j] = origin ? 0 : kZeroExp;
     }
     DiagCursor qs, qi;   // store cursor (diagonal d), issue cursor (diagonal d + PF)
     qs.init(c, 0);
-    store_diag<J>(c, p.alpha, qs, am, ae, lane);
+    store_diag<J>(c, cc, p.alpha, qs, am, ae, lane);
     qi.init(c, 0);
     for (int k = 0; k <= PF; ++k) {
-        ring_issue<J>(p, c, ring, qi, lane);
+        ring_issue<J>(p, c, cc, ring, qi, lane);
         cp_commit();
         qi.next(c);
     }
     for (int d = 1; d < c.D; ++d) {
-        ring_issue<J>(p, c, ring, qi, lane);
+        ring_issue<J>(p, c, cc, ring, qi, lane);
         cp_commit();
         qi.next(c);
         cp_wait<PF + 1>();
@@ -842,6 +863,18 @@ __device__ void dp_alpha(const Params& p, const Samp& c, int4* ring) {
             xf_mul(am[j], ae[j], __int_as_float(ed.x), ed.y, bm[j], be[j]);
             xf_mul(am[j], ae[j], __int_as_float(ed.z), ed.w, ym[j], ye[j]);
         }
+        float edge_m = 0.0f;
+        int edge_e = kZeroExp;
+        if (cc.nwd > 1) {
+            if (lane == 31 && cc.w + 1 < cc.nwd)
+                xch[(d & 1) * kDpWarps + cc.w] = make_float2(ym[J - 1], __int_as_float(ye[J - 1]));
+            named_barrier(1, nthreads);
+            if (lane == 0 && cc.w > 0) {
+                const float2 v = xch[(d & 1) * kDpWarps + cc.w - 1];
+                edge_m = v.x;
+                edge_e = __float_as_int(v.y);
+            }
+        }
         float sm[J];
         int se[J];
 #pragma unroll
@@ -851,63 +884,77 @@ __device__ void dp_alpha(const Params& p, const Samp& c, int4* ring) {
         }
 #pragma unroll
         for (int j = 0; j < J; ++j) {
-            const float nm = lane ? sm[j] : (j ? sm[j - 1] : 0.0f);
-            const int ne = lane ? se[j] : (j ? se[j - 1] : kZeroExp);
+            const float nm = lane ? sm[j] : (j ? sm[j - 1] : edge_m);
+            const int ne = lane ? se[j] : (j ? se[j - 1] : edge_e);
             xf_add(bm[j], be[j], nm, ne, am[j], ae[j]);
         }
         qs.next(c);
-        store_diag<J>(c, p.alpha, qs, am, ae, lane);
+        store_diag<J>(c, cc, p.alpha, qs, am, ae, lane);
     }
     // P(y|x) = alpha(T-1,U) p_blank(T-1,U): the terminal blank.
     cp_wait<0>();
-    const int e = c.D - 1, jU = c.U >> 5;
+    const int e = c.D - 1;
     const int4* sp = ring + (e % R) * (J * 32);
-    if (lane == (c.U & 31)) {
-        float m = 0.0f;
-        int x = kZeroExp;
 #pragma unroll
-        for (int j = 0; j < J; ++j)
-            if (j == jU) {
-                const int4 ed = sp[j * 32 + lane];
-                xf_mul(am[j], ae[j], __int_as_float(ed.x), ed.y, m, x);
-            }
-        xf_norm(m, x);
-        p.pm[c.b] = m;
-        p.pe[c.b] = x;
-        const double ll2 = (double)x + log2((double)m);
-        p.lossa[c.b] = -ll2 * kLn2d;
-        p.loss[c.b] = (float)(-ll2 * kLn2d);
+    for (int j = 0; j < J; ++j) {
+        if (cc.col(j, lane) == c.U) {
+            const int4 ed = sp[j * 32 + lane];
+            float m;
+            int x;
+            xf_mul(am[j], ae[j], __int_as_float(ed.x), ed.y, m, x);
+            xf_norm(m, x);
+            p.pm[c.b] = m;
+            p.pe[c.b] = x;
+            const double ll2 = (double)x + log2((double)m);
+            p.lossa[c.b] = -ll2 * kLn2d;
+            p.loss[c.b] = (float)(-ll2 * kLn2d);
+        }
     }
 }
 
 // Backward variable: beta(t,u) = beta(t+1,u) p_blank(t,u) + beta(t,u+1) p_label(t,u),
 // started from a virtual node after the terminal blank with beta = 1.
+// xch: [2][kDpWarps] (m, e) of each warp's first column on the previous diagonal.
 template <int J>
-__device__ void dp_beta(const Params& p, const Samp& c, int4* ring) {
+__device__ void dp_beta(const Params& p, const Samp& c, const Cols& cc, int4* ring,
+                        float2* xch) {
     constexpr int R = Ring<J>::R, PF = R - 2;
     const int lane = threadIdx.x & 31;
+    const int nthreads = cc.nwd * 32;
     float vm[J];
     int ve[J];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-        const bool top = lane + 32 * j == c.U;
+        const bool top = cc.col(j, lane) == c.U;
         vm[j] = top ? 1.0f : 0.0f;
         ve[j] = top ? 0 : kZeroExp;
     }
     DiagCursor qs, qi;   // store cursor (diagonal d), issue cursor (diagonal d - PF - 1)
     qi.init(c, c.D - 1);
     for (int k = 0; k <= PF; ++k) {
-        ring_issue<J>(p, c, ring, qi, lane);
+        ring_issue<J>(p, c, cc, ring, qi, lane);
         cp_commit();
-        if (qi.d > 0) qi.prev(c); else qi.d = -1;
+        qi.prev(c);
     }
     qs.init(c, c.D - 1);
     for (int d = c.D - 1; d >= 0; --d) {
-        ring_issue<J>(p, c, ring, qi, lane);
+        ring_issue<J>(p, c, cc, ring, qi, lane);
         cp_commit();
-        if (qi.d > 0) qi.prev(c); else qi.d = -1;
+        qi.prev(c);
         cp_wait<PF + 1>();
         const int4* sd = ring + (d % R) * (J * 32);
+        float edge_m = 0.0f;
+        int edge_e = kZeroExp;
+        if (cc.nwd > 1) {
+            if (lane == 0 && cc.w > 0)
+                xch[(d & 1) * kDpWarps + cc.w] = make_float2(vm[0], __int_as_float(ve[0]));
+            named_barrier(2, nthreads);
+            if (lane == 31 && cc.w + 1 < cc.nwd) {
+                const float2 v = xch[(d & 1) * kDpWarps + cc.w + 1];
+                edge_m = v.x;
+                edge_e = __float_as_int(v.y);
+            }
+        }
         float sm[J];
         int se[J];
 #pragma unroll
@@ -918,30 +965,54 @@ __device__ void dp_beta(const Params& p, const Samp& c, int4* ring) {
 #pragma unroll
         for (int j = 0; j < J; ++j) {
             const int4 ed = sd[j * 32 + lane];
-            const float nm = (lane < 31) ? sm[j] : (j + 1 < J ? sm[j + 1] : 0.0f);
-            const int ne = (lane < 31) ? se[j] : (j + 1 < J ? se[j + 1] : kZeroExp);
+            const float nm = (lane < 31) ? sm[j] : (j + 1 < J ? sm[j + 1] : edge_m);
+            const int ne = (lane < 31) ? se[j] : (j + 1 < J ? se[j + 1] : edge_e);
             float bm, ym;
             int be, ye;
             xf_mul(vm[j], ve[j], __int_as_float(ed.x), ed.y, bm, be);
             xf_mul(nm, ne, __int_as_float(ed.z), ed.w, ym, ye);
             xf_add(bm, be, ym, ye, vm[j], ve[j]);
         }
-        store_diag<J>(c, p.beta, qs, vm, ve, lane);
-        if (d > 0) qs.prev(c);
+        store_diag<J>(c, cc, p.beta, qs, vm, ve, lane);
+        qs.prev(c);
     }
     cp_wait<0>();
-    if (lane == 0) p.lossb[c.b] = -((double)ve[0] + log2((double)vm[0])) * kLn2d;
+    if (cc.w == 0 && lane == 0) p.lossb[c.b] = -((double)ve[0] + log2((double)vm[0])) * kLn2d;
+}
+
+__device__ __forceinline__ int dp_warps(int W) { return min(kDpWarps, (W + 31) / 32); }
+__device__ __forceinline__ int dp_slots(int W) {
+    const int n = dp_warps(W);
+    return (W + 32 * n - 1) / (32 * n);
 }
 
 template <int J>
-__device__ __forceinline__ void dp_run(const Params& p, const Samp& c, int4* ring) {
-    if (threadIdx.x < 32) dp_alpha<J>(p, c, ring);
-    else dp_beta<J>(p, c, ring + p.ring_int4);
+__device__ __forceinline__ void dp_run(const Params& p, const Samp& c, int4* smem, float2* xch) {
+    const int wid = threadIdx.x >> 5;
+    const int dir = wid / kDpWarps, w = wid % kDpWarps;
+    Cols cc;
+    cc.nwd = dp_warps(c.W);
+    cc.w = w;
+    cc.u0 = w * 32 * J;
+    if (w >= cc.nwd) return;
+    int4* ring = smem + (size_t)wid * Ring<J>::R * J * 32;
+    if (dir == 0) dp_alpha<J>(p, c, cc, ring, xch);
+    else dp_beta<J>(p, c, cc, ring, xch + 2 * kDpWarps);
 }
 
-__global__ void __launch_bounds__(64) k_dp(Params p) {
+// Dynamic shared memory of k_dp for lattices up to W columns (8 rings).
+__host__ __device__ inline size_t dp_smem_bytes(int W) {
+    const int n = W <= 32 ? 1 : (W <= 64 ? 2 : (W <= 96 ? 3 : 4));
+    const int J = (W + 32 * n - 1) / (32 * n);
+    const int Jc = J <= 1 ? 1 : J <= 2 ? 2 : J <= 3 ? 3 : J <= 4 ? 4 : J <= 6 ? 6 : 8;
+    const int R = Jc == 1 ? 16 : Jc == 2 ? 12 : Jc == 3 ? 10 : Jc == 4 ? 8 : 6;
+    return (size_t)2 * kDpWarps * R * Jc * 32 * sizeof(int4);
+}
+
+__global__ void __launch_bounds__(256) k_dp(Params p) {
     if (*p.err) return;
     extern __shared__ int4 smem[];
+    __shared__ float2 xch[4 * kDpWarps];
     Samp c;
     c.b = p.order[blockIdx.x];
     c.T = p.Tl[c.b];
@@ -949,13 +1020,13 @@ __global__ void __launch_bounds__(64) k_dp(Params p) {
     c.W = c.U + 1;
     c.D = c.T + c.U;
     c.off = p.off[c.b];
-    const int J = (c.W + 31) >> 5;
-    if (J <= 1) dp_run<1>(p, c, smem);
-    else if (J <= 2) dp_run<2>(p, c, smem);
-    else if (J <= 4) dp_run<4>(p, c, smem);
-    else if (J <= 8) dp_run<8>(p, c, smem);
-    else if (J <= 16) dp_run<16>(p, c, smem);
-    else dp_run<32>(p, c, smem);
+    const int J = dp_slots(c.W);
+    if (J <= 1) dp_run<1>(p, c, smem, xch);
+    else if (J <= 2) dp_run<2>(p, c, smem, xch);
+    else if (J <= 3) dp_run<3>(p, c, smem, xch);
+    else if (J <= 4) dp_run<4>(p, c, smem, xch);
+    else if (J <= 6) dp_run<6>(p, c, smem, xch);
+    else dp_run<8>(p, c, smem, xch);
 }
 
 // ---------------------------------------------------------------- combine
@@ -1298,16 +1369,12 @@ int num_sms(int dev) {
     return g_num_sms[dev];
 }
 
-// Per-warp DP ring (int4 records) covering every lattice width up to S+1.
-int ring_int4_for(int S) {
-    const int Jn = (S + 1 + 31) / 32;
-    const int Js[6] = {1, 2, 4, 8, 16, 32};
-    const int Rs[6] = {32, 32, 24, 12, 7, 4};
-    int best = 0;
-    for (int i = 0; i < 6; ++i) {
-        const int need = Rs[i] * Js[i] * 32;
-        if (need > best) best = need;
-        if (Js[i] >= Jn) break;
+// k_dp shared memory covering every lattice width up to S+1.
+size_t dp_smem_for(int S) {
+    size_t best = 0;
+    for (int W = 1; W <= S + 1; ++W) {
+        const size_t b = dp_smem_bytes(W);
+        if (b > best) best = b;
     }
     return best;
 }
@@ -1490,7 +1557,6 @@ extern "C" rnnt_status_t rnnt_loss_fused_staged(
     p.skip2 = zero_at - log2f(p.scale);
     p.fused = fused_log_softmax ? 1 : 0;
     p.red = reduction;
-    p.ring_int4 = ring_int4_for(targets_stride);
     p.stage_bytes = (int)(((size_t)V * es + 127) / 128 * 128);
     p.loss = loss;
     p.loss_red = loss_reduced;
@@ -1508,7 +1574,7 @@ extern "C" rnnt_status_t rnnt_loss_fused_staged(
     p.beta = reinterpret_cast<int2*>(w + L.beta);
     p.info = reinterpret_cast<float4*>(w + L.info);
 
-    const size_t dp_smem = (size_t)p.ring_int4 * 2 * sizeof(int4);
+    const size_t dp_smem = dp_smem_for(targets_stride);
     if (dev >= 0 && dev < 64 && g_dp_smem_set[dev] < (int)dp_smem) {
         if (cudaFuncSetAttribute(k_dp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dp_smem) !=
             cudaSuccess)
@@ -1526,7 +1592,7 @@ extern "C" rnnt_status_t rnnt_loss_fused_staged(
     if (dt == RNNT_F32) launch_rows<float>(p, st, sms);
     else launch_rows<__half>(p, st, sms);
     mark(2);
-    k_dp<<<B, 64, dp_smem, st>>>(p);
+    k_dp<<<B, 256, dp_smem, st>>>(p);
     mark(3);
     if (grad) launch_gs(k_combine, rows, sms, st, p);
     mark(4);
