@@ -36,6 +36,9 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
+
+#include <algorithm>
 
 #include "rnnt_gb300.h"
 
@@ -59,9 +62,19 @@ enum : int {
 };
 
 // ---------------------------------------------------------------- workspace
+constexpr int kTaskRows = 256;   // rows per row / gradient task of the persistent kernel
+
 struct Layout {
-    size_t err, off, order, lossa, lossb, pm, pe, lse2, edge, alpha, beta, info, total;
+    size_t err, off, order, lossa, lossb, pm, pe, lse2, edge, alpha, beta, info;
+    size_t rtasks, rdone, dpdone, tasks, total;
+    int64_t max_tasks;
 };
+
+// Upper bound of the persistent kernel's task count: per sample its row
+// chunks, one DP task and its gradient chunks.
+__host__ __device__ inline int64_t max_tasks_for(int B, int64_t rows) {
+    return 2 * (rows / kTaskRows + B) + B;
+}
 
 __host__ __device__ inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -81,6 +94,11 @@ __host__ __device__ inline Layout ws_layout(int B, int64_t rows) {
     L.alpha = p; p = al256(p + sizeof(int2) * R);
     L.beta = p;  p = al256(p + sizeof(int2) * R);
     L.info = p;  p = al256(p + sizeof(float4) * R);
+    L.max_tasks = max_tasks_for(B, rows);
+    L.rtasks = p; p = al256(p + sizeof(int32_t) * (size_t)B);
+    L.rdone = p;  p = al256(p + sizeof(int32_t) * (size_t)B);
+    L.dpdone = p; p = al256(p + sizeof(int32_t) * (size_t)B);
+    L.tasks = p;  p = al256(p + sizeof(int4) * (size_t)L.max_tasks);
     L.total = p;
     return L;
 }
@@ -100,6 +118,7 @@ struct Params {
     float clamp;      // +inf when clipping is off
     float scale;      // reduction scale applied to the gradient
     float skip2;      // log2-occupancy below which a gradient row is exactly zero
+    float lscale;     // log2(scale)
     int fused;
     int red;
     int stage_bytes;  // per-stage shared-memory row buffer of the TMA-staged passes
@@ -118,7 +137,12 @@ struct Params {
     int4* edge;       // per node (diagonal-packed): {p_blank.m, p_blank.e, p_label.m, p_label.e}
     int2* alpha;      // per node (diagonal-packed): {m, e}
     int2* beta;
-    float4* info;     // per row: {log2 occ - lse2, log2 occ, post_blank, post_label}
+    float4* info;     // per row: gradient record (see k_combine)
+    // persistent-kernel scheduler (err[1] = next task, err[2] = task count)
+    int32_t* rtasks;  // row tasks per sample
+    int32_t* rdone;   // finished row tasks per sample
+    int32_t* dpdone;  // DP finished flag per sample
+    int4* tasks;      // {kind | sample << 2, first row in sample, rows, 0}
 };
 
 // ---------------------------------------------------------------- helpers
@@ -375,6 +399,37 @@ struct WarpRows {
 };
 
 // ---------------------------------------------------------------- k_prepare
+enum : int { TASK_ROW = 0, TASK_DP = 1, TASK_GRAD = 2 };
+
+// Exclusive block-wide scan of one int64 per thread (all threads call it);
+// `carry` (shared) accumulates across successive calls.
+__device__ __forceinline__ int64_t block_scan_excl(int64_t n, int64_t* wsum, int64_t& carry) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    int64_t x = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int64_t w = (lane < (int)(blockDim.x >> 5)) ? wsum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        wsum[lane] = w;
+    }
+    __syncthreads();
+    const int64_t excl = carry + (wid ? wsum[wid - 1] : 0) + x - n;
+    __syncthreads();
+    if (tid == (int)blockDim.x - 1) carry = excl + n;
+    __syncthreads();
+    return excl;
+}
+
 __global__ void __launch_bounds__(1024) k_prepare(Params p) {
     __shared__ int64_t wsum[32];
     __shared__ int64_t carry;
@@ -387,7 +442,8 @@ __global__ void __launch_bounds__(1024) k_prepare(Params p) {
         int64_t n = 0;
         if (b < p.B) {
             const int T = p.Tl[b], U = p.Ul[b];
-            if (T < 1 || U < 0 || U > p.S || U + 1 > kMaxW) atomicOr(&errs, ERR_LENGTH);
+            if (T < 1 || U < 0 || U > p.S || U + 1 > kMaxW || (int64_t)T * (U + 1) > INT32_MAX)
+                atomicOr(&errs, ERR_LENGTH);
             else n = (int64_t)T * (U + 1);
         }
         int64_t x = n;
@@ -440,6 +496,64 @@ __global__ void __launch_bounds__(1024) k_prepare(Params p) {
             rank += (kj > kb) || (kj == kb && j < b);
         }
         p.order[rank] = b;
+    }
+    __syncthreads();
+    // Task list of the persistent kernel, in queue order: for each sample in
+    // DP order its row chunks then its DP task; then all gradient chunks in
+    // the same order.  Every task waits only on tasks queued before it.
+    if (errs == 0) {
+        if (tid == 0) carry = 0;
+        __syncthreads();
+        int64_t tot = 0;
+        for (int base = 0; base < p.B; base += blockDim.x) {
+            const int i = base + tid;
+            int b = 0, nch = 0;
+            int64_t nrows = 0;
+            if (i < p.B) {
+                b = p.order[i];
+                nrows = (int64_t)p.Tl[b] * (p.Ul[b] + 1);
+                nch = (int)((nrows + kTaskRows - 1) / kTaskRows);
+                p.rtasks[b] = nch;
+                p.rdone[b] = 0;
+                p.dpdone[b] = 0;
+            }
+            const int64_t before = block_scan_excl(nch, wsum, carry);   // row tasks before i
+            if (i < p.B) {
+                const int64_t q = before + i;                          // + one DP task per sample
+                for (int k = 0; k < nch; ++k) {
+                    const int r = k * kTaskRows;
+                    p.tasks[q + k] = make_int4(TASK_ROW | (b << 2), r,
+                                               (int)min((int64_t)kTaskRows, nrows - r), 0);
+                }
+                p.tasks[q + nch] = make_int4(TASK_DP | (b << 2), 0, 0, 0);
+            }
+            tot = carry;
+        }
+        // Gradient chunks after every row/DP task.
+        const int64_t g0 = tot + p.B;
+        if (tid == 0) carry = 0;
+        __syncthreads();
+        for (int base = 0; base < p.B; base += blockDim.x) {
+            const int i = base + tid;
+            int b = 0, nch = 0;
+            int64_t nrows = 0;
+            if (i < p.B) {
+                b = p.order[i];
+                nrows = (int64_t)p.Tl[b] * (p.Ul[b] + 1);
+                nch = (int)((nrows + kTaskRows - 1) / kTaskRows);
+            }
+            const int64_t before = block_scan_excl(nch, wsum, carry);
+            if (i < p.B)
+                for (int k = 0; k < nch; ++k) {
+                    const int r = k * kTaskRows;
+                    p.tasks[g0 + before + k] = make_int4(
+                        TASK_GRAD | (b << 2), r, (int)min((int64_t)kTaskRows, nrows - r), 0);
+                }
+        }
+        if (tid == 0) {
+            p.err[1] = 0;                          // next task
+            p.err[2] = (int)(g0 + tot);            // task count
+        }
     }
     __syncthreads();
     if (tid == 0) *p.err = errs;
@@ -1039,49 +1153,54 @@ __device__ __forceinline__ float xf_to_float(float m, int e) {
     return (m == 0.0f || e < -200) ? 0.0f : ldexpf(m, min(e, 200));
 }
 
+// One row's gradient record.  Everything it reads that the same call wrote
+// (alpha, beta, transition records, lse2, P) is loaded through L2 only
+// (ld.global.cg): in the persistent kernel other CTAs write these while this
+// SM may hold neighbouring lines in L1.
+__device__ __forceinline__ float4 combine_row(const Params& p, int64_t r, int b) {
+    const int T = __ldg(p.Tl + b), U = __ldg(p.Ul + b), W = U + 1;
+    const int64_t o = __ldg(p.off + b);
+    const unsigned rr = (unsigned)(r - o);
+    const int t = (int)(rr / (unsigned)W), u = (int)(rr - (unsigned)t * W);
+    const int64_t i = o + node_index(t, u, T, U);
+    const int2 A = __ldcg(p.alpha + i), Bt = __ldcg(p.beta + i);
+    const int4 Ed = __ldcg(p.edge + i);
+    const float Pm = __ldcg(p.pm + b);
+    const int Pe = __ldcg(p.pe + b);
+    const float am = __int_as_float(A.x), bm = __int_as_float(Bt.x);
+    const float inv = 1.0f / Pm;
+    float lc = -INFINITY;
+    if (am != 0.0f && bm != 0.0f) lc = (float)(A.y + Bt.y - Pe) + lg2(am * bm * inv);
+    const int y = (u < U) ? __ldg(p.targets + (int64_t)b * p.S + u) : -1;
+    if (!(lc >= p.skip2))   // every element of this gradient row rounds to zero
+        return make_float4(-INFINITY, 0.0f, 0.0f, __int_as_float(y));
+    float eb = 0.0f, ey = 0.0f;
+    if (t < T - 1) {
+        const int2 Bn = __ldcg(p.beta + o + node_index(t + 1, u, T, U));
+        const float pb = __int_as_float(Ed.x), bn = __int_as_float(Bn.x);
+        if (am != 0.0f && pb != 0.0f && bn != 0.0f)
+            eb = xf_to_float(am * pb * bn * inv, A.y + Ed.y + Bn.y - Pe);
+    } else if (u == U) {
+        eb = xf_to_float(am * bm * inv, A.y + Bt.y - Pe);
+    }
+    if (u < U) {
+        const int2 Bn = __ldcg(p.beta + o + node_index(t, u + 1, T, U));
+        const float py = __int_as_float(Ed.z), bn = __int_as_float(Bn.x);
+        if (am != 0.0f && py != 0.0f && bn != 0.0f)
+            ey = xf_to_float(am * py * bn * inv, A.y + Ed.w + Bn.y - Pe);
+    }
+    return make_float4(lc + p.lscale - __ldcg(p.lse2 + r), eb * p.scale, ey * p.scale,
+                       __int_as_float(y));
+}
+
 __global__ void __launch_bounds__(256) k_combine(Params p) {
     if (*p.err) return;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    const float lsc = log2f(p.scale);
     int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     int b = (r < p.rows) ? find_sample(p.off, p.B, r) : 0;
     for (; r < p.rows; r += stride) {
         b = advance_sample(p.off, p.B, b, r);
-        const int T = __ldg(p.Tl + b), U = __ldg(p.Ul + b), W = U + 1;
-        const int64_t o = __ldg(p.off + b);
-        const unsigned rr = (unsigned)(r - o);
-        const int t = (int)(rr / (unsigned)W), u = (int)(rr - (unsigned)t * W);
-        const int64_t i = o + node_index(t, u, T, U);
-        const int2 A = p.alpha[i], Bt = p.beta[i];
-        const int4 Ed = p.edge[i];
-        const float Pm = __ldg(p.pm + b);
-        const int Pe = __ldg(p.pe + b);
-        const float am = __int_as_float(A.x), bm = __int_as_float(Bt.x);
-        const float inv = 1.0f / Pm;
-        float lc = -INFINITY;
-        if (am != 0.0f && bm != 0.0f) lc = (float)(A.y + Bt.y - Pe) + lg2(am * bm * inv);
-        const int y = (u < U) ? __ldg(p.targets + (int64_t)b * p.S + u) : -1;
-        if (!(lc >= p.skip2)) {   // every element of this gradient row rounds to zero
-            p.info[r] = make_float4(-INFINITY, 0.0f, 0.0f, __int_as_float(y));
-            continue;
-        }
-        float eb = 0.0f, ey = 0.0f;
-        if (t < T - 1) {
-            const int2 Bn = p.beta[o + node_index(t + 1, u, T, U)];
-            const float pb = __int_as_float(Ed.x), bn = __int_as_float(Bn.x);
-            if (am != 0.0f && pb != 0.0f && bn != 0.0f)
-                eb = xf_to_float(am * pb * bn * inv, A.y + Ed.y + Bn.y - Pe);
-        } else if (u == U) {
-            eb = xf_to_float(am * bm * inv, A.y + Bt.y - Pe);
-        }
-        if (u < U) {
-            const int2 Bn = p.beta[o + node_index(t, u + 1, T, U)];
-            const float py = __int_as_float(Ed.z), bn = __int_as_float(Bn.x);
-            if (am != 0.0f && py != 0.0f && bn != 0.0f)
-                ey = xf_to_float(am * py * bn * inv, A.y + Ed.w + Bn.y - Pe);
-        }
-        p.info[r] = make_float4(lc + lsc - p.lse2[r], eb * p.scale, ey * p.scale,
-                                __int_as_float(y));
+        p.info[r] = combine_row(p, r, b);
     }
 }
 
@@ -1302,6 +1421,339 @@ __global__ void __launch_bounds__(256) k_grad_tma(Params p) {
             mbar_wait(&bars[k % kStages], (uint32_t)((k / kStages) & 1), p.err);
 }
 
+// ---------------------------------------------------------------- persistent kernel
+// One cooperative launch runs every row, DP and gradient task of the call.
+// A CTA takes the next task index from a global counter; the queue order
+// (built by k_prepare) puts each sample's row chunks before its DP task and
+// every DP task before the gradient chunks, so a task only ever waits on
+// tasks that were handed out earlier to CTAs that are running (all CTAs are
+// co-resident under a cooperative launch).  The DP of a sample therefore runs
+// on one CTA while the others stream the rows of later samples and the
+// gradients of earlier ones.  Waits are bounded; a timeout raises an error
+// flag, releases the waiters downstream and makes every CTA stop.
+constexpr int kSpinLimit = 1 << 24;
+
+__device__ __forceinline__ int ld_acquire(const int32_t* a) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ bool wait_at_least(const int32_t* a, int target, int32_t* err) {
+    for (int i = 0; i < kSpinLimit; ++i) {
+        if (ld_acquire(a) >= target) return true;
+        if (ld_acquire(err) & ERR_TIMEOUT) return false;
+        __nanosleep(128);
+    }
+    atomicOr(err, ERR_TIMEOUT);
+    return false;
+}
+
+// Warp: rows [r0, r0+n) (n <= 32) through the warp's TMA stage ring; kk counts
+// the ring's copies so far (stage kk % kStages, phase parity (kk / kStages) & 1).
+template <typename Tin, int NV>
+__device__ bool row_batch_tma(const Params& p, int64_t r0, int n, unsigned char* buf,
+                              uint64_t* bars, uint32_t& kk) {
+    using E = Elt<Tin>;
+    constexpr int EPV = E::kPerVec;
+    const int wl = threadIdx.x & 31, sb = p.stage_bytes;
+    const Tin* X = static_cast<const Tin*>(p.logits);
+    const int V = p.V, nvec = V / EPV;
+    const uint32_t rb = (uint32_t)V * sizeof(Tin);
+    if (wl == 0) {
+        fence_proxy_async();
+        for (int i = 0; i < min(kStages, n); ++i) {
+            const uint32_t st = (kk + i) % kStages;
+            tma_row_load(buf + st * sb, X + (r0 + i) * (int64_t)V, rb, &bars[st]);
+        }
+    }
+    float myM = 0.0f, mys = 0.0f;
+    int i = 0;
+    for (; i < n; ++i) {
+        const uint32_t k = kk + i, st = k % kStages;
+        if (!mbar_wait(&bars[st], (k / kStages) & 1, p.err)) break;
+        const uint4* rv = reinterpret_cast<const uint4*>(buf + st * sb);
+        uint4 q[NV];
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+            if (wl + 32 * v < nvec) q[v] = rv[wl + 32 * v];
+        __syncwarp();
+        if (wl == 0 && i + kStages < n) {
+            fence_proxy_async();
+            tma_row_load(buf + st * sb, X + (r0 + i + kStages) * (int64_t)V, rb, &bars[st]);
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+            if (wl + 32 * v < nvec) M = fmaxf(M, E::vmax(q[v]));
+        M = group_max<32>(M, 0xffffffffu);
+        float sum = 0.0f;
+        if (M != -INFINITY) {
+            const float ML = M * kLog2e;
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                if (wl + 32 * v < nvec) {
+                    float x[EPV];
+                    E::unpack(q[v], x);
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) sum += ex2(fmaf(x[e], kLog2e, -ML));
+                }
+            }
+        }
+        sum = group_sum<32>(sum, 0xffffffffu);
+        if (wl == i) {
+            myM = M;
+            mys = sum;
+        }
+    }
+    if (i < n) {   // timeout: wait (bounded) for the copies still in flight
+        for (int q = i; q < min(i + kStages, n); ++q)
+            mbar_wait(&bars[(kk + q) % kStages], ((kk + q) / kStages) & 1, p.err);
+        return false;
+    }
+    kk += n;
+    if (wl < n) row_finish<Tin>(p, r0 + wl, myM, mys);
+    return true;
+}
+
+// Warp: gradient rows [r0, r0+n) with their records in shared memory; only
+// rows that are not exactly zero are fetched through the TMA ring.
+template <typename Tin, int NV>
+__device__ bool grad_batch_tma(const Params& p, int64_t r0, int n, const float4* inf,
+                               unsigned char* buf, uint64_t* bars, uint32_t& kk) {
+    using E = Elt<Tin>;
+    constexpr int EPV = E::kPerVec;
+    const int wl = threadIdx.x & 31, sb = p.stage_bytes;
+    const Tin* X = static_cast<const Tin*>(p.logits);
+    Tin* Y = static_cast<Tin*>(p.grad);
+    const int V = p.V, nvec = V / EPV;
+    const uint32_t rb = (uint32_t)V * sizeof(Tin);
+    const float cl = p.clamp * p.scale;
+    const bool clip = p.clamp < INFINITY;
+    const int vb = p.blank / EPV, eb_i = p.blank % EPV;
+    const bool mine = wl < n && inf[min(wl, n - 1)].x != -INFINITY;
+    uint32_t pend = __ballot_sync(0xffffffffu, mine);
+    const uint32_t nnz = __popc(pend);
+    uint32_t issued = 0, consumed = 0;
+    if (wl == 0) fence_proxy_async();
+    while (issued < min((uint32_t)kStages, nnz)) {
+        const int bit = __ffs(pend) - 1;
+        pend &= pend - 1;
+        const uint32_t st = (kk + issued) % kStages;
+        if (wl == 0) tma_row_load(buf + st * sb, X + (r0 + bit) * (int64_t)V, rb, &bars[st]);
+        ++issued;
+    }
+    for (int it = 0; it < n; ++it) {
+        const float4 in = inf[it];
+        const float w2 = in.x, eb = in.y, ey = in.z;
+        const int y = __float_as_int(in.w);
+        const int vy = y >= 0 ? y / EPV : -1, ey_i = y >= 0 ? y % EPV : 0;
+        const bool zero = w2 == -INFINITY;
+        const uint4* rv = nullptr;
+        if (!zero) {
+            const uint32_t k = kk + consumed, st = k % kStages;
+            if (!mbar_wait(&bars[st], (k / kStages) & 1, p.err)) {
+                for (uint32_t q = consumed; q < issued; ++q)
+                    mbar_wait(&bars[(kk + q) % kStages], ((kk + q) / kStages) & 1, p.err);
+                return false;
+            }
+            rv = reinterpret_cast<const uint4*>(buf + st * sb);
+        }
+        uint4* ov = reinterpret_cast<uint4*>(Y + (r0 + it) * (int64_t)V);
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const int vi = wl + 32 * v;
+            if (vi >= nvec) continue;
+            float g[EPV];
+            if (!zero) {
+                float x[EPV];
+                E::unpack(rv[vi], x);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) g[e] = ex2(fmaf(x[e], kLog2e, w2));
+            } else {
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) g[e] = 0.0f;
+            }
+            if (vi == vb) {
+#pragma unroll
+                for (int e = 0; e < EPV; ++e)
+                    if (e == eb_i) g[e] -= eb;
+            }
+            if (vi == vy) {
+#pragma unroll
+                for (int e = 0; e < EPV; ++e)
+                    if (e == ey_i) g[e] -= ey;
+            }
+            if (clip) {
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) g[e] = fminf(fmaxf(g[e], -cl), cl);
+            }
+            __stcs(ov + vi, E::pack(g));
+        }
+        if (!zero) {
+            __syncwarp();
+            const uint32_t st = (kk + consumed) % kStages;
+            ++consumed;
+            if (pend) {
+                const int bit = __ffs(pend) - 1;
+                pend &= pend - 1;
+                if (wl == 0) {
+                    fence_proxy_async();
+                    tma_row_load(buf + st * sb, X + (r0 + bit) * (int64_t)V, rb, &bars[st]);
+                }
+                ++issued;
+            }
+        }
+    }
+    kk += nnz;
+    return true;
+}
+
+// Warp: gradient rows without staging (log-softmax off: nothing is read).
+template <typename Tin, int G, bool VEC, bool FUSED>
+__device__ void grad_batch_plain(const Params& p, int64_t r0, int n, const float4* inf) {
+    using E = Elt<Tin>;
+    constexpr int NG = 32 / G;
+    const Tin* X = static_cast<const Tin*>(p.logits);
+    Tin* Y = static_cast<Tin*>(p.grad);
+    const int V = p.V;
+    const int wl = threadIdx.x & 31, lane = wl & (G - 1), grp = wl / G;
+    const float cl = p.clamp * p.scale;
+    const bool clip = p.clamp < INFINITY;
+    for (int it = grp; it < n; it += NG) {
+        const float4 in = inf[it];
+        const bool zero = in.x == -INFINITY;
+        const float w2 = in.x, eb = in.y, ey = in.z;
+        const int y = __float_as_int(in.w);
+        const Tin* row = X + (r0 + it) * (int64_t)V;
+        Tin* out = Y + (r0 + it) * (int64_t)V;
+        if (VEC) {
+            constexpr int EPV = E::kPerVec;
+            const int nvec = V / EPV;
+            const uint4* rv = reinterpret_cast<const uint4*>(row);
+            uint4* ov = reinterpret_cast<uint4*>(out);
+            for (int vi = lane; vi < nvec; vi += G) {
+                float x[EPV], g[EPV];
+                if (FUSED && !zero) E::unpack(__ldcs(rv + vi), x);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) {
+                    const int k = vi * EPV + e;
+                    float gv = (FUSED && !zero) ? ex2(fmaf(x[e], kLog2e, w2)) : 0.0f;
+                    if (k == p.blank) gv -= eb;
+                    if (k == y) gv -= ey;
+                    g[e] = clip ? fminf(fmaxf(gv, -cl), cl) : gv;
+                }
+                __stcs(ov + vi, E::pack(g));
+            }
+        } else {
+            for (int k = lane; k < V; k += G) {
+                float gv = (FUSED && !zero) ? ex2(fmaf(E::to_f(row[k]), kLog2e, w2)) : 0.0f;
+                if (k == p.blank) gv -= eb;
+                if (k == y) gv -= ey;
+                out[k] = E::from_f(clip ? fminf(fmaxf(gv, -cl), cl) : gv);
+            }
+        }
+    }
+}
+
+// DP task: the sample's forward and backward recursions on this CTA's warps.
+__device__ __noinline__ void dp_task(const Params& p, int b, int4* smem, float2* xch) {
+    Samp c;
+    c.b = b;
+    c.T = __ldg(p.Tl + b);
+    c.U = __ldg(p.Ul + b);
+    c.W = c.U + 1;
+    c.D = c.T + c.U;
+    c.off = __ldg(p.off + b);
+    const int J = dp_slots(c.W);
+    if (J <= 1) dp_run<1>(p, c, smem, xch);
+    else if (J <= 2) dp_run<2>(p, c, smem, xch);
+    else if (J <= 3) dp_run<3>(p, c, smem, xch);
+    else if (J <= 4) dp_run<4>(p, c, smem, xch);
+    else if (J <= 6) dp_run<6>(p, c, smem, xch);
+    else dp_run<8>(p, c, smem, xch);
+}
+
+// NV > 0: log-softmax in kernel, rows staged by TMA (NV vectors per lane).
+// NV == 0: log-softmax off, rows gathered (2 elements) and gradients written
+// with G lanes per row (VEC: 16-byte rows).
+template <typename Tin, int NV, int G, bool VEC>
+__global__ void __launch_bounds__(256, 2) k_main(Params p) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    __shared__ uint64_t bars_all[8 * kStages];
+    __shared__ float4 s_info[kTaskRows];
+    __shared__ float2 xch[4 * kDpWarps];
+    __shared__ int s_task, s_go;
+    if (*p.err & (ERR_LENGTH | ERR_ROWS | ERR_TARGET)) return;   // uniform: set before launch
+    const int tid = threadIdx.x, wid = tid >> 5, wl = tid & 31;
+    unsigned char* buf = smem_raw + (size_t)wid * kStages * p.stage_bytes;
+    uint64_t* bars = bars_all + wid * kStages;
+    if (NV > 0 && wl == 0) {
+#pragma unroll
+        for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], 1);
+        fence_mbar_init();
+    }
+    uint32_t kk = 0;   // this warp's TMA ring position
+    const int ntasks = p.err[2];
+    for (;;) {
+        // Every branch below is taken by the whole CTA: decisions that depend on
+        // global state are made by thread 0 and broadcast through shared memory.
+        if (tid == 0) {
+            s_task = atomicAdd(&p.err[1], 1);
+            s_go = !(ld_acquire(p.err) & ERR_TIMEOUT);
+        }
+        __syncthreads();
+        const int t = s_task;
+        const bool go = s_go;
+        __syncthreads();
+        if (t >= ntasks || !go) break;
+        const int4 tk = p.tasks[t];
+        const int kind = tk.x & 3, b = tk.x >> 2, n = tk.z;
+        const int64_t r0 = __ldg(p.off + b) + tk.y;
+        if (NV > 0 && kind != TASK_DP) fence_proxy_async();   // smem may have been a DP ring
+        if (kind == TASK_ROW) {
+            const int64_t rw = r0 + 32 * wid;
+            const int nw = min(32, n - 32 * wid);
+            if (nw > 0) {
+                if (NV > 0) {
+                    row_batch_tma<Tin, (NV > 0 ? NV : 1)>(p, rw, nw, buf, bars, kk);
+                } else if (wl < nw) {
+                    row_finish<Tin>(p, rw + wl, 0.0f, 1.0f);
+                }
+            }
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) atomicAdd(&p.rdone[b], 1);
+        } else if (kind == TASK_DP) {
+            if (tid == 0) s_go = wait_at_least(&p.rdone[b], __ldg(p.rtasks + b), p.err);
+            __syncthreads();
+            const bool ready = s_go;
+            __syncthreads();
+            __threadfence();
+            if (ready) dp_task(p, b, reinterpret_cast<int4*>(smem_raw), xch);
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) atomicExch(&p.dpdone[b], 1);
+        } else {
+            if (tid == 0) s_go = wait_at_least(&p.dpdone[b], 1, p.err);
+            __syncthreads();
+            const bool ready = s_go;
+            __syncthreads();
+            __threadfence();
+            if (!ready) continue;   // uniform; the next iteration sees the error and stops
+            if (tid < n) s_info[tid] = combine_row(p, r0 + tid, b);
+            __syncthreads();
+            const int nw = min(32, n - 32 * wid);
+            if (nw > 0) {
+                if (NV > 0)
+                    grad_batch_tma<Tin, (NV > 0 ? NV : 1)>(p, r0 + 32 * wid, nw, s_info + 32 * wid,
+                                                          buf, bars, kk);
+                else
+                    grad_batch_plain<Tin, G, VEC, false>(p, r0 + 32 * wid, nw, s_info + 32 * wid);
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- finalize
 __global__ void __launch_bounds__(256) k_finalize(Params p) {
     __shared__ double part[256];
@@ -1493,6 +1945,52 @@ void launch_grad(const Params& p, cudaStream_t st, int sms) {
 #undef GRADK
 }
 
+int g_coop[64];
+
+bool coop_supported(int dev) {
+    if (dev < 0 || dev >= 64) return false;
+    if (!g_coop[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrCooperativeLaunch, dev);
+        g_coop[dev] = v ? 1 : -1;
+    }
+    return g_coop[dev] > 0;
+}
+
+// Persistent path: every row, DP and gradient task in one cooperative launch.
+// Returns false (nothing launched) when this shape is not covered.
+template <typename Tin>
+bool launch_persistent(const Params& p, cudaStream_t st, int sms, int dev) {
+    if (!coop_supported(dev)) return false;
+    const char* env = getenv("RNNT_GB300_SCHEDULE");
+    if (env && env[0] == 'k') return false;   // "kernels": one launch per stage
+    constexpr int EPV = Elt<Tin>::kPerVec;
+    const int V = p.V, nvec = V / EPV;
+    const bool vec = ((size_t)V * sizeof(Tin)) % 16 == 0;
+    const size_t dps = dp_smem_for(p.S);
+    const void* fn = nullptr;
+    size_t sm = dps;
+    if (p.fused) {
+        if (!(vec && nvec > 32 && nvec <= 256)) return false;
+        sm = std::max(sm, (size_t)8 * kStages * p.stage_bytes);
+        fn = nvec <= 64    ? reinterpret_cast<const void*>(k_main<Tin, 2, 32, true>)
+             : nvec <= 128 ? reinterpret_cast<const void*>(k_main<Tin, 4, 32, true>)
+                           : reinterpret_cast<const void*>(k_main<Tin, 8, 32, true>);
+    } else {
+        const bool wide = V >= 256;
+        fn = vec ? (wide ? reinterpret_cast<const void*>(k_main<Tin, 0, 32, true>)
+                         : reinterpret_cast<const void*>(k_main<Tin, 0, 8, true>))
+                 : (wide ? reinterpret_cast<const void*>(k_main<Tin, 0, 32, false>)
+                         : reinterpret_cast<const void*>(k_main<Tin, 0, 8, false>));
+    }
+    if (sm > 110 * 1024) return false;
+    const int occ = occupancy(fn, sm);
+    if (occ < 1) return false;
+    Params q = p;
+    void* args[] = {&q};
+    return cudaLaunchCooperativeKernel(fn, dim3(occ * sms), dim3(256), args, sm, st) == cudaSuccess;
+}
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
     return x < y + nb && y < x + na;
@@ -1555,6 +2053,7 @@ extern "C" rnnt_status_t rnnt_loss_fused_staged(
     // smallest subnormal of the output type, so every element rounds to zero.
     const float zero_at = dt == RNNT_F16 ? -25.5f : -151.0f;
     p.skip2 = zero_at - log2f(p.scale);
+    p.lscale = log2f(p.scale);
     p.fused = fused_log_softmax ? 1 : 0;
     p.red = reduction;
     p.stage_bytes = (int)(((size_t)V * es + 127) / 128 * 128);
@@ -1573,6 +2072,10 @@ extern "C" rnnt_status_t rnnt_loss_fused_staged(
     p.alpha = reinterpret_cast<int2*>(w + L.alpha);
     p.beta = reinterpret_cast<int2*>(w + L.beta);
     p.info = reinterpret_cast<float4*>(w + L.info);
+    p.rtasks = reinterpret_cast<int32_t*>(w + L.rtasks);
+    p.rdone = reinterpret_cast<int32_t*>(w + L.rdone);
+    p.dpdone = reinterpret_cast<int32_t*>(w + L.dpdone);
+    p.tasks = reinterpret_cast<int4*>(w + L.tasks);
 
     const size_t dp_smem = dp_smem_for(targets_stride);
     if (dev >= 0 && dev < 64 && g_dp_smem_set[dev] < (int)dp_smem) {
@@ -1589,6 +2092,16 @@ extern "C" rnnt_status_t rnnt_loss_fused_staged(
     mark(0);
     k_prepare<<<1, 1024, 0, st>>>(p);
     mark(1);
+    if (grad) {
+        const bool done = dt == RNNT_F32 ? launch_persistent<float>(p, st, sms, dev)
+                                         : launch_persistent<__half>(p, st, sms, dev);
+        if (done) {
+            for (int i = 2; i <= 5; ++i) mark(i);
+            k_finalize<<<1, 256, 0, st>>>(p);
+            mark(6);
+            return cudaGetLastError() == cudaSuccess ? RNNT_OK : RNNT_LAUNCH_FAILED;
+        }
+    }
     if (dt == RNNT_F32) launch_rows<float>(p, st, sms);
     else launch_rows<__half>(p, st, sms);
     mark(2);

@@ -241,3 +241,34 @@ def test_autograd_backward_scales(red):
     else:
         want *= float(w)
     assert_grad_close(to_np(x.grad), want, "f32")
+
+
+# ------------------------------------------------------------------ schedules
+# The library runs a call either as one persistent cooperative kernel (row,
+# DP and gradient tasks scheduled on the device) or, for shapes that kernel
+# does not cover, as one launch per stage.  RNNT_GB300_SCHEDULE=kernels forces
+# the latter; both must agree bit for bit and with the oracle.
+SCHED_CASES = [
+    dict(B=5, V=512, dtype="f16", fused=True, blank=-1, reduction="sum", clamp=-1.0),
+    dict(B=4, V=264, dtype="f32", fused=True, blank=0, reduction="mean", clamp=0.3),
+    dict(B=6, V=1024, dtype="f16", fused=True, blank=7, reduction="none", clamp=-1.0),
+    dict(B=5, V=512, dtype="f16", fused=False, blank=-1, reduction="mean", clamp=0.5),
+    dict(B=3, V=80, dtype="f32", fused=False, blank=2, reduction="sum", clamp=-1.0),
+]
+
+
+@pytest.mark.parametrize("case", range(len(SCHED_CASES)))
+def test_persistent_and_staged_schedules_agree(case, monkeypatch):
+    kw = dict(SCHED_CASES[case])
+    rng = np.random.default_rng(40 + case)
+    B = kw.pop("B")
+    T = rng.integers(1, 90, size=B)
+    U = rng.integers(0, 70, size=B)
+    wl = make(B, T, U, kw.pop("V"), sigma=1.3, seed=case, **kw)
+    monkeypatch.setenv("RNNT_GB300_SCHEDULE", "kernels")
+    ref_gpu = gpu_run(wl)
+    monkeypatch.delenv("RNNT_GB300_SCHEDULE")
+    got = gpu_run(wl)
+    for a, b in zip(ref_gpu, got):
+        assert torch.equal(a, b)
+    full_compare(wl)
