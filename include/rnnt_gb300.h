@@ -160,6 +160,19 @@ rnnt_status_t rnnt_grad_scale(void *grad, rnnt_dtype_t dt, int64_t rows, int32_t
                               const void *workspace, size_t workspace_bytes,
                               const float *factors, int32_t per_sample, rnnt_stream_t stream);
 
+/*
+ * rnnt_set_trace -- task tracing of the persistent kernel (a debugging aid;
+ * process-wide setting, not thread-safe).  While a buffer is set, every
+ * rnnt_loss_fused call that runs as one persistent kernel writes, for task t
+ * (t < bytes/16), the record int4 {kind | sample << 2, SM id, start ns,
+ * end ns} at index t (kind 0: row chunk, 1: DP, 2: gradient chunk);
+ * times are relative to the start of the call's first kernel.  Task order:
+ * for each sample (longest DP first) its row chunks and its DP task, then
+ * every gradient chunk.  device_buffer must be 16-byte aligned device memory
+ * that outlives the calls; NULL (or bytes < 16) turns tracing off.
+ */
+rnnt_status_t rnnt_set_trace(void *device_buffer, size_t bytes);
+
 /* Static English description of a status code. */
 const char *rnnt_status_string(rnnt_status_t status);
 

@@ -20,7 +20,7 @@ MAX_TARGET_LENGTH = 1023
 
 # Every symbol include/rnnt_gb300.h declares.
 EXPORTS = ("rnnt_workspace_size", "rnnt_loss_fused", "rnnt_loss_fused_staged", "rnnt_grad_scale",
-           "rnnt_status_string", "rnnt_abi_version")
+           "rnnt_set_trace", "rnnt_status_string", "rnnt_abi_version")
 
 _lib = None
 
@@ -51,6 +51,8 @@ def load() -> ctypes.CDLL:
     lib.rnnt_loss_fused_staged.restype = i32
     lib.rnnt_grad_scale.argtypes = [P, i32, i64, i32, i32, P, sz, P, i32, P]
     lib.rnnt_grad_scale.restype = i32
+    lib.rnnt_set_trace.argtypes = [P, sz]
+    lib.rnnt_set_trace.restype = i32
     lib.rnnt_status_string.argtypes = [i32]
     lib.rnnt_status_string.restype = ctypes.c_char_p
     lib.rnnt_abi_version.argtypes = []
@@ -102,3 +104,7 @@ def rnnt_grad_scale(grad, dt, rows, V, B, workspace, workspace_bytes, factors, p
                     stream) -> int:
     return int(load().rnnt_grad_scale(grad, dt, rows, V, B, workspace, workspace_bytes, factors,
                                       int(per_sample), stream))
+
+
+def rnnt_set_trace(buffer, nbytes) -> int:
+    return int(load().rnnt_set_trace(buffer, nbytes))

@@ -143,6 +143,8 @@ struct Params {
     int32_t* rdone;   // finished row tasks per sample
     int32_t* dpdone;  // DP finished flag per sample
     int4* tasks;      // {kind | sample << 2, first row in sample, rows, 0}
+    int4* trace;      // optional per-task trace records (see rnnt_set_trace), or null
+    int64_t trace_cap;
 };
 
 // ---------------------------------------------------------------- helpers
@@ -398,6 +400,17 @@ struct WarpRows {
     }
 };
 
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ int smid() {
+    int v;
+    asm volatile("mov.u32 %0, %%smid;\n" : "=r"(v));
+    return v;
+}
+
 // ---------------------------------------------------------------- k_prepare
 enum : int { TASK_ROW = 0, TASK_DP = 1, TASK_GRAD = 2 };
 
@@ -435,7 +448,11 @@ __global__ void __launch_bounds__(1024) k_prepare(Params p) {
     __shared__ int64_t carry;
     __shared__ int errs;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    if (tid == 0) { carry = 0; errs = 0; }
+    if (tid == 0) {
+        carry = 0;
+        errs = 0;
+        *reinterpret_cast<uint64_t*>(p.err + 4) = global_ns();   // trace origin
+    }
     __syncthreads();
     for (int base = 0; base < p.B; base += blockDim.x) {
         const int b = base + tid;
@@ -1673,11 +1690,19 @@ __device__ __noinline__ void dp_task(const Params& p, int b, int4* smem, float2*
     else dp_run<8>(p, c, smem, xch);
 }
 
+// Trace record of task t: {kind | sample << 2, sm, start, end}, times in ns
+// since k_prepare started (err[4..5] hold that origin).
+__device__ __forceinline__ void trace_task(const Params& p, int t, int code, uint64_t t_start) {
+    if (t >= p.trace_cap) return;
+    const uint64_t origin = *reinterpret_cast<const uint64_t*>(p.err + 4);
+    p.trace[t] = make_int4(code, smid(), (int)(t_start - origin), (int)(global_ns() - origin));
+}
+
 // NV > 0: log-softmax in kernel, rows staged by TMA (NV vectors per lane).
 // NV == 0: log-softmax off, rows gathered (2 elements) and gradients written
 // with G lanes per row (VEC: 16-byte rows).
 template <typename Tin, int NV, int G, bool VEC>
-__global__ void __launch_bounds__(256, 2) k_main(Params p) {
+__global__ void __launch_bounds__(256, 3) k_main(Params p) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ uint64_t bars_all[8 * kStages];
     __shared__ float4 s_info[kTaskRows];
@@ -1708,6 +1733,7 @@ __global__ void __launch_bounds__(256, 2) k_main(Params p) {
         if (t >= ntasks || !go) break;
         const int4 tk = p.tasks[t];
         const int kind = tk.x & 3, b = tk.x >> 2, n = tk.z;
+        const uint64_t t_start = (p.trace && tid == 0) ? global_ns() : 0;
         const int64_t r0 = __ldg(p.off + b) + tk.y;
         if (NV > 0 && kind != TASK_DP) fence_proxy_async();   // smem may have been a DP ring
         if (kind == TASK_ROW) {
@@ -1723,6 +1749,7 @@ __global__ void __launch_bounds__(256, 2) k_main(Params p) {
             __threadfence();
             __syncthreads();
             if (tid == 0) atomicAdd(&p.rdone[b], 1);
+            if (p.trace && tid == 0) trace_task(p, t, tk.x, t_start);
         } else if (kind == TASK_DP) {
             if (tid == 0) s_go = wait_at_least(&p.rdone[b], __ldg(p.rtasks + b), p.err);
             __syncthreads();
@@ -1733,6 +1760,7 @@ __global__ void __launch_bounds__(256, 2) k_main(Params p) {
             __threadfence();
             __syncthreads();
             if (tid == 0) atomicExch(&p.dpdone[b], 1);
+            if (p.trace && tid == 0) trace_task(p, t, tk.x, t_start);
         } else {
             if (tid == 0) s_go = wait_at_least(&p.dpdone[b], 1, p.err);
             __syncthreads();
@@ -1749,6 +1777,10 @@ __global__ void __launch_bounds__(256, 2) k_main(Params p) {
                                                           buf, bars, kk);
                 else
                     grad_batch_plain<Tin, G, VEC, false>(p, r0 + 32 * wid, nw, s_info + 32 * wid);
+            }
+            if (p.trace) {
+                __syncthreads();
+                if (tid == 0) trace_task(p, t, tk.x, t_start);
             }
         }
     }
@@ -1945,6 +1977,9 @@ void launch_grad(const Params& p, cudaStream_t st, int sms) {
 #undef GRADK
 }
 
+void* g_trace = nullptr;     // rnnt_set_trace: device buffer of int4 records
+size_t g_trace_bytes = 0;
+
 int g_coop[64];
 
 bool coop_supported(int dev) {
@@ -2076,6 +2111,8 @@ extern "C" rnnt_status_t rnnt_loss_fused_staged(
     p.rdone = reinterpret_cast<int32_t*>(w + L.rdone);
     p.dpdone = reinterpret_cast<int32_t*>(w + L.dpdone);
     p.tasks = reinterpret_cast<int4*>(w + L.tasks);
+    p.trace = static_cast<int4*>(g_trace);
+    p.trace_cap = (int64_t)(g_trace_bytes / sizeof(int4));
 
     const size_t dp_smem = dp_smem_for(targets_stride);
     if (dev >= 0 && dev < 64 && g_dp_smem_set[dev] < (int)dp_smem) {
@@ -2149,6 +2186,13 @@ extern "C" rnnt_status_t rnnt_grad_scale(void* grad, rnnt_dtype_t dt, int64_t ro
     if (dt == RNNT_F32) k_scale<float><<<grid, 256, 0, st>>>(grad, rows, V, B, off, factors, per_sample);
     else k_scale<__half><<<grid, 256, 0, st>>>(grad, rows, V, B, off, factors, per_sample);
     return cudaGetLastError() == cudaSuccess ? RNNT_OK : RNNT_LAUNCH_FAILED;
+}
+
+extern "C" rnnt_status_t rnnt_set_trace(void* device_buffer, size_t bytes) {
+    if (device_buffer && ((uintptr_t)device_buffer & 15)) return RNNT_INVALID_VALUE;
+    g_trace = bytes >= sizeof(int4) ? device_buffer : nullptr;
+    g_trace_bytes = g_trace ? bytes : 0;
+    return RNNT_OK;
 }
 
 extern "C" const char* rnnt_status_string(rnnt_status_t s) {
