@@ -66,7 +66,7 @@ constexpr int kTaskRows = 256;   // rows per row / gradient task of the persiste
 
 struct Layout {
     size_t err, off, order, lossa, lossb, pm, pe, lse2, edge, alpha, beta, info;
-    size_t rtasks, rdone, dpdone, tasks, total;
+    size_t rtasks, rdone, dpdone, dpclaim, tasks, total;
     int64_t max_tasks;
 };
 
@@ -98,6 +98,7 @@ __host__ __device__ inline Layout ws_layout(int B, int64_t rows) {
     L.rtasks = p; p = al256(p + sizeof(int32_t) * (size_t)B);
     L.rdone = p;  p = al256(p + sizeof(int32_t) * (size_t)B);
     L.dpdone = p; p = al256(p + sizeof(int32_t) * (size_t)B);
+    L.dpclaim = p; p = al256(p + sizeof(int32_t) * (size_t)B);
     L.tasks = p;  p = al256(p + sizeof(int4) * (size_t)L.max_tasks);
     L.total = p;
     return L;
@@ -142,6 +143,8 @@ struct Params {
     int32_t* rtasks;  // row tasks per sample
     int32_t* rdone;   // finished row tasks per sample
     int32_t* dpdone;  // DP finished flag per sample
+    int32_t* dpclaim; // DP started (claimed) flag per sample
+    int n_dp_sms;     // SMs whose CTAs only run DP tasks
     int4* tasks;      // {kind | sample << 2, first row in sample, rows, 0}
     int4* trace;      // optional per-task trace records (see rnnt_set_trace), or null
     int64_t trace_cap;
@@ -515,9 +518,9 @@ __global__ void __launch_bounds__(1024) k_prepare(Params p) {
         p.order[rank] = b;
     }
     __syncthreads();
-    // Task list of the persistent kernel, in queue order: for each sample in
-    // DP order its row chunks then its DP task; then all gradient chunks in
-    // the same order.  Every task waits only on tasks queued before it.
+    // Task queue of the persistent kernel: the row chunks of every sample in DP
+    // order, then the gradient chunks in the same order.  DP tasks are taken by
+    // ticket (err[3]) in the same sample order.
     if (errs == 0) {
         if (tid == 0) carry = 0;
         __syncthreads();
@@ -533,21 +536,20 @@ __global__ void __launch_bounds__(1024) k_prepare(Params p) {
                 p.rtasks[b] = nch;
                 p.rdone[b] = 0;
                 p.dpdone[b] = 0;
+                p.dpclaim[b] = 0;
             }
             const int64_t before = block_scan_excl(nch, wsum, carry);   // row tasks before i
             if (i < p.B) {
-                const int64_t q = before + i;                          // + one DP task per sample
                 for (int k = 0; k < nch; ++k) {
                     const int r = k * kTaskRows;
-                    p.tasks[q + k] = make_int4(TASK_ROW | (b << 2), r,
-                                               (int)min((int64_t)kTaskRows, nrows - r), 0);
+                    p.tasks[before + k] = make_int4(TASK_ROW | (b << 2), r,
+                                                    (int)min((int64_t)kTaskRows, nrows - r), 0);
                 }
-                p.tasks[q + nch] = make_int4(TASK_DP | (b << 2), 0, 0, 0);
             }
             tot = carry;
         }
-        // Gradient chunks after every row/DP task.
-        const int64_t g0 = tot + p.B;
+        // Gradient chunks after every row chunk.
+        const int64_t g0 = tot;
         if (tid == 0) carry = 0;
         __syncthreads();
         for (int base = 0; base < p.B; base += blockDim.x) {
@@ -570,6 +572,7 @@ __global__ void __launch_bounds__(1024) k_prepare(Params p) {
         if (tid == 0) {
             p.err[1] = 0;                          // next task
             p.err[2] = (int)(g0 + tot);            // task count
+            p.err[3] = 0;                          // next DP ticket
         }
     }
     __syncthreads();
@@ -1698,11 +1701,31 @@ __device__ __forceinline__ void trace_task(const Params& p, int t, int code, uin
     p.trace[t] = make_int4(code, smid(), (int)(t_start - origin), (int)(global_ns() - origin));
 }
 
+// Runs DP(b) on the calling CTA if nobody has claimed it yet (CTA-uniform).
+__device__ __forceinline__ void run_dp_and_signal(const Params& p, int b, int4* smem, float2* xch,
+                                                  int trace_slot, int tid) {
+    const uint64_t t0 = (p.trace && tid == 0) ? global_ns() : 0;
+    dp_task(p, b, smem, xch);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        atomicExch(&p.dpdone[b], 1);
+        if (p.trace) trace_task(p, trace_slot, TASK_DP | (b << 2), t0);
+    }
+}
+
 // NV > 0: log-softmax in kernel, rows staged by TMA (NV vectors per lane).
 // NV == 0: log-softmax off, rows gathered (2 elements) and gradients written
 // with G lanes per row (VEC: 16-byte rows).
+//
+// Roles.  CTAs on the first n_dp_sms SMs (by %smid) are DP workers: they take
+// samples by ticket in DP order, wait for the sample's row chunks and run its
+// recursions, undisturbed by the streaming warps that would otherwise share
+// their SM.  All other CTAs stream: row chunks, then gradient chunks.  A
+// gradient chunk whose DP nobody has started yet runs that DP itself, so
+// progress never depends on where CTAs land.
 template <typename Tin, int NV, int G, bool VEC>
-__global__ void __launch_bounds__(256, 3) k_main(Params p) {
+__global__ void __launch_bounds__(256, 2) k_main(Params p) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ uint64_t bars_all[8 * kStages];
     __shared__ float4 s_info[kTaskRows];
@@ -1710,6 +1733,44 @@ __global__ void __launch_bounds__(256, 3) k_main(Params p) {
     __shared__ int s_task, s_go;
     if (*p.err & (ERR_LENGTH | ERR_ROWS | ERR_TARGET)) return;   // uniform: set before launch
     const int tid = threadIdx.x, wid = tid >> 5, wl = tid & 31;
+    int4* dpsmem = reinterpret_cast<int4*>(smem_raw);
+    const int ntasks = p.err[2];
+
+    if (smid() < p.n_dp_sms) {
+        for (;;) {
+            if (tid == 0) {
+                const int i = atomicAdd(&p.err[3], 1);
+                int go = 0;
+                if (i < p.B) {
+                    const int b = __ldg(p.order + i);
+                    s_task = b;
+                    // Wait for the sample's rows unless a streaming CTA took the DP.
+                    for (int k = 0; k < kSpinLimit; ++k) {
+                        if (ld_acquire(&p.dpclaim[b])) break;
+                        if (ld_acquire(&p.rdone[b]) >= __ldg(p.rtasks + b)) {
+                            go = atomicCAS(&p.dpclaim[b], 0, 1) == 0;
+                            break;
+                        }
+                        if (ld_acquire(p.err) & ERR_TIMEOUT) break;
+                        __nanosleep(256);
+                        if (k == kSpinLimit - 1) atomicOr(p.err, ERR_TIMEOUT);
+                    }
+                    go = go ? 1 : 2;   // 1: run it, 2: skip this sample
+                }
+                s_go = go;
+            }
+            __syncthreads();
+            const int go = s_go, b = s_task;
+            __syncthreads();
+            if (go == 0) break;
+            if (go == 1) {
+                __threadfence();
+                run_dp_and_signal(p, b, dpsmem, xch, ntasks + b, tid);
+            }
+        }
+        return;
+    }
+
     unsigned char* buf = smem_raw + (size_t)wid * kStages * p.stage_bytes;
     uint64_t* bars = bars_all + wid * kStages;
     if (NV > 0 && wl == 0) {
@@ -1718,7 +1779,6 @@ __global__ void __launch_bounds__(256, 3) k_main(Params p) {
         fence_mbar_init();
     }
     uint32_t kk = 0;   // this warp's TMA ring position
-    const int ntasks = p.err[2];
     for (;;) {
         // Every branch below is taken by the whole CTA: decisions that depend on
         // global state are made by thread 0 and broadcast through shared memory.
@@ -1733,10 +1793,10 @@ __global__ void __launch_bounds__(256, 3) k_main(Params p) {
         if (t >= ntasks || !go) break;
         const int4 tk = p.tasks[t];
         const int kind = tk.x & 3, b = tk.x >> 2, n = tk.z;
-        const uint64_t t_start = (p.trace && tid == 0) ? global_ns() : 0;
         const int64_t r0 = __ldg(p.off + b) + tk.y;
-        if (NV > 0 && kind != TASK_DP) fence_proxy_async();   // smem may have been a DP ring
+        const uint64_t t_start = (p.trace && tid == 0) ? global_ns() : 0;
         if (kind == TASK_ROW) {
+            if (NV > 0) fence_proxy_async();   // smem may have been a DP ring
             const int64_t rw = r0 + 32 * wid;
             const int nw = min(32, n - 32 * wid);
             if (nw > 0) {
@@ -1750,38 +1810,50 @@ __global__ void __launch_bounds__(256, 3) k_main(Params p) {
             __syncthreads();
             if (tid == 0) atomicAdd(&p.rdone[b], 1);
             if (p.trace && tid == 0) trace_task(p, t, tk.x, t_start);
-        } else if (kind == TASK_DP) {
-            if (tid == 0) s_go = wait_at_least(&p.rdone[b], __ldg(p.rtasks + b), p.err);
-            __syncthreads();
-            const bool ready = s_go;
-            __syncthreads();
-            __threadfence();
-            if (ready) dp_task(p, b, reinterpret_cast<int4*>(smem_raw), xch);
-            __threadfence();
-            __syncthreads();
-            if (tid == 0) atomicExch(&p.dpdone[b], 1);
-            if (p.trace && tid == 0) trace_task(p, t, tk.x, t_start);
-        } else {
-            if (tid == 0) s_go = wait_at_least(&p.dpdone[b], 1, p.err);
-            __syncthreads();
-            const bool ready = s_go;
-            __syncthreads();
-            __threadfence();
-            if (!ready) continue;   // uniform; the next iteration sees the error and stops
-            if (tid < n) s_info[tid] = combine_row(p, r0 + tid, b);
-            __syncthreads();
-            const int nw = min(32, n - 32 * wid);
-            if (nw > 0) {
-                if (NV > 0)
-                    grad_batch_tma<Tin, (NV > 0 ? NV : 1)>(p, r0 + 32 * wid, nw, s_info + 32 * wid,
-                                                          buf, bars, kk);
-                else
-                    grad_batch_plain<Tin, G, VEC, false>(p, r0 + 32 * wid, nw, s_info + 32 * wid);
+            continue;
+        }
+        // Gradient chunk: its sample's DP must be done (or be run here).
+        if (tid == 0) {
+            int mode = 0;   // 0: error, 1: DP done, 2: run the DP here
+            for (int k = 0; k < kSpinLimit; ++k) {
+                if (ld_acquire(&p.dpdone[b])) {
+                    mode = 1;
+                    break;
+                }
+                if (ld_acquire(&p.rdone[b]) >= __ldg(p.rtasks + b) &&
+                    ld_acquire(&p.dpclaim[b]) == 0 && atomicCAS(&p.dpclaim[b], 0, 1) == 0) {
+                    mode = 2;
+                    break;
+                }
+                if (ld_acquire(p.err) & ERR_TIMEOUT) break;
+                __nanosleep(128);
+                if (k == kSpinLimit - 1) atomicOr(p.err, ERR_TIMEOUT);
             }
-            if (p.trace) {
-                __syncthreads();
-                if (tid == 0) trace_task(p, t, tk.x, t_start);
-            }
+            s_go = mode;
+        }
+        __syncthreads();
+        const int mode = s_go;
+        __syncthreads();
+        __threadfence();
+        if (mode == 0) continue;   // uniform; the next iteration sees the error and stops
+        if (mode == 2) {
+            run_dp_and_signal(p, b, dpsmem, xch, ntasks + b, tid);
+            __syncthreads();
+        }
+        if (NV > 0) fence_proxy_async();   // smem may have been a DP ring
+        if (tid < n) s_info[tid] = combine_row(p, r0 + tid, b);
+        __syncthreads();
+        const int nw = min(32, n - 32 * wid);
+        if (nw > 0) {
+            if (NV > 0)
+                grad_batch_tma<Tin, (NV > 0 ? NV : 1)>(p, r0 + 32 * wid, nw, s_info + 32 * wid,
+                                                      buf, bars, kk);
+            else
+                grad_batch_plain<Tin, G, VEC, false>(p, r0 + 32 * wid, nw, s_info + 32 * wid);
+        }
+        if (p.trace) {
+            __syncthreads();
+            if (tid == 0) trace_task(p, t, tk.x, t_start);
         }
     }
 }
@@ -2022,6 +2094,7 @@ bool launch_persistent(const Params& p, cudaStream_t st, int sms, int dev) {
     const int occ = occupancy(fn, sm);
     if (occ < 1) return false;
     Params q = p;
+    q.n_dp_sms = std::min(std::min(8, (p.B + 1) / 2), sms / 8);
     void* args[] = {&q};
     return cudaLaunchCooperativeKernel(fn, dim3(occ * sms), dim3(256), args, sm, st) == cudaSuccess;
 }
@@ -2110,6 +2183,7 @@ extern "C" rnnt_status_t rnnt_loss_fused_staged(
     p.rtasks = reinterpret_cast<int32_t*>(w + L.rtasks);
     p.rdone = reinterpret_cast<int32_t*>(w + L.rdone);
     p.dpdone = reinterpret_cast<int32_t*>(w + L.dpdone);
+    p.dpclaim = reinterpret_cast<int32_t*>(w + L.dpclaim);
     p.tasks = reinterpret_cast<int4*>(w + L.tasks);
     p.trace = static_cast<int4*>(g_trace);
     p.trace_cap = (int64_t)(g_trace_bytes / sizeof(int4));
