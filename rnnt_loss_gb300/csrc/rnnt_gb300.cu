@@ -51,6 +51,9 @@ constexpr float kSqrt2 = 1.4142135381698608f;
 constexpr double kLn2d = 0.69314718055994530942;
 constexpr int kMaxW = RNNT_MAX_TARGET_LENGTH + 1;
 constexpr int kZeroExp = -(1 << 29);               // exponent of an extended-range zero
+// Transition records store exponents + kEdgeBias, so an all-zero record is a
+// zero probability (m = 0, e = kZeroExp); the DP's zero-filled loads rely on it.
+constexpr int kEdgeBias = 1 << 29;
 
 enum : int {
     ERR_LENGTH = 1,
@@ -613,7 +616,7 @@ __device__ __forceinline__ void row_finish(const Params& p, int64_t r, float M, 
     if (!(t == T - 1 && u < U)) xf_prob(hb, M, s, bm, be);
     if (u < U) xf_prob(hy, M, s, ym, ye);
     p.edge[o + node_index(t, u, T, U)] =
-        make_int4(__float_as_int(bm), be, __float_as_int(ym), ye);
+        make_int4(__float_as_int(bm), be + kEdgeBias, __float_as_int(ym), ye + kEdgeBias);
 }
 
 // Group results (same in every lane of group g) for row it*NG+g of the batch
@@ -864,26 +867,30 @@ __global__ void __launch_bounds__(256) k_row_gather(Params p) {
 }
 
 // ---------------------------------------------------------------- DP
-// One CTA of 8 warps per sample: warps 0-3 run the forward recursion, warps
-// 4-7 the backward one.  The W = U+1 lattice columns are split into NWD <= 4
-// contiguous blocks of 32*J columns, one per warp; inside a warp lane l holds
-// columns base + 32*j + l.  The neighbouring column comes from the next lane
-// by shuffle, or, at a block edge, from the neighbouring warp through shared
-// memory with one named barrier per anti-diagonal (barrier 1: alpha, 2: beta).
-// Each warp prefetches its nodes' transition records with cp.async into a
-// ring of R anti-diagonals (prefetch distance R-2).
+// One CTA per sample (8 warps).  Per direction, nwd = ceil(W/128) compute
+// warps (W = U+1 lattice columns, at most 4) each own a contiguous block of
+// 32*J columns, J = ceil(W/(32*nwd)) <= 8; lane l holds columns
+// u0 + 32*j + l.  The neighbouring column comes from the next lane by
+// shuffle, or at a block edge from the neighbouring warp through shared
+// memory with one named barrier per anti-diagonal (1: alpha, 2: beta).
+// Warps 0..3 run alpha, 4..7 beta.  Each compute warp prefetches its nodes'
+// transition records with zero-filling cp.async into a ring of R diagonals
+// (prefetch distance R-2); the loop body is branch-free (predicated copies
+// and stores, 32-bit incremental diagonal bases).
 template <int J> struct Ring;
 template <> struct Ring<1> { static constexpr int R = 16; };
 template <> struct Ring<2> { static constexpr int R = 12; };
 template <> struct Ring<3> { static constexpr int R = 10; };
-template <> struct Ring<4> { static constexpr int R = 8; };
+template <> struct Ring<4> { static constexpr int R = 10; };
 template <> struct Ring<6> { static constexpr int R = 6; };
 template <> struct Ring<8> { static constexpr int R = 6; };
-constexpr int kDpWarps = 4;   // warps per direction
+constexpr int kDpWarps = 4;   // compute warps per direction, at most
 
-__device__ __forceinline__ void cp16(void* smem, const void* gmem) {
+__device__ __forceinline__ void cp16z(void* smem, const void* gmem, bool valid) {
     const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem) : "memory");
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(sa), "l"(gmem),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
@@ -897,114 +904,105 @@ struct Samp {
     int64_t off;
 };
 
-__device__ __forceinline__ bool on_lattice(const Samp& c, int d, int u) {
-    return u <= c.U && (unsigned)(d - u) < (unsigned)c.T;
-}
-
-// Walks the packed start N(d) of anti-diagonal d one step at a time:
-// N(d+1) = N(d) + (nodes on d), nodes on d = min(T-1, d) - max(0, d-U) + 1.
-struct DiagCursor {
-    int d;
-    int64_t n;
-    __device__ __forceinline__ static int64_t count(const Samp& c, int d) {
-        return (d < 0 || d >= c.D) ? 0 : (int64_t)(min(c.T - 1, d) - max(0, d - c.U) + 1);
+// Packed index (relative to the sample) of the node in column u on diagonal d
+// is base - u with base = N(d) - max(0, d-U) + d; N(d) = nodes before d.
+struct DBase {
+    int d, base;
+    __device__ __forceinline__ static int count(const Samp& c, int d) {
+        return (d < 0 || d >= c.D) ? 0 : min(c.T - 1, d) - max(0, d - c.U) + 1;
     }
     __device__ __forceinline__ void init(const Samp& c, int d0) {
         d = d0;
-        n = (d0 <= 0) ? 0 : diag_start(min(d0, c.D), c.T, c.W);
+        base = (int)(diag_start(d0, c.T, c.W) - max(0, d0 - c.U) + d0);
     }
-    __device__ __forceinline__ void next(const Samp& c) { n += count(c, d); ++d; }
-    __device__ __forceinline__ void prev(const Samp& c) { --d; n -= count(c, d); }
-    // Global packed index of the node in column u is base() - u.
-    __device__ __forceinline__ int64_t base(const Samp& c) const {
-        return c.off + n - max(0, d - c.U) + d;
+    __device__ __forceinline__ void next(const Samp& c) {
+        base += count(c, d) + 1 - (d + 1 > c.U ? 1 : 0);
+        ++d;
     }
-};
-
-// Columns of one warp of a direction.
-struct Cols {
-    int u0;    // first column of this warp's block
-    int w;     // warp index within the direction
-    int nwd;   // warps of the direction
-    __device__ __forceinline__ int col(int j, int lane) const { return u0 + 32 * j + lane; }
+    __device__ __forceinline__ void prev(const Samp& c) {
+        base -= count(c, d - 1) + 1 - (d > c.U ? 1 : 0);
+        --d;
+    }
 };
 
 template <int J>
-__device__ __forceinline__ void ring_issue(const Params& p, const Samp& c, const Cols& cc,
-                                           int4* ring, const DiagCursor& q, int lane) {
+struct Lanes {
+    int u[J];        // this lane's columns
+    bool col_ok[J];  // column exists (u <= U)
+};
+
+template <int J>
+__device__ __forceinline__ void ring_issue(const Samp& c, const int4* edge_s, int4* ring,
+                                           const DBase& q, const Lanes<J>& L, int lane) {
     constexpr int R = Ring<J>::R;
-    const int d = q.d;
-    if (d >= 0 && d < c.D) {
-        int4* sl = ring + (d % R) * (J * 32);
-        const int64_t base = q.base(c);
+    if (q.d < 0 || q.d >= c.D) return;
+    int4* sl = ring + (q.d % R) * (J * 32) + lane;
 #pragma unroll
-        for (int j = 0; j < J; ++j) {
-            const int u = cc.col(j, lane);
-            if (on_lattice(c, d, u)) cp16(sl + j * 32 + lane, p.edge + (base - u));
-            else sl[j * 32 + lane] = make_int4(0, kZeroExp, 0, kZeroExp);
-        }
+    for (int j = 0; j < J; ++j) {
+        const bool ok = L.col_ok[j] && (unsigned)(q.d - L.u[j]) < (unsigned)c.T;
+        cp16z(sl + j * 32, edge_s + (ok ? q.base - L.u[j] : 0), ok);
     }
 }
 
 template <int J>
-__device__ __forceinline__ void store_diag(const Samp& c, const Cols& cc, int2* out,
-                                           const DiagCursor& q, const float* m, const int* e,
-                                           int lane) {
-    const int64_t base = q.base(c);
+__device__ __forceinline__ void store_diag(const Samp& c, int2* out_s, const DBase& q,
+                                           const Lanes<J>& L, const float* m, const int* e) {
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-        const int u = cc.col(j, lane);
-        if (on_lattice(c, q.d, u)) out[base - u] = make_int2(__float_as_int(m[j]), e[j]);
+        const bool ok = L.col_ok[j] && (unsigned)(q.d - L.u[j]) < (unsigned)c.T;
+        if (ok) out_s[q.base - L.u[j]] = make_int2(__float_as_int(m[j]), e[j]);
     }
 }
 
 // Forward variable: alpha(t,u) = alpha(t-1,u) p_blank(t-1,u) + alpha(t,u-1) p_label(t,u-1).
 // xch: [2][kDpWarps] (m, e) of the label arc leaving each warp's last column.
 template <int J>
-__device__ void dp_alpha(const Params& p, const Samp& c, const Cols& cc, int4* ring,
+__device__ void dp_alpha(const Params& p, const Samp& c, int u0, int w, int nwd, int4* ring,
                          float2* xch) {
     constexpr int R = Ring<J>::R, PF = R - 2;
-    const int lane = threadIdx.x & 31;
-    const int nthreads = cc.nwd * 32;
+    const int lane = threadIdx.x & 31, nthreads = nwd * 32;
+    const int4* edge_s = p.edge + c.off;
+    int2* out_s = p.alpha + c.off;
+    Lanes<J> L;
     float am[J];
     int ae[J];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-        const bool origin = cc.col(j, lane) == 0;
-        am[j] = origin ? 1.0f : 0.0f;
-        ae[j] = origin ? 0 : kZeroExp;
+        L.u[j] = u0 + 32 * j + lane;
+        L.col_ok[j] = L.u[j] <= c.U;
+        am[j] = L.u[j] == 0 ? 1.0f : 0.0f;
+        ae[j] = L.u[j] == 0 ? 0 : kZeroExp;
     }
-    DiagCursor qs, qi;   // store cursor (diagonal d), issue cursor (diagonal d + PF)
+    DBase qs, qi;
     qs.init(c, 0);
-    store_diag<J>(c, cc, p.alpha, qs, am, ae, lane);
+    store_diag<J>(c, out_s, qs, L, am, ae);
     qi.init(c, 0);
     for (int k = 0; k <= PF; ++k) {
-        ring_issue<J>(p, c, cc, ring, qi, lane);
+        ring_issue<J>(c, edge_s, ring, qi, L, lane);
         cp_commit();
         qi.next(c);
     }
     for (int d = 1; d < c.D; ++d) {
-        ring_issue<J>(p, c, cc, ring, qi, lane);
+        ring_issue<J>(c, edge_s, ring, qi, L, lane);
         cp_commit();
         qi.next(c);
         cp_wait<PF + 1>();
-        const int4* sp = ring + ((d - 1) % R) * (J * 32);
+        const int4* sp = ring + ((d - 1) % R) * (J * 32) + lane;
         float bm[J], ym[J];
         int be[J], ye[J];
 #pragma unroll
         for (int j = 0; j < J; ++j) {
-            const int4 ed = sp[j * 32 + lane];
-            xf_mul(am[j], ae[j], __int_as_float(ed.x), ed.y, bm[j], be[j]);
-            xf_mul(am[j], ae[j], __int_as_float(ed.z), ed.w, ym[j], ye[j]);
+            const int4 ed = sp[j * 32];
+            xf_mul(am[j], ae[j], __int_as_float(ed.x), ed.y - kEdgeBias, bm[j], be[j]);
+            xf_mul(am[j], ae[j], __int_as_float(ed.z), ed.w - kEdgeBias, ym[j], ye[j]);
         }
         float edge_m = 0.0f;
         int edge_e = kZeroExp;
-        if (cc.nwd > 1) {
-            if (lane == 31 && cc.w + 1 < cc.nwd)
-                xch[(d & 1) * kDpWarps + cc.w] = make_float2(ym[J - 1], __int_as_float(ye[J - 1]));
+        if (nwd > 1) {
+            if (lane == 31) xch[(d & 1) * kDpWarps + w] = make_float2(ym[J - 1], __int_as_float(ye[J - 1]));
             named_barrier(1, nthreads);
-            if (lane == 0 && cc.w > 0) {
-                const float2 v = xch[(d & 1) * kDpWarps + cc.w - 1];
+            const float2 v = xch[(d & 1) * kDpWarps + max(w - 1, 0)];
+            if (w > 0) {
                 edge_m = v.x;
                 edge_e = __float_as_int(v.y);
             }
@@ -1023,19 +1021,18 @@ __device__ void dp_alpha(const Params& p, const Samp& c, const Cols& cc, int4* r
             xf_add(bm[j], be[j], nm, ne, am[j], ae[j]);
         }
         qs.next(c);
-        store_diag<J>(c, cc, p.alpha, qs, am, ae, lane);
+        store_diag<J>(c, out_s, qs, L, am, ae);
     }
     // P(y|x) = alpha(T-1,U) p_blank(T-1,U): the terminal blank.
     cp_wait<0>();
-    const int e = c.D - 1;
-    const int4* sp = ring + (e % R) * (J * 32);
+    const int4* sp = ring + ((c.D - 1) % R) * (J * 32) + lane;
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-        if (cc.col(j, lane) == c.U) {
-            const int4 ed = sp[j * 32 + lane];
+        if (L.u[j] == c.U) {
+            const int4 ed = sp[j * 32];
             float m;
             int x;
-            xf_mul(am[j], ae[j], __int_as_float(ed.x), ed.y, m, x);
+            xf_mul(am[j], ae[j], __int_as_float(ed.x), ed.y - kEdgeBias, m, x);
             xf_norm(m, x);
             p.pm[c.b] = m;
             p.pe[c.b] = x;
@@ -1050,41 +1047,43 @@ __device__ void dp_alpha(const Params& p, const Samp& c, const Cols& cc, int4* r
 // started from a virtual node after the terminal blank with beta = 1.
 // xch: [2][kDpWarps] (m, e) of each warp's first column on the previous diagonal.
 template <int J>
-__device__ void dp_beta(const Params& p, const Samp& c, const Cols& cc, int4* ring,
+__device__ void dp_beta(const Params& p, const Samp& c, int u0, int w, int nwd, int4* ring,
                         float2* xch) {
     constexpr int R = Ring<J>::R, PF = R - 2;
-    const int lane = threadIdx.x & 31;
-    const int nthreads = cc.nwd * 32;
+    const int lane = threadIdx.x & 31, nthreads = nwd * 32;
+    const int4* edge_s = p.edge + c.off;
+    int2* out_s = p.beta + c.off;
+    Lanes<J> L;
     float vm[J];
     int ve[J];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-        const bool top = cc.col(j, lane) == c.U;
-        vm[j] = top ? 1.0f : 0.0f;
-        ve[j] = top ? 0 : kZeroExp;
+        L.u[j] = u0 + 32 * j + lane;
+        L.col_ok[j] = L.u[j] <= c.U;
+        vm[j] = L.u[j] == c.U ? 1.0f : 0.0f;
+        ve[j] = L.u[j] == c.U ? 0 : kZeroExp;
     }
-    DiagCursor qs, qi;   // store cursor (diagonal d), issue cursor (diagonal d - PF - 1)
+    DBase qs, qi;
     qi.init(c, c.D - 1);
     for (int k = 0; k <= PF; ++k) {
-        ring_issue<J>(p, c, cc, ring, qi, lane);
+        ring_issue<J>(c, edge_s, ring, qi, L, lane);
         cp_commit();
         qi.prev(c);
     }
     qs.init(c, c.D - 1);
     for (int d = c.D - 1; d >= 0; --d) {
-        ring_issue<J>(p, c, cc, ring, qi, lane);
+        ring_issue<J>(c, edge_s, ring, qi, L, lane);
         cp_commit();
         qi.prev(c);
         cp_wait<PF + 1>();
-        const int4* sd = ring + (d % R) * (J * 32);
+        const int4* sd = ring + (d % R) * (J * 32) + lane;
         float edge_m = 0.0f;
         int edge_e = kZeroExp;
-        if (cc.nwd > 1) {
-            if (lane == 0 && cc.w > 0)
-                xch[(d & 1) * kDpWarps + cc.w] = make_float2(vm[0], __int_as_float(ve[0]));
+        if (nwd > 1) {
+            if (lane == 0) xch[(d & 1) * kDpWarps + w] = make_float2(vm[0], __int_as_float(ve[0]));
             named_barrier(2, nthreads);
-            if (lane == 31 && cc.w + 1 < cc.nwd) {
-                const float2 v = xch[(d & 1) * kDpWarps + cc.w + 1];
+            const float2 v = xch[(d & 1) * kDpWarps + min(w + 1, nwd - 1)];
+            if (w + 1 < nwd) {
                 edge_m = v.x;
                 edge_e = __float_as_int(v.y);
             }
@@ -1098,49 +1097,49 @@ __device__ void dp_beta(const Params& p, const Samp& c, const Cols& cc, int4* ri
         }
 #pragma unroll
         for (int j = 0; j < J; ++j) {
-            const int4 ed = sd[j * 32 + lane];
+            const int4 ed = sd[j * 32];
             const float nm = (lane < 31) ? sm[j] : (j + 1 < J ? sm[j + 1] : edge_m);
             const int ne = (lane < 31) ? se[j] : (j + 1 < J ? se[j + 1] : edge_e);
             float bm, ym;
             int be, ye;
-            xf_mul(vm[j], ve[j], __int_as_float(ed.x), ed.y, bm, be);
-            xf_mul(nm, ne, __int_as_float(ed.z), ed.w, ym, ye);
+            xf_mul(vm[j], ve[j], __int_as_float(ed.x), ed.y - kEdgeBias, bm, be);
+            xf_mul(nm, ne, __int_as_float(ed.z), ed.w - kEdgeBias, ym, ye);
             xf_add(bm, be, ym, ye, vm[j], ve[j]);
         }
-        store_diag<J>(c, cc, p.beta, qs, vm, ve, lane);
+        store_diag<J>(c, out_s, qs, L, vm, ve);
         qs.prev(c);
     }
     cp_wait<0>();
-    if (cc.w == 0 && lane == 0) p.lossb[c.b] = -((double)ve[0] + log2((double)vm[0])) * kLn2d;
+    if (u0 == 0 && lane == 0) p.lossb[c.b] = -((double)ve[0] + log2((double)vm[0])) * kLn2d;
 }
 
-__device__ __forceinline__ int dp_warps(int W) { return min(kDpWarps, (W + 31) / 32); }
-__device__ __forceinline__ int dp_slots(int W) {
+__host__ __device__ inline int dp_warps(int W) { return min(kDpWarps, (W + 127) / 128); }
+__host__ __device__ inline int dp_slots(int W) {
     const int n = dp_warps(W);
     return (W + 32 * n - 1) / (32 * n);
+}
+__host__ __device__ inline int dp_jclass(int J) {
+    return J <= 1 ? 1 : J <= 2 ? 2 : J <= 3 ? 3 : J <= 4 ? 4 : J <= 6 ? 6 : 8;
+}
+__host__ __device__ inline int dp_ring_depth(int Jc) {
+    return Jc == 1 ? 16 : Jc == 2 ? 12 : Jc <= 4 ? 10 : 6;
 }
 
 template <int J>
 __device__ __forceinline__ void dp_run(const Params& p, const Samp& c, int4* smem, float2* xch) {
     const int wid = threadIdx.x >> 5;
     const int dir = wid / kDpWarps, w = wid % kDpWarps;
-    Cols cc;
-    cc.nwd = dp_warps(c.W);
-    cc.w = w;
-    cc.u0 = w * 32 * J;
-    if (w >= cc.nwd) return;
+    const int nwd = dp_warps(c.W);
+    if (w >= nwd) return;
     int4* ring = smem + (size_t)wid * Ring<J>::R * J * 32;
-    if (dir == 0) dp_alpha<J>(p, c, cc, ring, xch);
-    else dp_beta<J>(p, c, cc, ring, xch + 2 * kDpWarps);
+    if (dir == 0) dp_alpha<J>(p, c, w * 32 * J, w, nwd, ring, xch);
+    else dp_beta<J>(p, c, w * 32 * J, w, nwd, ring, xch + 2 * kDpWarps);
 }
 
-// Dynamic shared memory of k_dp for lattices up to W columns (8 rings).
+// Dynamic shared memory of the DP for lattices up to W columns (8 rings).
 __host__ __device__ inline size_t dp_smem_bytes(int W) {
-    const int n = W <= 32 ? 1 : (W <= 64 ? 2 : (W <= 96 ? 3 : 4));
-    const int J = (W + 32 * n - 1) / (32 * n);
-    const int Jc = J <= 1 ? 1 : J <= 2 ? 2 : J <= 3 ? 3 : J <= 4 ? 4 : J <= 6 ? 6 : 8;
-    const int R = Jc == 1 ? 16 : Jc == 2 ? 12 : Jc == 3 ? 10 : Jc == 4 ? 8 : 6;
-    return (size_t)2 * kDpWarps * R * Jc * 32 * sizeof(int4);
+    const int Jc = dp_jclass(dp_slots(W));
+    return (size_t)2 * kDpWarps * dp_ring_depth(Jc) * Jc * 32 * sizeof(int4);
 }
 
 __global__ void __launch_bounds__(256) k_dp(Params p) {
@@ -1154,12 +1153,12 @@ __global__ void __launch_bounds__(256) k_dp(Params p) {
     c.W = c.U + 1;
     c.D = c.T + c.U;
     c.off = p.off[c.b];
-    const int J = dp_slots(c.W);
-    if (J <= 1) dp_run<1>(p, c, smem, xch);
-    else if (J <= 2) dp_run<2>(p, c, smem, xch);
-    else if (J <= 3) dp_run<3>(p, c, smem, xch);
-    else if (J <= 4) dp_run<4>(p, c, smem, xch);
-    else if (J <= 6) dp_run<6>(p, c, smem, xch);
+    const int J = dp_jclass(dp_slots(c.W));
+    if (J == 1) dp_run<1>(p, c, smem, xch);
+    else if (J == 2) dp_run<2>(p, c, smem, xch);
+    else if (J == 3) dp_run<3>(p, c, smem, xch);
+    else if (J == 4) dp_run<4>(p, c, smem, xch);
+    else if (J == 6) dp_run<6>(p, c, smem, xch);
     else dp_run<8>(p, c, smem, xch);
 }
 
@@ -1199,7 +1198,7 @@ __device__ __forceinline__ float4 combine_row(const Params& p, int64_t r, int b)
         const int2 Bn = __ldcg(p.beta + o + node_index(t + 1, u, T, U));
         const float pb = __int_as_float(Ed.x), bn = __int_as_float(Bn.x);
         if (am != 0.0f && pb != 0.0f && bn != 0.0f)
-            eb = xf_to_float(am * pb * bn * inv, A.y + Ed.y + Bn.y - Pe);
+            eb = xf_to_float(am * pb * bn * inv, A.y + (Ed.y - kEdgeBias) + Bn.y - Pe);
     } else if (u == U) {
         eb = xf_to_float(am * bm * inv, A.y + Bt.y - Pe);
     }
@@ -1207,7 +1206,7 @@ __device__ __forceinline__ float4 combine_row(const Params& p, int64_t r, int b)
         const int2 Bn = __ldcg(p.beta + o + node_index(t, u + 1, T, U));
         const float py = __int_as_float(Ed.z), bn = __int_as_float(Bn.x);
         if (am != 0.0f && py != 0.0f && bn != 0.0f)
-            ey = xf_to_float(am * py * bn * inv, A.y + Ed.w + Bn.y - Pe);
+            ey = xf_to_float(am * py * bn * inv, A.y + (Ed.w - kEdgeBias) + Bn.y - Pe);
     }
     return make_float4(lc + p.lscale - __ldcg(p.lse2 + r), eb * p.scale, ey * p.scale,
                        __int_as_float(y));
@@ -1684,12 +1683,12 @@ __device__ __noinline__ void dp_task(const Params& p, int b, int4* smem, float2*
     c.W = c.U + 1;
     c.D = c.T + c.U;
     c.off = __ldg(p.off + b);
-    const int J = dp_slots(c.W);
-    if (J <= 1) dp_run<1>(p, c, smem, xch);
-    else if (J <= 2) dp_run<2>(p, c, smem, xch);
-    else if (J <= 3) dp_run<3>(p, c, smem, xch);
-    else if (J <= 4) dp_run<4>(p, c, smem, xch);
-    else if (J <= 6) dp_run<6>(p, c, smem, xch);
+    const int J = dp_jclass(dp_slots(c.W));
+    if (J == 1) dp_run<1>(p, c, smem, xch);
+    else if (J == 2) dp_run<2>(p, c, smem, xch);
+    else if (J == 3) dp_run<3>(p, c, smem, xch);
+    else if (J == 4) dp_run<4>(p, c, smem, xch);
+    else if (J == 6) dp_run<6>(p, c, smem, xch);
     else dp_run<8>(p, c, smem, xch);
 }
 
