@@ -1131,7 +1131,7 @@ __device__ __forceinline__ void dp_run(const Params& p, const Samp& c, int4* sme
     const int dir = wid / kDpWarps, w = wid % kDpWarps;
     const int nwd = dp_warps(c.W);
     if (w >= nwd) return;
-    int4* ring = smem + (size_t)wid * Ring<J>::R * J * 32;
+    int4* ring = smem + (size_t)(dir * nwd + w) * Ring<J>::R * J * 32;
     if (dir == 0) dp_alpha<J>(p, c, w * 32 * J, w, nwd, ring, xch);
     else dp_beta<J>(p, c, w * 32 * J, w, nwd, ring, xch + 2 * kDpWarps);
 }
@@ -1139,7 +1139,7 @@ __device__ __forceinline__ void dp_run(const Params& p, const Samp& c, int4* sme
 // Dynamic shared memory of the DP for lattices up to W columns (8 rings).
 __host__ __device__ inline size_t dp_smem_bytes(int W) {
     const int Jc = dp_jclass(dp_slots(W));
-    return (size_t)2 * kDpWarps * dp_ring_depth(Jc) * Jc * 32 * sizeof(int4);
+    return (size_t)2 * dp_warps(W) * dp_ring_depth(Jc) * Jc * 32 * sizeof(int4);
 }
 
 __global__ void __launch_bounds__(256) k_dp(Params p) {
