@@ -242,12 +242,19 @@ __device__ __forceinline__ void xf_prob(float h, float M, float s, float& m, int
     }
 }
 
+// Product of two extended-range numbers.  Exponents stay >= kZeroExp because
+// every sum below clamps its result, so a product of two zeros (2*kZeroExp)
+// cannot overflow.
 __device__ __forceinline__ void xf_mul(float am, int ae, float pm, int pe, float& m, int& e) {
     m = am * pm;
-    e = max(ae + pe, kZeroExp);
+    e = ae + pe;
 }
 
 // (m1 2^e1) + (m2 2^e2): exact alignment by the exponent difference, one FMA.
+// With NORM the mantissa is brought back to [1,2); without it the mantissa may
+// grow (by at most 2^3 per step: inputs are products of two mantissas below
+// 2^w and 2 each), which the exponent alignment tolerates exactly.
+template <bool NORM = true>
 __device__ __forceinline__ void xf_add(float m1, int e1, float m2, int e2, float& m, int& e) {
     const bool first = e1 >= e2;
     const float big = first ? m1 : m2, small = first ? m2 : m1;
@@ -255,8 +262,8 @@ __device__ __forceinline__ void xf_add(float m1, int e1, float m2, int e2, float
     const int k = first ? e2 - e1 : e1 - e2;                   // <= 0
     const float sc = __int_as_float(max(k + 127, 0) << 23);    // 2^k (0 below 2^-126)
     m = fmaf(small, sc, big);
-    e = E;
-    xf_norm(m, e);
+    e = max(E, kZeroExp);
+    if (NORM) xf_norm(m, e);
 }
 
 template <typename Tin> struct Elt;
@@ -1014,11 +1021,20 @@ __device__ void dp_alpha(const Params& p, const Samp& c, int u0, int w, int nwd,
             sm[j] = __shfl_sync(0xffffffffu, ym[j], (lane + 31) & 31);
             se[j] = __shfl_sync(0xffffffffu, ye[j], (lane + 31) & 31);
         }
+        if (d & 1) {
 #pragma unroll
-        for (int j = 0; j < J; ++j) {
-            const float nm = lane ? sm[j] : (j ? sm[j - 1] : edge_m);
-            const int ne = lane ? se[j] : (j ? se[j - 1] : edge_e);
-            xf_add(bm[j], be[j], nm, ne, am[j], ae[j]);
+            for (int j = 0; j < J; ++j) {
+                const float nm = lane ? sm[j] : (j ? sm[j - 1] : edge_m);
+                const int ne = lane ? se[j] : (j ? se[j - 1] : edge_e);
+                xf_add<false>(bm[j], be[j], nm, ne, am[j], ae[j]);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const float nm = lane ? sm[j] : (j ? sm[j - 1] : edge_m);
+                const int ne = lane ? se[j] : (j ? se[j - 1] : edge_e);
+                xf_add<true>(bm[j], be[j], nm, ne, am[j], ae[j]);
+            }
         }
         qs.next(c);
         store_diag<J>(c, out_s, qs, L, am, ae);
@@ -1104,7 +1120,8 @@ __device__ void dp_beta(const Params& p, const Samp& c, int u0, int w, int nwd, 
             int be, ye;
             xf_mul(vm[j], ve[j], __int_as_float(ed.x), ed.y - kEdgeBias, bm, be);
             xf_mul(nm, ne, __int_as_float(ed.z), ed.w - kEdgeBias, ym, ye);
-            xf_add(bm, be, ym, ye, vm[j], ve[j]);
+            if (d & 1) xf_add<false>(bm, be, ym, ye, vm[j], ve[j]);
+            else xf_add<true>(bm, be, ym, ye, vm[j], ve[j]);
         }
         store_diag<J>(c, out_s, qs, L, vm, ve);
         qs.prev(c);
@@ -1127,8 +1144,10 @@ __host__ __device__ inline int dp_ring_depth(int Jc) {
 
 template <int J>
 __device__ __forceinline__ void dp_run(const Params& p, const Samp& c, int4* smem, float2* xch) {
+    // Direction warps interleave (alpha on even warp ids, beta on odd) so the
+    // two recursions of a sample run on different SM sub-partitions.
     const int wid = threadIdx.x >> 5;
-    const int dir = wid / kDpWarps, w = wid % kDpWarps;
+    const int dir = wid & 1, w = wid >> 1;
     const int nwd = dp_warps(c.W);
     if (w >= nwd) return;
     int4* ring = smem + (size_t)(dir * nwd + w) * Ring<J>::R * J * 32;
