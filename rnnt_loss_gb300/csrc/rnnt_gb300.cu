@@ -1130,7 +1130,13 @@ __device__ void dp_beta(const Params& p, const Samp& c, int u0, int w, int nwd, 
     if (u0 == 0 && lane == 0) p.lossb[c.b] = -((double)ve[0] + log2((double)vm[0])) * kLn2d;
 }
 
-__host__ __device__ inline int dp_warps(int W) { return min(kDpWarps, (W + 127) / 128); }
+// Target lattice columns per lane before another compute warp is added.
+#ifndef RNNT_DP_SLOTS
+#define RNNT_DP_SLOTS 4
+#endif
+__host__ __device__ inline int dp_warps(int W) {
+    return min(kDpWarps, (W + 32 * RNNT_DP_SLOTS - 1) / (32 * RNNT_DP_SLOTS));
+}
 __host__ __device__ inline int dp_slots(int W) {
     const int n = dp_warps(W);
     return (W + 32 * n - 1) / (32 * n);
