@@ -893,17 +893,39 @@ template <> struct Ring<6> { static constexpr int R = 6; };
 template <> struct Ring<8> { static constexpr int R = 6; };
 constexpr int kDpWarps = 4;   // compute warps per direction, at most
 
+// The DP's ring copies, waits and ring reads are all volatile asm without a
+// "memory" clobber: volatile asm statements keep their relative order (copy,
+// wait, read), while the compiler stays free to move the recursion's
+// arithmetic and its global stores around them.
 __device__ __forceinline__ void cp16z(void* smem, const void* gmem, bool valid) {
     const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(sa), "l"(gmem),
-                 "r"(valid ? 16 : 0)
-                 : "memory");
+                 "r"(valid ? 16 : 0));
 }
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+__device__ __forceinline__ int4 lds128(const int4* ptr) {
+    int4 v;
+    asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"((unsigned)__cvta_generic_to_shared(ptr)));
+    return v;
+}
+__device__ __forceinline__ void sts64(float2* ptr, float2 v) {
+    asm volatile("st.shared.v2.f32 [%0], {%1, %2};\n" ::"r"((unsigned)__cvta_generic_to_shared(ptr)),
+                 "f"(v.x), "f"(v.y));
+}
+__device__ __forceinline__ float2 lds64(const float2* ptr) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];\n"
+                 : "=f"(v.x), "=f"(v.y)
+                 : "r"((unsigned)__cvta_generic_to_shared(ptr)));
+    return v;
+}
+// Orders the volatile shared-memory exchange (sts64 before, lds64 after).
 __device__ __forceinline__ void named_barrier(int id, int threads) {
-    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads));
 }
 
 struct Samp {
@@ -999,16 +1021,17 @@ __device__ void dp_alpha(const Params& p, const Samp& c, int u0, int w, int nwd,
         int be[J], ye[J];
 #pragma unroll
         for (int j = 0; j < J; ++j) {
-            const int4 ed = sp[j * 32];
+            const int4 ed = lds128(sp + j * 32);
             xf_mul(am[j], ae[j], __int_as_float(ed.x), ed.y - kEdgeBias, bm[j], be[j]);
             xf_mul(am[j], ae[j], __int_as_float(ed.z), ed.w - kEdgeBias, ym[j], ye[j]);
         }
         float edge_m = 0.0f;
         int edge_e = kZeroExp;
         if (nwd > 1) {
-            if (lane == 31) xch[(d & 1) * kDpWarps + w] = make_float2(ym[J - 1], __int_as_float(ye[J - 1]));
+            if (lane == 31)
+                sts64(xch + (d & 1) * kDpWarps + w, make_float2(ym[J - 1], __int_as_float(ye[J - 1])));
             named_barrier(1, nthreads);
-            const float2 v = xch[(d & 1) * kDpWarps + max(w - 1, 0)];
+            const float2 v = lds64(xch + (d & 1) * kDpWarps + max(w - 1, 0));
             if (w > 0) {
                 edge_m = v.x;
                 edge_e = __float_as_int(v.y);
@@ -1045,7 +1068,7 @@ __device__ void dp_alpha(const Params& p, const Samp& c, int u0, int w, int nwd,
 #pragma unroll
     for (int j = 0; j < J; ++j) {
         if (L.u[j] == c.U) {
-            const int4 ed = sp[j * 32];
+            const int4 ed = lds128(sp + j * 32);
             float m;
             int x;
             xf_mul(am[j], ae[j], __int_as_float(ed.x), ed.y - kEdgeBias, m, x);
@@ -1096,9 +1119,9 @@ __device__ void dp_beta(const Params& p, const Samp& c, int u0, int w, int nwd, 
         float edge_m = 0.0f;
         int edge_e = kZeroExp;
         if (nwd > 1) {
-            if (lane == 0) xch[(d & 1) * kDpWarps + w] = make_float2(vm[0], __int_as_float(ve[0]));
+            if (lane == 0) sts64(xch + (d & 1) * kDpWarps + w, make_float2(vm[0], __int_as_float(ve[0])));
             named_barrier(2, nthreads);
-            const float2 v = xch[(d & 1) * kDpWarps + min(w + 1, nwd - 1)];
+            const float2 v = lds64(xch + (d & 1) * kDpWarps + min(w + 1, nwd - 1));
             if (w + 1 < nwd) {
                 edge_m = v.x;
                 edge_e = __float_as_int(v.y);
@@ -1113,7 +1136,7 @@ __device__ void dp_beta(const Params& p, const Samp& c, int u0, int w, int nwd, 
         }
 #pragma unroll
         for (int j = 0; j < J; ++j) {
-            const int4 ed = sd[j * 32];
+            const int4 ed = lds128(sd + j * 32);
             const float nm = (lane < 31) ? sm[j] : (j + 1 < J ? sm[j + 1] : edge_m);
             const int ne = (lane < 31) ? se[j] : (j + 1 < J ? se[j + 1] : edge_e);
             float bm, ym;
@@ -1132,7 +1155,7 @@ __device__ void dp_beta(const Params& p, const Samp& c, int u0, int w, int nwd, 
 
 // Target lattice columns per lane before another compute warp is added.
 #ifndef RNNT_DP_SLOTS
-#define RNNT_DP_SLOTS 4
+#define RNNT_DP_SLOTS 1
 #endif
 __host__ __device__ inline int dp_warps(int W) {
     return min(kDpWarps, (W + 32 * RNNT_DP_SLOTS - 1) / (32 * RNNT_DP_SLOTS));
