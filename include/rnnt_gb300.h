@@ -21,8 +21,9 @@
  *
  * Memory and streams: every pointer argument named "device" must point to
  * memory the current CUDA device can access.  The library allocates nothing
- * and keeps no state between calls other than per-device kernel attributes;
- * all work is enqueued on `stream` and the host never synchronises.
+ * and keeps no state between calls other than per-device kernel attributes
+ * (and, for rnnt_loss_fused_noalloc, its fixed scratch array); all work is
+ * enqueued on `stream` and the host never synchronises.
  */
 #ifndef RNNT_GB300_H
 #define RNNT_GB300_H
@@ -172,6 +173,44 @@ rnnt_status_t rnnt_grad_scale(void *grad, rnnt_dtype_t dt, int64_t rows, int32_t
  * that outlives the calls; NULL (or bytes < 16) turns tracing off.
  */
 rnnt_status_t rnnt_set_trace(void *device_buffer, size_t bytes);
+
+/* Size of the fixed device scratch array rnnt_loss_fused_noalloc uses: 32 MiB,
+ * enough for rnnt_workspace_size() up to about 640,000 logit rows. */
+#define RNNT_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * rnnt_loss_fused_noalloc -- rnnt_loss_fused for callers that cannot hand
+ * out device memory.  The paper has no counterpart: this is an interface of
+ * this library only.
+ *
+ * Same arguments and results as rnnt_loss_fused without workspace and
+ * workspace_bytes.  The scratch is a file-scope device array of
+ * RNNT_NOALLOC_SCRATCH_BYTES bytes inside this library, one per device; the
+ * call allocates nothing (no cudaMalloc/cudaFree, no allocating library
+ * routine).  The first call on a device, made with that device current,
+ * looks up the array's device address (cudaGetSymbolAddress) once and
+ * caches it; make that first call before any stream capture.
+ *
+ * Every call on a device shares the one array and leaves its contents
+ * behind; each call rewrites everything it reads before reading it.  Calls
+ * whose kernels overlap on the GPU (other streams, other host threads)
+ * race on the array and give undefined results: serialize them, e.g. on
+ * one stream.  rnnt_grad_scale, which reads a caller workspace, does not
+ * apply to this call's gradient.
+ *
+ * Returns RNNT_WORKSPACE_TOO_SMALL, before any device work, when
+ * rnnt_workspace_size(B, rows, V, dt) exceeds RNNT_NOALLOC_SCRATCH_BYTES;
+ * RNNT_LAUNCH_FAILED when the address lookup fails; otherwise what
+ * rnnt_loss_fused returns.
+ */
+rnnt_status_t rnnt_loss_fused_noalloc(const void *logits, rnnt_dtype_t dt, int64_t rows,
+                                      int32_t V, const int32_t *targets, int32_t targets_stride,
+                                      const int32_t *logit_lengths,
+                                      const int32_t *target_lengths, int32_t B, int32_t blank,
+                                      float clamp, int32_t fused_log_softmax,
+                                      rnnt_reduction_t reduction, float *loss,
+                                      float *loss_reduced, void *grad, int32_t *status_dev,
+                                      rnnt_stream_t stream);
 
 /* Static English description of a status code. */
 const char *rnnt_status_string(rnnt_status_t status);

@@ -17,10 +17,12 @@ RNNT_LAUNCH_FAILED, RNNT_LOSS_MISMATCH, RNNT_TIMEOUT = 3, 4, 5
 RNNT_F32, RNNT_F16 = 0, 1
 REDUCTIONS = {"none": 0, "sum": 1, "mean": 2}
 MAX_TARGET_LENGTH = 1023
+NOALLOC_SCRATCH_BYTES = 32 << 20     # RNNT_NOALLOC_SCRATCH_BYTES
 
 # Every symbol include/rnnt_gb300.h declares.
 EXPORTS = ("rnnt_workspace_size", "rnnt_loss_fused", "rnnt_loss_fused_staged", "rnnt_grad_scale",
-           "rnnt_set_trace", "rnnt_status_string", "rnnt_abi_version")
+           "rnnt_set_trace", "rnnt_loss_fused_noalloc", "rnnt_status_string",
+           "rnnt_abi_version")
 
 _lib = None
 
@@ -49,6 +51,8 @@ def load() -> ctypes.CDLL:
     lib.rnnt_loss_fused.restype = i32
     lib.rnnt_loss_fused_staged.argtypes = lib.rnnt_loss_fused.argtypes + [P]
     lib.rnnt_loss_fused_staged.restype = i32
+    lib.rnnt_loss_fused_noalloc.argtypes = lib.rnnt_loss_fused.argtypes[:16] + [P, P]
+    lib.rnnt_loss_fused_noalloc.restype = i32
     lib.rnnt_grad_scale.argtypes = [P, i32, i64, i32, i32, P, sz, P, i32, P]
     lib.rnnt_grad_scale.restype = i32
     lib.rnnt_set_trace.argtypes = [P, sz]
@@ -98,6 +102,16 @@ def rnnt_loss_fused_staged(logits, dt, rows, V, targets, targets_stride, logit_l
                                              float(clamp), int(fused_log_softmax), reduction,
                                              loss, loss_reduced, grad, workspace,
                                              workspace_bytes, status_dev, stream, arr))
+
+
+def rnnt_loss_fused_noalloc(logits, dt, rows, V, targets, targets_stride, logit_lengths,
+                            target_lengths, B, blank, clamp, fused_log_softmax, reduction, loss,
+                            loss_reduced, grad, status_dev, stream) -> int:
+    """rnnt_loss_fused over the library's fixed device scratch (no workspace argument)."""
+    return int(load().rnnt_loss_fused_noalloc(logits, dt, rows, V, targets, targets_stride,
+                                              logit_lengths, target_lengths, B, blank,
+                                              float(clamp), int(fused_log_softmax), reduction,
+                                              loss, loss_reduced, grad, status_dev, stream))
 
 
 def rnnt_grad_scale(grad, dt, rows, V, B, workspace, workspace_bytes, factors, per_sample,

@@ -39,6 +39,7 @@
 #include <stdlib.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "rnnt_gb300.h"
 
@@ -2329,3 +2330,50 @@ extern "C" const char* rnnt_status_string(rnnt_status_t s) {
 }
 
 extern "C" int32_t rnnt_abi_version(void) { return 100; }
+
+// ---------------------------------------------------------------- no-alloc entry
+// rnnt_loss_fused_noalloc runs rnnt_loss_fused over a fixed scratch array of
+// this module instead of a caller workspace.  The array's device address is
+// looked up once per device (with that device current) and cached; the
+// lookup allocates nothing.  The workspace path rewrites every scratch word
+// it reads (k_prepare resets the counters, offsets and task list first), so
+// the contents a previous call left need no clearing.
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[RNNT_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kNoallocMaxDevices] = {};
+
+}  // namespace
+
+extern "C" rnnt_status_t rnnt_loss_fused_noalloc(
+    const void* logits, rnnt_dtype_t dt, int64_t rows, int32_t V, const int32_t* targets,
+    int32_t targets_stride, const int32_t* logit_lengths, const int32_t* target_lengths, int32_t B,
+    int32_t blank, float clamp, int32_t fused_log_softmax, rnnt_reduction_t reduction, float* loss,
+    float* loss_reduced, void* grad, int32_t* status_dev, rnnt_stream_t stream) {
+    if (B < 1 || rows < 1 || V < 1 || (dt != RNNT_F32 && dt != RNNT_F16)) return RNNT_INVALID_VALUE;
+    const size_t need = ws_layout(B, rows).total;
+    if (need > RNNT_NOALLOC_SCRATCH_BYTES) return RNNT_WORKSPACE_TOO_SMALL;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoallocMaxDevices)
+        return RNNT_LAUNCH_FAILED;
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        if (!g_noalloc_ptr[dev]) {
+            void* ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+                cudaGetLastError();   // leave no error behind for the next launch check
+                return RNNT_LAUNCH_FAILED;
+            }
+            g_noalloc_ptr[dev] = ptr;
+        }
+        scratch = g_noalloc_ptr[dev];
+    }
+    return rnnt_loss_fused(logits, dt, rows, V, targets, targets_stride, logit_lengths,
+                           target_lengths, B, blank, clamp, fused_log_softmax, reduction, loss,
+                           loss_reduced, grad, scratch, RNNT_NOALLOC_SCRATCH_BYTES, status_dev,
+                           stream);
+}
