@@ -7,9 +7,10 @@
 //               rnnt-loss-ascend README (架构设计 "Host 侧").
 //   k_row_*     one pass over the logits: per row the log-softmax denominator
 //               (max, then sum of exponentials, group-shuffle reductions) and
-//               the blank / target transition probabilities, scattered into
-//               an anti-diagonal-packed layout for the DP (README 对角线遍历
-//               α/β).  With the in-kernel log-softmax off only the two needed
+//               the blank / target transition probabilities, stored per
+//               lattice node in anti-diagonal-packed order so that each
+//               step of the DP's anti-diagonal sweep (README 对角线遍历 α/β)
+//               reads and writes one contiguous run.  With the in-kernel log-softmax off only the two needed
 //               elements of a row are read.
 //   k_dp        one CTA of two warps per sample: warp 0 runs the forward
 //               (alpha) recursion over anti-diagonals d = 0..T+U-1, warp 1
@@ -40,6 +41,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "rnnt_gb300.h"
 
@@ -127,6 +129,8 @@ struct Params {
     int fused;
     int red;
     int stage_bytes;  // per-stage shared-memory row buffer of the TMA-staged passes
+    int zero_off;     // persistent kernel: shared-memory offset of a zeroed buffer ...
+    int zero_rows;    // ... of zero_rows gradient rows, the source of zero-row bulk stores
     float* loss;
     float* loss_red;
     int32_t* status;
@@ -139,8 +143,8 @@ struct Params {
     float* pm;        // P(y|x) of each sample, extended range
     int32_t* pe;
     float* lse2;      // per row (row order): log2 sum_k 2^(h_k log2 e)
-    int4* edge;       // per node (diagonal-packed): {p_blank.m, p_blank.e, p_label.m, p_label.e}
-    int2* alpha;      // per node (diagonal-packed): {m, e}
+    int4* edge;       // per node (node_index order): {p_blank.m, p_blank.e, p_label.m, p_label.e}
+    int2* alpha;      // per node (node_index order): {m, e}
     int2* beta;
     float4* info;     // per row: gradient record (see k_combine)
     // persistent-kernel scheduler (err[1] = next task, err[2] = task count)
@@ -166,13 +170,16 @@ __device__ __forceinline__ float lg2(float x) {
     return y;
 }
 
-// Number of lattice nodes (t,u), 0<=t<T, 0<=u<W, with t+u < d: first packed
-// index of anti-diagonal d (inclusion-exclusion over the rectangle).
+// Number of lattice nodes (t,u), 0<=t<T, 0<=u<W, with t+u < d: first index
+// of anti-diagonal d in the per-node arrays (inclusion-exclusion over the
+// rectangle).
 __device__ __forceinline__ int64_t tri(int64_t n) { return n > 0 ? n * (n + 1) / 2 : 0; }
 __device__ __forceinline__ int64_t diag_start(int d, int T, int W) {
     return tri(d) - tri((int64_t)d - T) - tri((int64_t)d - W) + tri((int64_t)d - T - W);
 }
-// Packed index of node (t,u) relative to its sample's first row.
+// Index of node (t,u) relative to its sample's first record in the per-node
+// arrays (transition records, alpha, beta): anti-diagonal-packed, so each
+// diagonal d = t+u is one contiguous run ordered by t.
 __device__ __forceinline__ int64_t node_index(int t, int u, int T, int U) {
     const int d = t + u;
     return diag_start(d, T, U + 1) + (t - max(0, d - U));
@@ -374,6 +381,19 @@ __device__ __forceinline__ void tma_row_load(void* dst, const void* src, uint32_
             "r"(smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+// Bulk (TMA) store of `bytes` from shared to global memory, in this thread's
+// bulk group; both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void tma_store(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_store_commit() {
+    asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
@@ -597,7 +617,7 @@ __global__ void __launch_bounds__(1024) k_prepare(Params p) {
 // scalar per-row work costs one warp instruction per 32 rows.
 
 // One row per lane: log2 of the softmax denominator in row order, and the
-// node's two transition probabilities at its packed index.  A blank from the
+// node's two transition probabilities at its node index.  A blank from the
 // last frame before every label is out, and a label at u = U, have
 // probability 0 (the lattice has no such arc).
 template <typename Tin>
@@ -875,16 +895,17 @@ __global__ void __launch_bounds__(256) k_row_gather(Params p) {
 }
 
 // ---------------------------------------------------------------- DP
-// One CTA per sample (8 warps).  Per direction, nwd = ceil(W/128) compute
-// warps (W = U+1 lattice columns, at most 4) each own a contiguous block of
-// 32*J columns, J = ceil(W/(32*nwd)) <= 8; lane l holds columns
-// u0 + 32*j + l.  The neighbouring column comes from the next lane by
-// shuffle, or at a block edge from the neighbouring warp through shared
-// memory with one named barrier per anti-diagonal (1: alpha, 2: beta).
-// Warps 0..3 run alpha, 4..7 beta.  Each compute warp prefetches its nodes'
+// One CTA per sample (8 warps).  Per direction, nwd compute warps (at most
+// 4; W = U+1 lattice columns) each own a contiguous block of 32*J columns,
+// J = ceil(W/(32*nwd)) <= 8; lane l holds columns u0 + 32*j + l.  The
+// neighbouring column comes from the next lane by shuffle, or at a block
+// edge from the neighbouring warp through shared memory with one named
+// barrier per anti-diagonal (1: alpha, 2: beta).  Alpha and beta warps
+// interleave (even / odd warp ids).  Each compute warp prefetches its nodes'
 // transition records with zero-filling cp.async into a ring of R diagonals
-// (prefetch distance R-2); the loop body is branch-free (predicated copies
-// and stores, 32-bit incremental diagonal bases).
+// (prefetch distance R-2).  Per-diagonal bookkeeping is kept small: the
+// diagonal's base index comes by shuffle from a 32-diagonal window, and
+// each lane keeps per-column pointers.
 template <int J> struct Ring;
 template <> struct Ring<1> { static constexpr int R = 16; };
 template <> struct Ring<2> { static constexpr int R = 12; };
@@ -934,54 +955,71 @@ struct Samp {
     int64_t off;
 };
 
-// Packed index (relative to the sample) of the node in column u on diagonal d
-// is base - u with base = N(d) - max(0, d-U) + d; N(d) = nodes before d.
-struct DBase {
-    int d, base;
-    __device__ __forceinline__ static int count(const Samp& c, int d) {
-        return (d < 0 || d >= c.D) ? 0 : min(c.T - 1, d) - max(0, d - c.U) + 1;
+// The node in column u on diagonal d is at index base(d) - u with
+// base(d) = N(d) - max(0, d-U) + d (N(d) = nodes before diagonal d).
+__device__ __forceinline__ int diag_base(const Samp& c, int d) {
+    return (int)(diag_start(d, c.T, c.W) - max(0, d - c.U) + d);
+}
+
+// Diagonal bases for a window of 32 consecutive diagonals, one per lane
+// (lane l: diagonal first + dir*l); a diagonal's base is then one shuffle.
+struct BaseWin {
+    int first, dir, mine;
+    __device__ __forceinline__ void load(const Samp& c, int f, int dr, int lane) {
+        first = f;
+        dir = dr;
+        const int d = f + dr * lane;
+        mine = (d >= 0 && d < c.D) ? diag_base(c, d) : 0;
     }
-    __device__ __forceinline__ void init(const Samp& c, int d0) {
-        d = d0;
-        base = (int)(diag_start(d0, c.T, c.W) - max(0, d0 - c.U) + d0);
-    }
-    __device__ __forceinline__ void next(const Samp& c) {
-        base += count(c, d) + 1 - (d + 1 > c.U ? 1 : 0);
-        ++d;
-    }
-    __device__ __forceinline__ void prev(const Samp& c) {
-        base -= count(c, d - 1) + 1 - (d > c.U ? 1 : 0);
-        --d;
+    // Base of diagonal d (warp-uniform d inside or just past the window).
+    __device__ __forceinline__ int get(const Samp& c, int d, int lane) {
+        int k = (d - first) * dir;
+        if (k >= 32) {   // warp-uniform refill
+            load(c, first + 32 * dir, dir, lane);
+            k -= 32;
+        }
+        return __shfl_sync(0xffffffffu, mine, k);
     }
 };
 
 template <int J>
 struct Lanes {
-    int u[J];        // this lane's columns
-    bool col_ok[J];  // column exists (u <= U)
+    int u[J];          // this lane's columns u0 + 32j + lane
+    int Tl[J];         // T if the column exists (u <= U), else 0
+    const int4* e[J];  // edge records of this column: e[j][base(d)] is node (d-u, u)
+    int2* o[J];        // output (alpha or beta) of this column, same indexing
 };
 
 template <int J>
-__device__ __forceinline__ void ring_issue(const Samp& c, const int4* edge_s, int4* ring,
-                                           const DBase& q, const Lanes<J>& L, int lane) {
-    constexpr int R = Ring<J>::R;
-    if (q.d < 0 || q.d >= c.D) return;
-    int4* sl = ring + (q.d % R) * (J * 32) + lane;
+__device__ __forceinline__ void lanes_init(const Samp& c, int u0, int lane, const int4* edge_s,
+                                           int2* out_s, Lanes<J>& L) {
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-        const bool ok = L.col_ok[j] && (unsigned)(q.d - L.u[j]) < (unsigned)c.T;
-        cp16z(sl + j * 32, edge_s + (ok ? q.base - L.u[j] : 0), ok);
+        L.u[j] = u0 + 32 * j + lane;
+        L.Tl[j] = L.u[j] <= c.U ? c.T : 0;
+        L.e[j] = edge_s - L.u[j];
+        L.o[j] = out_s - L.u[j];
+    }
+}
+
+// Zero-filling copies of the transition records of diagonal e (base be)
+// into a ring slot; records of missing nodes read as probability 0.
+template <int J>
+__device__ __forceinline__ void ring_issue(int4* slot, int e, int be, const Lanes<J>& L) {
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const bool ok = (unsigned)(e - L.u[j]) < (unsigned)L.Tl[j];
+        cp16z(slot + j * 32, ok ? L.e[j] + be : L.e[j] + L.u[j], ok);
     }
 }
 
 template <int J>
-__device__ __forceinline__ void store_diag(const Samp& c, int2* out_s, const DBase& q,
-                                           const Lanes<J>& L, const float* m, const int* e) {
+__device__ __forceinline__ void store_diag(int d, int bd, const Lanes<J>& L, const float* m,
+                                           const int* e) {
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-        const bool ok = L.col_ok[j] && (unsigned)(q.d - L.u[j]) < (unsigned)c.T;
-        if (ok) out_s[q.base - L.u[j]] = make_int2(__float_as_int(m[j]), e[j]);
-    }
+    for (int j = 0; j < J; ++j)
+        if ((unsigned)(d - L.u[j]) < (unsigned)L.Tl[j])
+            L.o[j][bd] = make_int2(__float_as_int(m[j]), e[j]);
 }
 
 // Forward variable: alpha(t,u) = alpha(t-1,u) p_blank(t-1,u) + alpha(t,u-1) p_label(t,u-1).
@@ -991,33 +1029,40 @@ __device__ void dp_alpha(const Params& p, const Samp& c, int u0, int w, int nwd,
                          float2* xch) {
     constexpr int R = Ring<J>::R, PF = R - 2;
     const int lane = threadIdx.x & 31, nthreads = nwd * 32;
-    const int4* edge_s = p.edge + c.off;
-    int2* out_s = p.alpha + c.off;
     Lanes<J> L;
+    lanes_init<J>(c, u0, lane, p.edge + c.off, p.alpha + c.off, L);
     float am[J];
     int ae[J];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-        L.u[j] = u0 + 32 * j + lane;
-        L.col_ok[j] = L.u[j] <= c.U;
         am[j] = L.u[j] == 0 ? 1.0f : 0.0f;
         ae[j] = L.u[j] == 0 ? 0 : kZeroExp;
     }
-    DBase qs, qi;
-    qs.init(c, 0);
-    store_diag<J>(c, out_s, qs, L, am, ae);
-    qi.init(c, 0);
-    for (int k = 0; k <= PF; ++k) {
-        ring_issue<J>(c, edge_s, ring, qi, L, lane);
+    store_diag<J>(0, 0, L, am, ae);   // alpha(0,0) = 1 (base(0) = 0)
+    int4* const rl = ring + lane;
+    BaseWin wi, ws;
+    wi.load(c, 0, 1, lane);
+    ws.load(c, 1, 1, lane);
+    // Diagonal e's records feed diagonal e+1; prefetch PF diagonals.
+    int e = 0, si = 0;
+    for (; e < PF; ++e) {
+        const int be = wi.get(c, e, lane);
+        if (e < c.D) ring_issue<J>(rl + si * (J * 32), e, be, L);
         cp_commit();
-        qi.next(c);
+        si = si + 1 == R ? 0 : si + 1;
     }
-    for (int d = 1; d < c.D; ++d) {
-        ring_issue<J>(c, edge_s, ring, qi, L, lane);
-        cp_commit();
-        qi.next(c);
-        cp_wait<PF + 1>();
-        const int4* sp = ring + ((d - 1) % R) * (J * 32) + lane;
+    int so = 0;
+    auto step = [&](int d, auto norm) {
+        {
+            const int be = wi.get(c, e, lane);
+            if (e < c.D) ring_issue<J>(rl + si * (J * 32), e, be, L);
+            cp_commit();
+            ++e;
+            si = si + 1 == R ? 0 : si + 1;
+        }
+        cp_wait<PF>();
+        const int4* sp = rl + so * (J * 32);
+        so = so + 1 == R ? 0 : so + 1;
         float bm[J], ym[J];
         int be[J], ye[J];
 #pragma unroll
@@ -1045,27 +1090,23 @@ __device__ void dp_alpha(const Params& p, const Samp& c, int u0, int w, int nwd,
             sm[j] = __shfl_sync(0xffffffffu, ym[j], (lane + 31) & 31);
             se[j] = __shfl_sync(0xffffffffu, ye[j], (lane + 31) & 31);
         }
-        if (d & 1) {
 #pragma unroll
-            for (int j = 0; j < J; ++j) {
-                const float nm = lane ? sm[j] : (j ? sm[j - 1] : edge_m);
-                const int ne = lane ? se[j] : (j ? se[j - 1] : edge_e);
-                xf_add<false>(bm[j], be[j], nm, ne, am[j], ae[j]);
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < J; ++j) {
-                const float nm = lane ? sm[j] : (j ? sm[j - 1] : edge_m);
-                const int ne = lane ? se[j] : (j ? se[j - 1] : edge_e);
-                xf_add<true>(bm[j], be[j], nm, ne, am[j], ae[j]);
-            }
+        for (int j = 0; j < J; ++j) {
+            const float nm = lane ? sm[j] : (j ? sm[j - 1] : edge_m);
+            const int ne = lane ? se[j] : (j ? se[j - 1] : edge_e);
+            xf_add<decltype(norm)::value>(bm[j], be[j], nm, ne, am[j], ae[j]);
         }
-        qs.next(c);
-        store_diag<J>(c, out_s, qs, L, am, ae);
+        store_diag<J>(d, ws.get(c, d, lane), L, am, ae);
+    };
+    int d = 1;
+    for (; d + 1 < c.D; d += 2) {
+        step(d, std::false_type());
+        step(d + 1, std::true_type());
     }
-    // P(y|x) = alpha(T-1,U) p_blank(T-1,U): the terminal blank.
+    if (d < c.D) step(d, std::false_type());
+    // P(y|x) = alpha(T-1,U) p_blank(T-1,U): the terminal blank (diagonal D-1).
     cp_wait<0>();
-    const int4* sp = ring + ((c.D - 1) % R) * (J * 32) + lane;
+    const int4* sp = rl + so * (J * 32);
 #pragma unroll
     for (int j = 0; j < J; ++j) {
         if (L.u[j] == c.U) {
@@ -1091,32 +1132,38 @@ __device__ void dp_beta(const Params& p, const Samp& c, int u0, int w, int nwd, 
                         float2* xch) {
     constexpr int R = Ring<J>::R, PF = R - 2;
     const int lane = threadIdx.x & 31, nthreads = nwd * 32;
-    const int4* edge_s = p.edge + c.off;
-    int2* out_s = p.beta + c.off;
     Lanes<J> L;
+    lanes_init<J>(c, u0, lane, p.edge + c.off, p.beta + c.off, L);
     float vm[J];
     int ve[J];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-        L.u[j] = u0 + 32 * j + lane;
-        L.col_ok[j] = L.u[j] <= c.U;
         vm[j] = L.u[j] == c.U ? 1.0f : 0.0f;
         ve[j] = L.u[j] == c.U ? 0 : kZeroExp;
     }
-    DBase qs, qi;
-    qi.init(c, c.D - 1);
-    for (int k = 0; k <= PF; ++k) {
-        ring_issue<J>(c, edge_s, ring, qi, L, lane);
+    int4* const rl = ring + lane;
+    BaseWin wi, ws;
+    wi.load(c, c.D - 1, -1, lane);
+    ws.load(c, c.D - 1, -1, lane);
+    int e = c.D - 1, si = 0;
+    for (int k = 0; k < PF; ++k, --e) {
+        const int be = wi.get(c, e, lane);
+        if (e >= 0) ring_issue<J>(rl + si * (J * 32), e, be, L);
         cp_commit();
-        qi.prev(c);
+        si = si + 1 == R ? 0 : si + 1;
     }
-    qs.init(c, c.D - 1);
-    for (int d = c.D - 1; d >= 0; --d) {
-        ring_issue<J>(c, edge_s, ring, qi, L, lane);
-        cp_commit();
-        qi.prev(c);
-        cp_wait<PF + 1>();
-        const int4* sd = ring + (d % R) * (J * 32) + lane;
+    int so = 0;
+    auto step = [&](int d, auto norm) {
+        {
+            const int be = wi.get(c, e, lane);
+            if (e >= 0) ring_issue<J>(rl + si * (J * 32), e, be, L);
+            cp_commit();
+            --e;
+            si = si + 1 == R ? 0 : si + 1;
+        }
+        cp_wait<PF>();
+        const int4* sd = rl + so * (J * 32);
+        so = so + 1 == R ? 0 : so + 1;
         float edge_m = 0.0f;
         int edge_e = kZeroExp;
         if (nwd > 1) {
@@ -1144,12 +1191,16 @@ __device__ void dp_beta(const Params& p, const Samp& c, int u0, int w, int nwd, 
             int be, ye;
             xf_mul(vm[j], ve[j], __int_as_float(ed.x), ed.y - kEdgeBias, bm, be);
             xf_mul(nm, ne, __int_as_float(ed.z), ed.w - kEdgeBias, ym, ye);
-            if (d & 1) xf_add<false>(bm, be, ym, ye, vm[j], ve[j]);
-            else xf_add<true>(bm, be, ym, ye, vm[j], ve[j]);
+            xf_add<decltype(norm)::value>(bm, be, ym, ye, vm[j], ve[j]);
         }
-        store_diag<J>(c, out_s, qs, L, vm, ve);
-        qs.prev(c);
+        store_diag<J>(d, ws.get(c, d, lane), L, vm, ve);
+    };
+    int d = c.D - 1;
+    for (; d >= 1; d -= 2) {
+        step(d, std::false_type());
+        step(d - 1, std::true_type());
     }
+    if (d == 0) step(0, std::true_type());
     cp_wait<0>();
     if (u0 == 0 && lane == 0) p.lossb[c.b] = -((double)ve[0] + log2((double)vm[0])) * kLn2d;
 }
@@ -1583,11 +1634,17 @@ __device__ bool row_batch_tma(const Params& p, int64_t r0, int n, unsigned char*
     return true;
 }
 
-// Warp: gradient rows [r0, r0+n) with their records in shared memory; only
-// rows that are not exactly zero are fetched through the TMA ring.
+// Warp: the exactly-zero rows of its own 32-row slice [r0+s0, r0+s0+n) by
+// bulk stores from the zeroed shared buffer (zmask: zero rows of the slice),
+// then the non-zero rows list[first], list[first+stride], ... (cnt entries,
+// row offsets from r0) of the whole task, fetched through the warp's TMA ring.
+// Dealing the task's non-zero rows round-robin keeps the warps balanced: they
+// cluster along the alignment path, so a 32-row slice may hold none or all.
 template <typename Tin, int NV>
-__device__ bool grad_batch_tma(const Params& p, int64_t r0, int n, const float4* inf,
-                               unsigned char* buf, uint64_t* bars, uint32_t& kk) {
+__device__ bool grad_batch_tma(const Params& p, int64_t r0, int s0, uint32_t zmask,
+                               const uint16_t* list, int cnt, int first, int stride,
+                               const float4* inf, unsigned char* buf, uint64_t* bars,
+                               uint32_t& kk, const unsigned char* zbuf) {
     using E = Elt<Tin>;
     constexpr int EPV = E::kPerVec;
     const int wl = threadIdx.x & 31, sb = p.stage_bytes;
@@ -1598,48 +1655,52 @@ __device__ bool grad_batch_tma(const Params& p, int64_t r0, int n, const float4*
     const float cl = p.clamp * p.scale;
     const bool clip = p.clamp < INFINITY;
     const int vb = p.blank / EPV, eb_i = p.blank % EPV;
-    const bool mine = wl < n && inf[min(wl, n - 1)].x != -INFINITY;
-    uint32_t pend = __ballot_sync(0xffffffffu, mine);
-    const uint32_t nnz = __popc(pend);
-    uint32_t issued = 0, consumed = 0;
-    if (wl == 0) fence_proxy_async();
-    while (issued < min((uint32_t)kStages, nnz)) {
-        const int bit = __ffs(pend) - 1;
-        pend &= pend - 1;
-        const uint32_t st = (kk + issued) % kStages;
-        if (wl == 0) tma_row_load(buf + st * sb, X + (r0 + bit) * (int64_t)V, rb, &bars[st]);
-        ++issued;
+    const int my = cnt > first ? (cnt - first + stride - 1) / stride : 0;
+    if (wl == 0) {
+        uint32_t zm = zmask;
+        while (zm) {
+            const int a = __ffs(zm) - 1;
+            const uint32_t after = ~(zm >> a);
+            const int len = after ? __ffs(after) - 1 : 32 - a;
+            for (int k = 0; k < len; k += p.zero_rows) {
+                const int nr = min(p.zero_rows, len - k);
+                tma_store(Y + (r0 + s0 + a + k) * (int64_t)V, zbuf, (uint32_t)nr * rb);
+            }
+            zm &= len >= 32 ? 0u : ~(((1u << len) - 1u) << a);
+        }
+        tma_store_commit();
+        fence_proxy_async();
+        for (int i = 0; i < min(kStages, my); ++i) {
+            const uint32_t st = (kk + i) % kStages;
+            tma_row_load(buf + st * sb, X + (r0 + list[first + i * stride]) * (int64_t)V, rb,
+                         &bars[st]);
+        }
     }
-    for (int it = 0; it < n; ++it) {
-        const float4 in = inf[it];
+    for (int i = 0; i < my; ++i) {
+        const int row = list[first + i * stride];
+        const float4 in = inf[row];
         const float w2 = in.x, eb = in.y, ey = in.z;
         const int y = __float_as_int(in.w);
         const int vy = y >= 0 ? y / EPV : -1, ey_i = y >= 0 ? y % EPV : 0;
-        const bool zero = w2 == -INFINITY;
-        const uint4* rv = nullptr;
-        if (!zero) {
-            const uint32_t k = kk + consumed, st = k % kStages;
-            if (!mbar_wait(&bars[st], (k / kStages) & 1, p.err)) {
-                for (uint32_t q = consumed; q < issued; ++q)
-                    mbar_wait(&bars[(kk + q) % kStages], ((kk + q) / kStages) & 1, p.err);
-                return false;
-            }
-            rv = reinterpret_cast<const uint4*>(buf + st * sb);
+        const uint32_t k = kk + i, st = k % kStages;
+        if (!mbar_wait(&bars[st], (k / kStages) & 1, p.err)) {
+            // Timeout: wait (bounded) for the copies still in flight.
+            for (int q = i + 1; q < min(i + kStages, my); ++q)
+                mbar_wait(&bars[(kk + q) % kStages], ((kk + q) / kStages) & 1, p.err);
+            return false;
         }
-        uint4* ov = reinterpret_cast<uint4*>(Y + (r0 + it) * (int64_t)V);
+        const uint4* rv = reinterpret_cast<const uint4*>(buf + st * sb);
+        uint4* ov = reinterpret_cast<uint4*>(Y + (r0 + row) * (int64_t)V);
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             const int vi = wl + 32 * v;
             if (vi >= nvec) continue;
             float g[EPV];
-            if (!zero) {
+            {
                 float x[EPV];
                 E::unpack(rv[vi], x);
 #pragma unroll
                 for (int e = 0; e < EPV; ++e) g[e] = ex2(fmaf(x[e], kLog2e, w2));
-            } else {
-#pragma unroll
-                for (int e = 0; e < EPV; ++e) g[e] = 0.0f;
             }
             if (vi == vb) {
 #pragma unroll
@@ -1657,22 +1718,14 @@ __device__ bool grad_batch_tma(const Params& p, int64_t r0, int n, const float4*
             }
             __stcs(ov + vi, E::pack(g));
         }
-        if (!zero) {
-            __syncwarp();
-            const uint32_t st = (kk + consumed) % kStages;
-            ++consumed;
-            if (pend) {
-                const int bit = __ffs(pend) - 1;
-                pend &= pend - 1;
-                if (wl == 0) {
-                    fence_proxy_async();
-                    tma_row_load(buf + st * sb, X + (r0 + bit) * (int64_t)V, rb, &bars[st]);
-                }
-                ++issued;
-            }
+        __syncwarp();
+        if (wl == 0 && i + kStages < my) {
+            fence_proxy_async();
+            tma_row_load(buf + st * sb, X + (r0 + list[first + (i + kStages) * stride]) * (int64_t)V,
+                         rb, &bars[st]);
         }
     }
-    kk += nnz;
+    kk += my;
     return true;
 }
 
@@ -1777,6 +1830,8 @@ __global__ void __launch_bounds__(256, 2) k_main(Params p) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ uint64_t bars_all[8 * kStages];
     __shared__ float4 s_info[kTaskRows];
+    __shared__ uint16_t s_nz[kTaskRows];
+    __shared__ int s_cnt[8];
     __shared__ float2 xch[4 * kDpWarps];
     __shared__ int s_task, s_go;
     if (*p.err & (ERR_LENGTH | ERR_ROWS | ERR_TARGET)) return;   // uniform: set before launch
@@ -1821,6 +1876,14 @@ __global__ void __launch_bounds__(256, 2) k_main(Params p) {
 
     unsigned char* buf = smem_raw + (size_t)wid * kStages * p.stage_bytes;
     uint64_t* bars = bars_all + wid * kStages;
+    const unsigned char* zbuf = smem_raw + p.zero_off;
+    if (NV > 0) {
+        const int zn = p.zero_rows * p.V * (int)sizeof(Tin) / 16;
+        for (int i = tid; i < zn; i += blockDim.x)
+            reinterpret_cast<uint4*>(smem_raw + p.zero_off)[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async();   // generic writes before the bulk stores read them
+        __syncthreads();
+    }
     if (NV > 0 && wl == 0) {
 #pragma unroll
         for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], 1);
@@ -1892,18 +1955,34 @@ __global__ void __launch_bounds__(256, 2) k_main(Params p) {
         if (tid < n) s_info[tid] = combine_row(p, r0 + tid, b);
         __syncthreads();
         const int nw = min(32, n - 32 * wid);
-        if (nw > 0) {
-            if (NV > 0)
-                grad_batch_tma<Tin, (NV > 0 ? NV : 1)>(p, r0 + 32 * wid, nw, s_info + 32 * wid,
-                                                      buf, bars, kk);
-            else
-                grad_batch_plain<Tin, G, VEC, false>(p, r0 + 32 * wid, nw, s_info + 32 * wid);
+        if (NV > 0) {
+            // Compact the task's non-zero rows (in row order) for round-robin dealing.
+            const bool nz = tid < n && s_info[tid].x != -INFINITY;
+            const uint32_t bal = __ballot_sync(0xffffffffu, nz);
+            if (wl == 0) s_cnt[wid] = __popc(bal);
+            __syncthreads();
+            int before = 0, cnt = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int ck = s_cnt[k];
+                before += k < wid ? ck : 0;
+                cnt += ck;
+            }
+            if (nz) s_nz[before + __popc(bal & ((1u << wl) - 1u))] = (uint16_t)tid;
+            __syncthreads();
+            const uint32_t zmask = nw > 0 ? ~bal & (nw >= 32 ? 0xffffffffu : ((1u << nw) - 1u)) : 0u;
+            grad_batch_tma<Tin, (NV > 0 ? NV : 1)>(p, r0, 32 * wid, zmask, s_nz, cnt, wid, 8,
+                                                  s_info, buf, bars, kk, zbuf);
+        } else if (nw > 0) {
+            grad_batch_plain<Tin, G, VEC, false>(p, r0 + 32 * wid, nw, s_info + 32 * wid);
         }
         if (p.trace) {
             __syncthreads();
             if (tid == 0) trace_task(p, t, tk.x, t_start);
         }
     }
+    // Zero-row bulk stores read the shared buffer until they complete.
+    if (NV > 0 && wl == 0) tma_store_wait_all();
 }
 
 // ---------------------------------------------------------------- finalize
@@ -2125,9 +2204,16 @@ bool launch_persistent(const Params& p, cudaStream_t st, int sms, int dev) {
     const size_t dps = dp_smem_for(p.S);
     const void* fn = nullptr;
     size_t sm = dps;
+    int zero_off = 0, zero_rows = 0;
     if (p.fused) {
         if (!(vec && nvec > 32 && nvec <= 256)) return false;
         sm = std::max(sm, (size_t)8 * kStages * p.stage_bytes);
+        sm = (sm + 127) / 128 * 128;
+        const int rb = V * (int)sizeof(Tin);
+        const int room = sm < 110 * 1024 ? (int)(110 * 1024 - sm) / rb : 0;
+        zero_rows = std::max(1, std::min(16384 / rb, room));
+        zero_off = (int)sm;
+        sm += (size_t)zero_rows * rb;
         fn = nvec <= 64    ? reinterpret_cast<const void*>(k_main<Tin, 2, 32, true>)
              : nvec <= 128 ? reinterpret_cast<const void*>(k_main<Tin, 4, 32, true>)
                            : reinterpret_cast<const void*>(k_main<Tin, 8, 32, true>);
@@ -2143,6 +2229,8 @@ bool launch_persistent(const Params& p, cudaStream_t st, int sms, int dev) {
     if (occ < 1) return false;
     Params q = p;
     q.n_dp_sms = std::min(std::min(8, (p.B + 1) / 2), sms / 8);
+    q.zero_off = zero_off;
+    q.zero_rows = zero_rows;
     void* args[] = {&q};
     return cudaLaunchCooperativeKernel(fn, dim3(occ * sms), dim3(256), args, sm, st) == cudaSuccess;
 }

@@ -50,6 +50,19 @@ def summary(r) -> dict:
     if dp.any():
         out["dp_by_sample_us"] = {int(s): [float(a), float(b)] for s, a, b in
                                   zip(r["sample"][dp], r["start_us"][dp], r["end_us"][dp])}
+    # Per sample: when its last row chunk ended, its DP ran, and its gradient
+    # chunks started and ended (the critical path of the persistent kernel).
+    per = {}
+    for b in np.unique(r["sample"]):
+        m = r["sample"] == b
+        ent = {}
+        for k, name in enumerate(KINDS):
+            mk = m & (r["kind"] == k)
+            if mk.any():
+                ent[name] = [round(float(r["start_us"][mk].min()), 1),
+                             round(float(r["end_us"][mk].max()), 1)]
+        per[int(b)] = ent
+    out["per_sample_us"] = per
     busy = {}
     for sm, a, b in zip(r["sm"], r["start_us"], r["end_us"]):
         busy[int(sm)] = busy.get(int(sm), 0.0) + float(b - a)
