@@ -445,6 +445,61 @@ __device__ __forceinline__ int smid() {
     return v;
 }
 
+// Packed fp32x2 arithmetic (two lanes of one 64-bit register pair).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// Log-softmax statistics of one row held as NV 16-byte vectors per lane
+// (vector wl + 32 i of the row): M = max_k h_k and s = sum_k 2^(h_k log2 e -
+// M log2 e), both reduced over the warp.  Exponent arguments and partial sums
+// are formed two elements at a time with packed fp32x2 arithmetic (even and
+// odd elements in separate partial sums), in one fixed order shared by every
+// kernel that stages rows this way.
+template <typename Tin, int NV>
+__device__ __forceinline__ void row_stats(const uint4* q, int nvec, int wl, float& M, float& s) {
+    using E = Elt<Tin>;
+    constexpr int EPV = E::kPerVec;
+    M = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+        if (wl + 32 * i < nvec) M = fmaxf(M, E::vmax(q[i]));
+    M = group_max<32>(M, 0xffffffffu);
+    float2 acc = make_float2(0.0f, 0.0f);
+    if (M != -INFINITY) {
+        const float ML = M * kLog2e;
+        const float2 l2 = make_float2(kLog2e, kLog2e), c2 = make_float2(-ML, -ML);
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            if (wl + 32 * i < nvec) {
+                float x[EPV];
+                E::unpack(q[i], x);
+#pragma unroll
+                for (int e = 0; e < EPV; e += 2) {
+                    float2 t = fma2(make_float2(x[e], x[e + 1]), l2, c2);
+                    t.x = ex2(t.x);
+                    t.y = ex2(t.y);
+                    acc = add2(acc, t);
+                }
+            }
+        }
+    }
+    s = group_sum<32>(acc.x + acc.y, 0xffffffffu);
+}
+
 // ---------------------------------------------------------------- k_prepare
 enum : int { TASK_ROW = 0, TASK_DP = 1, TASK_GRAD = 2 };
 
@@ -477,10 +532,55 @@ __device__ __forceinline__ int64_t block_scan_excl(int64_t n, int64_t* wsum, int
     return excl;
 }
 
+// Appends the chunk tasks of `kind` for every sample in DP order (p.order),
+// starting at task index t0, and returns how many it appended; chunks hold
+// kTaskRows rows (the last one of a sample fewer).  The row pass also resets
+// the per-sample scheduler counters.
+// The chunks of one sample are written by one warp, a chunk per lane.
+__device__ int64_t append_chunks(const Params& p, int64_t t0, int kind, int64_t* wsum,
+                                 int64_t& carry, int64_t* s_before, int* s_nch) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nwarps = blockDim.x >> 5;
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < p.B; base += blockDim.x) {
+        const int i = base + tid;
+        int nch = 0;
+        if (i < p.B) {
+            const int b = p.order[i];
+            const int64_t nrows = (int64_t)p.Tl[b] * (p.Ul[b] + 1);
+            nch = (int)((nrows + kTaskRows - 1) / kTaskRows);
+            if (kind == TASK_ROW) {
+                p.rtasks[b] = nch;
+                p.rdone[b] = 0;
+                p.dpdone[b] = 0;
+                p.dpclaim[b] = 0;
+            }
+        }
+        s_before[tid] = block_scan_excl(nch, wsum, carry);   // chunks before position i
+        s_nch[tid] = nch;
+        __syncthreads();
+        const int nb = min((int)blockDim.x, p.B - base);
+        for (int j = wid; j < nb; j += nwarps) {
+            const int ii = base + j;
+            const int b = p.order[ii];
+            const int64_t nrows = (int64_t)p.Tl[b] * (p.Ul[b] + 1);
+            for (int k = lane; k < s_nch[j]; k += 32) {
+                const int r = k * kTaskRows;
+                p.tasks[t0 + s_before[j] + k] =
+                    make_int4(kind | (b << 2), r, (int)min((int64_t)kTaskRows, nrows - r), 0);
+            }
+        }
+        __syncthreads();
+    }
+    return carry;
+}
+
 __global__ void __launch_bounds__(1024) k_prepare(Params p) {
     __shared__ int64_t wsum[32];
     __shared__ int64_t carry;
     __shared__ int errs;
+    __shared__ int64_t s_before[1024];
+    __shared__ int s_nch[1024];
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     if (tid == 0) {
         carry = 0;
@@ -553,56 +653,11 @@ __global__ void __launch_bounds__(1024) k_prepare(Params p) {
     // order, then the gradient chunks in the same order.  DP tasks are taken by
     // ticket (err[3]) in the same sample order.
     if (errs == 0) {
-        if (tid == 0) carry = 0;
-        __syncthreads();
-        int64_t tot = 0;
-        for (int base = 0; base < p.B; base += blockDim.x) {
-            const int i = base + tid;
-            int b = 0, nch = 0;
-            int64_t nrows = 0;
-            if (i < p.B) {
-                b = p.order[i];
-                nrows = (int64_t)p.Tl[b] * (p.Ul[b] + 1);
-                nch = (int)((nrows + kTaskRows - 1) / kTaskRows);
-                p.rtasks[b] = nch;
-                p.rdone[b] = 0;
-                p.dpdone[b] = 0;
-                p.dpclaim[b] = 0;
-            }
-            const int64_t before = block_scan_excl(nch, wsum, carry);   // row tasks before i
-            if (i < p.B) {
-                for (int k = 0; k < nch; ++k) {
-                    const int r = k * kTaskRows;
-                    p.tasks[before + k] = make_int4(TASK_ROW | (b << 2), r,
-                                                    (int)min((int64_t)kTaskRows, nrows - r), 0);
-                }
-            }
-            tot = carry;
-        }
-        // Gradient chunks after every row chunk.
-        const int64_t g0 = tot;
-        if (tid == 0) carry = 0;
-        __syncthreads();
-        for (int base = 0; base < p.B; base += blockDim.x) {
-            const int i = base + tid;
-            int b = 0, nch = 0;
-            int64_t nrows = 0;
-            if (i < p.B) {
-                b = p.order[i];
-                nrows = (int64_t)p.Tl[b] * (p.Ul[b] + 1);
-                nch = (int)((nrows + kTaskRows - 1) / kTaskRows);
-            }
-            const int64_t before = block_scan_excl(nch, wsum, carry);
-            if (i < p.B)
-                for (int k = 0; k < nch; ++k) {
-                    const int r = k * kTaskRows;
-                    p.tasks[g0 + before + k] = make_int4(
-                        TASK_GRAD | (b << 2), r, (int)min((int64_t)kTaskRows, nrows - r), 0);
-                }
-        }
+        const int64_t nrow = append_chunks(p, 0, TASK_ROW, wsum, carry, s_before, s_nch);
+        const int64_t ngrad = append_chunks(p, nrow, TASK_GRAD, wsum, carry, s_before, s_nch);
         if (tid == 0) {
             p.err[1] = 0;                          // next task
-            p.err[2] = (int)(g0 + tot);            // task count
+            p.err[2] = (int)(nrow + ngrad);        // task count
             p.err[3] = 0;                          // next DP ticket
         }
     }
@@ -765,25 +820,8 @@ __global__ void __launch_bounds__(256) k_row_tma(Params p) {
             fence_proxy_async();
             tma_row_load(buf + st * sb, X + seq.row(k + kStages) * (int64_t)V, rb, &bars[st]);
         }
-        float M = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < NV; ++i)
-            if (wl + 32 * i < nvec) M = fmaxf(M, E::vmax(q[i]));
-        M = group_max<32>(M, 0xffffffffu);
-        float s = 0.0f;
-        if (M != -INFINITY) {
-            const float ML = M * kLog2e;
-#pragma unroll
-            for (int i = 0; i < NV; ++i) {
-                if (wl + 32 * i < nvec) {
-                    float x[EPV];
-                    E::unpack(q[i], x);
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) s += ex2(fmaf(x[e], kLog2e, -ML));
-                }
-            }
-        }
-        s = group_sum<32>(s, 0xffffffffu);
+        float M, s;
+        row_stats<Tin, NV>(q, nvec, wl, M, s);
         const int it = (int)(k & 31);
         if (wl == it) {
             myM = M;
@@ -1600,25 +1638,8 @@ __device__ bool row_batch_tma(const Params& p, int64_t r0, int n, unsigned char*
             fence_proxy_async();
             tma_row_load(buf + st * sb, X + (r0 + i + kStages) * (int64_t)V, rb, &bars[st]);
         }
-        float M = -INFINITY;
-#pragma unroll
-        for (int v = 0; v < NV; ++v)
-            if (wl + 32 * v < nvec) M = fmaxf(M, E::vmax(q[v]));
-        M = group_max<32>(M, 0xffffffffu);
-        float sum = 0.0f;
-        if (M != -INFINITY) {
-            const float ML = M * kLog2e;
-#pragma unroll
-            for (int v = 0; v < NV; ++v) {
-                if (wl + 32 * v < nvec) {
-                    float x[EPV];
-                    E::unpack(q[v], x);
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) sum += ex2(fmaf(x[e], kLog2e, -ML));
-                }
-            }
-        }
-        sum = group_sum<32>(sum, 0xffffffffu);
+        float M, sum;
+        row_stats<Tin, NV>(q, nvec, wl, M, sum);
         if (wl == i) {
             myM = M;
             mys = sum;
@@ -1908,8 +1929,9 @@ __global__ void __launch_bounds__(256, 2) k_main(Params p) {
         const uint64_t t_start = (p.trace && tid == 0) ? global_ns() : 0;
         if (kind == TASK_ROW) {
             if (NV > 0) fence_proxy_async();   // smem may have been a DP ring
-            const int64_t rw = r0 + 32 * wid;
-            const int nw = min(32, n - 32 * wid);
+            const int per = (n + 7) >> 3;   // rows per warp: 32 for a full task
+            const int64_t rw = r0 + per * wid;
+            const int nw = min(per, n - per * wid);
             if (nw > 0) {
                 if (NV > 0) {
                     row_batch_tma<Tin, (NV > 0 ? NV : 1)>(p, rw, nw, buf, bars, kk);
