@@ -65,6 +65,8 @@ enum : int {
     ERR_MISMATCH = 8,
     ERR_NONFINITE = 16,
     ERR_TIMEOUT = 32,
+    ERR_INTERNAL = 64,   // a configuration the launching host code rules out
+
 };
 
 // ---------------------------------------------------------------- workspace
@@ -1243,6 +1245,249 @@ __device__ void dp_beta(const Params& p, const Samp& c, int u0, int w, int nwd, 
     if (u0 == 0 && lane == 0) p.lossb[c.b] = -((double)ve[0] + log2((double)vm[0])) * kLn2d;
 }
 
+// ---- DP over a table of diagonal bases (lattices with T+U <= kTabMax) ----
+// The same recursions with branch-free steps: every step issues the copy of
+// a future diagonal, waits for the next diagonal's records and loads them
+// one step ahead, so the only latency left inside a step is the
+// multiply -> shuffle -> add chain.  Warps of one direction are skewed by
+// kSkew diagonals (warp w of alpha works on diagonal e at step e + kSkew*w;
+// mirrored for beta), so a value crossing from one warp to the next was
+// written at least kSkew steps before it is read, and one named barrier per
+// kSkew steps orders the exchange.  Diagonal bases come from a shared table
+// filled once per sample.
+constexpr int kTabMax = 2048;   // table entries (diagonals)
+constexpr int kSkew = 4;        // steps between barriers = skew between warps
+constexpr int kXch = 16;        // exchange ring per warp (>= 2*kSkew + 2, a power of two)
+
+template <int N>
+__device__ __forceinline__ void cp_wait_mem() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void named_barrier_mem(int id, int threads) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Copies of diagonal e's records (base be) into a ring slot; `live` false
+// (e past the lattice) issues zero-filling copies that read nothing.
+template <int J>
+__device__ __forceinline__ void ring_issue_t(int4* slot, int e, int be, const Lanes<J>& L,
+                                             bool live) {
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const bool ok = live && (unsigned)(e - L.u[j]) < (unsigned)L.Tl[j];
+        cp16z(slot + j * 32, L.e[j] + (ok ? be : L.u[j]), ok);
+    }
+}
+
+template <int R>
+__device__ __forceinline__ int ring_next(int i) { return i + 1 == R ? 0 : i + 1; }
+
+template <int J>
+__device__ void dp_alpha_t(const Params& p, const Samp& c, int u0, int w, int nwd, int4* ring,
+                           float2* xch, const int* tab) {
+    constexpr int R = Ring<J>::R, PF = R - 2;
+    const int lane = threadIdx.x & 31, nthreads = nwd * 32;
+    Lanes<J> L;
+    lanes_init<J>(c, u0, lane, p.edge + c.off, p.alpha + c.off, L);
+    float am[J];
+    int ae[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        am[j] = L.u[j] == 0 ? 1.0f : 0.0f;
+        ae[j] = L.u[j] == 0 ? 0 : kZeroExp;
+    }
+    store_diag<J>(0, 0, L, am, ae);   // alpha(0,0) = 1 (base(0) = 0)
+    int4* const rl = ring + lane;
+    float2* const mine = xch + w * kXch;
+    const float2* const left = xch + (w > 0 ? w - 1 : 0) * kXch;
+    // Step e (e = 0..D-2) forms alpha(e+1) from the records of diagonal e.
+    int si = 0;
+    for (int k = 0; k < PF; ++k) {
+        ring_issue_t<J>(rl + si * (J * 32), k, tab[min(k, c.D - 1)], L, k < c.D);
+        cp_commit();
+        si = ring_next<R>(si);
+    }
+    const int nwork = c.D - 1;
+    const int nblk = (nwork + kSkew - 1) / kSkew;
+    if (nwd > 1)
+        for (int k = 0; k < w; ++k) named_barrier_mem(1, nthreads);
+    cp_wait_mem<PF - 1>();
+    int so = 0;
+    int4 edn[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) edn[j] = rl[j * 32];
+    so = ring_next<R>(so);
+    int e = 0;
+    for (int bk = 0; bk < nblk; ++bk) {
+#pragma unroll
+        for (int k = 0; k < kSkew; ++k, ++e) {
+            const bool act = e < nwork;
+            int4 ed[J];
+#pragma unroll
+            for (int j = 0; j < J; ++j) ed[j] = edn[j];
+            const int xs = (e + 1) & (kXch - 1);
+            const float2 nv = left[xs];
+            const int bst = tab[min(e + 1, c.D - 1)];
+            {
+                const int ee = e + PF;
+                ring_issue_t<J>(rl + si * (J * 32), ee, tab[min(ee, c.D - 1)], L, ee < c.D);
+                cp_commit();
+                si = ring_next<R>(si);
+            }
+            cp_wait_mem<PF - 1>();
+#pragma unroll
+            for (int j = 0; j < J; ++j) edn[j] = rl[so * (J * 32) + j * 32];
+            so = ring_next<R>(so);
+            float bm[J], ym[J];
+            int be[J], ye[J];
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                xf_mul(am[j], ae[j], __int_as_float(ed[j].x), ed[j].y - kEdgeBias, bm[j], be[j]);
+                xf_mul(am[j], ae[j], __int_as_float(ed[j].z), ed[j].w - kEdgeBias, ym[j], ye[j]);
+            }
+            if (lane == 31 && act) mine[xs] = make_float2(ym[J - 1], __int_as_float(ye[J - 1]));
+            float sm[J];
+            int se[J];
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                sm[j] = __shfl_sync(0xffffffffu, ym[j], (lane + 31) & 31);
+                se[j] = __shfl_sync(0xffffffffu, ye[j], (lane + 31) & 31);
+            }
+            const float edge_m = w > 0 ? nv.x : 0.0f;
+            const int edge_e = w > 0 ? __float_as_int(nv.y) : kZeroExp;
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const float nm = lane ? sm[j] : (j ? sm[j - 1] : edge_m);
+                const int ne = lane ? se[j] : (j ? se[j - 1] : edge_e);
+                float m;
+                int x;
+                if (k & 1) xf_add<true>(bm[j], be[j], nm, ne, m, x);
+                else xf_add<false>(bm[j], be[j], nm, ne, m, x);
+                am[j] = act ? m : am[j];
+                ae[j] = act ? x : ae[j];
+            }
+            if (act) store_diag<J>(e + 1, bst, L, am, ae);
+        }
+        if (nwd > 1) named_barrier_mem(1, nthreads);
+    }
+    if (nwd > 1)
+        for (int k = 0; k < nwd - 1 - w; ++k) named_barrier_mem(1, nthreads);
+    cp_wait<0>();
+    // P(y|x) = alpha(T-1,U) p_blank(T-1,U): the terminal blank (diagonal D-1).
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        if (L.u[j] == c.U) {
+            const int4 ed = __ldcg(L.e[j] + tab[c.D - 1]);
+            float m;
+            int x;
+            xf_mul(am[j], ae[j], __int_as_float(ed.x), ed.y - kEdgeBias, m, x);
+            xf_norm(m, x);
+            p.pm[c.b] = m;
+            p.pe[c.b] = x;
+            const double ll2 = (double)x + log2((double)m);
+            p.lossa[c.b] = -ll2 * kLn2d;
+            p.loss[c.b] = (float)(-ll2 * kLn2d);
+        }
+    }
+}
+
+template <int J>
+__device__ void dp_beta_t(const Params& p, const Samp& c, int u0, int w, int nwd, int4* ring,
+                          float2* xch, const int* tab) {
+    constexpr int R = Ring<J>::R, PF = R - 2;
+    const int lane = threadIdx.x & 31, nthreads = nwd * 32;
+    Lanes<J> L;
+    lanes_init<J>(c, u0, lane, p.edge + c.off, p.beta + c.off, L);
+    float vm[J];
+    int ve[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        vm[j] = L.u[j] == c.U ? 1.0f : 0.0f;
+        ve[j] = L.u[j] == c.U ? 0 : kZeroExp;
+    }
+    int4* const rl = ring + lane;
+    float2* const mine = xch + w * kXch;
+    const float2* const right = xch + (w + 1 < nwd ? w + 1 : w) * kXch;
+    // The slot of diagonal D holds this warp's first-column start value (read
+    // by warp w-1 at d = D-1, after the first barrier).
+    if (lane == 0) mine[c.D & (kXch - 1)] = make_float2(vm[0], __int_as_float(ve[0]));
+    // Step j (j = 0..D-1) forms beta on diagonal d = D-1-j from its records.
+    int si = 0;
+    for (int k = 0; k < PF; ++k) {
+        const int d = c.D - 1 - k;
+        ring_issue_t<J>(rl + si * (J * 32), d, tab[max(d, 0)], L, d >= 0);
+        cp_commit();
+        si = ring_next<R>(si);
+    }
+    const int nblk = (c.D + kSkew - 1) / kSkew;
+    if (nwd > 1)
+        for (int k = 0; k < nwd - 1 - w; ++k) named_barrier_mem(2, nthreads);
+    cp_wait_mem<PF - 1>();
+    int so = 0;
+    int4 edn[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) edn[j] = rl[j * 32];
+    so = ring_next<R>(so);
+    int d = c.D - 1;
+    for (int bk = 0; bk < nblk; ++bk) {
+#pragma unroll
+        for (int k = 0; k < kSkew; ++k, --d) {
+            const bool act = d >= 0;
+            int4 ed[J];
+#pragma unroll
+            for (int j = 0; j < J; ++j) ed[j] = edn[j];
+            const float2 nv = right[(d + 1) & (kXch - 1)];
+            const int bst = tab[max(d, 0)];
+            {
+                const int dd = d - PF;
+                ring_issue_t<J>(rl + si * (J * 32), dd, tab[max(dd, 0)], L, dd >= 0);
+                cp_commit();
+                si = ring_next<R>(si);
+            }
+            cp_wait_mem<PF - 1>();
+#pragma unroll
+            for (int j = 0; j < J; ++j) edn[j] = rl[so * (J * 32) + j * 32];
+            so = ring_next<R>(so);
+            float sm[J];
+            int se[J];
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                sm[j] = __shfl_sync(0xffffffffu, vm[j], (lane + 1) & 31);
+                se[j] = __shfl_sync(0xffffffffu, ve[j], (lane + 1) & 31);
+            }
+            const float edge_m = w + 1 < nwd ? nv.x : 0.0f;
+            const int edge_e = w + 1 < nwd ? __float_as_int(nv.y) : kZeroExp;
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const float nm = (lane < 31) ? sm[j] : (j + 1 < J ? sm[j + 1] : edge_m);
+                const int ne = (lane < 31) ? se[j] : (j + 1 < J ? se[j + 1] : edge_e);
+                float bm, ym, m;
+                int be, ye, x;
+                xf_mul(vm[j], ve[j], __int_as_float(ed[j].x), ed[j].y - kEdgeBias, bm, be);
+                xf_mul(nm, ne, __int_as_float(ed[j].z), ed[j].w - kEdgeBias, ym, ye);
+                if (k & 1) xf_add<true>(bm, be, ym, ye, m, x);
+                else xf_add<false>(bm, be, ym, ye, m, x);
+                vm[j] = act ? m : vm[j];
+                ve[j] = act ? x : ve[j];
+            }
+            if (act) {
+                store_diag<J>(d, bst, L, vm, ve);
+                if (lane == 0) mine[d & (kXch - 1)] = make_float2(vm[0], __int_as_float(ve[0]));
+            }
+        }
+        if (nwd > 1) named_barrier_mem(2, nthreads);
+    }
+    if (nwd > 1)
+        for (int k = 0; k < w; ++k) named_barrier_mem(2, nthreads);
+    cp_wait<0>();
+    if (u0 == 0 && lane == 0) {
+        float m = vm[0];
+        int x = ve[0];
+        xf_norm(m, x);
+        p.lossb[c.b] = -((double)x + log2((double)m)) * kLn2d;
+    }
+}
+
 // Target lattice columns per lane before another compute warp is added.
 #ifndef RNNT_DP_SLOTS
 #define RNNT_DP_SLOTS 1
@@ -1261,8 +1506,25 @@ __host__ __device__ inline int dp_ring_depth(int Jc) {
     return Jc == 1 ? 16 : Jc == 2 ? 12 : Jc <= 4 ? 10 : 6;
 }
 
+// Dynamic shared memory of the DP for lattices up to W columns: the rings of
+// the compute warps, then the table of diagonal bases.
+__host__ __device__ inline size_t dp_ring_bytes(int W) {
+    const int Jc = dp_jclass(dp_slots(W));
+    return (size_t)2 * dp_warps(W) * dp_ring_depth(Jc) * Jc * 32 * sizeof(int4);
+}
+__host__ __device__ inline size_t dp_smem_bytes(int W) {
+    return dp_ring_bytes(W) + (size_t)kTabMax * sizeof(int);
+}
+
+// Called by every thread of the CTA.  xch: 2 * kDpWarps * kXch entries.
 template <int J>
 __device__ __forceinline__ void dp_run(const Params& p, const Samp& c, int4* smem, float2* xch) {
+    int* tab = reinterpret_cast<int*>(reinterpret_cast<char*>(smem) + dp_ring_bytes(c.W));
+    const bool use_tab = c.D <= kTabMax;
+    if (use_tab) {
+        for (int d = threadIdx.x; d < c.D; d += blockDim.x) tab[d] = diag_base(c, d);
+        __syncthreads();
+    }
     // Direction warps interleave (alpha on even warp ids, beta on odd) so the
     // two recursions of a sample run on different SM sub-partitions.
     const int wid = threadIdx.x >> 5;
@@ -1270,20 +1532,19 @@ __device__ __forceinline__ void dp_run(const Params& p, const Samp& c, int4* sme
     const int nwd = dp_warps(c.W);
     if (w >= nwd) return;
     int4* ring = smem + (size_t)(dir * nwd + w) * Ring<J>::R * J * 32;
-    if (dir == 0) dp_alpha<J>(p, c, w * 32 * J, w, nwd, ring, xch);
-    else dp_beta<J>(p, c, w * 32 * J, w, nwd, ring, xch + 2 * kDpWarps);
-}
-
-// Dynamic shared memory of the DP for lattices up to W columns (8 rings).
-__host__ __device__ inline size_t dp_smem_bytes(int W) {
-    const int Jc = dp_jclass(dp_slots(W));
-    return (size_t)2 * dp_warps(W) * dp_ring_depth(Jc) * Jc * 32 * sizeof(int4);
+    if (use_tab) {
+        if (dir == 0) dp_alpha_t<J>(p, c, w * 32 * J, w, nwd, ring, xch, tab);
+        else dp_beta_t<J>(p, c, w * 32 * J, w, nwd, ring, xch + kDpWarps * kXch, tab);
+    } else {
+        if (dir == 0) dp_alpha<J>(p, c, w * 32 * J, w, nwd, ring, xch);
+        else dp_beta<J>(p, c, w * 32 * J, w, nwd, ring, xch + 2 * kDpWarps);
+    }
 }
 
 __global__ void __launch_bounds__(256) k_dp(Params p) {
     if (*p.err) return;
     extern __shared__ int4 smem[];
-    __shared__ float2 xch[4 * kDpWarps];
+    __shared__ float2 xch[2 * kDpWarps * kXch];
     Samp c;
     c.b = p.order[blockIdx.x];
     c.T = p.Tl[c.b];
@@ -1806,13 +2067,12 @@ __device__ __noinline__ void dp_task(const Params& p, int b, int4* smem, float2*
     c.W = c.U + 1;
     c.D = c.T + c.U;
     c.off = __ldg(p.off + b);
+    // The persistent kernel is launched only when every lattice's DP fits its
+    // shared memory, i.e. at most 2 columns per lane (W <= 256).
     const int J = dp_jclass(dp_slots(c.W));
     if (J == 1) dp_run<1>(p, c, smem, xch);
     else if (J == 2) dp_run<2>(p, c, smem, xch);
-    else if (J == 3) dp_run<3>(p, c, smem, xch);
-    else if (J == 4) dp_run<4>(p, c, smem, xch);
-    else if (J == 6) dp_run<6>(p, c, smem, xch);
-    else dp_run<8>(p, c, smem, xch);
+    else if (threadIdx.x == 0) atomicOr(p.err, ERR_INTERNAL);
 }
 
 // Trace record of task t: {kind | sample << 2, sm, start, end}, times in ns
@@ -1853,7 +2113,7 @@ __global__ void __launch_bounds__(256, 2) k_main(Params p) {
     __shared__ float4 s_info[kTaskRows];
     __shared__ uint16_t s_nz[kTaskRows];
     __shared__ int s_cnt[8];
-    __shared__ float2 xch[4 * kDpWarps];
+    __shared__ float2 xch[2 * kDpWarps * kXch];
     __shared__ int s_task, s_go;
     if (*p.err & (ERR_LENGTH | ERR_ROWS | ERR_TARGET)) return;   // uniform: set before launch
     const int tid = threadIdx.x, wid = tid >> 5, wl = tid & 31;
@@ -2014,7 +2274,7 @@ __global__ void __launch_bounds__(256) k_finalize(Params p) {
     const int tid = threadIdx.x;
     if (tid == 0) errs = *p.err;
     __syncthreads();
-    const bool ok_in = (errs & (ERR_LENGTH | ERR_ROWS | ERR_TARGET | ERR_TIMEOUT)) == 0;
+    const bool ok_in = (errs & (ERR_LENGTH | ERR_ROWS | ERR_TARGET | ERR_TIMEOUT | ERR_INTERNAL)) == 0;
     double s = 0.0;
     if (ok_in) {
         for (int b = tid; b < p.B; b += blockDim.x) {
@@ -2035,6 +2295,7 @@ __global__ void __launch_bounds__(256) k_finalize(Params p) {
         int st = RNNT_OK;
         if (errs & (ERR_LENGTH | ERR_ROWS | ERR_TARGET)) st = RNNT_INVALID_VALUE;
         else if (errs & ERR_TIMEOUT) st = RNNT_TIMEOUT;
+        else if (errs & ERR_INTERNAL) st = RNNT_LAUNCH_FAILED;
         else if (errs & (ERR_MISMATCH | ERR_NONFINITE)) st = RNNT_LOSS_MISMATCH;
         *p.err = errs;
         if (p.status) *p.status = st;
