@@ -678,16 +678,9 @@ __global__ void __launch_bounds__(1024) k_prepare(Params p) {
 // last frame before every label is out, and a label at u = U, have
 // probability 0 (the lattice has no such arc).
 template <typename Tin>
-__device__ __forceinline__ void row_finish(const Params& p, int64_t r, float M, float s) {
-    using E = Elt<Tin>;
-    const Tin* row = static_cast<const Tin*>(p.logits) + r * (int64_t)p.V;
-    const int b = find_sample(p.off, p.B, r);
-    const int T = __ldg(p.Tl + b), U = __ldg(p.Ul + b), W = U + 1;
-    const int64_t o = __ldg(p.off + b);
-    const unsigned rr = (unsigned)(r - o);
-    const int t = (int)(rr / (unsigned)W), u = (int)(rr - (unsigned)t * W);
-    const float hb = E::get(row, p.blank);
-    const float hy = (u < U) ? E::get(row, __ldg(p.targets + (int64_t)b * p.S + u)) : 0.0f;
+__device__ __forceinline__ void row_finish_at(const Params& p, int64_t r, float M, float s,
+                                              float hb, float hy, int t, int u, int T, int U,
+                                              int64_t o) {
     if (p.fused) {
         const float lse2v = fmaf(M, kLog2e, lg2(s));
         p.lse2[r] = lse2v;
@@ -702,6 +695,22 @@ __device__ __forceinline__ void row_finish(const Params& p, int64_t r, float M, 
     if (u < U) xf_prob(hy, M, s, ym, ye);
     p.edge[o + node_index(t, u, T, U)] =
         make_int4(__float_as_int(bm), be + kEdgeBias, __float_as_int(ym), ye + kEdgeBias);
+}
+
+// Row r with its sample looked up: the blank and label logits are read from
+// global memory.
+template <typename Tin>
+__device__ __forceinline__ void row_finish(const Params& p, int64_t r, float M, float s) {
+    using E = Elt<Tin>;
+    const Tin* row = static_cast<const Tin*>(p.logits) + r * (int64_t)p.V;
+    const int b = find_sample(p.off, p.B, r);
+    const int T = __ldg(p.Tl + b), U = __ldg(p.Ul + b), W = U + 1;
+    const int64_t o = __ldg(p.off + b);
+    const unsigned rr = (unsigned)(r - o);
+    const int t = (int)(rr / (unsigned)W), u = (int)(rr - (unsigned)t * W);
+    const float hb = E::get(row, p.blank);
+    const float hy = (u < U) ? E::get(row, __ldg(p.targets + (int64_t)b * p.S + u)) : 0.0f;
+    row_finish_at<Tin>(p, r, M, s, hb, hy, t, u, T, U, o);
 }
 
 // Group results (same in every lane of group g) for row it*NG+g of the batch
@@ -1868,15 +1877,24 @@ __device__ __forceinline__ bool wait_at_least(const int32_t* a, int target, int3
 
 // Warp: rows [r0, r0+n) (n <= 32) through the warp's TMA stage ring; kk counts
 // the ring's copies so far (stage kk % kStages, phase parity (kk / kStages) & 1).
+// Warp: rows [r0, r0+n) of sample b (T, U, first row o), one row per stage
+// of the warp's TMA ring; the lane that owns a row also takes the row's blank
+// and label logits from the staged copy.
 template <typename Tin, int NV>
 __device__ bool row_batch_tma(const Params& p, int64_t r0, int n, unsigned char* buf,
-                              uint64_t* bars, uint32_t& kk) {
+                              uint64_t* bars, uint32_t& kk, int b, int T, int U, int64_t o) {
     using E = Elt<Tin>;
     constexpr int EPV = E::kPerVec;
     const int wl = threadIdx.x & 31, sb = p.stage_bytes;
     const Tin* X = static_cast<const Tin*>(p.logits);
     const int V = p.V, nvec = V / EPV;
     const uint32_t rb = (uint32_t)V * sizeof(Tin);
+    // This lane's row (lane wl owns row r0 + wl): lattice node and label.
+    const unsigned rr = (unsigned)(r0 + wl - o);
+    const int W = U + 1;
+    const int t = (int)(rr / (unsigned)W), u = (int)(rr - (unsigned)t * W);
+    const int y = (wl < n && u < U) ? __ldg(p.targets + (int64_t)b * p.S + u) : -1;
+    float myhb = 0.0f, myhy = 0.0f;
     if (wl == 0) {
         fence_proxy_async();
         for (int i = 0; i < min(kStages, n); ++i) {
@@ -1894,6 +1912,11 @@ __device__ bool row_batch_tma(const Params& p, int64_t r0, int n, unsigned char*
 #pragma unroll
         for (int v = 0; v < NV; ++v)
             if (wl + 32 * v < nvec) q[v] = rv[wl + 32 * v];
+        if (wl == i) {
+            const Tin* rowp = reinterpret_cast<const Tin*>(buf + st * sb);
+            myhb = E::to_f(rowp[p.blank]);
+            myhy = y >= 0 ? E::to_f(rowp[y]) : 0.0f;
+        }
         __syncwarp();
         if (wl == 0 && i + kStages < n) {
             fence_proxy_async();
@@ -1912,7 +1935,7 @@ __device__ bool row_batch_tma(const Params& p, int64_t r0, int n, unsigned char*
         return false;
     }
     kk += n;
-    if (wl < n) row_finish<Tin>(p, r0 + wl, myM, mys);
+    if (wl < n) row_finish_at<Tin>(p, r0 + wl, myM, mys, myhb, myhy, t, u, T, U, o);
     return true;
 }
 
@@ -2194,7 +2217,9 @@ __global__ void __launch_bounds__(256, 2) k_main(Params p) {
             const int nw = min(per, n - per * wid);
             if (nw > 0) {
                 if (NV > 0) {
-                    row_batch_tma<Tin, (NV > 0 ? NV : 1)>(p, rw, nw, buf, bars, kk);
+                    row_batch_tma<Tin, (NV > 0 ? NV : 1)>(p, rw, nw, buf, bars, kk, b,
+                                                          __ldg(p.Tl + b), __ldg(p.Ul + b),
+                                                          __ldg(p.off + b));
                 } else if (wl < nw) {
                     row_finish<Tin>(p, rw + wl, 0.0f, 1.0f);
                 }
