@@ -447,30 +447,11 @@ __device__ __forceinline__ int smid() {
     return v;
 }
 
-// Packed fp32x2 arithmetic (two lanes of one 64-bit register pair).
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-    float2 d;
-    asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-        " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return d;
-}
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-    float2 d;
-    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-        " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-
 // Log-softmax statistics of one row held as NV 16-byte vectors per lane
 // (vector wl + 32 i of the row): M = max_k h_k and s = sum_k 2^(h_k log2 e -
-// M log2 e), both reduced over the warp.  Exponent arguments and partial sums
-// are formed two elements at a time with packed fp32x2 arithmetic (even and
-// odd elements in separate partial sums), in one fixed order shared by every
-// kernel that stages rows this way.
+// M log2 e), both reduced over the warp.  Even and odd elements go to two
+// partial sums, in one fixed order shared by every kernel that stages rows
+// this way.
 template <typename Tin, int NV>
 __device__ __forceinline__ void row_stats(const uint4* q, int nvec, int wl, float& M, float& s) {
     using E = Elt<Tin>;
@@ -480,10 +461,9 @@ __device__ __forceinline__ void row_stats(const uint4* q, int nvec, int wl, floa
     for (int i = 0; i < NV; ++i)
         if (wl + 32 * i < nvec) M = fmaxf(M, E::vmax(q[i]));
     M = group_max<32>(M, 0xffffffffu);
-    float2 acc = make_float2(0.0f, 0.0f);
+    float s0 = 0.0f, s1 = 0.0f;
     if (M != -INFINITY) {
         const float ML = M * kLog2e;
-        const float2 l2 = make_float2(kLog2e, kLog2e), c2 = make_float2(-ML, -ML);
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
             if (wl + 32 * i < nvec) {
@@ -491,15 +471,13 @@ __device__ __forceinline__ void row_stats(const uint4* q, int nvec, int wl, floa
                 E::unpack(q[i], x);
 #pragma unroll
                 for (int e = 0; e < EPV; e += 2) {
-                    float2 t = fma2(make_float2(x[e], x[e + 1]), l2, c2);
-                    t.x = ex2(t.x);
-                    t.y = ex2(t.y);
-                    acc = add2(acc, t);
+                    s0 += ex2(fmaf(x[e], kLog2e, -ML));
+                    s1 += ex2(fmaf(x[e + 1], kLog2e, -ML));
                 }
             }
         }
     }
-    s = group_sum<32>(acc.x + acc.y, 0xffffffffu);
+    s = group_sum<32>(s0 + s1, 0xffffffffu);
 }
 
 // ---------------------------------------------------------------- k_prepare
