@@ -45,6 +45,26 @@ def dist_info():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """The maximum of a per-rank scalar over all ranks (identity on one rank).
+
+    The GPU arm passes its CUDA device (NCCL); the multi-rank CPU tests pass
+    "cpu" with a gloo process group."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: int, ms: float, world: int) -> float:
+    """Whole-job units/s: every rank processes units_per_rank units (weak
+    scaling, one replica per rank) within the slowest rank's ms."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 def load_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -305,12 +325,8 @@ def run_gpu(args, rank, world, local_rank):
     step_ms = [ev[0].elapsed_time(ev[6]) for ev in evs]
     stage_ms = {s: statistics.mean(ev[i].elapsed_time(ev[i + 1]) for ev in evs)
                 for i, s in enumerate(STAGES)}
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * wl.elements / (ms / 1e3)
+    ms = max_over_ranks(statistics.mean(step_ms), world, dev)
+    value = job_throughput(wl.elements, ms, world)
 
     peak, peak_kind = load_peak()
     step_bytes = 2 * wl.elements * esize   # algorithmic: one logit read + one grad write
@@ -369,11 +385,7 @@ def run_gpu(args, rank, world, local_rank):
         b.record(stream)
         torch.cuda.synchronize()
         e2e_ms.append(a.elapsed_time(b))
-    e2e_t = statistics.mean(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_t], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_t = float(t.item())
+    e2e_t = max_over_ranks(statistics.mean(e2e_ms), world, dev)
     h2d = (h_logits.numel() * h_logits.element_size() + h_targets.numel() * 4
            + h_T.numel() * 4 + h_U.numel() * 4)
     d2h = h_loss.numel() * 4 + 4
@@ -382,7 +394,7 @@ def run_gpu(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "storage_dtype": cfg.dtype,
-        "data": "synthetic (seeded; shapes and value distribution of the BPE-ASR workload)",
+        "data": f"synthetic (seeded; shapes and value distribution of the {cfg.name} workload)",
         "config": config_of(wl, args, l2="flushed between steps (512 MiB write, then "
                                          "512 MiB read of another buffer); inputs 1 GB > L2"),
         "roofline": roof,
@@ -391,7 +403,7 @@ def run_gpu(args, rank, world, local_rank):
                           "algorithmic_bytes": step_bytes,
                           "note": "whole call: one logit read + one grad write per element"},
         "stages_ms": stage_ms,
-        "e2e": {"value": world * wl.elements / (e2e_t / 1e3), "unit": UNIT,
+        "e2e": {"value": job_throughput(wl.elements, e2e_t, world), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_t},
         "gpu_launches": (3 if persistent else 6) * args.steps,
         "clocks": clk,
