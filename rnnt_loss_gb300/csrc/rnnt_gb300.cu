@@ -449,35 +449,60 @@ __device__ __forceinline__ int smid() {
 
 // Log-softmax statistics of one row held as NV 16-byte vectors per lane
 // (vector wl + 32 i of the row): M = max_k h_k and s = sum_k 2^(h_k log2 e -
-// M log2 e), both reduced over the warp.  Even and odd elements go to two
-// partial sums, in one fixed order shared by every kernel that stages rows
-// this way.
+// M log2 e), both reduced over the warp.  The maximum is folded over packed
+// half2 (or float) words first and widened once; exponent arguments and the
+// two partial sums (even and odd elements) use packed fp32x2 FMA/add.  One
+// fixed order, shared by every kernel that stages rows this way.
 template <typename Tin, int NV>
 __device__ __forceinline__ void row_stats(const uint4* q, int nvec, int wl, float& M, float& s) {
-    using E = Elt<Tin>;
-    constexpr int EPV = E::kPerVec;
-    M = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < NV; ++i)
-        if (wl + 32 * i < nvec) M = fmaxf(M, E::vmax(q[i]));
-    M = group_max<32>(M, 0xffffffffu);
-    float s0 = 0.0f, s1 = 0.0f;
-    if (M != -INFINITY) {
-        const float ML = M * kLog2e;
+    if constexpr (std::is_same<Tin, __half>::value) {
+        __half2 m2 = __half2half2(__ushort_as_half((unsigned short)0xfc00u));   // -inf
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
             if (wl + 32 * i < nvec) {
-                float x[EPV];
-                E::unpack(q[i], x);
+                const __half2* h = reinterpret_cast<const __half2*>(&q[i]);
+                m2 = __hmax2(m2, __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3])));
+            }
+        }
+        const float2 mf = __half22float2(m2);
+        M = fmaxf(mf.x, mf.y);
+    } else {
+        M = -INFINITY;
 #pragma unroll
-                for (int e = 0; e < EPV; e += 2) {
-                    s0 += ex2(fmaf(x[e], kLog2e, -ML));
-                    s1 += ex2(fmaf(x[e + 1], kLog2e, -ML));
+        for (int i = 0; i < NV; ++i)
+            if (wl + 32 * i < nvec)
+                M = fmaxf(M, fmaxf(fmaxf(__uint_as_float(q[i].x), __uint_as_float(q[i].y)),
+                                   fmaxf(__uint_as_float(q[i].z), __uint_as_float(q[i].w))));
+    }
+    M = group_max<32>(M, 0xffffffffu);
+    float2 acc = make_float2(0.0f, 0.0f);
+    if (M != -INFINITY) {
+        const float ML = M * kLog2e;
+        const float2 l2 = make_float2(kLog2e, kLog2e), c2 = make_float2(-ML, -ML);
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            if (wl + 32 * i < nvec) {
+                float2 f[4];
+                if constexpr (std::is_same<Tin, __half>::value) {
+                    const __half2* h = reinterpret_cast<const __half2*>(&q[i]);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) f[k] = __half22float2(h[k]);
+                } else {
+                    f[0] = make_float2(__uint_as_float(q[i].x), __uint_as_float(q[i].y));
+                    f[1] = make_float2(__uint_as_float(q[i].z), __uint_as_float(q[i].w));
+                }
+                constexpr int NF = std::is_same<Tin, __half>::value ? 4 : 2;
+#pragma unroll
+                for (int k = 0; k < NF; ++k) {
+                    float2 t = __ffma2_rn(f[k], l2, c2);
+                    t.x = ex2(t.x);
+                    t.y = ex2(t.y);
+                    acc = __fadd2_rn(acc, t);
                 }
             }
         }
     }
-    s = group_sum<32>(s0 + s1, 0xffffffffu);
+    s = group_sum<32>(acc.x + acc.y, 0xffffffffu);
 }
 
 // ---------------------------------------------------------------- k_prepare
@@ -566,6 +591,7 @@ __global__ void __launch_bounds__(1024) k_prepare(Params p) {
         carry = 0;
         errs = 0;
         *reinterpret_cast<uint64_t*>(p.err + 4) = global_ns();   // trace origin
+        p.err[8] = 0;   // CTAs of the persistent kernel that have finished
     }
     __syncthreads();
     for (int base = 0; base < p.B; base += blockDim.x) {
@@ -2107,8 +2133,10 @@ __device__ __forceinline__ void run_dp_and_signal(const Params& p, int b, int4* 
 // their SM.  All other CTAs stream: row chunks, then gradient chunks.  A
 // gradient chunk whose DP nobody has started yet runs that DP itself, so
 // progress never depends on where CTAs land.
+__device__ void finalize_block(const Params& p);
+
 template <typename Tin, int NV, int G, bool VEC>
-__global__ void __launch_bounds__(256, 2) k_main(Params p) {
+__device__ __forceinline__ void main_body(const Params& p) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ uint64_t bars_all[8 * kStages];
     __shared__ float4 s_info[kTaskRows];
@@ -2270,18 +2298,36 @@ __global__ void __launch_bounds__(256, 2) k_main(Params p) {
     if (NV > 0 && wl == 0) tma_store_wait_all();
 }
 
+
+// The last CTA to finish runs the loss check and reduction (no separate
+// finalize launch): every CTA publishes its writes and counts itself out.
+template <typename Tin, int NV, int G, bool VEC>
+__global__ void __launch_bounds__(256, 2) k_main(Params p) {
+    main_body<Tin, NV, G, VEC>(p);
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&p.err[8], 1) == (int)gridDim.x - 1;
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        finalize_block(p);
+    }
+}
+
 // ---------------------------------------------------------------- finalize
-__global__ void __launch_bounds__(256) k_finalize(Params p) {
+// Loss check, reduction and status, by one CTA of 256 threads (every thread).
+__device__ void finalize_block(const Params& p) {
     __shared__ double part[256];
     __shared__ int errs;
     const int tid = threadIdx.x;
-    if (tid == 0) errs = *p.err;
+    if (tid == 0) errs = __ldcg(p.err);
     __syncthreads();
     const bool ok_in = (errs & (ERR_LENGTH | ERR_ROWS | ERR_TARGET | ERR_TIMEOUT | ERR_INTERNAL)) == 0;
     double s = 0.0;
     if (ok_in) {
         for (int b = tid; b < p.B; b += blockDim.x) {
-            const double la = p.lossa[b], lb = p.lossb[b];
+            const double la = __ldcg(p.lossa + b), lb = __ldcg(p.lossb + b);
             if (!(fabs(la - lb) <= 1e-3 * fmax(1.0, fabs(la)))) atomicOr(&errs, ERR_MISMATCH);
             s += la;
         }
@@ -2304,6 +2350,8 @@ __global__ void __launch_bounds__(256) k_finalize(Params p) {
         if (p.status) *p.status = st;
     }
 }
+
+__global__ void __launch_bounds__(256) k_finalize(Params p) { finalize_block(p); }
 
 // ---------------------------------------------------------------- grad scale
 template <typename Tin>
@@ -2629,9 +2677,7 @@ extern "C" rnnt_status_t rnnt_loss_fused_staged(
         const bool done = dt == RNNT_F32 ? launch_persistent<float>(p, st, sms, dev)
                                          : launch_persistent<__half>(p, st, sms, dev);
         if (done) {
-            for (int i = 2; i <= 5; ++i) mark(i);
-            k_finalize<<<1, 256, 0, st>>>(p);
-            mark(6);
+            for (int i = 2; i <= 6; ++i) mark(i);   // the kernel's last CTA finalized
             return cudaGetLastError() == cudaSuccess ? RNNT_OK : RNNT_LAUNCH_FAILED;
         }
     }
