@@ -342,11 +342,11 @@ def run_gpu(args, rank, world, local_rank):
     kernel_bytes = {"row_pass": wl.elements * esize if cfg.fused else 2 * rows * esize,
                     "grad_pass": 2 * wl.elements * esize if cfg.fused
                     else wl.elements * esize + 2 * rows * esize}
-    persistent = stage_ms["alpha_beta_dp"] + stage_ms["combine"] + stage_ms["grad_pass"] < 0.02
+    persistent = sum(stage_ms[s] for s in STAGES[1:]) < 0.03
     if persistent:
-        # One cooperative kernel ran every row, DP and gradient task.
-        # (its last CTA also runs the loss check and reduction: no finalize launch)
-        stage_ms = {"prepare": stage_ms["prepare"], "persistent_main": stage_ms["row_pass"]}
+        # One cooperative kernel ran everything: the preparation on its CTA 0, every
+        # row, DP and gradient task, and the loss check / reduction on its last CTA.
+        stage_ms = {"persistent_main": stage_ms["prepare"] + stage_ms["row_pass"]}
         kernel_bytes = {"persistent_main": step_bytes}
         dom = "persistent_main"
     else:
@@ -414,7 +414,7 @@ def run_gpu(args, rank, world, local_rank):
         "stages_ms": stage_ms,
         "e2e": {"value": job_throughput(wl.elements, e2e_t, world), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_t},
-        "gpu_launches": (2 if persistent else 6) * args.steps,
+        "gpu_launches": (1 if persistent else 6) * args.steps,
         "clocks": clk,
         "wall_ms_timed_region": wall * 1e3,
         "kernel_source_sha256_16": kernel_source_hash(),

@@ -39,6 +39,8 @@
 #include <stdint.h>
 #include <stdlib.h>
 
+#include <cooperative_groups.h>
+
 #include <algorithm>
 #include <mutex>
 #include <type_traits>
@@ -191,13 +193,13 @@ __device__ __forceinline__ int find_sample(const int64_t* off, int B, int64_t r)
     int lo = 0, hi = B;
     while (hi - lo > 1) {
         int mid = (lo + hi) >> 1;
-        if (__ldg(off + mid) <= r) lo = mid; else hi = mid;
+        if (__ldcg(off + mid) <= r) lo = mid; else hi = mid;
     }
     return lo;
 }
 // Rows are visited in increasing order; step to r's sample, searching only on a change.
 __device__ __forceinline__ int advance_sample(const int64_t* off, int B, int b, int64_t r) {
-    return (__ldg(off + b + 1) <= r) ? find_sample(off, B, r) : b;
+    return (__ldcg(off + b + 1) <= r) ? find_sample(off, B, r) : b;
 }
 
 // ------------------------------------------------ extended-range arithmetic
@@ -407,11 +409,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// A bounded wait gave up: set the timeout bit and, for diagnosis, record the
+// first site (err[9]: 1 TMA ring, 2 DP worker waiting for rows, 3 gradient
+// chunk waiting for its DP) and its argument (err[10]).
+__device__ __forceinline__ void report_timeout(int32_t* err, int site, int arg) {
+    if (atomicCAS(err + 9, 0, site) == 0) atomicExch(err + 10, arg);
+    atomicOr(err, ERR_TIMEOUT);
+}
 // Bounded wait for the copy of phase `parity`; false (error flag raised) on timeout.
+
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
     for (int i = 0; i < kWaitSpins; ++i)
         if (mbar_try_wait(bar, parity)) return true;
-    atomicOr(err, ERR_TIMEOUT);
+    report_timeout(err, 1, (int)parity);
     return false;
 }
 
@@ -577,21 +587,26 @@ __device__ int64_t append_chunks(const Params& p, int64_t t0, int kind, int64_t*
         }
         __syncthreads();
     }
-    return carry;
+    // Every thread reads the total before the next call's thread 0 resets carry.
+    const int64_t total = carry;
+    __syncthreads();
+    return total;
 }
 
-__global__ void __launch_bounds__(1024) k_prepare(Params p) {
+// Validation, offsets, DP order and task list, by one CTA (every thread);
+// s_before / s_nch: shared scratch of blockDim.x entries each.
+__device__ void prepare_block(const Params& p, int64_t* s_before, int* s_nch) {
     __shared__ int64_t wsum[32];
     __shared__ int64_t carry;
     __shared__ int errs;
-    __shared__ int64_t s_before[1024];
-    __shared__ int s_nch[1024];
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     if (tid == 0) {
         carry = 0;
         errs = 0;
         *reinterpret_cast<uint64_t*>(p.err + 4) = global_ns();   // trace origin
         p.err[8] = 0;   // CTAs of the persistent kernel that have finished
+        p.err[9] = 0;   // first timeout site (diagnosis)
+        p.err[10] = 0;
     }
     __syncthreads();
     for (int base = 0; base < p.B; base += blockDim.x) {
@@ -632,14 +647,26 @@ __global__ void __launch_bounds__(1024) k_prepare(Params p) {
         if (carry != p.rows) atomicOr(&errs, ERR_ROWS);
     }
     // Labels: in range and not blank (warp-transducer blog 5.2).
+    // Eight labels per thread per round, their loads issued together.
     const int64_t nt = (int64_t)p.B * p.S;
-    for (int64_t i = tid; i < nt; i += blockDim.x) {
-        const int b = (int)(i / p.S), u = (int)(i % p.S);
-        const int U = p.Ul[b];
-        if (U >= 0 && U <= p.S && u < U) {
-            const int y = p.targets[i];
-            if (y < 0 || y >= p.V || y == p.blank) atomicOr(&errs, ERR_TARGET);
+    for (int64_t i0 = tid; i0 < nt; i0 += 8 * (int64_t)blockDim.x) {
+        int y[8];
+        bool need[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int64_t i = i0 + (int64_t)k * blockDim.x;
+            need[k] = false;
+            y[k] = 0;
+            if (i < nt) {
+                const int b = (int)(i / p.S), u = (int)(i % p.S);
+                const int U = __ldg(p.Ul + b);
+                need[k] = U >= 0 && U <= p.S && u < U;
+                if (need[k]) y[k] = __ldg(p.targets + i);
+            }
         }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (need[k] && (y[k] < 0 || y[k] >= p.V || y[k] == p.blank)) atomicOr(&errs, ERR_TARGET);
     }
     // Longest DP first: key (T+U, area), ties by index.  O(B^2) rank sort.
     for (int b = tid; b < p.B; b += blockDim.x) {
@@ -669,6 +696,12 @@ __global__ void __launch_bounds__(1024) k_prepare(Params p) {
     }
     __syncthreads();
     if (tid == 0) *p.err = errs;
+}
+
+__global__ void __launch_bounds__(1024) k_prepare(Params p) {
+    __shared__ int64_t s_before[1024];
+    __shared__ int s_nch[1024];
+    prepare_block(p, s_before, s_nch);
 }
 
 // ---------------------------------------------------------------- row pass
@@ -709,7 +742,7 @@ __device__ __forceinline__ void row_finish(const Params& p, int64_t r, float M, 
     const Tin* row = static_cast<const Tin*>(p.logits) + r * (int64_t)p.V;
     const int b = find_sample(p.off, p.B, r);
     const int T = __ldg(p.Tl + b), U = __ldg(p.Ul + b), W = U + 1;
-    const int64_t o = __ldg(p.off + b);
+    const int64_t o = __ldcg(p.off + b);
     const unsigned rr = (unsigned)(r - o);
     const int t = (int)(rr / (unsigned)W), u = (int)(rr - (unsigned)t * W);
     const float hb = E::get(row, p.blank);
@@ -1590,7 +1623,7 @@ __device__ __forceinline__ float xf_to_float(float m, int e) {
 // SM may hold neighbouring lines in L1.
 __device__ __forceinline__ float4 combine_row(const Params& p, int64_t r, int b) {
     const int T = __ldg(p.Tl + b), U = __ldg(p.Ul + b), W = U + 1;
-    const int64_t o = __ldg(p.off + b);
+    const int64_t o = __ldcg(p.off + b);
     const unsigned rr = (unsigned)(r - o);
     const int t = (int)(rr / (unsigned)W), u = (int)(rr - (unsigned)t * W);
     const int64_t i = o + node_index(t, u, T, U);
@@ -2093,7 +2126,7 @@ __device__ __noinline__ void dp_task(const Params& p, int b, int4* smem, float2*
     c.U = __ldg(p.Ul + b);
     c.W = c.U + 1;
     c.D = c.T + c.U;
-    c.off = __ldg(p.off + b);
+    c.off = __ldcg(p.off + b);
     // The persistent kernel is launched only when every lattice's DP fits its
     // shared memory, i.e. at most 2 columns per lane (W <= 256).
     const int J = dp_jclass(dp_slots(c.W));
@@ -2144,10 +2177,13 @@ __device__ __forceinline__ void main_body(const Params& p) {
     __shared__ int s_cnt[8];
     __shared__ float2 xch[2 * kDpWarps * kXch];
     __shared__ int s_task, s_go;
-    if (*p.err & (ERR_LENGTH | ERR_ROWS | ERR_TARGET)) return;   // uniform: set before launch
+    // Set by the preparation before the grid barrier; read through L2 because
+    // the preparation ran inside this kernel (as are the offsets, order and
+    // task list: none of them is read through the read-only cache here).
+    if (__ldcg(p.err) & (ERR_LENGTH | ERR_ROWS | ERR_TARGET)) return;
     const int tid = threadIdx.x, wid = tid >> 5, wl = tid & 31;
     int4* dpsmem = reinterpret_cast<int4*>(smem_raw);
-    const int ntasks = p.err[2];
+    const int ntasks = __ldcg(p.err + 2);
 
     if (smid() < p.n_dp_sms) {
         for (;;) {
@@ -2155,18 +2191,18 @@ __device__ __forceinline__ void main_body(const Params& p) {
                 const int i = atomicAdd(&p.err[3], 1);
                 int go = 0;
                 if (i < p.B) {
-                    const int b = __ldg(p.order + i);
+                    const int b = __ldcg(p.order + i);
                     s_task = b;
                     // Wait for the sample's rows unless a streaming CTA took the DP.
                     for (int k = 0; k < kSpinLimit; ++k) {
                         if (ld_acquire(&p.dpclaim[b])) break;
-                        if (ld_acquire(&p.rdone[b]) >= __ldg(p.rtasks + b)) {
+                        if (ld_acquire(&p.rdone[b]) >= __ldcg(p.rtasks + b)) {
                             go = atomicCAS(&p.dpclaim[b], 0, 1) == 0;
                             break;
                         }
                         if (ld_acquire(p.err) & ERR_TIMEOUT) break;
                         __nanosleep(256);
-                        if (k == kSpinLimit - 1) atomicOr(p.err, ERR_TIMEOUT);
+                        if (k == kSpinLimit - 1) report_timeout(p.err, 2, b);
                     }
                     go = go ? 1 : 2;   // 1: run it, 2: skip this sample
                 }
@@ -2212,9 +2248,9 @@ __device__ __forceinline__ void main_body(const Params& p) {
         const bool go = s_go;
         __syncthreads();
         if (t >= ntasks || !go) break;
-        const int4 tk = p.tasks[t];
+        const int4 tk = __ldcg(p.tasks + t);
         const int kind = tk.x & 3, b = tk.x >> 2, n = tk.z;
-        const int64_t r0 = __ldg(p.off + b) + tk.y;
+        const int64_t r0 = __ldcg(p.off + b) + tk.y;
         const uint64_t t_start = (p.trace && tid == 0) ? global_ns() : 0;
         if (kind == TASK_ROW) {
             if (NV > 0) fence_proxy_async();   // smem may have been a DP ring
@@ -2225,7 +2261,7 @@ __device__ __forceinline__ void main_body(const Params& p) {
                 if (NV > 0) {
                     row_batch_tma<Tin, (NV > 0 ? NV : 1)>(p, rw, nw, buf, bars, kk, b,
                                                           __ldg(p.Tl + b), __ldg(p.Ul + b),
-                                                          __ldg(p.off + b));
+                                                          __ldcg(p.off + b));
                 } else if (wl < nw) {
                     row_finish<Tin>(p, rw + wl, 0.0f, 1.0f);
                 }
@@ -2244,14 +2280,14 @@ __device__ __forceinline__ void main_body(const Params& p) {
                     mode = 1;
                     break;
                 }
-                if (ld_acquire(&p.rdone[b]) >= __ldg(p.rtasks + b) &&
+                if (ld_acquire(&p.rdone[b]) >= __ldcg(p.rtasks + b) &&
                     ld_acquire(&p.dpclaim[b]) == 0 && atomicCAS(&p.dpclaim[b], 0, 1) == 0) {
                     mode = 2;
                     break;
                 }
                 if (ld_acquire(p.err) & ERR_TIMEOUT) break;
                 __nanosleep(128);
-                if (k == kSpinLimit - 1) atomicOr(p.err, ERR_TIMEOUT);
+                if (k == kSpinLimit - 1) report_timeout(p.err, 3, b);
             }
             s_go = mode;
         }
@@ -2301,8 +2337,15 @@ __device__ __forceinline__ void main_body(const Params& p) {
 
 // The last CTA to finish runs the loss check and reduction (no separate
 // finalize launch): every CTA publishes its writes and counts itself out.
+// The call's preparation runs first on CTA 0 (no separate launch); a grid-wide
+// barrier of the cooperative launch then releases every CTA.
 template <typename Tin, int NV, int G, bool VEC>
 __global__ void __launch_bounds__(256, 2) k_main(Params p) {
+    extern __shared__ __align__(128) unsigned char smem_dyn[];
+    if (blockIdx.x == 0)
+        prepare_block(p, reinterpret_cast<int64_t*>(smem_dyn),
+                      reinterpret_cast<int*>(smem_dyn + sizeof(int64_t) * blockDim.x));
+    cooperative_groups::this_grid().sync();
     main_body<Tin, NV, G, VEC>(p);
     __shared__ int s_last;
     __threadfence();
@@ -2403,19 +2446,40 @@ int grid_for(int64_t work_threads, int sms, int per_sm) {
 }
 
 // Resident 256-thread blocks per SM of a kernel (cached per kernel).
+// Resident CTAs per SM of `kernel` with 256 threads and `smem` bytes of
+// dynamic shared memory; sets the kernel's dynamic shared memory limit to
+// exactly `smem` (the limit, not only the launch's request, decides how many
+// CTAs a cooperative launch may place on an SM).  Cached per (kernel, smem).
 int occupancy(const void* kernel, size_t smem) {
     static const void* keys[128];
     static size_t smems[128];
     static int vals[128];
+    static const void* attr_fn[64];
+    static size_t attr_val[64];
+    // The kernel's current limit (per process; one device's attributes are
+    // assumed to match the others').
+    int slot = -1;
+    for (int i = 0; i < 64; ++i)
+        if (attr_fn[i] == kernel || !attr_fn[i]) {
+            slot = i;
+            break;
+        }
+    if (slot >= 0 && (attr_fn[slot] != kernel || attr_val[slot] != smem)) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        attr_fn[slot] = kernel;
+        attr_val[slot] = smem;
+    }
     for (int i = 0; i < 128 && keys[i]; ++i)
         if (keys[i] == kernel && smems[i] == smem) return vals[i];
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-        return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 256, smem) != cudaSuccess || n < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 256, smem) != cudaSuccess || n < 1) {
+        cudaGetLastError();
         n = 0;
+    }
     for (int i = 0; i < 128 && n > 0; ++i)
         if (!keys[i]) {
             vals[i] = n;
@@ -2566,7 +2630,11 @@ bool launch_persistent(const Params& p, cudaStream_t st, int sms, int dev) {
     q.zero_off = zero_off;
     q.zero_rows = zero_rows;
     void* args[] = {&q};
-    return cudaLaunchCooperativeKernel(fn, dim3(occ * sms), dim3(256), args, sm, st) == cudaSuccess;
+    if (cudaLaunchCooperativeKernel(fn, dim3(occ * sms), dim3(256), args, sm, st) != cudaSuccess) {
+        cudaGetLastError();   // not launched: the caller runs the staged kernels instead
+        return false;
+    }
+    return true;
 }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -2671,16 +2739,18 @@ extern "C" rnnt_status_t rnnt_loss_fused_staged(
             cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), st);
     };
     mark(0);
-    k_prepare<<<1, 1024, 0, st>>>(p);
-    mark(1);
     if (grad) {
+        // One cooperative kernel: preparation on its CTA 0, every task, and the
+        // loss check / reduction on its last CTA.
         const bool done = dt == RNNT_F32 ? launch_persistent<float>(p, st, sms, dev)
                                          : launch_persistent<__half>(p, st, sms, dev);
         if (done) {
-            for (int i = 2; i <= 6; ++i) mark(i);   // the kernel's last CTA finalized
+            for (int i = 1; i <= 6; ++i) mark(i);
             return cudaGetLastError() == cudaSuccess ? RNNT_OK : RNNT_LAUNCH_FAILED;
         }
     }
+    k_prepare<<<1, 1024, 0, st>>>(p);
+    mark(1);
     if (dt == RNNT_F32) launch_rows<float>(p, st, sms);
     else launch_rows<__half>(p, st, sms);
     mark(2);

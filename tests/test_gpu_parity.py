@@ -272,3 +272,21 @@ def test_persistent_and_staged_schedules_agree(case, monkeypatch):
     for a, b in zip(ref_gpu, got):
         assert torch.equal(a, b)
     full_compare(wl)
+
+
+def test_repeated_persistent_calls_all_succeed():
+    # Task-list construction and the scheduler's counters are rebuilt on every
+    # call: 25 calls in a row (one workspace, then fresh ones) must all succeed
+    # and agree bit for bit.
+    wl = W.subset(W.make("bpe_asr", "cuda"), 6)
+    dev = "cuda"
+    t = torch.as_tensor(wl.targets, device=dev)
+    Tl, Ul = torch.as_tensor(wl.T, device=dev), torch.as_tensor(wl.U, device=dev)
+    first = None
+    for i in range(25):
+        loss, red, grad, _ = rnnt_loss_forward(wl.logits, t, Tl, Ul, wl.cfg.blank, wl.cfg.clamp,
+                                               wl.cfg.reduction, wl.cfg.fused)   # raises on a bad status
+        if first is None:
+            first = (loss.clone(), grad.clone())
+        else:
+            assert torch.equal(loss, first[0]) and torch.equal(grad, first[1])
