@@ -359,7 +359,10 @@ __device__ __forceinline__ float group_sum(float v, unsigned gm) {
 // Each warp of the streaming passes owns kStages shared-memory row buffers,
 // each with an mbarrier; lane 0 issues one 1-D bulk copy (cp.async.bulk) per
 // row, the warp waits on the barrier's phase parity.  Every wait is bounded.
-constexpr int kStages = 4;
+#ifndef RNNT_KSTAGES
+#define RNNT_KSTAGES 4
+#endif
+constexpr int kStages = RNNT_KSTAGES;
 constexpr int kWaitSpins = 1 << 22;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
@@ -457,14 +460,15 @@ __device__ __forceinline__ int smid() {
     return v;
 }
 
-// Log-softmax statistics of one row held as NV 16-byte vectors per lane
-// (vector wl + 32 i of the row): M = max_k h_k and s = sum_k 2^(h_k log2 e -
-// M log2 e), both reduced over the warp.  The maximum is folded over packed
-// half2 (or float) words first and widened once; exponent arguments and the
-// two partial sums (even and odd elements) use packed fp32x2 FMA/add.  One
-// fixed order, shared by every kernel that stages rows this way.
+// Log-softmax partials of one row held as NV 16-byte vectors per lane
+// (vector wl + 32 i of the row), for this lane's elements only: m = their
+// maximum and s = sum of 2^(h log2 e - m log2 e) over them (m = -inf, s = 0
+// for a lane without finite elements).  No cross-lane work: the partials of
+// eight rows are merged together by lse_group8.  The maximum is folded over
+// packed half2 (or float) words first and widened once; exponent arguments
+// and the two partial sums (even and odd elements) use packed fp32x2 FMA/add.
 template <typename Tin, int NV>
-__device__ __forceinline__ void row_stats(const uint4* q, int nvec, int wl, float& M, float& s) {
+__device__ __forceinline__ void row_partial(const uint4* q, int nvec, int wl, float& m, float& s) {
     if constexpr (std::is_same<Tin, __half>::value) {
         __half2 m2 = __half2half2(__ushort_as_half((unsigned short)0xfc00u));   // -inf
 #pragma unroll
@@ -475,44 +479,98 @@ __device__ __forceinline__ void row_stats(const uint4* q, int nvec, int wl, floa
             }
         }
         const float2 mf = __half22float2(m2);
-        M = fmaxf(mf.x, mf.y);
+        m = fmaxf(mf.x, mf.y);
     } else {
-        M = -INFINITY;
+        m = -INFINITY;
 #pragma unroll
         for (int i = 0; i < NV; ++i)
             if (wl + 32 * i < nvec)
-                M = fmaxf(M, fmaxf(fmaxf(__uint_as_float(q[i].x), __uint_as_float(q[i].y)),
+                m = fmaxf(m, fmaxf(fmaxf(__uint_as_float(q[i].x), __uint_as_float(q[i].y)),
                                    fmaxf(__uint_as_float(q[i].z), __uint_as_float(q[i].w))));
     }
-    M = group_max<32>(M, 0xffffffffu);
     float2 acc = make_float2(0.0f, 0.0f);
-    if (M != -INFINITY) {
-        const float ML = M * kLog2e;
-        const float2 l2 = make_float2(kLog2e, kLog2e), c2 = make_float2(-ML, -ML);
+    const float mL = (m == -INFINITY) ? 0.0f : m * kLog2e;
+    const float2 l2 = make_float2(kLog2e, kLog2e), c2 = make_float2(-mL, -mL);
 #pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            if (wl + 32 * i < nvec) {
-                float2 f[4];
-                if constexpr (std::is_same<Tin, __half>::value) {
-                    const __half2* h = reinterpret_cast<const __half2*>(&q[i]);
+    for (int i = 0; i < NV; ++i) {
+        if (wl + 32 * i < nvec) {
+            float2 f[4];
+            if constexpr (std::is_same<Tin, __half>::value) {
+                const __half2* h = reinterpret_cast<const __half2*>(&q[i]);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) f[k] = __half22float2(h[k]);
-                } else {
-                    f[0] = make_float2(__uint_as_float(q[i].x), __uint_as_float(q[i].y));
-                    f[1] = make_float2(__uint_as_float(q[i].z), __uint_as_float(q[i].w));
-                }
-                constexpr int NF = std::is_same<Tin, __half>::value ? 4 : 2;
+                for (int k = 0; k < 4; ++k) f[k] = __half22float2(h[k]);
+            } else {
+                f[0] = make_float2(__uint_as_float(q[i].x), __uint_as_float(q[i].y));
+                f[1] = make_float2(__uint_as_float(q[i].z), __uint_as_float(q[i].w));
+            }
+            constexpr int NF = std::is_same<Tin, __half>::value ? 4 : 2;
 #pragma unroll
-                for (int k = 0; k < NF; ++k) {
-                    float2 t = __ffma2_rn(f[k], l2, c2);
-                    t.x = ex2(t.x);
-                    t.y = ex2(t.y);
-                    acc = __fadd2_rn(acc, t);
-                }
+            for (int k = 0; k < NF; ++k) {
+                float2 t = __ffma2_rn(f[k], l2, c2);
+                t.x = ex2(t.x);
+                t.y = ex2(t.y);
+                acc = __fadd2_rn(acc, t);
             }
         }
     }
-    s = group_sum<32>(acc.x + acc.y, 0xffffffffu);
+    s = acc.x + acc.y;
+}
+
+// Merges the log-softmax partial (bm, bs) into (am, as): the result stands for
+// max(am, bm) and the sum rescaled to it.  Bit-for-bit symmetric in its two
+// operands (the larger maximum's sum plus the other sum times 2^-|d|), so the
+// lanes of a butterfly all end with the same value.
+__device__ __forceinline__ void lse_merge(float& am, float& as, float bm, float bs) {
+    const float d = (bm - am) * kLog2e;
+    const float e = ex2(-fabsf(d));
+    const bool bigger = d > 0.0f;
+    const float hi = bigger ? bs : as, lo = bigger ? as : bs;
+    const bool skip = bm == -INFINITY;   // nothing to merge (also covers both -inf)
+    as = skip ? as : fmaf(lo, e, hi);
+    am = skip ? am : (bigger ? bm : am);
+}
+
+// Warp: merges every lane's partials (lm[j], ls[j]) of eight rows j = 0..7 by a
+// transposing butterfly (9 merges and 18 shuffles per lane for all eight
+// rows); on return lanes 4j..4j+3 hold row j's maximum M and sum S (relative
+// to M).  A row's result depends only on its own partials, whatever rows
+// share the group.
+__device__ __forceinline__ void lse_group8(const float (&lm)[8], const float (&ls)[8], int wl,
+                                           float& M, float& S) {
+    constexpr unsigned F = 0xffffffffu;
+    float am[4], as[4];
+    const bool h16 = wl & 16;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        am[k] = h16 ? lm[4 + k] : lm[k];
+        as[k] = h16 ? ls[4 + k] : ls[k];
+        const float rm = __shfl_xor_sync(F, h16 ? lm[k] : lm[4 + k], 16);
+        const float rs = __shfl_xor_sync(F, h16 ? ls[k] : ls[4 + k], 16);
+        lse_merge(am[k], as[k], rm, rs);
+    }
+    float bm[2], bs[2];
+    const bool h8 = wl & 8;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        bm[k] = h8 ? am[2 + k] : am[k];
+        bs[k] = h8 ? as[2 + k] : as[k];
+        const float rm = __shfl_xor_sync(F, h8 ? am[k] : am[2 + k], 8);
+        const float rs = __shfl_xor_sync(F, h8 ? as[k] : as[2 + k], 8);
+        lse_merge(bm[k], bs[k], rm, rs);
+    }
+    const bool h4 = wl & 4;
+    M = h4 ? bm[1] : bm[0];
+    S = h4 ? bs[1] : bs[0];
+    {
+        const float rm = __shfl_xor_sync(F, h4 ? bm[0] : bm[1], 4);
+        const float rs = __shfl_xor_sync(F, h4 ? bs[0] : bs[1], 4);
+        lse_merge(M, S, rm, rs);
+    }
+#pragma unroll
+    for (int o = 2; o > 0; o >>= 1) {
+        const float rm = __shfl_xor_sync(F, M, o), rs = __shfl_xor_sync(F, S, o);
+        lse_merge(M, S, rm, rs);
+    }
 }
 
 // ---------------------------------------------------------------- k_prepare
@@ -853,35 +911,56 @@ __global__ void __launch_bounds__(256) k_row_tma(Params p) {
         for (int64_t k = 0; k < min((int64_t)kStages, seq.count); ++k)
             tma_row_load(buf + (k % kStages) * sb, X + seq.row(k) * (int64_t)V, rb,
                          &bars[k % kStages]);
+    // Groups of 8 sequence positions (8-aligned, so inside one 32-row batch):
+    // per-lane partials of each row, then one butterfly merge per group.
     float myM = 0.0f, mys = 0.0f;
-    int64_t k = 0;
-    for (; k < seq.count; ++k) {
-        const int st = (int)(k % kStages);
-        if (!mbar_wait(&bars[st], (uint32_t)((k / kStages) & 1), p.err)) break;
-        const uint4* rv = reinterpret_cast<const uint4*>(buf + st * sb);
-        uint4 q[NV];
+    int64_t kfail = -1;
+    for (int64_t k0 = 0; k0 < seq.count; k0 += 8) {
+        float lm[8], ls[8];
 #pragma unroll
-        for (int i = 0; i < NV; ++i)
-            if (wl + 32 * i < nvec) q[i] = rv[wl + 32 * i];
-        __syncwarp();
-        if (wl == 0 && k + kStages < seq.count) {   // refill this stage
-            fence_proxy_async();
-            tma_row_load(buf + st * sb, X + seq.row(k + kStages) * (int64_t)V, rb, &bars[st]);
+        for (int j = 0; j < 8; ++j) {
+            lm[j] = -INFINITY;
+            ls[j] = 0.0f;
+            const int64_t k = k0 + j;
+            if (kfail < 0 && k < seq.count) {
+                const int st = (int)(k % kStages);
+                if (!mbar_wait(&bars[st], (uint32_t)((k / kStages) & 1), p.err)) {
+                    kfail = k;
+                } else {
+                    const uint4* rv = reinterpret_cast<const uint4*>(buf + st * sb);
+                    uint4 q[NV];
+#pragma unroll
+                    for (int i = 0; i < NV; ++i)
+                        if (wl + 32 * i < nvec) q[i] = rv[wl + 32 * i];
+                    __syncwarp();
+                    if (wl == 0 && k + kStages < seq.count) {   // refill this stage
+                        fence_proxy_async();
+                        tma_row_load(buf + st * sb, X + seq.row(k + kStages) * (int64_t)V, rb,
+                                     &bars[st]);
+                    }
+                    row_partial<Tin, NV>(q, nvec, wl, lm[j], ls[j]);
+                }
+            }
         }
-        float M, s;
-        row_stats<Tin, NV>(q, nvec, wl, M, s);
-        const int it = (int)(k & 31);
-        if (wl == it) {
-            myM = M;
-            mys = s;
+        if (kfail >= 0) break;
+        float M, S;
+        lse_group8(lm, ls, wl, M, S);
+        const float vM = __shfl_sync(0xffffffffu, M, 4 * (wl & 7));
+        const float vS = __shfl_sync(0xffffffffu, S, 4 * (wl & 7));
+        if ((wl & 24) == (int)(k0 & 31)) {
+            myM = vM;
+            mys = vS;
         }
-        if (it == 31 || k == seq.count - 1) {
-            if (wl <= it) row_finish<Tin>(p, seq.row(k - it + wl), myM, mys);
+        const int64_t kl = min(k0 + 7, seq.count - 1);
+        const int it = (int)(kl & 31);
+        if (it == 31 || kl == seq.count - 1) {
+            if (wl <= it) row_finish<Tin>(p, seq.row(kl - it + wl), myM, mys);
         }
     }
     // After a timeout, wait (bounded) for the copies still in flight before exiting.
-    for (int64_t q = k; q < min(k + kStages, seq.count); ++q)
-        mbar_wait(&bars[q % kStages], (uint32_t)((q / kStages) & 1), p.err);
+    if (kfail >= 0)
+        for (int64_t q = kfail; q < min(kfail + kStages, seq.count); ++q)
+            mbar_wait(&bars[q % kStages], (uint32_t)((q / kStages) & 1), p.err);
 }
 
 // Long rows (or rows not 16-byte aligned): streaming max/sum with rescale.
@@ -1940,34 +2019,51 @@ __device__ bool row_batch_tma(const Params& p, int64_t r0, int n, unsigned char*
         }
     }
     float myM = 0.0f, mys = 0.0f;
-    int i = 0;
-    for (; i < n; ++i) {
-        const uint32_t k = kk + i, st = k % kStages;
-        if (!mbar_wait(&bars[st], (k / kStages) & 1, p.err)) break;
-        const uint4* rv = reinterpret_cast<const uint4*>(buf + st * sb);
-        uint4 q[NV];
+    int ifail = -1;
+    for (int g0 = 0; g0 < n; g0 += 8) {
+        float lm[8], ls[8];
 #pragma unroll
-        for (int v = 0; v < NV; ++v)
-            if (wl + 32 * v < nvec) q[v] = rv[wl + 32 * v];
-        if (wl == i) {
-            const Tin* rowp = reinterpret_cast<const Tin*>(buf + st * sb);
-            myhb = E::to_f(rowp[p.blank]);
-            myhy = y >= 0 ? E::to_f(rowp[y]) : 0.0f;
+        for (int j = 0; j < 8; ++j) {
+            lm[j] = -INFINITY;
+            ls[j] = 0.0f;
+            const int i = g0 + j;
+            if (ifail < 0 && i < n) {
+                const uint32_t k = kk + i, st = k % kStages;
+                if (!mbar_wait(&bars[st], (k / kStages) & 1, p.err)) {
+                    ifail = i;
+                } else {
+                    const uint4* rv = reinterpret_cast<const uint4*>(buf + st * sb);
+                    uint4 q[NV];
+#pragma unroll
+                    for (int v = 0; v < NV; ++v)
+                        if (wl + 32 * v < nvec) q[v] = rv[wl + 32 * v];
+                    if (wl == i) {
+                        const Tin* rowp = reinterpret_cast<const Tin*>(buf + st * sb);
+                        myhb = E::to_f(rowp[p.blank]);
+                        myhy = y >= 0 ? E::to_f(rowp[y]) : 0.0f;
+                    }
+                    __syncwarp();
+                    if (wl == 0 && i + kStages < n) {
+                        fence_proxy_async();
+                        tma_row_load(buf + st * sb, X + (r0 + i + kStages) * (int64_t)V, rb,
+                                     &bars[st]);
+                    }
+                    row_partial<Tin, NV>(q, nvec, wl, lm[j], ls[j]);
+                }
+            }
         }
-        __syncwarp();
-        if (wl == 0 && i + kStages < n) {
-            fence_proxy_async();
-            tma_row_load(buf + st * sb, X + (r0 + i + kStages) * (int64_t)V, rb, &bars[st]);
-        }
-        float M, sum;
-        row_stats<Tin, NV>(q, nvec, wl, M, sum);
-        if (wl == i) {
-            myM = M;
-            mys = sum;
+        if (ifail >= 0) break;
+        float M, S;
+        lse_group8(lm, ls, wl, M, S);
+        const float vM = __shfl_sync(0xffffffffu, M, 4 * (wl & 7));
+        const float vS = __shfl_sync(0xffffffffu, S, 4 * (wl & 7));
+        if ((wl & 24) == g0) {
+            myM = vM;
+            mys = vS;
         }
     }
-    if (i < n) {   // timeout: wait (bounded) for the copies still in flight
-        for (int q = i; q < min(i + kStages, n); ++q)
+    if (ifail >= 0) {   // timeout: wait (bounded) for the copies still in flight
+        for (int q = ifail; q < min(ifail + kStages, n); ++q)
             mbar_wait(&bars[(kk + q) % kStages], ((kk + q) / kStages) & 1, p.err);
         return false;
     }
@@ -2608,7 +2704,11 @@ bool launch_persistent(const Params& p, cudaStream_t st, int sms, int dev) {
         sm = std::max(sm, (size_t)8 * kStages * p.stage_bytes);
         sm = (sm + 127) / 128 * 128;
         const int rb = V * (int)sizeof(Tin);
-        const int room = sm < 110 * 1024 ? (int)(110 * 1024 - sm) / rb : 0;
+        // Zero-row buffer from what is left of the dynamic shared memory that
+        // still lets two CTAs share an SM (228 KB per SM, ~8.3 KB static and
+        // 1 KB reserved per CTA).
+        constexpr int kTwoCtaSmem = 104 * 1024;
+        const int room = sm < kTwoCtaSmem ? (int)(kTwoCtaSmem - sm) / rb : 0;
         zero_rows = std::max(1, std::min(16384 / rb, room));
         zero_off = (int)sm;
         sm += (size_t)zero_rows * rb;
