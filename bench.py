@@ -36,7 +36,7 @@ METRIC = "RNN-T loss+grad logit elements/s (fwd+bwd, 1 GB300); % of HBM roofline
 UNIT = "logit elements/s"
 FALLBACK_HBM_GBS = 6800.0
 STAGES = ("prepare", "row_pass", "alpha_beta_dp", "combine", "grad_pass", "finalize")
-KERNEL_FILE = os.path.join(ROOT, "rnnt_loss_gb300", "csrc", "rnnt_gb300.cu")
+KERNEL_FILE = os.path.join(ROOT, "rnn_transducer_loss_gb300", "csrc", "rnnt_gb300.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 
 
@@ -180,7 +180,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     import oracle
-    from rnnt_loss_gb300 import workloads as W
+    from rnn_transducer_loss_gb300 import workloads as W
     oracle.build()
     wl = W.make(args.workload, "cpu")
     cores = oracle.num_threads()
@@ -218,10 +218,10 @@ def config_of(wl, args, l2):
 def run_gpu(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
-    from rnnt_loss_gb300 import _native as N
-    from rnnt_loss_gb300 import build as B
-    from rnnt_loss_gb300 import workloads as W
-    from rnnt_loss_gb300.functional import _DT, rnnt_loss_forward
+    from rnn_transducer_loss_gb300 import _native as N
+    from rnn_transducer_loss_gb300 import build as B
+    from rnn_transducer_loss_gb300 import workloads as W
+    from rnn_transducer_loss_gb300.functional import _DT, rnnt_loss_forward
 
     B.build()
     N.load()
@@ -277,7 +277,7 @@ def run_gpu(args, rank, world, local_rank):
 
     if args.trace:
         # Task timeline of the persistent kernel (after two warm calls).
-        from rnnt_loss_gb300 import trace as TR
+        from rnn_transducer_loss_gb300 import trace as TR
         ev = make_events()
         for _ in range(2):
             flush_l2()

@@ -1,4 +1,4 @@
-"""rnnt_loss_gb300: fused RNN-T (transducer) loss forward+backward for GB300.
+"""rnn_transducer_loss_gb300: fused RNN-T (transducer) loss forward+backward for GB300.
 
 The compute path is a C-ABI shared library (``librnnt_gb300.so``, declared in
 ``include/rnnt_gb300.h``) of hand-written CUDA kernels for sm_103a.  This

@@ -1,7 +1,7 @@
 """ctypes binding of librnnt_gb300.so (include/rnnt_gb300.h); argument marshalling only.
 
 The function names mirror the C ABI.  The library is loaded lazily; if it is
-missing the call raises (build it with ``python -m rnnt_loss_gb300.build`` or
+missing the call raises (build it with ``python -m rnn_transducer_loss_gb300.build`` or
 ``__graft_entry__.build()``).  Nothing here computes any part of the loss.
 """
 from __future__ import annotations
@@ -40,7 +40,7 @@ def load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise RuntimeError(
             f"{LIB_PATH} not found: the CUDA library is required (there is no fallback); "
-            "build it with `python -m rnnt_loss_gb300.build`")
+            "build it with `python -m rnn_transducer_loss_gb300.build`")
     lib = ctypes.CDLL(LIB_PATH)
     P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
                             ctypes.c_size_t)

@@ -6,8 +6,8 @@ import numpy as np
 import torch
 
 import oracle
-from rnnt_loss_gb300 import workloads as W
-from rnnt_loss_gb300.functional import rnnt_loss_forward
+from rnn_transducer_loss_gb300 import workloads as W
+from rnn_transducer_loss_gb300.functional import rnnt_loss_forward
 
 # Tolerances of the benchmark spec: fp32 inputs loss rel 1e-5 / grad abs 1e-5,
 # fp16 inputs (fp32 accumulation) loss rel 1e-3 / grad abs 2e-3.

@@ -6,8 +6,8 @@ import re
 
 import pytest
 
-from rnnt_loss_gb300 import _native as N
-from rnnt_loss_gb300 import build as B
+from rnn_transducer_loss_gb300 import _native as N
+from rnn_transducer_loss_gb300 import build as B
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 

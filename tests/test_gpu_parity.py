@@ -8,9 +8,9 @@ import pytest
 import torch
 
 import oracle
-from rnnt_loss_gb300 import workloads as W
-from rnnt_loss_gb300 import _native as N
-from rnnt_loss_gb300.functional import rnnt_loss, rnnt_loss_forward
+from rnn_transducer_loss_gb300 import workloads as W
+from rnn_transducer_loss_gb300 import _native as N
+from rnn_transducer_loss_gb300.functional import rnnt_loss, rnnt_loss_forward
 
 from parity_util import (TOL, assert_grad_close, assert_loss_close, gpu_run, oracle_full,
                          sampled_rows, to_np)

@@ -12,9 +12,9 @@ import numpy as np
 import pytest
 import torch
 
-from rnnt_loss_gb300 import _native as N
-from rnnt_loss_gb300 import workloads as W
-from rnnt_loss_gb300.functional import _DT
+from rnn_transducer_loss_gb300 import _native as N
+from rnn_transducer_loss_gb300 import workloads as W
+from rnn_transducer_loss_gb300.functional import _DT
 
 from parity_util import TOL, assert_grad_close, assert_loss_close, to_np
 
