@@ -63,10 +63,10 @@ def _load():
     lib.rnnt_oracle_forward.argtypes = [P, i32, i32, i32, i32, P, i32, i32, P, P, P, P, P]
     lib.rnnt_oracle_forward.restype = i32
     lib.rnnt_oracle_grad.argtypes = [P, i32, i32, i32, i32, P, i32, i32, P, P, P, P, dbl, dbl,
-                                     i64, i64, P]
+                                     dbl, i64, i64, P]
     lib.rnnt_oracle_grad.restype = i32
     lib.rnnt_oracle_batch.argtypes = [P, i32, i64, i32, P, i32, P, P, i32, i32, dbl, i32, i32,
-                                      P, P, P, P]
+                                      dbl, P, P, P, P]
     lib.rnnt_oracle_batch.restype = i32
     lib.rnnt_oracle_num_threads.argtypes = []
     lib.rnnt_oracle_num_threads.restype = i32
@@ -143,7 +143,8 @@ def sample_forward(x: np.ndarray, T: int, U: int, y, blank: int, fused: bool) ->
 
 
 def sample_grad(x: np.ndarray, fw: SampleForward, y, blank: int, fused: bool, clamp: float,
-                scale: float, r0: int = 0, r1: int | None = None) -> np.ndarray:
+                scale: float, r0: int = 0, r1: int | None = None,
+                fastemit_lambda: float = 0.0) -> np.ndarray:
     """Gradient rows [r0, r1) of one sample (float64, (r1-r0, V))."""
     x = np.ascontiguousarray(x)
     V = x.shape[1]
@@ -153,7 +154,8 @@ def sample_grad(x: np.ndarray, fw: SampleForward, y, blank: int, fused: bool, cl
     g = np.empty((r1 - r0, V))
     rc = _load().rnnt_oracle_grad(_ptr(x), _dtype_code(x), V, fw.T, fw.U, _ptr(yy), blank,
                                   int(bool(fused)), _ptr(fw.lpb), _ptr(fw.lpy), _ptr(fw.alpha),
-                                  _ptr(fw.beta), float(clamp), float(scale), r0, r1, _ptr(g))
+                                  _ptr(fw.beta), float(clamp), float(scale),
+                                  float(fastemit_lambda), r0, r1, _ptr(g))
     if rc != 0:
         raise ValueError("oracle grad rejected its arguments")
     return g
@@ -169,8 +171,12 @@ class BatchResult:
 
 def rnnt_loss(logits: np.ndarray, targets, logit_lengths, target_lengths, blank: int = -1,
               clamp: float = -1.0, reduction: str = "mean", fused_log_softmax: bool = True,
-              want_grad: bool = True) -> BatchResult:
-    """Whole-batch oracle; samples run in parallel on the host cores."""
+              want_grad: bool = True, fastemit_lambda: float = 0.0) -> BatchResult:
+    """Whole-batch oracle; samples run in parallel on the host cores.
+
+    ``fastemit_lambda`` (>= 0) scales the gradient of every label-emission
+    log-probability by 1 + lambda (FastEmit); the losses do not depend on it.
+    """
     x = np.ascontiguousarray(logits)
     rows, V = x.shape
     tg = np.ascontiguousarray(np.asarray(targets, dtype=np.int32))
@@ -186,7 +192,8 @@ def rnnt_loss(logits: np.ndarray, targets, logit_lengths, target_lengths, blank:
     grad = np.empty((rows, V)) if want_grad else None
     rc = _load().rnnt_oracle_batch(_ptr(x), _dtype_code(x), rows, V, _ptr(tg), tg.shape[1],
                                    _ptr(T), _ptr(U), B, blank, float(clamp),
-                                   int(bool(fused_log_softmax)), _RED[reduction], _ptr(losses),
+                                   int(bool(fused_log_softmax)), _RED[reduction],
+                                   float(fastemit_lambda), _ptr(losses),
                                    _ptr(losses_b), _ptr(red),
                                    _ptr(grad) if grad is not None else None)
     if rc != 0:

@@ -11,6 +11,13 @@ GPURNNT docs: negative log likelihood over all alignments; warp-transducer
 blog section 1.1: the loss sums over every legal alignment).  The loss is
 -logsumexp over alignments; the gradient is float64 autograd of that
 expression, through log_softmax when the rows are raw logits.
+
+FastEmit (``fastemit_lambda``, the GPURNNT docs' regulariser weight): the
+objective that is differentiated adds, for every alignment, lambda times its
+posterior weight (a constant, computed here by enumeration) times the sum of
+its label-emission log-probabilities, with a minus sign.  Its gradient is the
+transducer gradient with every label-emission log-probability's term scaled
+by 1 + lambda; the reported loss stays -log P(y|x).
 """
 from __future__ import annotations
 
@@ -34,31 +41,45 @@ def num_alignments(T: int, U: int) -> int:
     return math.comb(T - 1 + U, U)
 
 
-def sample_loss(h: torch.Tensor, T: int, U: int, y, blank: int, fused: bool) -> torch.Tensor:
-    """-log P(y|x) of one sample; h is its (T*(U+1), V) block (float64, may require grad)."""
+def sample_loss(h: torch.Tensor, T: int, U: int, y, blank: int, fused: bool,
+                fastemit_lambda: float = 0.0):
+    """-log P(y|x) of one sample; h is its (T*(U+1), V) block (float64, may require grad).
+
+    With ``fastemit_lambda`` != 0 returns (loss, objective): the objective is
+    the loss plus the FastEmit term (module docstring); differentiate it for
+    the gradient."""
     V = h.shape[1]
     blank = blank + V if blank < 0 else blank
     lp = torch.log_softmax(h, dim=1) if fused else h
     W = U + 1
-    scores = []
+    scores, label_scores = [], []
     for path in alignments(T, U):
         t = u = 0
         s = h.new_zeros(())
+        sl = h.new_zeros(())
         for move in path:
             r = t * W + u
             if move == "b":
                 s = s + lp[r, blank]
                 t += 1
             else:
-                s = s + lp[r, int(y[u])]
+                e = lp[r, int(y[u])]
+                s = s + e
+                sl = sl + e
                 u += 1
         s = s + lp[(T - 1) * W + U, blank]
         scores.append(s)
-    return -torch.logsumexp(torch.stack(scores), dim=0)
+        label_scores.append(sl)
+    sc = torch.stack(scores)
+    loss = -torch.logsumexp(sc, dim=0)
+    if not fastemit_lambda:
+        return loss
+    weight = torch.softmax(sc.detach(), dim=0)   # posterior of every alignment
+    return loss, loss - fastemit_lambda * (weight * torch.stack(label_scores)).sum()
 
 
 def rnnt_loss(logits, targets, logit_lengths, target_lengths, blank=-1, clamp=-1.0,
-              reduction="mean", fused_log_softmax=True):
+              reduction="mean", fused_log_softmax=True, fastemit_lambda=0.0):
     """Batch loss and gradient; returns (per-sample losses, reduced, grad) in float64."""
     x = torch.as_tensor(logits).to(torch.float64).detach().clone().requires_grad_(True)
     T = [int(v) for v in logit_lengths]
@@ -71,8 +92,9 @@ def rnnt_loss(logits, targets, logit_lengths, target_lengths, blank=-1, clamp=-1
         n = T[b] * (U[b] + 1)
         hb = x[rows:rows + n]
         yb = [int(v) for v in list(targets[b])[:U[b]]]
-        lb = sample_loss(hb, T[b], U[b], yb, blank, fused_log_softmax)
-        (g,) = torch.autograd.grad(lb, hb)
+        lb = sample_loss(hb, T[b], U[b], yb, blank, fused_log_softmax, fastemit_lambda)
+        lb, obj = lb if fastemit_lambda else (lb, lb)
+        (g,) = torch.autograd.grad(obj, hb)
         per.append(lb.detach())
         grads.append(g)
         rows += n

@@ -20,6 +20,11 @@
  *   - warp-transducer blog, section 5.2: targets must not contain blank.
  *
  * Readings of points the pages leave open (each restated in the tests):
+ *   - FastEmit (the fastemit_lambda argument of the GPURNNT docs and of
+ *     compute_multiblank_grad_kernel, after the FastEmit paper they cite):
+ *     the gradient with respect to every label-emission log-probability is
+ *     scaled by (1 + lambda); blank terms and the reported loss are not
+ *     changed;
  *   - rows of one sample are ordered (t, u) with u fastest;
  *   - target_lengths may be 0 (lattice width U+1 >= 1);
  *   - the terminal step is the blank emitted at (T-1, U);
@@ -187,17 +192,18 @@ int rnnt_oracle_forward(const void *x, int dtype, int V, int T, int U, const int
  * Gradient rows [r0, r1) of one sample, written to grad ((r1-r0) x V, double).
  * Uses the forward() outputs.  Per node (t,u):
  *   dL/dlp(blank) = -exp(alpha + lpb + beta(after blank) - ll)
- *   dL/dlp(y_u+1) = -exp(alpha + lpy + beta(t,u+1) - ll)          (u < U)
+ *   dL/dlp(y_u+1) = -(1 + lambda) * exp(alpha + lpy + beta(t,u+1) - ll)   (u < U)
  * where ll = alpha(T-1,U) + lpb(T-1,U), beta after the terminal blank is
- * log 1 = 0, and a blank from t = T-1 with u < U leaves the lattice (-inf).
+ * log 1 = 0, a blank from t = T-1 with u < U leaves the lattice (-inf), and
+ * lambda is the FastEmit weight (0 for the plain transducer loss).
  * With fused log-softmax the chain rule through lp = h - logsumexp(h) gives
  *   dL/dh_k = dL/dlp_k - p_k * sum_j dL/dlp_j.
  * Then clamp (if clamp > 0) and multiply by scale.
  */
 int rnnt_oracle_grad(const void *x, int dtype, int V, int T, int U, const int32_t *y, int blank,
                      int fused, const double *lpb, const double *lpy, const double *alpha,
-                     const double *beta, double clamp, double scale, int64_t r0, int64_t r1,
-                     double *grad)
+                     const double *beta, double clamp, double scale, double fastemit_lambda,
+                     int64_t r0, int64_t r1, double *grad)
 {
     if (T < 1 || U < 0 || V < 1)
         return -1;
@@ -228,7 +234,7 @@ int rnnt_oracle_grad(const void *x, int dtype, int V, int T, int U, const int32_
             g[k] = 0.0;
         g[blank] -= post_blank;
         if (u < U)
-            g[y[u]] -= post_label;
+            g[y[u]] -= (1.0 + fastemit_lambda) * post_label;
 
         if (fused) {
             double *lp = (double *)malloc(sizeof(double) * (size_t)V);
@@ -264,8 +270,8 @@ int rnnt_oracle_grad(const void *x, int dtype, int V, int T, int U, const int32_
  */
 int rnnt_oracle_batch(const void *logits, int dtype, int64_t rows, int V, const int32_t *targets,
                       int S, const int32_t *T, const int32_t *U, int B, int blank, double clamp,
-                      int fused, int reduction, double *losses, double *losses_beta,
-                      double *reduced, double *grad)
+                      int fused, int reduction, double fastemit_lambda, double *losses,
+                      double *losses_beta, double *reduced, double *grad)
 {
     if (B < 1 || V < 1)
         return -1;
@@ -298,7 +304,7 @@ int rnnt_oracle_batch(const void *logits, int dtype, int64_t rows, int V, const 
         losses[b] = ls[0];
         losses_beta[b] = ls[1];
         if (grad && rnnt_oracle_grad(xb, dtype, V, T[b], U[b], targets + (int64_t)b * S, blank,
-                                     fused, lpb, lpy, al, be, clamp, scale, 0, n,
+                                     fused, lpb, lpy, al, be, clamp, scale, fastemit_lambda, 0, n,
                                      grad + off[b] * (int64_t)V) != 0)
             failed = 1;
         free(buf);

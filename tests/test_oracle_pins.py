@@ -246,3 +246,66 @@ def test_rejects_bad_arguments():
         oracle.sample_forward(h, 0, 3, [0, 1, 0], 2, True)
     with pytest.raises(ValueError):
         oracle.rnnt_loss(h.astype(np.float32), [[0]], [2], [2], blank=2)
+
+
+# ---------------------------------------------------------------- FastEmit
+# The GPURNNT docs and compute_multiblank_grad_kernel take a FastEmit weight
+# lambda; the reading used here: the gradient term of every label-emission
+# log-probability is scaled by 1 + lambda, blank terms and the loss are not.
+
+@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("fused", [True, False])
+def test_fastemit_brute_force(seed, fused):
+    rng = np.random.default_rng(700 + seed)
+    V = int(rng.integers(2, 7))
+    x, y, T, U, blank = rand_case(rng, B=3, Tmax=4, Umax=4, V=V, fused=fused)
+    lam = [0.01, 0.3, 1.0, 2.5][seed % 4]
+    clamp = [-1.0, 0.2][seed % 2]
+    red = ["none", "sum", "mean"][seed % 3]
+    got = oracle.rnnt_loss(x, y, T, U, blank=blank, clamp=clamp, reduction=red,
+                           fused_log_softmax=fused, fastemit_lambda=lam)
+    want_l, want_red, want_g = brute.rnnt_loss(x.astype(np.float64), y, T, U, blank=blank,
+                                               clamp=clamp, reduction=red,
+                                               fused_log_softmax=fused, fastemit_lambda=lam)
+    np.testing.assert_allclose(got.losses, want_l, rtol=1e-12, atol=1e-12)
+    assert got.reduced == pytest.approx(want_red, rel=1e-12, abs=1e-12)
+    np.testing.assert_allclose(got.grad, want_g, rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_fastemit_linear_in_lambda_and_loss_unchanged(fused):
+    rng = np.random.default_rng(77)
+    x, y, T, U, blank = rand_case(rng, B=4, Tmax=9, Umax=6, V=6, fused=fused)
+    r = {lam: oracle.rnnt_loss(x, y, T, U, blank=blank, reduction="sum", fused_log_softmax=fused,
+                               fastemit_lambda=lam) for lam in (0.0, 1.0, 0.37)}
+    np.testing.assert_array_equal(r[0.37].losses, r[0.0].losses)
+    d1 = r[1.0].grad - r[0.0].grad
+    np.testing.assert_allclose(r[0.37].grad - r[0.0].grad, 0.37 * d1, rtol=1e-9, atol=1e-13)
+    assert np.abs(d1).max() > 1e-3   # the term is not empty
+
+
+def test_fastemit_label_gradients_sum_per_label():
+    # Non-fused: the gradient at label entries is -(1+lambda) times the label
+    # posteriors, and every label is emitted exactly once on every alignment,
+    # so summing over frames gives -(1+lambda) for each label position u.
+    rng = np.random.default_rng(78)
+    lam = 0.6
+    x, y, T, U, blank = rand_case(rng, B=1, Tmax=12, Umax=7, V=9, fused=False, blank=-1)
+    T0, U0 = int(T[0]), int(U[0])
+    if U0 == 0:
+        pytest.skip("no labels drawn")
+    res = oracle.rnnt_loss(x, y, T, U, blank=blank, reduction="sum", fused_log_softmax=False,
+                           fastemit_lambda=lam)
+    g = res.grad.reshape(T0, U0 + 1, -1)
+    for u in range(U0):
+        assert g[:, u, y[0, u]].sum() == pytest.approx(-(1 + lam), abs=1e-12)
+    # blank entries: each frame is left by exactly one blank
+    for t in range(T0):
+        assert g[t, :, 8].sum() == pytest.approx(-1.0, abs=1e-12)
+
+
+def test_fastemit_fused_rows_sum_to_zero():
+    rng = np.random.default_rng(79)
+    x, y, T, U, blank = rand_case(rng, B=3, Tmax=10, Umax=6, V=7)
+    g = oracle.rnnt_loss(x, y, T, U, blank=blank, reduction="sum", fastemit_lambda=1.3).grad
+    np.testing.assert_allclose(g.sum(axis=1), 0.0, atol=1e-12)
