@@ -199,3 +199,34 @@ def rnnt_loss(logits: np.ndarray, targets, logit_lengths, target_lengths, blank:
     if rc != 0:
         raise ValueError("oracle batch rejected its arguments")
     return BatchResult(losses, losses_b, float(red[0]), grad)
+
+
+def rnnt_loss_padded(logits: np.ndarray, targets, logit_lengths, target_lengths,
+                     **kw) -> BatchResult:
+    """Oracle on the padded (B, max_T, max_U+1, V) layout of the ESPnet GPURNNT docs.
+
+    Node (t, u) of sample b is ``logits[b, t, u]``; entries with t >= T_b or
+    u > U_b belong to no lattice, are never read and get a zero gradient.
+    The lattices are gathered into the compact layout, ``rnnt_loss`` runs on
+    it, and the gradient is scattered back into a zero (B, max_T, max_U+1, V)
+    array.  Keyword arguments are those of ``rnnt_loss``.
+    """
+    x = np.asarray(logits)
+    if x.ndim != 4:
+        raise ValueError("padded logits must be (B, max_T, max_U+1, V)")
+    B, maxT, maxW, V = x.shape
+    T = np.asarray(logit_lengths, dtype=np.int64)
+    U = np.asarray(target_lengths, dtype=np.int64)
+    if T.shape[0] != B or (T > maxT).any() or (U + 1 > maxW).any():
+        raise ValueError("lengths do not fit the padded tensor")
+    compact = np.concatenate([x[b, :T[b], :U[b] + 1, :].reshape(-1, V) for b in range(B)])
+    res = rnnt_loss(compact, targets, T.astype(np.int32), U.astype(np.int32), **kw)
+    if res.grad is not None:
+        g = np.zeros((B, maxT, maxW, V))
+        r = 0
+        for b in range(B):
+            n = int(T[b] * (U[b] + 1))
+            g[b, :T[b], :U[b] + 1, :] = res.grad[r:r + n].reshape(int(T[b]), int(U[b]) + 1, V)
+            r += n
+        res.grad = g
+    return res

@@ -106,3 +106,28 @@ def rnnt_loss(logits, targets, logit_lengths, target_lengths, blank=-1, clamp=-1
     grad = grad * scale
     reduced = losses.sum() * scale
     return losses.numpy(), float(reduced), grad.numpy()
+
+
+def rnnt_loss_padded(logits, targets, logit_lengths, target_lengths, blank=-1, clamp=-1.0,
+                     reduction="mean", fused_log_softmax=True, fastemit_lambda=0.0):
+    """Brute force on the padded (B, max_T, max_U+1, V) layout: every alignment
+    indexes node (t, u) of sample b as logits[b, t, u] directly; padded entries
+    take no part, so their gradient is zero.  Returns (losses, reduced, grad)."""
+    x = torch.as_tensor(logits).to(torch.float64).detach().clone().requires_grad_(True)
+    B, maxT, maxW, V = x.shape
+    per, objs = [], []
+    for b in range(B):
+        T, U = int(logit_lengths[b]), int(target_lengths[b])
+        hb = x[b, :T, :U + 1, :].reshape(T * (U + 1), V)
+        yb = [int(v) for v in list(targets[b])[:U]]
+        lb = sample_loss(hb, T, U, yb, blank, fused_log_softmax, fastemit_lambda)
+        lb, obj = lb if fastemit_lambda else (lb, lb)
+        per.append(lb.detach())
+        objs.append(obj)
+    (grad,) = torch.autograd.grad(torch.stack(objs).sum(), x)
+    losses = torch.stack(per)
+    scale = 1.0 / B if reduction == "mean" else 1.0
+    if clamp > 0:
+        grad = grad.clamp(-clamp, clamp)
+    grad = grad * scale
+    return losses.numpy(), float(losses.sum() * scale), grad.numpy()

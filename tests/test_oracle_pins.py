@@ -309,3 +309,58 @@ def test_fastemit_fused_rows_sum_to_zero():
     x, y, T, U, blank = rand_case(rng, B=3, Tmax=10, Umax=6, V=7)
     g = oracle.rnnt_loss(x, y, T, U, blank=blank, reduction="sum", fastemit_lambda=1.3).grad
     np.testing.assert_allclose(g.sum(axis=1), 0.0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- padded layout
+# The ESPnet GPURNNT docs take activations of shape [B, T, U, V+1]: node (t, u)
+# of sample b at [b, t, u]; positions outside a sample's lattice are padding.
+
+def rand_padded(rng, B, maxT, maxU, V, fused=True, junk=50.0):
+    T = rng.integers(1, maxT + 1, size=B).astype(np.int32)
+    U = rng.integers(0, maxU + 1, size=B).astype(np.int32)
+    T[0], U[-1] = maxT, maxU          # some sample fills each padded dimension
+    x = rng.normal(0.0, 1.0, size=(B, maxT, maxU + 1, V))
+    if not fused:
+        x = log_softmax(x, axis=-1)
+    for b in range(B):                # junk outside the lattices
+        x[b, T[b]:] = junk
+        x[b, :, U[b] + 1:] = -junk
+    blank = -1
+    y = rng.integers(0, V - 1, size=(B, max(1, maxU))).astype(np.int32)
+    return x, y, T, U, blank
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("fused", [True, False])
+def test_padded_brute_force(seed, fused):
+    rng = np.random.default_rng(900 + seed)
+    x, y, T, U, blank = rand_padded(rng, B=3, maxT=4, maxU=3, V=5, fused=fused)
+    lam = [0.0, 0.5][seed % 2]
+    clamp = [-1.0, 0.1, 0.3][seed % 3]
+    red = ["none", "sum", "mean"][seed % 3]
+    got = oracle.rnnt_loss_padded(x, y, T, U, blank=blank, clamp=clamp, reduction=red,
+                                  fused_log_softmax=fused, fastemit_lambda=lam)
+    wl, wr, wg = brute.rnnt_loss_padded(x, y, T, U, blank=blank, clamp=clamp, reduction=red,
+                                        fused_log_softmax=fused, fastemit_lambda=lam)
+    np.testing.assert_allclose(got.losses, wl, rtol=1e-12, atol=1e-12)
+    assert got.reduced == pytest.approx(wr, rel=1e-12, abs=1e-12)
+    np.testing.assert_allclose(got.grad, wg, rtol=1e-10, atol=1e-12)
+
+
+def test_padded_ignores_padding_and_zeroes_its_gradient():
+    rng = np.random.default_rng(950)
+    x, y, T, U, blank = rand_padded(rng, B=4, maxT=9, maxU=6, V=7)
+    a = oracle.rnnt_loss_padded(x, y, T, U, blank=blank, reduction="sum")
+    x2 = x.copy()
+    for b in range(4):
+        x2[b, T[b]:] = rng.normal(size=x2[b, T[b]:].shape) * 1e3
+        x2[b, :, U[b] + 1:] = np.nan
+    b2 = oracle.rnnt_loss_padded(x2, y, T, U, blank=blank, reduction="sum")
+    np.testing.assert_array_equal(a.losses, b2.losses)
+    np.testing.assert_array_equal(a.grad, b2.grad)
+    for b in range(4):
+        assert not a.grad[b, T[b]:].any() and not a.grad[b, :, U[b] + 1:].any()
+        # inside the lattice the gradient is the compact oracle's
+        c = oracle.rnnt_loss(np.ascontiguousarray(x[b, :T[b], :U[b] + 1].reshape(-1, 7)),
+                             y[b:b + 1], T[b:b + 1], U[b:b + 1], blank=blank, reduction="sum")
+        np.testing.assert_array_equal(a.grad[b, :T[b], :U[b] + 1].reshape(-1, 7), c.grad)
