@@ -125,6 +125,52 @@ rnnt_status_t rnnt_loss_fused(const void *logits, rnnt_dtype_t dt, int64_t rows,
                               int32_t *status_dev, rnnt_stream_t stream);
 
 /*
+ * Options of rnnt_loss_fused_ex.  A zero-initialised struct (or a NULL
+ * pointer) gives the behaviour of rnnt_loss_fused.
+ *
+ *   fastemit_lambda   >= 0.  FastEmit weight (the fastemit_lambda argument of
+ *                     the ESPnet GPURNNT docs and of compute_multiblank_grad_kernel,
+ *                     after the FastEmit paper they cite): the gradient term of
+ *                     every label-emission log-probability is multiplied by
+ *                     1 + fastemit_lambda; blank terms and the loss are not
+ *                     changed.  0 is the plain transducer gradient.
+ *   padded            0: compact layout (rows = sum_b T_b*(U_b+1)).
+ *                     1: padded layout of the GPURNNT docs (the activation
+ *                     tensor of cost_and_grad, shape [B, T, U, V+1]; also the
+ *                     torchaudio.functional.rnnt_loss layout): logits and grad are
+ *                     (B, max_T, max_U + 1, V) row-major, rows must equal
+ *                     B*max_T*(max_U+1), node (t, u) of sample b is row
+ *                     (b*max_T + t)*(max_U+1) + u.  Rows outside a sample's
+ *                     lattice (t >= T_b or u > U_b) are never read and get a
+ *                     zero gradient.  T_b <= max_T and U_b <= max_U are
+ *                     checked on the device (RNNT_INVALID_VALUE).
+ *   max_T, max_U      padded layout only: max_T >= 1, 0 <= max_U <=
+ *                     RNNT_MAX_TARGET_LENGTH, max_T*(max_U+1) < 2^31.
+ */
+typedef struct {
+    float fastemit_lambda;
+    int32_t padded;
+    int32_t max_T;
+    int32_t max_U;
+} rnnt_options_t;
+
+/*
+ * rnnt_loss_fused_ex -- rnnt_loss_fused with options (FastEmit, padded
+ * layout).  Same arguments, results and errors as rnnt_loss_fused, plus
+ * `options` (NULL = defaults); RNNT_INVALID_VALUE for a negative or
+ * non-finite fastemit_lambda or inconsistent padded sizes.  The workspace is
+ * sized by rnnt_workspace_size(B, rows, V, dt) with the same `rows`.
+ */
+rnnt_status_t rnnt_loss_fused_ex(const void *logits, rnnt_dtype_t dt, int64_t rows, int32_t V,
+                                 const int32_t *targets, int32_t targets_stride,
+                                 const int32_t *logit_lengths, const int32_t *target_lengths,
+                                 int32_t B, int32_t blank, float clamp, int32_t fused_log_softmax,
+                                 rnnt_reduction_t reduction, float *loss, float *loss_reduced,
+                                 void *grad, void *workspace, size_t workspace_bytes,
+                                 int32_t *status_dev, rnnt_stream_t stream,
+                                 const rnnt_options_t *options);
+
+/*
  * rnnt_loss_fused_staged -- rnnt_loss_fused with stage timing (tracing aid).
  * Same arguments, plus stage_events: NULL, or an array of 7 cudaEvent_t
  * handles (entries may be NULL) that the call records on `stream` at its
@@ -154,6 +200,8 @@ rnnt_status_t rnnt_loss_fused_staged(const void *logits, rnnt_dtype_t dt, int64_
  *                       (per_sample == 0) or factors[b] for sample b's rows
  *                       (per_sample != 0).  Rows whose factor is exactly 1
  *                       are left untouched (no memory traffic).
+ * The layout (compact or padded) is the one of that call; `rows` is the
+ * gradient's row count passed to it.
  * Returns RNNT_INVALID_VALUE / RNNT_WORKSPACE_TOO_SMALL / RNNT_LAUNCH_FAILED
  * as rnnt_loss_fused does.
  */

@@ -20,9 +20,15 @@ MAX_TARGET_LENGTH = 1023
 NOALLOC_SCRATCH_BYTES = 32 << 20     # RNNT_NOALLOC_SCRATCH_BYTES
 
 # Every symbol include/rnnt_gb300.h declares.
-EXPORTS = ("rnnt_workspace_size", "rnnt_loss_fused", "rnnt_loss_fused_staged", "rnnt_grad_scale",
-           "rnnt_set_trace", "rnnt_loss_fused_noalloc", "rnnt_status_string",
-           "rnnt_abi_version")
+EXPORTS = ("rnnt_workspace_size", "rnnt_loss_fused", "rnnt_loss_fused_ex",
+           "rnnt_loss_fused_staged", "rnnt_grad_scale", "rnnt_set_trace",
+           "rnnt_loss_fused_noalloc", "rnnt_status_string", "rnnt_abi_version")
+
+
+class Options(ctypes.Structure):
+    """rnnt_options_t: FastEmit weight and the padded (B, max_T, max_U + 1, V) layout."""
+    _fields_ = [("fastemit_lambda", ctypes.c_float), ("padded", ctypes.c_int32),
+                ("max_T", ctypes.c_int32), ("max_U", ctypes.c_int32)]
 
 _lib = None
 
@@ -49,6 +55,8 @@ def load() -> ctypes.CDLL:
     lib.rnnt_loss_fused.argtypes = [P, i32, i64, i32, P, i32, P, P, i32, i32, f32, i32, i32,
                                     P, P, P, P, sz, P, P]
     lib.rnnt_loss_fused.restype = i32
+    lib.rnnt_loss_fused_ex.argtypes = lib.rnnt_loss_fused.argtypes + [ctypes.POINTER(Options)]
+    lib.rnnt_loss_fused_ex.restype = i32
     lib.rnnt_loss_fused_staged.argtypes = lib.rnnt_loss_fused.argtypes + [P]
     lib.rnnt_loss_fused_staged.restype = i32
     lib.rnnt_loss_fused_noalloc.argtypes = lib.rnnt_loss_fused.argtypes[:16] + [P, P]
@@ -89,6 +97,20 @@ def rnnt_loss_fused(logits, dt, rows, V, targets, targets_stride, logit_lengths,
                                       logit_lengths, target_lengths, B, blank, float(clamp),
                                       int(fused_log_softmax), reduction, loss, loss_reduced, grad,
                                       workspace, workspace_bytes, status_dev, stream))
+
+
+def rnnt_loss_fused_ex(logits, dt, rows, V, targets, targets_stride, logit_lengths, target_lengths,
+                       B, blank, clamp, fused_log_softmax, reduction, loss, loss_reduced, grad,
+                       workspace, workspace_bytes, status_dev, stream, fastemit_lambda=0.0,
+                       padded=None) -> int:
+    """rnnt_loss_fused with options; padded = (max_T, max_U) selects the padded layout."""
+    opt = Options(float(fastemit_lambda), 1 if padded else 0,
+                  int(padded[0]) if padded else 0, int(padded[1]) if padded else 0)
+    return int(load().rnnt_loss_fused_ex(logits, dt, rows, V, targets, targets_stride,
+                                         logit_lengths, target_lengths, B, blank, float(clamp),
+                                         int(fused_log_softmax), reduction, loss, loss_reduced,
+                                         grad, workspace, workspace_bytes, status_dev, stream,
+                                         ctypes.byref(opt)))
 
 
 def rnnt_loss_fused_staged(logits, dt, rows, V, targets, targets_stride, logit_lengths,

@@ -132,6 +132,10 @@ struct Params {
     float lscale;     // log2(scale)
     int fused;
     int red;
+    float fe;         // FastEmit weight: label-emission gradient terms scaled by 1 + fe
+    float fe_l2;      // log2(1 + fe)
+    int padded;       // logits/grad are the padded (B, maxT, maxW, V) tensor
+    int maxT, maxW;   // padded layout: frames and lattice columns of a sample slot
     int stage_bytes;  // per-stage shared-memory row buffer of the TMA-staged passes
     int zero_off;     // persistent kernel: shared-memory offset of a zeroed buffer ...
     int zero_rows;    // ... of zero_rows gradient rows, the source of zero-row bulk stores
@@ -196,6 +200,28 @@ __device__ __forceinline__ int find_sample(const int64_t* off, int B, int64_t r)
         if (__ldcg(off + mid) <= r) lo = mid; else hi = mid;
     }
     return lo;
+}
+
+// Logits / gradient row holding lattice row r (compact numbering) of sample b,
+// whose compact rows start at o and whose lattice is W nodes wide: r itself in
+// the compact layout, (b*maxT + t)*maxW + u in the padded one.
+__device__ __forceinline__ int64_t lrow_s(const Params& p, int64_t r, int b, int64_t o, int W) {
+    if (!p.padded) return r;
+    const unsigned i = (unsigned)(r - o);
+    const int t = (int)(i / (unsigned)W), u = (int)(i - (unsigned)t * W);
+    return ((int64_t)b * p.maxT + t) * p.maxW + u;
+}
+// Lattice nodes of the batch (compact rows): the logits' row count in the
+// compact layout, sum_b T_b*(U_b+1) (written earlier in this call) in the
+// padded one.
+__device__ __forceinline__ int64_t nodes(const Params& p) {
+    return p.padded ? __ldcg(p.off + p.B) : p.rows;
+}
+// The same with the sample looked up (offsets written earlier in this call).
+__device__ __forceinline__ int64_t lrow(const Params& p, int64_t r) {
+    if (!p.padded) return r;
+    const int b = find_sample(p.off, p.B, r);
+    return lrow_s(p, r, b, __ldcg(p.off + b), __ldg(p.Ul + b) + 1);
 }
 // Rows are visited in increasing order; step to r's sample, searching only on a change.
 __device__ __forceinline__ int advance_sample(const int64_t* off, int B, int b, int64_t r) {
@@ -665,6 +691,8 @@ __device__ void prepare_block(const Params& p, int64_t* s_before, int* s_nch) {
         p.err[8] = 0;   // CTAs of the persistent kernel that have finished
         p.err[9] = 0;   // first timeout site (diagnosis)
         p.err[10] = 0;
+        // Rows per sample slot of the padded layout (0: compact), for rnnt_grad_scale.
+        p.err[12] = p.padded ? p.maxT * p.maxW : 0;
     }
     __syncthreads();
     for (int base = 0; base < p.B; base += blockDim.x) {
@@ -672,7 +700,8 @@ __device__ void prepare_block(const Params& p, int64_t* s_before, int* s_nch) {
         int64_t n = 0;
         if (b < p.B) {
             const int T = p.Tl[b], U = p.Ul[b];
-            if (T < 1 || U < 0 || U > p.S || U + 1 > kMaxW || (int64_t)T * (U + 1) > INT32_MAX)
+            if (T < 1 || U < 0 || U > p.S || U + 1 > kMaxW || (int64_t)T * (U + 1) > INT32_MAX ||
+                (p.padded && (T > p.maxT || U + 1 > p.maxW)))
                 atomicOr(&errs, ERR_LENGTH);
             else n = (int64_t)T * (U + 1);
         }
@@ -702,7 +731,7 @@ __device__ void prepare_block(const Params& p, int64_t* s_before, int* s_nch) {
     }
     if (tid == 0) {
         p.off[p.B] = carry;
-        if (carry != p.rows) atomicOr(&errs, ERR_ROWS);
+        if (!p.padded && carry != p.rows) atomicOr(&errs, ERR_ROWS);
     }
     // Labels: in range and not blank (warp-transducer blog 5.2).
     // Eight labels per thread per round, their loads issued together.
@@ -797,10 +826,10 @@ __device__ __forceinline__ void row_finish_at(const Params& p, int64_t r, float 
 template <typename Tin>
 __device__ __forceinline__ void row_finish(const Params& p, int64_t r, float M, float s) {
     using E = Elt<Tin>;
-    const Tin* row = static_cast<const Tin*>(p.logits) + r * (int64_t)p.V;
     const int b = find_sample(p.off, p.B, r);
     const int T = __ldg(p.Tl + b), U = __ldg(p.Ul + b), W = U + 1;
     const int64_t o = __ldcg(p.off + b);
+    const Tin* row = static_cast<const Tin*>(p.logits) + lrow_s(p, r, b, o, W) * (int64_t)p.V;
     const unsigned rr = (unsigned)(r - o);
     const int t = (int)(rr / (unsigned)W), u = (int)(rr - (unsigned)t * W);
     const float hb = E::get(row, p.blank);
@@ -833,16 +862,16 @@ __global__ void __launch_bounds__(256) k_row_regs(Params p) {
     const int V = p.V, nvec = V / EPV;
     const int wl = threadIdx.x & 31, lane = wl & (G - 1), grp = wl / G;
     const unsigned gm = group_mask<G>();
-    const int64_t nbatch = (p.rows + 31) / 32;
+    const int64_t nbatch = (nodes(p) + 31) / 32;
     const int64_t wstride = (int64_t)gridDim.x * (blockDim.x / 32);
     for (int64_t bt = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32; bt < nbatch;
          bt += wstride) {
         const int64_t r0 = bt * 32;
-        const int nrows = (int)min((int64_t)32, p.rows - r0);
+        const int nrows = (int)min((int64_t)32, nodes(p) - r0);
         float myM = 0.0f, mys = 0.0f;
         uint4 cur[NV];
         if (grp < nrows) {
-            const uint4* rv = reinterpret_cast<const uint4*>(X + (r0 + grp) * (int64_t)V);
+            const uint4* rv = reinterpret_cast<const uint4*>(X + lrow(p, r0 + grp) * (int64_t)V);
 #pragma unroll
             for (int k = 0; k < NV; ++k)
                 if (lane + k * G < nvec) cur[k] = __ldg(rv + lane + k * G);
@@ -851,7 +880,8 @@ __global__ void __launch_bounds__(256) k_row_regs(Params p) {
             const int ri = it * NG + grp;
             uint4 nxt[NV];
             if (ri + NG < nrows) {
-                const uint4* rv = reinterpret_cast<const uint4*>(X + (r0 + ri + NG) * (int64_t)V);
+                const uint4* rv =
+                    reinterpret_cast<const uint4*>(X + lrow(p, r0 + ri + NG) * (int64_t)V);
 #pragma unroll
                 for (int k = 0; k < NV; ++k)
                     if (lane + k * G < nvec) nxt[k] = __ldg(rv + lane + k * G);
@@ -906,10 +936,10 @@ __global__ void __launch_bounds__(256) k_row_tma(Params p) {
     const int V = p.V, nvec = V / EPV;
     const uint32_t rb = (uint32_t)V * sizeof(Tin);
     WarpRows seq;
-    seq.init(p.rows, (int64_t)blockIdx.x * nw + wid, (int64_t)gridDim.x * nw);
+    seq.init(nodes(p), (int64_t)blockIdx.x * nw + wid, (int64_t)gridDim.x * nw);
     if (wl == 0)
         for (int64_t k = 0; k < min((int64_t)kStages, seq.count); ++k)
-            tma_row_load(buf + (k % kStages) * sb, X + seq.row(k) * (int64_t)V, rb,
+            tma_row_load(buf + (k % kStages) * sb, X + lrow(p, seq.row(k)) * (int64_t)V, rb,
                          &bars[k % kStages]);
     // Groups of 8 sequence positions (8-aligned, so inside one 32-row batch):
     // per-lane partials of each row, then one butterfly merge per group.
@@ -935,7 +965,7 @@ __global__ void __launch_bounds__(256) k_row_tma(Params p) {
                     __syncwarp();
                     if (wl == 0 && k + kStages < seq.count) {   // refill this stage
                         fence_proxy_async();
-                        tma_row_load(buf + st * sb, X + seq.row(k + kStages) * (int64_t)V, rb,
+                        tma_row_load(buf + st * sb, X + lrow(p, seq.row(k + kStages)) * (int64_t)V, rb,
                                      &bars[st]);
                     }
                     row_partial<Tin, NV>(q, nvec, wl, lm[j], ls[j]);
@@ -1032,18 +1062,19 @@ __global__ void __launch_bounds__(256) k_row_stream(Params p) {
     const Tin* X = static_cast<const Tin*>(p.logits);
     const int wl = threadIdx.x & 31, lane = wl & (G - 1), grp = wl / G;
     const unsigned gm = group_mask<G>();
-    const int64_t nbatch = (p.rows + 31) / 32;
+    const int64_t nbatch = (nodes(p) + 31) / 32;
     const int64_t wstride = (int64_t)gridDim.x * (blockDim.x / 32);
     for (int64_t bt = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32; bt < nbatch;
          bt += wstride) {
         const int64_t r0 = bt * 32;
-        const int nrows = (int)min((int64_t)32, p.rows - r0);
+        const int nrows = (int)min((int64_t)32, nodes(p) - r0);
         float myM = 0.0f, mys = 0.0f;
         for (int it = 0; it < G; ++it) {
             const int ri = it * NG + grp;
             float M = -INFINITY, s = 0.0f;
             if (ri < nrows)
-                row_stats_stream<Tin, G, VEC>(X + (r0 + ri) * (int64_t)p.V, p.V, lane, gm, M, s);
+                row_stats_stream<Tin, G, VEC>(X + lrow(p, r0 + ri) * (int64_t)p.V, p.V, lane, gm,
+                                              M, s);
             hand_over<G>(it, wl, M, s, myM, mys);
         }
         if (wl < nrows) row_finish<Tin>(p, r0 + wl, myM, mys);
@@ -1055,7 +1086,7 @@ template <typename Tin>
 __global__ void __launch_bounds__(256) k_row_gather(Params p) {
     if (*p.err) return;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < p.rows; r += stride)
+    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < nodes(p); r += stride)
         row_finish<Tin>(p, r, 0.0f, 1.0f);
 }
 
@@ -1715,7 +1746,9 @@ __device__ __forceinline__ float4 combine_row(const Params& p, int64_t r, int b)
     float lc = -INFINITY;
     if (am != 0.0f && bm != 0.0f) lc = (float)(A.y + Bt.y - Pe) + lg2(am * bm * inv);
     const int y = (u < U) ? __ldg(p.targets + (int64_t)b * p.S + u) : -1;
-    if (!(lc >= p.skip2))   // every element of this gradient row rounds to zero
+    // Every element of this gradient row rounds to zero (with FastEmit the
+    // row's elements are bounded by (1 + fe) times the occupancy).
+    if (!(lc + p.fe_l2 >= p.skip2))
         return make_float4(-INFINITY, 0.0f, 0.0f, __int_as_float(y));
     float eb = 0.0f, ey = 0.0f;
     if (t < T - 1) {
@@ -1729,8 +1762,18 @@ __device__ __forceinline__ float4 combine_row(const Params& p, int64_t r, int b)
     if (u < U) {
         const int2 Bn = __ldcg(p.beta + o + node_index(t, u + 1, T, U));
         const float py = __int_as_float(Ed.z), bn = __int_as_float(Bn.x);
-        if (am != 0.0f && py != 0.0f && bn != 0.0f)
+        if (am != 0.0f && py != 0.0f && bn != 0.0f) {
             ey = xf_to_float(am * py * bn * inv, A.y + (Ed.w - kEdgeBias) + Bn.y - Pe);
+            if (p.fe > 0.0f) {
+                // FastEmit: the label term is (1 + fe) post_label, so the
+                // softmax term p_k * (post_blank + (1 + fe) post_label) has
+                // occupancy occ (1 + fe post_label / occ), post_label / occ =
+                // p_label beta(t,u+1) / beta(t,u).
+                const float ratio = xf_to_float(py * bn / bm, (Ed.w - kEdgeBias) + Bn.y - Bt.y);
+                lc += lg2(fmaf(p.fe, ratio, 1.0f));
+                ey *= 1.0f + p.fe;
+            }
+        }
     }
     return make_float4(lc + p.lscale - __ldcg(p.lse2 + r), eb * p.scale, ey * p.scale,
                        __int_as_float(y));
@@ -1740,8 +1783,8 @@ __global__ void __launch_bounds__(256) k_combine(Params p) {
     if (*p.err) return;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    int b = (r < p.rows) ? find_sample(p.off, p.B, r) : 0;
-    for (; r < p.rows; r += stride) {
+    int b = (r < nodes(p)) ? find_sample(p.off, p.B, r) : 0;
+    for (; r < nodes(p); r += stride) {
         b = advance_sample(p.off, p.B, b, r);
         p.info[r] = combine_row(p, r, b);
     }
@@ -1763,13 +1806,14 @@ __global__ void __launch_bounds__(256) k_grad(Params p) {
     const float cl = p.clamp * p.scale;
     const bool clip = p.clamp < INFINITY;
     const int vb = p.blank / EPV, eb_i = p.blank % EPV;
-    for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G; r < p.rows; r += ng) {
+    for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G; r < nodes(p); r += ng) {
         const float4 in = p.info[r];
         const bool zero = in.x == -INFINITY;
         const float w2 = in.x, eb = in.y, ey = in.z;
         const int y = __float_as_int(in.w);
-        const Tin* row = X + r * (int64_t)V;
-        Tin* out = Y + r * (int64_t)V;
+        const int64_t lr = lrow(p, r);
+        const Tin* row = X + lr * (int64_t)V;
+        Tin* out = Y + lr * (int64_t)V;
         if (VEC) {
             const int nvec = V / EPV;
             const int vy = y >= 0 ? y / EPV : -1, ey_i = y >= 0 ? y % EPV : 0;
@@ -1843,7 +1887,7 @@ __global__ void __launch_bounds__(256) k_grad_tma(Params p) {
     const bool clip = p.clamp < INFINITY;
     const int vb = p.blank / EPV, eb_i = p.blank % EPV;
     WarpRows seq;
-    seq.init(p.rows, (int64_t)blockIdx.x * nw + wid, (int64_t)gridDim.x * nw);
+    seq.init(nodes(p), (int64_t)blockIdx.x * nw + wid, (int64_t)gridDim.x * nw);
     const int64_t nb = (seq.count + 31) / 32;   // batches of this warp
 
     auto load_info = [&](int64_t j) -> float4 {
@@ -1880,7 +1924,7 @@ __global__ void __launch_bounds__(256) k_grad_tma(Params p) {
             const int st = (int)(issued % kStages);
             if (wl == 0) {
                 fence_proxy_async();
-                tma_row_load(buf + st * sb, X + row * (int64_t)V, rb, &bars[st]);
+                tma_row_load(buf + st * sb, X + lrow(p, row) * (int64_t)V, rb, &bars[st]);
             }
             ++issued;
         }
@@ -1897,7 +1941,7 @@ __global__ void __launch_bounds__(256) k_grad_tma(Params p) {
             const float ey = __shfl_sync(0xffffffffu, cur.z, it);
             const int y = __shfl_sync(0xffffffffu, __float_as_int(cur.w), it);
             const int vy = y >= 0 ? y / EPV : -1, ey_i = y >= 0 ? y % EPV : 0;
-            uint4* ov = reinterpret_cast<uint4*>(Y + r * (int64_t)V);
+            uint4* ov = reinterpret_cast<uint4*>(Y + lrow(p, r) * (int64_t)V);
             const bool zero = w2 == -INFINITY;
             const uint4* rv = nullptr;
             int st = 0;
@@ -2015,7 +2059,8 @@ __device__ bool row_batch_tma(const Params& p, int64_t r0, int n, unsigned char*
         fence_proxy_async();
         for (int i = 0; i < min(kStages, n); ++i) {
             const uint32_t st = (kk + i) % kStages;
-            tma_row_load(buf + st * sb, X + (r0 + i) * (int64_t)V, rb, &bars[st]);
+            tma_row_load(buf + st * sb, X + lrow_s(p, r0 + i, b, o, W) * (int64_t)V, rb,
+                         &bars[st]);
         }
     }
     float myM = 0.0f, mys = 0.0f;
@@ -2045,7 +2090,8 @@ __device__ bool row_batch_tma(const Params& p, int64_t r0, int n, unsigned char*
                     __syncwarp();
                     if (wl == 0 && i + kStages < n) {
                         fence_proxy_async();
-                        tma_row_load(buf + st * sb, X + (r0 + i + kStages) * (int64_t)V, rb,
+                        tma_row_load(buf + st * sb,
+                                     X + lrow_s(p, r0 + i + kStages, b, o, W) * (int64_t)V, rb,
                                      &bars[st]);
                     }
                     row_partial<Tin, NV>(q, nvec, wl, lm[j], ls[j]);
@@ -2082,7 +2128,8 @@ template <typename Tin, int NV>
 __device__ bool grad_batch_tma(const Params& p, int64_t r0, int s0, uint32_t zmask,
                                const uint16_t* list, int cnt, int first, int stride,
                                const float4* inf, unsigned char* buf, uint64_t* bars,
-                               uint32_t& kk, const unsigned char* zbuf) {
+                               uint32_t& kk, const unsigned char* zbuf, int b, int64_t o,
+                               int W) {
     using E = Elt<Tin>;
     constexpr int EPV = E::kPerVec;
     const int wl = threadIdx.x & 31, sb = p.stage_bytes;
@@ -2100,9 +2147,14 @@ __device__ bool grad_batch_tma(const Params& p, int64_t r0, int s0, uint32_t zma
             const int a = __ffs(zm) - 1;
             const uint32_t after = ~(zm >> a);
             const int len = after ? __ffs(after) - 1 : 32 - a;
-            for (int k = 0; k < len; k += p.zero_rows) {
-                const int nr = min(p.zero_rows, len - k);
-                tma_store(Y + (r0 + s0 + a + k) * (int64_t)V, zbuf, (uint32_t)nr * rb);
+            for (int k = 0; k < len;) {
+                // One bulk store per run of rows that are consecutive in memory
+                // (in the padded layout a run ends with its lattice row).
+                const int64_t rs = r0 + s0 + a + k;
+                int nr = min(p.zero_rows, len - k);
+                if (p.padded) nr = min(nr, W - (int)((unsigned)(rs - o) % (unsigned)W));
+                tma_store(Y + lrow_s(p, rs, b, o, W) * (int64_t)V, zbuf, (uint32_t)nr * rb);
+                k += nr;
             }
             zm &= len >= 32 ? 0u : ~(((1u << len) - 1u) << a);
         }
@@ -2110,7 +2162,8 @@ __device__ bool grad_batch_tma(const Params& p, int64_t r0, int s0, uint32_t zma
         fence_proxy_async();
         for (int i = 0; i < min(kStages, my); ++i) {
             const uint32_t st = (kk + i) % kStages;
-            tma_row_load(buf + st * sb, X + (r0 + list[first + i * stride]) * (int64_t)V, rb,
+            tma_row_load(buf + st * sb,
+                         X + lrow_s(p, r0 + list[first + i * stride], b, o, W) * (int64_t)V, rb,
                          &bars[st]);
         }
     }
@@ -2128,7 +2181,7 @@ __device__ bool grad_batch_tma(const Params& p, int64_t r0, int s0, uint32_t zma
             return false;
         }
         const uint4* rv = reinterpret_cast<const uint4*>(buf + st * sb);
-        uint4* ov = reinterpret_cast<uint4*>(Y + (r0 + row) * (int64_t)V);
+        uint4* ov = reinterpret_cast<uint4*>(Y + lrow_s(p, r0 + row, b, o, W) * (int64_t)V);
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             const int vi = wl + 32 * v;
@@ -2159,8 +2212,10 @@ __device__ bool grad_batch_tma(const Params& p, int64_t r0, int s0, uint32_t zma
         __syncwarp();
         if (wl == 0 && i + kStages < my) {
             fence_proxy_async();
-            tma_row_load(buf + st * sb, X + (r0 + list[first + (i + kStages) * stride]) * (int64_t)V,
-                         rb, &bars[st]);
+            tma_row_load(
+                buf + st * sb,
+                X + lrow_s(p, r0 + list[first + (i + kStages) * stride], b, o, W) * (int64_t)V, rb,
+                &bars[st]);
         }
     }
     kk += my;
@@ -2169,7 +2224,8 @@ __device__ bool grad_batch_tma(const Params& p, int64_t r0, int s0, uint32_t zma
 
 // Warp: gradient rows without staging (log-softmax off: nothing is read).
 template <typename Tin, int G, bool VEC, bool FUSED>
-__device__ void grad_batch_plain(const Params& p, int64_t r0, int n, const float4* inf) {
+__device__ void grad_batch_plain(const Params& p, int64_t r0, int n, const float4* inf, int b,
+                                 int64_t o, int W) {
     using E = Elt<Tin>;
     constexpr int NG = 32 / G;
     const Tin* X = static_cast<const Tin*>(p.logits);
@@ -2183,8 +2239,9 @@ __device__ void grad_batch_plain(const Params& p, int64_t r0, int n, const float
         const bool zero = in.x == -INFINITY;
         const float w2 = in.x, eb = in.y, ey = in.z;
         const int y = __float_as_int(in.w);
-        const Tin* row = X + (r0 + it) * (int64_t)V;
-        Tin* out = Y + (r0 + it) * (int64_t)V;
+        const int64_t lr = lrow_s(p, r0 + it, b, o, W);
+        const Tin* row = X + lr * (int64_t)V;
+        Tin* out = Y + lr * (int64_t)V;
         if (VEC) {
             constexpr int EPV = E::kPerVec;
             const int nvec = V / EPV;
@@ -2346,7 +2403,9 @@ __device__ __forceinline__ void main_body(const Params& p) {
         if (t >= ntasks || !go) break;
         const int4 tk = __ldcg(p.tasks + t);
         const int kind = tk.x & 3, b = tk.x >> 2, n = tk.z;
-        const int64_t r0 = __ldcg(p.off + b) + tk.y;
+        const int64_t o_b = __ldcg(p.off + b);
+        const int W_b = __ldg(p.Ul + b) + 1;
+        const int64_t r0 = o_b + tk.y;
         const uint64_t t_start = (p.trace && tid == 0) ? global_ns() : 0;
         if (kind == TASK_ROW) {
             if (NV > 0) fence_proxy_async();   // smem may have been a DP ring
@@ -2417,9 +2476,10 @@ __device__ __forceinline__ void main_body(const Params& p) {
             __syncthreads();
             const uint32_t zmask = nw > 0 ? ~bal & (nw >= 32 ? 0xffffffffu : ((1u << nw) - 1u)) : 0u;
             grad_batch_tma<Tin, (NV > 0 ? NV : 1)>(p, r0, 32 * wid, zmask, s_nz, cnt, wid, 8,
-                                                  s_info, buf, bars, kk, zbuf);
+                                                  s_info, buf, bars, kk, zbuf, b, o_b, W_b);
         } else if (nw > 0) {
-            grad_batch_plain<Tin, G, VEC, false>(p, r0 + 32 * wid, nw, s_info + 32 * wid);
+            grad_batch_plain<Tin, G, VEC, false>(p, r0 + 32 * wid, nw, s_info + 32 * wid, b, o_b,
+                                                 W_b);
         }
         if (p.trace) {
             __syncthreads();
@@ -2492,18 +2552,47 @@ __device__ void finalize_block(const Params& p) {
 
 __global__ void __launch_bounds__(256) k_finalize(Params p) { finalize_block(p); }
 
+// ---------------------------------------------------------------- padding
+// Padded layout: zero gradient rows outside every lattice (t >= T_b or
+// u > U_b), one warp per row; rows inside a lattice are left to the gradient
+// pass.  Reads only the lengths, so it needs nothing from the preparation.
+template <typename Tin>
+__global__ void __launch_bounds__(256) k_pad_zero(Params p) {
+    const int64_t per = (int64_t)p.maxT * p.maxW;
+    const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
+    const int lane = threadIdx.x & 31;
+    const int64_t rb = (int64_t)p.V * sizeof(Tin);
+    for (int64_t R = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32; R < p.rows; R += nw) {
+        const int b = (int)(R / per);
+        const int64_t q = R - (int64_t)b * per;
+        const int t = (int)(q / p.maxW), u = (int)(q - (int64_t)t * p.maxW);
+        if (t < __ldg(p.Tl + b) && u <= __ldg(p.Ul + b)) continue;
+        char* row = static_cast<char*>(p.grad) + R * rb;
+        if (rb % 16 == 0) {
+            for (int64_t k = lane; k < rb / 16; k += 32)
+                __stcs(reinterpret_cast<uint4*>(row) + k, make_uint4(0, 0, 0, 0));
+        } else {
+            for (int k = lane; k < p.V; k += 32) reinterpret_cast<Tin*>(row)[k] = Elt<Tin>::from_f(0.0f);
+        }
+    }
+}
+
 // ---------------------------------------------------------------- grad scale
+// hdr: the call's workspace header; hdr[12] = rows per sample slot of the
+// padded layout, 0 for the compact one.
 template <typename Tin>
 __global__ void __launch_bounds__(256) k_scale(void* grad, int64_t rows, int V, int B,
-                                               const int64_t* off, const float* factors,
-                                               int per_sample) {
+                                               const int64_t* off, const int32_t* hdr,
+                                               const float* factors, int per_sample) {
     if (!per_sample && factors[0] == 1.0f) return;
     using E = Elt<Tin>;
     Tin* G = static_cast<Tin*>(grad);
     const int64_t ng = (int64_t)gridDim.x * (blockDim.x / 32);
     const int lane = threadIdx.x & 31;
+    const int64_t per = hdr[12];
     for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32; r < rows; r += ng) {
-        const float f = per_sample ? factors[find_sample(off, B, r)] : factors[0];
+        const int b = per > 0 ? (int)min(r / per, (int64_t)B - 1) : find_sample(off, B, r);
+        const float f = per_sample ? factors[b] : factors[0];
         if (f == 1.0f) continue;
         Tin* row = G + r * (int64_t)V;
         for (int k = lane; k < V; k += 32) row[k] = E::from_f(E::to_f(row[k]) * f);
@@ -2752,14 +2841,33 @@ extern "C" rnnt_status_t rnnt_workspace_size(int32_t B, int64_t rows, int32_t V,
     return RNNT_OK;
 }
 
-extern "C" rnnt_status_t rnnt_loss_fused_staged(
-    const void* logits, rnnt_dtype_t dt, int64_t rows, int32_t V, const int32_t* targets,
-    int32_t targets_stride, const int32_t* logit_lengths, const int32_t* target_lengths, int32_t B,
-    int32_t blank, float clamp, int32_t fused_log_softmax, rnnt_reduction_t reduction, float* loss,
-    float* loss_reduced, void* grad, void* workspace, size_t workspace_bytes, int32_t* status_dev,
-    rnnt_stream_t stream, void* const* stage_events) {
+// Every loss entry point: argument checks, then the persistent kernel or the
+// staged kernels.  opts may be null (compact layout, no FastEmit).
+static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows, int32_t V,
+                        const int32_t* targets, int32_t targets_stride,
+                        const int32_t* logit_lengths, const int32_t* target_lengths, int32_t B,
+                        int32_t blank, float clamp, int32_t fused_log_softmax,
+                        rnnt_reduction_t reduction, float* loss, float* loss_reduced, void* grad,
+                        void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                        rnnt_stream_t stream, const rnnt_options_t* opts,
+                        void* const* stage_events) {
     if (!logits || !targets || !logit_lengths || !target_lengths || !loss || !workspace)
         return RNNT_INVALID_VALUE;
+    float fe = 0.0f;
+    int padded = 0, maxT = 0, maxW = 0;
+    if (opts) {
+        fe = opts->fastemit_lambda;
+        if (!(fe >= 0.0f) || !(fe < INFINITY)) return RNNT_INVALID_VALUE;
+        if (opts->padded) {
+            padded = 1;
+            maxT = opts->max_T;
+            maxW = opts->max_U + 1;
+            if (maxT < 1 || opts->max_U < 0 || opts->max_U > RNNT_MAX_TARGET_LENGTH)
+                return RNNT_INVALID_VALUE;
+            if ((int64_t)maxT * maxW > INT32_MAX || B < 1 || rows != (int64_t)B * maxT * maxW)
+                return RNNT_INVALID_VALUE;
+        }
+    }
     if (dt != RNNT_F32 && dt != RNNT_F16) return RNNT_INVALID_VALUE;
     if (B < 1 || rows < 1 || V < 1 || rows < B) return RNNT_INVALID_VALUE;
     if (targets_stride < 1 || targets_stride > RNNT_MAX_TARGET_LENGTH) return RNNT_INVALID_VALUE;
@@ -2802,6 +2910,11 @@ extern "C" rnnt_status_t rnnt_loss_fused_staged(
     p.lscale = log2f(p.scale);
     p.fused = fused_log_softmax ? 1 : 0;
     p.red = reduction;
+    p.fe = fe;
+    p.fe_l2 = log2f(1.0f + fe);
+    p.padded = padded;
+    p.maxT = maxT;
+    p.maxW = maxW;
     p.stage_bytes = (int)(((size_t)V * es + 127) / 128 * 128);
     p.loss = loss;
     p.loss_red = loss_reduced;
@@ -2839,6 +2952,10 @@ extern "C" rnnt_status_t rnnt_loss_fused_staged(
             cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), st);
     };
     mark(0);
+    if (grad && padded) {   // zero gradient rows outside the lattices
+        if (dt == RNNT_F32) launch_gs(k_pad_zero<float>, rows * 32, sms, st, p);
+        else launch_gs(k_pad_zero<__half>, rows * 32, sms, st, p);
+    }
     if (grad) {
         // One cooperative kernel: preparation on its CTA 0, every task, and the
         // loss check / reduction on its last CTA.
@@ -2868,6 +2985,28 @@ extern "C" rnnt_status_t rnnt_loss_fused_staged(
     return cudaGetLastError() == cudaSuccess ? RNNT_OK : RNNT_LAUNCH_FAILED;
 }
 
+extern "C" rnnt_status_t rnnt_loss_fused_staged(
+    const void* logits, rnnt_dtype_t dt, int64_t rows, int32_t V, const int32_t* targets,
+    int32_t targets_stride, const int32_t* logit_lengths, const int32_t* target_lengths, int32_t B,
+    int32_t blank, float clamp, int32_t fused_log_softmax, rnnt_reduction_t reduction, float* loss,
+    float* loss_reduced, void* grad, void* workspace, size_t workspace_bytes, int32_t* status_dev,
+    rnnt_stream_t stream, void* const* stage_events) {
+    return loss_impl(logits, dt, rows, V, targets, targets_stride, logit_lengths, target_lengths,
+                     B, blank, clamp, fused_log_softmax, reduction, loss, loss_reduced, grad,
+                     workspace, workspace_bytes, status_dev, stream, nullptr, stage_events);
+}
+
+extern "C" rnnt_status_t rnnt_loss_fused_ex(
+    const void* logits, rnnt_dtype_t dt, int64_t rows, int32_t V, const int32_t* targets,
+    int32_t targets_stride, const int32_t* logit_lengths, const int32_t* target_lengths, int32_t B,
+    int32_t blank, float clamp, int32_t fused_log_softmax, rnnt_reduction_t reduction, float* loss,
+    float* loss_reduced, void* grad, void* workspace, size_t workspace_bytes, int32_t* status_dev,
+    rnnt_stream_t stream, const rnnt_options_t* options) {
+    return loss_impl(logits, dt, rows, V, targets, targets_stride, logit_lengths, target_lengths,
+                     B, blank, clamp, fused_log_softmax, reduction, loss, loss_reduced, grad,
+                     workspace, workspace_bytes, status_dev, stream, options, nullptr);
+}
+
 extern "C" rnnt_status_t rnnt_loss_fused(const void* logits, rnnt_dtype_t dt, int64_t rows, int32_t V,
                                          const int32_t* targets, int32_t targets_stride,
                                          const int32_t* logit_lengths, const int32_t* target_lengths,
@@ -2893,10 +3032,14 @@ extern "C" rnnt_status_t rnnt_grad_scale(void* grad, rnnt_dtype_t dt, int64_t ro
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return RNNT_LAUNCH_FAILED;
     const int grid = grid_for(rows * 32, num_sms(dev), 4);
-    const int64_t* off = reinterpret_cast<const int64_t*>(static_cast<const char*>(workspace) + L.off);
+    const char* w = static_cast<const char*>(workspace);
+    const int64_t* off = reinterpret_cast<const int64_t*>(w + L.off);
+    const int32_t* hdr = reinterpret_cast<const int32_t*>(w + L.err);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (dt == RNNT_F32) k_scale<float><<<grid, 256, 0, st>>>(grad, rows, V, B, off, factors, per_sample);
-    else k_scale<__half><<<grid, 256, 0, st>>>(grad, rows, V, B, off, factors, per_sample);
+    if (dt == RNNT_F32)
+        k_scale<float><<<grid, 256, 0, st>>>(grad, rows, V, B, off, hdr, factors, per_sample);
+    else
+        k_scale<__half><<<grid, 256, 0, st>>>(grad, rows, V, B, off, hdr, factors, per_sample);
     return cudaGetLastError() == cudaSuccess ? RNNT_OK : RNNT_LAUNCH_FAILED;
 }
 
@@ -2919,7 +3062,7 @@ extern "C" const char* rnnt_status_string(rnnt_status_t s) {
     return "unknown status";
 }
 
-extern "C" int32_t rnnt_abi_version(void) { return 100; }
+extern "C" int32_t rnnt_abi_version(void) { return 101; }
 
 // ---------------------------------------------------------------- no-alloc entry
 // rnnt_loss_fused_noalloc runs rnnt_loss_fused over a fixed scratch array of

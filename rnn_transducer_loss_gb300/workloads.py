@@ -166,3 +166,20 @@ def custom(B, T, U, V, dtype="f32", sigma=1.0, blank=-1, clamp=-1.0, fused=True,
     cfg = Config("custom", B, V, dtype, sigma, blank, clamp, fused, reduction, seed,
                  T=tuple(int(t) for t in T), U=tuple(int(u) for u in U))
     return make(cfg, device=device)
+
+
+def to_padded(wl: Workload, max_T: int | None = None, max_U: int | None = None,
+              fill: float = 0.0) -> torch.Tensor:
+    """The workload's logits laid out as a padded (B, max_T, max_U+1, V) tensor.
+
+    Node (t, u) of sample b goes to [b, t, u]; every other entry holds `fill`
+    (padding).  Layout only: the same bytes as the compact rows."""
+    cfg = wl.cfg
+    mT = int(wl.T.max()) if max_T is None else int(max_T)
+    mU = int(wl.U.max()) if max_U is None else int(max_U)
+    x = torch.full((cfg.B, mT, mU + 1, cfg.V), fill, dtype=wl.logits.dtype,
+                   device=wl.logits.device)
+    for b in range(cfg.B):
+        T, U = int(wl.T[b]), int(wl.U[b])
+        x[b, :T, :U + 1].copy_(wl.logits[wl.sample_rows(b)].view(T, U + 1, cfg.V))
+    return x

@@ -40,7 +40,7 @@ def test_exports_every_declared_symbol(lib):
 def test_status_strings(lib):
     for code in range(6):
         assert N.status_string(code)
-    assert N.abi_version() == 100
+    assert N.abi_version() == 101
 
 
 def test_workspace_size(lib):
@@ -75,6 +75,28 @@ def _call(**kw):
 ])
 def test_host_validation_rejects(lib, bad):
     assert _call(**bad) == N.RNNT_INVALID_VALUE
+
+
+def _call_ex(fastemit_lambda=0.0, padded=None, **kw):
+    args = dict(logits=4096, dt=N.RNNT_F32, rows=50, V=16, targets=8192, targets_stride=3,
+                logit_lengths=8448, target_lengths=8704, B=2, blank=-1, clamp=-1.0,
+                fused_log_softmax=1, reduction=0, loss=8960, loss_reduced=None, grad=None,
+                workspace=1 << 20, workspace_bytes=1 << 30, status_dev=None, stream=None)
+    args.update(kw)
+    return N.rnnt_loss_fused_ex(**args, fastemit_lambda=fastemit_lambda, padded=padded)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(fastemit_lambda=-0.1), dict(fastemit_lambda=float("nan")),
+    dict(fastemit_lambda=float("inf")),
+    dict(padded=(8, 3), rows=50),            # rows must be B*max_T*(max_U+1) = 64
+    dict(padded=(0, 3), rows=0),
+    dict(padded=(8, -1), rows=0),
+    dict(padded=(8, 1024), rows=2 * 8 * 1025),
+    dict(padded=(1 << 22, 1023), rows=2 * (1 << 22) * 1024),   # a slot of 2^32 rows
+])
+def test_ex_options_validation_rejects(lib, bad):
+    assert _call_ex(**bad) == N.RNNT_INVALID_VALUE
 
 
 def test_workspace_too_small(lib):
