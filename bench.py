@@ -149,7 +149,8 @@ def oracle_sample_run(wl, n_samples: int):
     import oracle
     n = min(n_samples, wl.cfg.B)
     r1 = int(wl.offsets[n])
-    x = wl.logits[:r1].cpu().numpy()
+    t = wl.logits[:r1]
+    x = (t.float() if str(t.dtype) == "torch.bfloat16" else t).cpu().numpy()   # exact widening
     t0 = time.perf_counter()
     oracle.rnnt_loss(x, wl.targets[:n], wl.T[:n], wl.U[:n], blank=wl.cfg.blank,
                      clamp=wl.cfg.clamp, reduction=wl.cfg.reduction,
@@ -208,11 +209,28 @@ def run_reference(args, rank, world):
 
 def config_of(wl, args, l2):
     c = wl.cfg
-    return {"workload": c.name, "B": c.B, "V": c.V, "rows": wl.rows, "elements": wl.elements,
-            "logit_dtype": c.dtype, "T_range": list(c.T_range), "U_range": list(c.U_range),
-            "blank": c.blank, "clamp": c.clamp, "fused_log_softmax": c.fused,
-            "reduction": c.reduction, "seed": c.seed, "l2": l2,
-            "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+    out = {"workload": c.name, "B": c.B, "V": c.V, "rows": wl.rows, "elements": wl.elements,
+           "logit_dtype": c.dtype, "T_range": list(c.T_range), "U_range": list(c.U_range),
+           "blank": c.blank, "clamp": c.clamp, "fused_log_softmax": c.fused,
+           "reduction": c.reduction, "seed": c.seed, "l2": l2,
+           "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+    if getattr(args, "padded", False):
+        out["layout"] = (f"padded (B, max_T, max_U+1, V) = ({c.B}, {int(wl.T.max())}, "
+                         f"{int(wl.U.max()) + 1}, {c.V})")
+    if getattr(args, "fastemit", 0.0):
+        out["fastemit_lambda"] = args.fastemit
+    return out
+
+
+def make_workload(args, device):
+    """The named workload, optionally cut to its first samples or stored in another dtype."""
+    from dataclasses import replace
+    from rnn_transducer_loss_gb300 import workloads as W
+    cfg = W.CONFIGS[args.workload]
+    if args.dtype and args.dtype != cfg.dtype:
+        cfg = replace(cfg, name=f"{cfg.name}_{args.dtype}", dtype=args.dtype)
+    wl = W.make(cfg, device)
+    return W.subset(wl, args.samples) if args.samples else wl
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -230,22 +248,28 @@ def run_gpu(args, rank, world, local_rank):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
-    wl = W.make(args.workload, dev)
-    if args.samples:
-        wl = W.subset(wl, args.samples)
+    wl = make_workload(args, dev)
     cfg = wl.cfg
     rows, V = wl.rows, cfg.V
     dt = _DT[wl.logits.dtype]
     esize = wl.logits.element_size()
+    # Options of rnnt_loss_fused_ex: the padded layout and the FastEmit weight.
+    x_in = wl.logits
+    padded = None
+    if args.padded:
+        x_in = W.to_padded(wl)
+        padded = (x_in.shape[1], x_in.shape[2] - 1)
+    in_rows = x_in.numel() // V
+    use_ex = padded is not None or args.fastemit > 0
     targets = torch.as_tensor(wl.targets, device=dev)
     Tl = torch.as_tensor(wl.T, device=dev)
     Ul = torch.as_tensor(wl.U, device=dev)
-    nbytes = N.rnnt_workspace_size(cfg.B, rows, V, dt)
+    nbytes = N.rnnt_workspace_size(cfg.B, in_rows, V, dt)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     loss = torch.empty(cfg.B, dtype=torch.float32, device=dev)
     red = torch.empty((), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    grad = torch.empty_like(wl.logits)
+    grad = torch.empty_like(x_in)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     flush_rd = torch.ones(128 << 20, dtype=torch.float32, device=dev)
 
@@ -266,6 +290,20 @@ def run_gpu(args, rank, world, local_rank):
     def step(ev, stages=True):
         # Timed steps record only the first and last event (each extra event
         # record is a few microseconds of stream work); stage breakdowns all 7.
+        if use_ex:
+            # rnnt_loss_fused_ex records no stage events: time the whole call.
+            ev[0].record(stream)
+            rc = N.rnnt_loss_fused_ex(
+                x_in.data_ptr(), dt, in_rows, V, targets.data_ptr(), targets.shape[1],
+                Tl.data_ptr(), Ul.data_ptr(), cfg.B, cfg.blank, cfg.clamp, cfg.fused, red_code,
+                loss.data_ptr(), red.data_ptr(), grad.data_ptr(), ws.data_ptr(), nbytes,
+                status.data_ptr(), stream.cuda_stream, fastemit_lambda=args.fastemit,
+                padded=padded)
+            for e in ev[1:]:
+                e.record(stream)
+            if rc != N.RNNT_OK:
+                raise N.RNNTError(rc, "rnnt_loss_fused_ex")
+            return
         handles = [e.cuda_event if (stages or i in (0, 6)) else None for i, e in enumerate(ev)]
         rc = N.rnnt_loss_fused_staged(
             wl.logits.data_ptr(), dt, rows, V, targets.data_ptr(), targets.shape[1],
@@ -338,12 +376,19 @@ def run_gpu(args, rank, world, local_rank):
     value = job_throughput(wl.elements, ms, world)
 
     peak, peak_kind = load_peak()
-    step_bytes = 2 * wl.elements * esize   # algorithmic: one logit read + one grad write
+    # Algorithmic bytes: one read of every lattice element and one write of
+    # every gradient element (padding rows included in the padded layout).
+    step_bytes = wl.elements * esize + x_in.numel() * esize
     kernel_bytes = {"row_pass": wl.elements * esize if cfg.fused else 2 * rows * esize,
                     "grad_pass": 2 * wl.elements * esize if cfg.fused
                     else wl.elements * esize + 2 * rows * esize}
-    persistent = sum(stage_ms[s] for s in STAGES[1:]) < 0.03
-    if persistent:
+    persistent = use_ex or sum(stage_ms[s] for s in STAGES[1:]) < 0.03
+    if use_ex:
+        # The whole call (padding zeroing, if any, and the persistent kernel).
+        stage_ms = {"call": statistics.mean(step_ms)}
+        kernel_bytes = {"call": step_bytes}
+        dom = "call"
+    elif persistent:
         # One cooperative kernel ran everything: the preparation on its CTA 0, every
         # row, DP and gradient task, and the loss check / reduction on its last CTA.
         stage_ms = {"persistent_main": stage_ms["prepare"] + stage_ms["row_pass"]}
@@ -364,10 +409,10 @@ def run_gpu(args, rank, world, local_rank):
     step_ach = step_bytes / (ms / 1e3) / 1e9
 
     # End to end through the public API: pinned host inputs -> device, loss -> host.
-    h_logits = wl.logits.cpu().pin_memory()
+    h_logits = x_in.cpu().pin_memory()
     h_targets = targets.cpu().pin_memory()
     h_T, h_U = Tl.cpu().pin_memory(), Ul.cpu().pin_memory()
-    d_logits = torch.empty_like(wl.logits)
+    d_logits = torch.empty_like(x_in)
     d_targets, d_T, d_U = torch.empty_like(targets), torch.empty_like(Tl), torch.empty_like(Ul)
     h_loss = torch.empty(cfg.B, dtype=torch.float32).pin_memory()
     h_red = torch.empty((), dtype=torch.float32).pin_memory()
@@ -378,7 +423,8 @@ def run_gpu(args, rank, world, local_rank):
         d_T.copy_(h_T, non_blocking=True)
         d_U.copy_(h_U, non_blocking=True)
         l, r, g, _ = rnnt_loss_forward(d_logits, d_targets, d_T, d_U, cfg.blank, cfg.clamp,
-                                       cfg.reduction, cfg.fused, check=False)
+                                       cfg.reduction, cfg.fused, check=False,
+                                       fastemit_lambda=args.fastemit)
         h_loss.copy_(l, non_blocking=True)
         h_red.copy_(r, non_blocking=True)
 
@@ -414,7 +460,7 @@ def run_gpu(args, rank, world, local_rank):
         "stages_ms": stage_ms,
         "e2e": {"value": job_throughput(wl.elements, e2e_t, world), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_t},
-        "gpu_launches": (1 if persistent else 6) * args.steps,
+        "gpu_launches": ((2 if padded else 1) if persistent else 6) * args.steps,
         "clocks": clk,
         "wall_ms_timed_region": wall * 1e3,
         "kernel_source_sha256_16": kernel_source_hash(),
@@ -436,6 +482,12 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
     ap.add_argument("--workload", default="bpe_asr")
+    ap.add_argument("--dtype", choices=("f32", "f16", "bf16"), default=None,
+                    help="store the workload's logits in another dtype")
+    ap.add_argument("--padded", action="store_true",
+                    help="time the padded (B, max_T, max_U+1, V) layout (rnnt_loss_fused_ex)")
+    ap.add_argument("--fastemit", type=float, default=0.0,
+                    help="FastEmit weight (rnnt_loss_fused_ex)")
     ap.add_argument("--ref-samples", type=int, default=0,
                     help="samples per reference step (default: host core count)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -9,7 +9,8 @@
  *   - section 参数说明 (parameter table): compact 2D logits, int32 targets and
  *     lengths, blank, clamp, fused_log_softmax, per-sample loss, grad with
  *     the shape of the logits;
- *   - section 约束说明 (constraints): float32/float16 logits, blank in
+ *   - section 约束说明 (constraints): float32/float16 logits (bfloat16 added
+ *     here), blank in
  *     [-V, V-1] with -1 meaning V-1, sum of T_b*(U_b+1) equal to the number
  *     of logit rows, clamp <= 0 meaning no clipping;
  *   - section 架构设计 (architecture): a two-phase interface, workspace size
@@ -47,7 +48,10 @@ typedef enum {
     RNNT_TIMEOUT = 5              /* reserved: a bounded device wait gave up             */
 } rnnt_status_t;
 
-typedef enum { RNNT_F32 = 0, RNNT_F16 = 1 } rnnt_dtype_t;
+/* Storage type of the logits and the gradient (arithmetic is float32 for
+ * every type; bfloat16 is this library's addition to the README's
+ * float32/float16). */
+typedef enum { RNNT_F32 = 0, RNNT_F16 = 1, RNNT_BF16 = 2 } rnnt_dtype_t;
 
 typedef enum { RNNT_RED_NONE = 0, RNNT_RED_SUM = 1, RNNT_RED_MEAN = 2 } rnnt_reduction_t;
 

@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(_HERE, "librnnt_gb300.so")
 
 RNNT_OK, RNNT_INVALID_VALUE, RNNT_WORKSPACE_TOO_SMALL = 0, 1, 2
 RNNT_LAUNCH_FAILED, RNNT_LOSS_MISMATCH, RNNT_TIMEOUT = 3, 4, 5
-RNNT_F32, RNNT_F16 = 0, 1
+RNNT_F32, RNNT_F16, RNNT_BF16 = 0, 1, 2
 REDUCTIONS = {"none": 0, "sum": 1, "mean": 2}
 MAX_TARGET_LENGTH = 1023
 NOALLOC_SCRATCH_BYTES = 32 << 20     # RNNT_NOALLOC_SCRATCH_BYTES

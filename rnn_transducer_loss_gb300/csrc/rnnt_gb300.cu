@@ -33,6 +33,7 @@
 // round-to-nearest multiplies/adds and nothing underflows, which is the
 // same protection the README's log-domain recursion ("全程在 log 域") is
 // after, without evaluating a transcendental function per lattice node.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -357,6 +358,38 @@ template <> struct Elt<__half> {
         return fmaxf(f.x, f.y);
     }
 };
+// bfloat16 storage: widening to float is exact (the bits shifted up by 16).
+template <> struct Elt<__nv_bfloat16> {
+    static constexpr int kPerVec = 8;
+    __device__ static float get(const __nv_bfloat16* p, int64_t i) {
+        return __bfloat162float(__ldg(p + i));
+    }
+    __device__ static void unpack(const uint4& q, float* x) {
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            x[2 * k] = __uint_as_float(w[k] << 16);
+            x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+        }
+    }
+    __device__ static uint4 pack(const float* g) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(g[2 * k], g[2 * k + 1]);
+            w[k] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __device__ static float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+    __device__ static __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+    __device__ static float vmax(const uint4& q) {
+        float x[8];
+        unpack(q, x);
+        return fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
+                     fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+    }
+};
 
 template <int G>
 __device__ __forceinline__ unsigned group_mask() {
@@ -506,6 +539,17 @@ __device__ __forceinline__ void row_partial(const uint4* q, int nvec, int wl, fl
         }
         const float2 mf = __half22float2(m2);
         m = fmaxf(mf.x, mf.y);
+    } else if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
+        __nv_bfloat162 m2 = __bfloat162bfloat162(__ushort_as_bfloat16((unsigned short)0xff80u));
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            if (wl + 32 * i < nvec) {
+                const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q[i]);
+                m2 = __hmax2(m2, __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3])));
+            }
+        }
+        const float2 mf = __bfloat1622float2(m2);
+        m = fmaxf(mf.x, mf.y);
     } else {
         m = -INFINITY;
 #pragma unroll
@@ -525,11 +569,17 @@ __device__ __forceinline__ void row_partial(const uint4* q, int nvec, int wl, fl
                 const __half2* h = reinterpret_cast<const __half2*>(&q[i]);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) f[k] = __half22float2(h[k]);
+            } else if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
+                const uint32_t w[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    f[k] = make_float2(__uint_as_float(w[k] << 16),
+                                       __uint_as_float(w[k] & 0xffff0000u));
             } else {
                 f[0] = make_float2(__uint_as_float(q[i].x), __uint_as_float(q[i].y));
                 f[1] = make_float2(__uint_as_float(q[i].z), __uint_as_float(q[i].w));
             }
-            constexpr int NF = std::is_same<Tin, __half>::value ? 4 : 2;
+            constexpr int NF = sizeof(Tin) == 2 ? 4 : 2;
 #pragma unroll
             for (int k = 0; k < NF; ++k) {
                 float2 t = __ffma2_rn(f[k], l2, c2);
@@ -2600,6 +2650,15 @@ __global__ void __launch_bounds__(256) k_scale(void* grad, int64_t rows, int V, 
 }
 
 // ---------------------------------------------------------------- host side
+// Runs f(T{}) with T the storage type of dt (float, __half or __nv_bfloat16).
+template <typename F>
+auto with_type(rnnt_dtype_t dt, F&& f) {
+    if (dt == RNNT_F32) return f(float{});
+    if (dt == RNNT_F16) return f(__half{});
+    return f(__nv_bfloat16{});
+}
+bool valid_dtype(rnnt_dtype_t dt) { return dt == RNNT_F32 || dt == RNNT_F16 || dt == RNNT_BF16; }
+
 int g_num_sms[64];
 int g_dp_smem_set[64];
 
@@ -2835,7 +2894,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 extern "C" rnnt_status_t rnnt_workspace_size(int32_t B, int64_t rows, int32_t V, rnnt_dtype_t dt,
                                              size_t* bytes) {
-    if (!bytes || B < 1 || rows < 1 || V < 1 || (dt != RNNT_F32 && dt != RNNT_F16))
+    if (!bytes || B < 1 || rows < 1 || V < 1 || !valid_dtype(dt))
         return RNNT_INVALID_VALUE;
     *bytes = ws_layout(B, rows).total;
     return RNNT_OK;
@@ -2868,7 +2927,7 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
                 return RNNT_INVALID_VALUE;
         }
     }
-    if (dt != RNNT_F32 && dt != RNNT_F16) return RNNT_INVALID_VALUE;
+    if (!valid_dtype(dt)) return RNNT_INVALID_VALUE;
     if (B < 1 || rows < 1 || V < 1 || rows < B) return RNNT_INVALID_VALUE;
     if (targets_stride < 1 || targets_stride > RNNT_MAX_TARGET_LENGTH) return RNNT_INVALID_VALUE;
     if (blank < -V || blank >= V) return RNNT_INVALID_VALUE;
@@ -2905,7 +2964,8 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
     p.scale = reduction == RNNT_RED_MEAN ? 1.0f / (float)B : 1.0f;
     // A row whose occupancy is below 2^skip2 has every |grad| below half the
     // smallest subnormal of the output type, so every element rounds to zero.
-    const float zero_at = dt == RNNT_F16 ? -25.5f : -151.0f;
+    // (Smallest subnormals: 2^-24 fp16, 2^-133 bf16, 2^-149 fp32.)
+    const float zero_at = dt == RNNT_F16 ? -25.5f : (dt == RNNT_BF16 ? -134.5f : -151.0f);
     p.skip2 = zero_at - log2f(p.scale);
     p.lscale = log2f(p.scale);
     p.fused = fused_log_softmax ? 1 : 0;
@@ -2953,14 +3013,16 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
     };
     mark(0);
     if (grad && padded) {   // zero gradient rows outside the lattices
-        if (dt == RNNT_F32) launch_gs(k_pad_zero<float>, rows * 32, sms, st, p);
-        else launch_gs(k_pad_zero<__half>, rows * 32, sms, st, p);
+        with_type(dt, [&](auto tag) {
+            launch_gs(k_pad_zero<decltype(tag)>, rows * 32, sms, st, p);
+            return 0;
+        });
     }
     if (grad) {
         // One cooperative kernel: preparation on its CTA 0, every task, and the
         // loss check / reduction on its last CTA.
-        const bool done = dt == RNNT_F32 ? launch_persistent<float>(p, st, sms, dev)
-                                         : launch_persistent<__half>(p, st, sms, dev);
+        const bool done = with_type(
+            dt, [&](auto tag) { return launch_persistent<decltype(tag)>(p, st, sms, dev); });
         if (done) {
             for (int i = 1; i <= 6; ++i) mark(i);
             return cudaGetLastError() == cudaSuccess ? RNNT_OK : RNNT_LAUNCH_FAILED;
@@ -2968,16 +3030,20 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
     }
     k_prepare<<<1, 1024, 0, st>>>(p);
     mark(1);
-    if (dt == RNNT_F32) launch_rows<float>(p, st, sms);
-    else launch_rows<__half>(p, st, sms);
+    with_type(dt, [&](auto tag) {
+        launch_rows<decltype(tag)>(p, st, sms);
+        return 0;
+    });
     mark(2);
     k_dp<<<B, 256, dp_smem, st>>>(p);
     mark(3);
     if (grad) launch_gs(k_combine, rows, sms, st, p);
     mark(4);
     if (grad) {
-        if (dt == RNNT_F32) launch_grad<float>(p, st, sms);
-        else launch_grad<__half>(p, st, sms);
+        with_type(dt, [&](auto tag) {
+            launch_grad<decltype(tag)>(p, st, sms);
+            return 0;
+        });
     }
     mark(5);
     k_finalize<<<1, 256, 0, st>>>(p);
@@ -3026,7 +3092,7 @@ extern "C" rnnt_status_t rnnt_grad_scale(void* grad, rnnt_dtype_t dt, int64_t ro
                                          const float* factors, int32_t per_sample,
                                          rnnt_stream_t stream) {
     if (!grad || !workspace || !factors || rows < 1 || V < 1 || B < 1) return RNNT_INVALID_VALUE;
-    if (dt != RNNT_F32 && dt != RNNT_F16) return RNNT_INVALID_VALUE;
+    if (!valid_dtype(dt)) return RNNT_INVALID_VALUE;
     const Layout L = ws_layout(B, rows);
     if (workspace_bytes < L.total) return RNNT_WORKSPACE_TOO_SMALL;
     int dev = 0;
@@ -3036,10 +3102,11 @@ extern "C" rnnt_status_t rnnt_grad_scale(void* grad, rnnt_dtype_t dt, int64_t ro
     const int64_t* off = reinterpret_cast<const int64_t*>(w + L.off);
     const int32_t* hdr = reinterpret_cast<const int32_t*>(w + L.err);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (dt == RNNT_F32)
-        k_scale<float><<<grid, 256, 0, st>>>(grad, rows, V, B, off, hdr, factors, per_sample);
-    else
-        k_scale<__half><<<grid, 256, 0, st>>>(grad, rows, V, B, off, hdr, factors, per_sample);
+    with_type(dt, [&](auto tag) {
+        k_scale<decltype(tag)><<<grid, 256, 0, st>>>(grad, rows, V, B, off, hdr, factors,
+                                                     per_sample);
+        return 0;
+    });
     return cudaGetLastError() == cudaSuccess ? RNNT_OK : RNNT_LAUNCH_FAILED;
 }
 
@@ -3086,7 +3153,7 @@ extern "C" rnnt_status_t rnnt_loss_fused_noalloc(
     int32_t targets_stride, const int32_t* logit_lengths, const int32_t* target_lengths, int32_t B,
     int32_t blank, float clamp, int32_t fused_log_softmax, rnnt_reduction_t reduction, float* loss,
     float* loss_reduced, void* grad, int32_t* status_dev, rnnt_stream_t stream) {
-    if (B < 1 || rows < 1 || V < 1 || (dt != RNNT_F32 && dt != RNNT_F16)) return RNNT_INVALID_VALUE;
+    if (B < 1 || rows < 1 || V < 1 || !valid_dtype(dt)) return RNNT_INVALID_VALUE;
     const size_t need = ws_layout(B, rows).total;
     if (need > RNNT_NOALLOC_SCRATCH_BYTES) return RNNT_WORKSPACE_TOO_SMALL;
     int dev = 0;

@@ -13,14 +13,14 @@ import torch
 
 from . import _native as N
 
-_DT = {torch.float32: N.RNNT_F32, torch.float16: N.RNNT_F16}
+_DT = {torch.float32: N.RNNT_F32, torch.float16: N.RNNT_F16, torch.bfloat16: N.RNNT_BF16}
 
 
 def _check_inputs(logits, targets, logit_lengths, target_lengths):
     if not logits.is_cuda:
         raise ValueError("logits must be a CUDA tensor")
     if logits.dtype not in _DT:
-        raise ValueError(f"logits must be float32 or float16, got {logits.dtype}")
+        raise ValueError(f"logits must be float32, float16 or bfloat16, got {logits.dtype}")
     if logits.dim() not in (2, 4):
         raise ValueError("logits must be 2-D (sum_b T_b*(U_b+1), V) or 4-D "
                          "(B, max_T, max_U+1, V)")

@@ -35,7 +35,7 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-_DT = {"f32": torch.float32, "f16": torch.float16}
+_DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 
 
 @dataclass(frozen=True)

@@ -10,12 +10,18 @@ from rnn_transducer_loss_gb300 import workloads as W
 from rnn_transducer_loss_gb300.functional import rnnt_loss_forward
 
 # Tolerances of the benchmark spec: fp32 inputs loss rel 1e-5 / grad abs 1e-5,
-# fp16 inputs (fp32 accumulation) loss rel 1e-3 / grad abs 2e-3.
-TOL = {"f32": dict(loss_rel=1e-5, grad_abs=1e-5), "f16": dict(loss_rel=1e-3, grad_abs=2e-3)}
+# fp16 inputs (fp32 accumulation) loss rel 1e-3 / grad abs 2e-3.  bf16 storage
+# (not in the statement): the same loss bound as fp16, and a gradient bound of
+# two bf16 half-ulps at magnitude 1 (the gradient is rounded once to 8
+# significant bits; |grad| <= 1): 2 * 2^-9 ~ 4e-3.
+TOL = {"f32": dict(loss_rel=1e-5, grad_abs=1e-5), "f16": dict(loss_rel=1e-3, grad_abs=2e-3),
+       "bf16": dict(loss_rel=1e-3, grad_abs=4e-3)}
 
 
 def to_np(x: torch.Tensor) -> np.ndarray:
-    return x.detach().cpu().numpy()
+    # bfloat16 has no numpy type; widening it to float32 is exact.
+    x = x.detach()
+    return (x.float() if x.dtype == torch.bfloat16 else x).cpu().numpy()
 
 
 def gpu_run(wl: W.Workload, device="cuda", want_grad=True, inplace=False, **over):

@@ -170,3 +170,39 @@ def test_padded_lengths_beyond_the_tensor_are_rejected():
     with pytest.raises(ValueError):
         rnnt_loss_forward(xp, torch.as_tensor(wl.targets, device=d), T,
                           torch.as_tensor(wl.U, device=d), blank=0, reduction="sum")
+
+
+# ------------------------------------------------------------------ bfloat16 storage
+BF16_CASES = [
+    dict(V=1024, fused=True, blank=-1, clamp=-1.0, reduction="sum"),     # persistent, TMA rows
+    dict(V=512, fused=False, blank=-1, clamp=0.5, reduction="mean"),     # persistent, gather
+    dict(V=2048, fused=True, blank=3, clamp=-1.0, reduction="none"),     # per-stage TMA (4 KB rows)
+    dict(V=29, fused=True, blank=0, clamp=0.1, reduction="mean"),        # per-stage kernels
+    dict(V=5000, fused=True, blank=0, clamp=-1.0, reduction="mean"),     # long rows (streamed)
+]
+
+
+@pytest.mark.parametrize("case", range(len(BF16_CASES)))
+def test_bf16_elementwise(case):
+    wl = rand_wl(120 + case, B=4, Tmax=60, Umax=30, dtype="bf16", sigma=1.5, **BF16_CASES[case])
+    loss, red, grad = gpu_run(wl)
+    ref = oracle_full(wl)
+    assert grad.dtype == torch.bfloat16
+    assert_loss_close(to_np(loss), ref.losses, "bf16")
+    assert_grad_close(to_np(grad.float()), ref.grad, "bf16")
+
+
+def test_bf16_schedules_agree_and_options(monkeypatch):
+    wl = rand_wl(130, B=6, Tmax=80, Umax=50, V=1024, dtype="bf16", sigma=1.3, reduction="sum")
+    monkeypatch.setenv("RNNT_GB300_SCHEDULE", "kernels")
+    a = gpu_run(wl, fastemit_lambda=0.4)
+    monkeypatch.delenv("RNNT_GB300_SCHEDULE")
+    b = gpu_run(wl, fastemit_lambda=0.4)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    xp = W.to_padded(wl, fill=float("nan"))
+    lp, rp, gp = run_padded(wl, xp, fastemit_lambda=0.4)
+    assert torch.equal(lp, b[0])
+    ref = oracle.rnnt_loss_padded(to_np(xp), wl.targets, wl.T, wl.U, blank=-1, reduction="sum",
+                                  fastemit_lambda=0.4)
+    assert_grad_close(to_np(gp.float()), ref.grad, "bf16")
