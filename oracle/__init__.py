@@ -230,3 +230,56 @@ def rnnt_loss_padded(logits: np.ndarray, targets, logit_lengths, target_lengths,
             r += n
         res.grad = g
     return res
+
+
+def rnnt_loss_multiblank(logits: np.ndarray, targets, logit_lengths, target_lengths,
+                         big_blanks, blank: int = -1, sigma: float = 0.0, clamp: float = -1.0,
+                         reduction: str = "mean", fused_log_softmax: bool = True,
+                         want_grad: bool = True, fastemit_lambda: float = 0.0) -> BatchResult:
+    """Multi-blank transducer loss on the compact layout (ESPnet
+    compute_multiblank_grad_kernel docs): ``big_blanks`` is a list of
+    (output index, duration >= 2) pairs, ``sigma`` the logit
+    under-normalisation subtracted from every log-probability.  Sample by
+    sample in float64 (``rnnt_oracle_mb_sample``); with no big blanks and
+    sigma = 0 it is the standard transducer loss."""
+    lib = _load()
+    if not hasattr(lib, "_mb_ready"):
+        P, i32, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+        lib.rnnt_oracle_mb_sample.argtypes = [P, i32, i32, i32, i32, P, i32, i32, i32, P, P, dbl,
+                                              dbl, dbl, dbl, P, P]
+        lib.rnnt_oracle_mb_sample.restype = i32
+        lib._mb_ready = True
+    x = np.ascontiguousarray(logits)
+    rows, V = x.shape
+    T = np.asarray(logit_lengths, dtype=np.int64)
+    U = np.asarray(target_lengths, dtype=np.int64)
+    B = T.shape[0]
+    off = np.zeros(B + 1, dtype=np.int64)
+    off[1:] = np.cumsum(T * (U + 1))
+    if off[-1] != rows:
+        raise ValueError("rows != sum T*(U+1)")
+    ids = np.ascontiguousarray([int(i) + (V if int(i) < 0 else 0) for i, _ in big_blanks] or [0],
+                               dtype=np.int32)
+    durs = np.ascontiguousarray([int(d) for _, d in big_blanks] or [0], dtype=np.int32)
+    K = len(big_blanks)
+    scale = 1.0 / B if reduction == "mean" else 1.0
+    tg = np.asarray(targets, dtype=np.int32).reshape(B, -1)
+    losses, losses_b = np.empty(B), np.empty(B)
+    grad = np.empty((rows, V)) if want_grad else None
+    for b in range(B):
+        xb = np.ascontiguousarray(x[off[b]:off[b + 1]])
+        yb = _labels(tg[b], int(U[b]))
+        ls = np.empty(2)
+        gb = np.empty((int(off[b + 1] - off[b]), V)) if want_grad else None
+        rc = lib.rnnt_oracle_mb_sample(_ptr(xb), _dtype_code(xb), V, int(T[b]), int(U[b]),
+                                       _ptr(yb), blank, int(bool(fused_log_softmax)), K,
+                                       _ptr(ids), _ptr(durs), float(sigma),
+                                       float(fastemit_lambda), float(clamp), scale, _ptr(ls),
+                                       _ptr(gb) if gb is not None else None)
+        if rc != 0:
+            raise ValueError("oracle multi-blank rejected its arguments")
+        losses[b], losses_b[b] = ls
+        if grad is not None:
+            grad[off[b]:off[b + 1]] = gb
+    red = losses.sum() * (1.0 / B if reduction == "mean" else 1.0)
+    return BatchResult(losses, losses_b, float(red), grad)

@@ -131,3 +131,85 @@ def rnnt_loss_padded(logits, targets, logit_lengths, target_lengths, blank=-1, c
         grad = grad.clamp(-clamp, clamp)
     grad = grad * scale
     return losses.numpy(), float(losses.sum() * scale), grad.numpy()
+
+
+def multiblank_paths(T: int, U: int, durations):
+    """Every multi-blank alignment: move sequences from (0, 0) to the end (frame
+    T with U labels).  A move is 'b' (one frame), 'y' (one label) or an int i
+    (big blank i, durations[i] frames); no move passes frame T, and a
+    blank-type move may reach frame T only with every label emitted."""
+    out = []
+
+    def walk(t, u, seq):
+        if t == T:
+            if u == U:
+                out.append(tuple(seq))
+            return
+        if u < U:
+            walk(t, u + 1, seq + ["y"])
+        for mv, d in [("b", 1)] + [(i, d) for i, d in enumerate(durations)]:
+            if t + d < T or (t + d == T and u == U):
+                walk(t + d, u, seq + [mv])
+
+    walk(0, 0, [])
+    return out
+
+
+def multiblank_loss(h, T, U, y, blank, big_blanks, sigma, fused, fastemit_lambda=0.0):
+    """(loss, objective) of one sample by enumeration of multi-blank alignments."""
+    V = h.shape[1]
+    blank = blank + V if blank < 0 else blank
+    ids = [i + V if i < 0 else i for i, _ in big_blanks]
+    durs = [d for _, d in big_blanks]
+    lp = (torch.log_softmax(h, dim=1) if fused else h) - sigma
+    W = U + 1
+    scores, label_scores = [], []
+    for path in multiblank_paths(T, U, durs):
+        t = u = 0
+        s = h.new_zeros(())
+        sl = h.new_zeros(())
+        for mv in path:
+            r = t * W + u
+            if mv == "y":
+                e = lp[r, int(y[u])]
+                s, sl = s + e, sl + e
+                u += 1
+            elif mv == "b":
+                s = s + lp[r, blank]
+                t += 1
+            else:
+                s = s + lp[r, ids[mv]]
+                t += durs[mv]
+        scores.append(s)
+        label_scores.append(sl)
+    sc = torch.stack(scores)
+    loss = -torch.logsumexp(sc, dim=0)
+    weight = torch.softmax(sc.detach(), dim=0)
+    return loss, loss - fastemit_lambda * (weight * torch.stack(label_scores)).sum()
+
+
+def rnnt_loss_multiblank(logits, targets, logit_lengths, target_lengths, big_blanks, blank=-1,
+                         sigma=0.0, clamp=-1.0, reduction="mean", fused_log_softmax=True,
+                         fastemit_lambda=0.0):
+    """Brute-force multi-blank loss and gradient (compact layout); (losses, reduced, grad)."""
+    x = torch.as_tensor(logits).to(torch.float64).detach().clone().requires_grad_(True)
+    T = [int(v) for v in logit_lengths]
+    U = [int(v) for v in target_lengths]
+    B = len(T)
+    rows, per, grads = 0, [], []
+    for b in range(B):
+        n = T[b] * (U[b] + 1)
+        hb = x[rows:rows + n]
+        yb = [int(v) for v in list(targets[b])[:U[b]]]
+        lb, obj = multiblank_loss(hb, T[b], U[b], yb, blank, big_blanks, sigma,
+                                  fused_log_softmax, fastemit_lambda)
+        (g,) = torch.autograd.grad(obj, hb)
+        per.append(lb.detach())
+        grads.append(g)
+        rows += n
+    losses = torch.stack(per)
+    scale = 1.0 / B if reduction == "mean" else 1.0
+    grad = torch.cat(grads, dim=0)
+    if clamp > 0:
+        grad = grad.clamp(-clamp, clamp)
+    return losses.numpy(), float(losses.sum() * scale), (grad * scale).numpy()

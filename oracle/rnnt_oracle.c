@@ -325,3 +325,140 @@ int rnnt_oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/*
+ * Multi-blank transducer (ESPnet compute_multiblank_grad_kernel docs, after
+ * the multi-blank transducer paper they cite).  Besides the standard blank
+ * (one frame), K big blanks: big blank i is output bb_id[i] and advances
+ * bb_dur[i] >= 2 frames.  sigma >= 0 is subtracted from every log-probability
+ * used by the lattice (logit under-normalisation).  Readings of what the docs
+ * leave open:
+ *   - a path starts at (0,0) and ends when a blank-type step reaches frame T
+ *     with all U labels emitted: the standard blank from (T-1,U) or big
+ *     blank i from (T-bb_dur[i], U); no step may jump past frame T, and a
+ *     blank-type step reaching frame T with labels left is not a path;
+ *   - the gradient follows the same chain rule as the standard loss: arc
+ *     posteriors at their output index, minus p_k times their sum through
+ *     log-softmax; FastEmit scales label arcs by 1 + lambda.
+ * One sample, rows t*(U+1)+u of x.  losses[0] from alpha, losses[1] = -beta(0,0).
+ * grad (T*(U+1) x V, may be NULL) receives the clamped, scaled gradient.
+ */
+int rnnt_oracle_mb_sample(const void *x, int dtype, int V, int T, int U, const int32_t *y,
+                          int blank, int fused, int K, const int32_t *bb_id,
+                          const int32_t *bb_dur, double sigma, double fastemit_lambda,
+                          double clamp, double scale, double *losses, double *grad)
+{
+    if (T < 1 || U < 0 || V < 1 || K < 0 || K > 8)
+        return -1;
+    blank = rnnt_oracle_normalize_blank(blank, V);
+    for (int i = 0; i < K; ++i)
+        if (bb_dur[i] < 2 || bb_id[i] < 0 || bb_id[i] >= V || bb_id[i] == blank)
+            return -1;
+    const int W = U + 1;
+    const int64_t n = (int64_t)T * W;
+    /* per node: lp'(blank), lp'(label), lp'(big blank i); then alpha, beta */
+    double *lpb = (double *)malloc(sizeof(double) * (size_t)n * (4 + K));
+    double *lp = (double *)malloc(sizeof(double) * (size_t)V);
+    if (!lpb || !lp) {
+        free(lpb);
+        free(lp);
+        return -1;
+    }
+    double *lpy = lpb + n, *alpha = lpb + 2 * n, *beta = lpb + 3 * n, *lpg = lpb + 4 * n;
+    for (int64_t r = 0; r < n; ++r) {
+        int u = (int)(r % W);
+        node_logprobs(x, dtype, r, V, fused, lp);
+        lpb[r] = lp[blank] - sigma;
+        lpy[r] = (u < U) ? lp[y[u]] - sigma : -INFINITY;
+        for (int i = 0; i < K; ++i)
+            lpg[(int64_t)i * n + r] = lp[bb_id[i]] - sigma;
+    }
+    for (int t = 0; t < T; ++t) {
+        for (int u = 0; u <= U; ++u) {
+            int64_t r = (int64_t)t * W + u;
+            if (t == 0 && u == 0) {
+                alpha[r] = 0.0;
+                continue;
+            }
+            double a = (t > 0) ? alpha[r - W] + lpb[r - W] : -INFINITY;
+            if (u > 0)
+                a = log_add(a, alpha[r - 1] + lpy[r - 1]);
+            for (int i = 0; i < K; ++i) {
+                int t0 = t - bb_dur[i];
+                if (t0 >= 0) {
+                    int64_t r0 = (int64_t)t0 * W + u;
+                    a = log_add(a, alpha[r0] + lpg[(int64_t)i * n + r0]);
+                }
+            }
+            alpha[r] = a;
+        }
+    }
+    /* beta(t,u): log-probability of finishing from (t,u); frame T is the end. */
+    for (int t = T - 1; t >= 0; --t) {
+        for (int u = U; u >= 0; --u) {
+            int64_t r = (int64_t)t * W + u;
+            double b = -INFINITY;
+            if (t + 1 < T)
+                b = beta[r + W] + lpb[r];
+            else if (u == U)
+                b = lpb[r];
+            if (u < U)
+                b = log_add(b, beta[r + 1] + lpy[r]);
+            for (int i = 0; i < K; ++i) {
+                int t1 = t + bb_dur[i];
+                double g = lpg[(int64_t)i * n + r];
+                if (t1 < T)
+                    b = log_add(b, beta[(int64_t)t1 * W + u] + g);
+                else if (t1 == T && u == U)
+                    b = log_add(b, g);
+            }
+            beta[r] = b;
+        }
+    }
+    double ll = alpha[n - 1] + lpb[n - 1];
+    for (int i = 0; i < K; ++i) {
+        int t0 = T - bb_dur[i];
+        if (t0 >= 0) {
+            int64_t r0 = (int64_t)t0 * W + U;
+            ll = log_add(ll, alpha[r0] + lpg[(int64_t)i * n + r0]);
+        }
+    }
+    losses[0] = -ll;
+    losses[1] = -beta[0];
+
+    if (grad) {
+        for (int64_t r = 0; r < n; ++r) {
+            int t = (int)(r / W), u = (int)(r % W);
+            double *g = grad + r * (int64_t)V;
+            for (int k = 0; k < V; ++k)
+                g[k] = 0.0;
+            double bn = (t + 1 < T) ? beta[r + W] : (u == U ? 0.0 : -INFINITY);
+            g[blank] -= exp(alpha[r] + lpb[r] + bn - ll);
+            if (u < U)
+                g[y[u]] -= (1.0 + fastemit_lambda) * exp(alpha[r] + lpy[r] + beta[r + 1] - ll);
+            for (int i = 0; i < K; ++i) {
+                int t1 = t + bb_dur[i];
+                double bb = (t1 < T) ? beta[(int64_t)t1 * W + u]
+                                     : ((t1 == T && u == U) ? 0.0 : -INFINITY);
+                g[bb_id[i]] -= exp(alpha[r] + lpg[(int64_t)i * n + r] + bb - ll);
+            }
+            if (fused) {
+                node_logprobs(x, dtype, r, V, 1, lp);
+                double s = 0.0;
+                for (int k = 0; k < V; ++k)
+                    s += g[k];
+                for (int k = 0; k < V; ++k)
+                    g[k] -= exp(lp[k]) * s;
+            }
+            for (int k = 0; k < V; ++k) {
+                double v = g[k];
+                if (clamp > 0.0)
+                    v = v < -clamp ? -clamp : (v > clamp ? clamp : v);
+                g[k] = v * scale;
+            }
+        }
+    }
+    free(lpb);
+    free(lp);
+    return 0;
+}

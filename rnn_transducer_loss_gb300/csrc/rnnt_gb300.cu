@@ -2843,6 +2843,8 @@ bool launch_persistent(const Params& p, cudaStream_t st, int sms, int dev) {
     constexpr int EPV = Elt<Tin>::kPerVec;
     const int V = p.V, nvec = V / EPV;
     const bool vec = ((size_t)V * sizeof(Tin)) % 16 == 0;
+    // Its DP task runs lattices of at most two columns per lane (W <= 256).
+    if (dp_jclass(dp_slots(p.S + 1)) > 2) return false;
     const size_t dps = dp_smem_for(p.S);
     const void* fn = nullptr;
     size_t sm = dps;

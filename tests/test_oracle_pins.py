@@ -364,3 +364,87 @@ def test_padded_ignores_padding_and_zeroes_its_gradient():
         c = oracle.rnnt_loss(np.ascontiguousarray(x[b, :T[b], :U[b] + 1].reshape(-1, 7)),
                              y[b:b + 1], T[b:b + 1], U[b:b + 1], blank=blank, reduction="sum")
         np.testing.assert_array_equal(a.grad[b, :T[b], :U[b] + 1].reshape(-1, 7), c.grad)
+
+
+# ---------------------------------------------------------------- multi-blank
+# ESPnet compute_multiblank_grad_kernel docs: big blanks with durations and a
+# logit under-normalisation sigma.  Readings are stated in rnnt_oracle.c.
+
+def rand_mb(rng, B, Tmax, Umax, V, K, fused=True):
+    x, y, T, U, _ = rand_case(rng, B=B, Tmax=Tmax, Umax=Umax, V=V, fused=fused, blank=V - 1)
+    # big blanks take the outputs just below the standard blank (V-1); labels avoid them
+    big = [(V - 2 - i, [2, 3, 4][i % 3]) for i in range(K)]
+    y = (y % (V - 1 - K)).astype(np.int32)
+    return x, y, T, U, V - 1, big
+
+
+@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("fused", [True, False])
+def test_multiblank_brute_force(seed, fused):
+    rng = np.random.default_rng(300 + seed)
+    K = 1 + seed % 2
+    x, y, T, U, blank, big = rand_mb(rng, B=3, Tmax=6, Umax=3, V=6, K=K, fused=fused)
+    sigma = [0.0, 0.05, 0.3][seed % 3]
+    lam = [0.0, 0.4][seed % 2]
+    clamp = [-1.0, 0.2][(seed // 2) % 2]
+    red = ["none", "sum", "mean"][seed % 3]
+    got = oracle.rnnt_loss_multiblank(x, y, T, U, big, blank=blank, sigma=sigma, clamp=clamp,
+                                      reduction=red, fused_log_softmax=fused,
+                                      fastemit_lambda=lam)
+    wl, wr, wg = brute.rnnt_loss_multiblank(x.astype(np.float64), y, T, U, big, blank=blank,
+                                            sigma=sigma, clamp=clamp, reduction=red,
+                                            fused_log_softmax=fused, fastemit_lambda=lam)
+    np.testing.assert_allclose(got.losses, wl, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(got.losses_beta, wl, rtol=1e-12, atol=1e-12)
+    assert got.reduced == pytest.approx(wr, rel=1e-12, abs=1e-12)
+    np.testing.assert_allclose(got.grad, wg, rtol=1e-10, atol=1e-12)
+
+
+def test_multiblank_path_counts():
+    # one big blank of duration 2, U=0: compositions of T into parts 1 and 2
+    # (Fibonacci numbers); with U labels interleaved the count grows accordingly.
+    fib = [1, 1]
+    for _ in range(10):
+        fib.append(fib[-1] + fib[-2])
+    for T in range(1, 9):
+        assert len(brute.multiblank_paths(T, 0, [2])) == fib[T]
+    assert len(brute.multiblank_paths(4, 0, [])) == 1
+    assert len(brute.multiblank_paths(3, 2, [])) == math.comb(3 - 1 + 2, 2)
+
+
+def test_multiblank_without_big_blanks_is_the_transducer_loss():
+    rng = np.random.default_rng(310)
+    x, y, T, U, blank = rand_case(rng, B=4, Tmax=9, Umax=5, V=7, blank=-1)
+    a = oracle.rnnt_loss_multiblank(x, y, T, U, [], blank=blank, reduction="sum")
+    b = oracle.rnnt_loss(x, y, T, U, blank=blank, reduction="sum")
+    np.testing.assert_allclose(a.losses, b.losses, rtol=1e-13)
+    np.testing.assert_allclose(a.grad, b.grad, atol=1e-14)
+
+
+def test_multiblank_sigma_shifts_standard_loss_exactly():
+    # With no big blanks every alignment has T+U emissions: the loss grows by
+    # (T+U)*sigma and the gradient is unchanged.
+    rng = np.random.default_rng(311)
+    x, y, T, U, blank = rand_case(rng, B=3, Tmax=8, Umax=5, V=6, blank=2)
+    a = oracle.rnnt_loss_multiblank(x, y, T, U, [], blank=blank, sigma=0.0, reduction="sum")
+    b = oracle.rnnt_loss_multiblank(x, y, T, U, [], blank=blank, sigma=0.7, reduction="sum")
+    np.testing.assert_allclose(b.losses - a.losses, 0.7 * (T + U), rtol=1e-12)
+    np.testing.assert_allclose(a.grad, b.grad, atol=1e-13)
+
+
+def test_multiblank_rows_sum_to_zero_and_finite_differences():
+    rng = np.random.default_rng(312)
+    x, y, T, U, blank, big = rand_mb(rng, B=2, Tmax=9, Umax=4, V=7, K=2)
+    x = x.astype(np.float64)
+    r = oracle.rnnt_loss_multiblank(x, y, T, U, big, blank=blank, sigma=0.1, reduction="sum")
+    np.testing.assert_allclose(r.grad.sum(axis=1), 0.0, atol=1e-12)
+    eps = 1e-6
+    for (i, k) in [(0, 0), (3, blank), (5, big[0][0]), (7, big[1][0]), (x.shape[0] - 1, 1)]:
+        xp, xm = x.copy(), x.copy()
+        xp[i, k] += eps
+        xm[i, k] -= eps
+        lp_ = oracle.rnnt_loss_multiblank(xp, y, T, U, big, blank=blank, sigma=0.1,
+                                          reduction="sum", want_grad=False).reduced
+        lm_ = oracle.rnnt_loss_multiblank(xm, y, T, U, big, blank=blank, sigma=0.1,
+                                          reduction="sum", want_grad=False).reduced
+        assert (lp_ - lm_) / (2 * eps) == pytest.approx(r.grad[i, k], abs=1e-7)
