@@ -150,20 +150,50 @@ rnnt_status_t rnnt_loss_fused(const void *logits, rnnt_dtype_t dt, int64_t rows,
  *                     checked on the device (RNNT_INVALID_VALUE).
  *   max_T, max_U      padded layout only: max_T >= 1, 0 <= max_U <=
  *                     RNNT_MAX_TARGET_LENGTH, max_T*(max_U+1) < 2^31.
+ *   num_big_blanks    0..RNNT_MAX_BIG_BLANKS.  Multi-blank transducer (ESPnet
+ *                     compute_multiblank_grad_kernel docs and the multi-blank
+ *                     paper they cite): besides `blank` (one frame), big blank
+ *                     i is output big_blank_ids[i] (in [-V, V-1], negative
+ *                     counting from the end; distinct, not blank, never a
+ *                     label) and advances big_blank_durations[i] frames
+ *                     (2..RNNT_MAX_BIG_BLANK_DURATION).  A path ends when a
+ *                     blank-type step reaches frame T with every label
+ *                     emitted; no step passes frame T.
+ *   sigma             >= 0.  Logit under-normalisation of the same docs:
+ *                     subtracted from every log-probability the lattice uses.
+ *                     With num_big_blanks == 0 and sigma == 0 the call is the
+ *                     standard transducer loss; otherwise it runs the
+ *                     multi-blank kernels (workspace: rnnt_workspace_size_ex).
  */
+#define RNNT_MAX_BIG_BLANKS 8
+#define RNNT_MAX_BIG_BLANK_DURATION 16
 typedef struct {
     float fastemit_lambda;
     int32_t padded;
     int32_t max_T;
     int32_t max_U;
+    int32_t num_big_blanks;
+    int32_t big_blank_ids[RNNT_MAX_BIG_BLANKS];
+    int32_t big_blank_durations[RNNT_MAX_BIG_BLANKS];
+    float sigma;
 } rnnt_options_t;
+
+/*
+ * rnnt_workspace_size_ex -- workspace bytes of rnnt_loss_fused_ex with these
+ * options (NULL: as rnnt_workspace_size).  The multi-blank kernels need 8
+ * more bytes per big blank and lattice node.  RNNT_INVALID_VALUE as
+ * rnnt_workspace_size, or for num_big_blanks outside 0..RNNT_MAX_BIG_BLANKS.
+ */
+rnnt_status_t rnnt_workspace_size_ex(int32_t B, int64_t rows, int32_t V, rnnt_dtype_t dt,
+                                     const rnnt_options_t *options, size_t *bytes);
 
 /*
  * rnnt_loss_fused_ex -- rnnt_loss_fused with options (FastEmit, padded
  * layout).  Same arguments, results and errors as rnnt_loss_fused, plus
  * `options` (NULL = defaults); RNNT_INVALID_VALUE for a negative or
- * non-finite fastemit_lambda or inconsistent padded sizes.  The workspace is
- * sized by rnnt_workspace_size(B, rows, V, dt) with the same `rows`.
+ * non-finite fastemit_lambda or sigma, inconsistent padded sizes or invalid
+ * big blanks.  The workspace is sized by rnnt_workspace_size_ex(B, rows, V,
+ * dt, options) with the same `rows`.
  */
 rnnt_status_t rnnt_loss_fused_ex(const void *logits, rnnt_dtype_t dt, int64_t rows, int32_t V,
                                  const int32_t *targets, int32_t targets_stride,

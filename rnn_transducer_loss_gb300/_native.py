@@ -20,15 +20,38 @@ MAX_TARGET_LENGTH = 1023
 NOALLOC_SCRATCH_BYTES = 32 << 20     # RNNT_NOALLOC_SCRATCH_BYTES
 
 # Every symbol include/rnnt_gb300.h declares.
-EXPORTS = ("rnnt_workspace_size", "rnnt_loss_fused", "rnnt_loss_fused_ex",
+EXPORTS = ("rnnt_workspace_size", "rnnt_workspace_size_ex", "rnnt_loss_fused", "rnnt_loss_fused_ex",
            "rnnt_loss_fused_staged", "rnnt_grad_scale", "rnnt_set_trace",
            "rnnt_loss_fused_noalloc", "rnnt_status_string", "rnnt_abi_version")
 
 
+MAX_BIG_BLANKS = 8                    # RNNT_MAX_BIG_BLANKS
+MAX_BIG_BLANK_DURATION = 16           # RNNT_MAX_BIG_BLANK_DURATION
+
+
 class Options(ctypes.Structure):
-    """rnnt_options_t: FastEmit weight and the padded (B, max_T, max_U + 1, V) layout."""
+    """rnnt_options_t: FastEmit weight, the padded (B, max_T, max_U + 1, V) layout,
+    and the multi-blank transducer's big blanks and under-normalisation sigma."""
     _fields_ = [("fastemit_lambda", ctypes.c_float), ("padded", ctypes.c_int32),
-                ("max_T", ctypes.c_int32), ("max_U", ctypes.c_int32)]
+                ("max_T", ctypes.c_int32), ("max_U", ctypes.c_int32),
+                ("num_big_blanks", ctypes.c_int32),
+                ("big_blank_ids", ctypes.c_int32 * MAX_BIG_BLANKS),
+                ("big_blank_durations", ctypes.c_int32 * MAX_BIG_BLANKS),
+                ("sigma", ctypes.c_float)]
+
+
+def make_options(fastemit_lambda=0.0, padded=None, big_blanks=(), sigma=0.0) -> Options:
+    """padded = (max_T, max_U) or None; big_blanks = [(output index, duration), ...]."""
+    o = Options()
+    o.fastemit_lambda = float(fastemit_lambda)
+    if padded:
+        o.padded, o.max_T, o.max_U = 1, int(padded[0]), int(padded[1])
+    big = list(big_blanks or ())
+    o.num_big_blanks = len(big)
+    for i, (idx, dur) in enumerate(big[:MAX_BIG_BLANKS]):
+        o.big_blank_ids[i], o.big_blank_durations[i] = int(idx), int(dur)
+    o.sigma = float(sigma)
+    return o
 
 _lib = None
 
@@ -55,6 +78,9 @@ def load() -> ctypes.CDLL:
     lib.rnnt_loss_fused.argtypes = [P, i32, i64, i32, P, i32, P, P, i32, i32, f32, i32, i32,
                                     P, P, P, P, sz, P, P]
     lib.rnnt_loss_fused.restype = i32
+    lib.rnnt_workspace_size_ex.argtypes = [i32, i64, i32, i32, ctypes.POINTER(Options),
+                                           ctypes.POINTER(sz)]
+    lib.rnnt_workspace_size_ex.restype = i32
     lib.rnnt_loss_fused_ex.argtypes = lib.rnnt_loss_fused.argtypes + [ctypes.POINTER(Options)]
     lib.rnnt_loss_fused_ex.restype = i32
     lib.rnnt_loss_fused_staged.argtypes = lib.rnnt_loss_fused.argtypes + [P]
@@ -89,6 +115,16 @@ def rnnt_workspace_size(B: int, rows: int, V: int, dt: int) -> int:
     return int(out.value)
 
 
+def rnnt_workspace_size_ex(B: int, rows: int, V: int, dt: int, **options) -> int:
+    """Workspace bytes of rnnt_loss_fused_ex; options as make_options."""
+    out = ctypes.c_size_t(0)
+    opt = make_options(**options)
+    rc = load().rnnt_workspace_size_ex(B, rows, V, dt, ctypes.byref(opt), ctypes.byref(out))
+    if rc != RNNT_OK:
+        raise RNNTError(rc, "rnnt_workspace_size_ex")
+    return int(out.value)
+
+
 def rnnt_loss_fused(logits, dt, rows, V, targets, targets_stride, logit_lengths, target_lengths,
                     B, blank, clamp, fused_log_softmax, reduction, loss, loss_reduced, grad,
                     workspace, workspace_bytes, status_dev, stream) -> int:
@@ -102,10 +138,10 @@ def rnnt_loss_fused(logits, dt, rows, V, targets, targets_stride, logit_lengths,
 def rnnt_loss_fused_ex(logits, dt, rows, V, targets, targets_stride, logit_lengths, target_lengths,
                        B, blank, clamp, fused_log_softmax, reduction, loss, loss_reduced, grad,
                        workspace, workspace_bytes, status_dev, stream, fastemit_lambda=0.0,
-                       padded=None) -> int:
-    """rnnt_loss_fused with options; padded = (max_T, max_U) selects the padded layout."""
-    opt = Options(float(fastemit_lambda), 1 if padded else 0,
-                  int(padded[0]) if padded else 0, int(padded[1]) if padded else 0)
+                       padded=None, big_blanks=(), sigma=0.0) -> int:
+    """rnnt_loss_fused with options (make_options): padded = (max_T, max_U) selects the
+    padded layout, big_blanks = [(index, duration), ...] and sigma the multi-blank loss."""
+    opt = make_options(fastemit_lambda, padded, big_blanks, sigma)
     return int(load().rnnt_loss_fused_ex(logits, dt, rows, V, targets, targets_stride,
                                          logit_lengths, target_lengths, B, blank, float(clamp),
                                          int(fused_log_softmax), reduction, loss, loss_reduced,

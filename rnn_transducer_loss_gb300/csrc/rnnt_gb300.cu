@@ -115,6 +115,12 @@ __host__ __device__ inline Layout ws_layout(int B, int64_t rows) {
     return L;
 }
 
+// Workspace of the multi-blank kernels: the common layout plus one
+// extended-range probability per big blank and lattice node.
+__host__ __device__ inline size_t ws_total_mb(int B, int64_t rows, int K) {
+    return ws_layout(B, rows).total + al256(sizeof(int2) * (size_t)K * (size_t)rows);
+}
+
 struct Params {
     const void* logits;
     void* grad;
@@ -137,6 +143,14 @@ struct Params {
     float fe_l2;      // log2(1 + fe)
     int padded;       // logits/grad are the padded (B, maxT, maxW, V) tensor
     int maxT, maxW;   // padded layout: frames and lattice columns of a sample slot
+    // Multi-blank transducer: K big blanks (output bb_id[i], bb_dur[i] frames),
+    // every transition probability times bb_c = e^-sigma; pbb[i * rows + node]
+    // holds big blank i's probability at a node (extended range, biased exponent).
+    int K;
+    int bb_id[RNNT_MAX_BIG_BLANKS];
+    int bb_dur[RNNT_MAX_BIG_BLANKS];
+    float bb_c;
+    int2* pbb;
     int stage_bytes;  // per-stage shared-memory row buffer of the TMA-staged passes
     int zero_off;     // persistent kernel: shared-memory offset of a zeroed buffer ...
     int zero_rows;    // ... of zero_rows gradient rows, the source of zero-row bulk stores
@@ -802,8 +816,11 @@ __device__ void prepare_block(const Params& p, int64_t* s_before, int* s_nch) {
             }
         }
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
+        for (int k = 0; k < 8; ++k) {
             if (need[k] && (y[k] < 0 || y[k] >= p.V || y[k] == p.blank)) atomicOr(&errs, ERR_TARGET);
+            for (int i = 0; i < p.K; ++i)   // a big blank is never a label
+                if (need[k] && y[k] == p.bb_id[i]) atomicOr(&errs, ERR_TARGET);
+        }
     }
     // Longest DP first: key (T+U, area), ties by index.  O(B^2) rank sort.
     for (int b = tid; b < p.B; b += blockDim.x) {
@@ -885,6 +902,14 @@ __device__ __forceinline__ void row_finish(const Params& p, int64_t r, float M, 
     const float hb = E::get(row, p.blank);
     const float hy = (u < U) ? E::get(row, __ldg(p.targets + (int64_t)b * p.S + u)) : 0.0f;
     row_finish_at<Tin>(p, r, M, s, hb, hy, t, u, T, U, o);
+    // Multi-blank: every big blank's probability at this node.
+    const int64_t nd = o + node_index(t, u, T, U);
+    for (int i = 0; i < p.K; ++i) {
+        float m;
+        int e;
+        xf_prob(E::get(row, p.bb_id[i]), M, s, m, e);
+        p.pbb[(int64_t)i * p.rows + nd] = make_int2(__float_as_int(m), e + kEdgeBias);
+    }
 }
 
 // Group results (same in every lane of group g) for row it*NG+g of the batch
@@ -2602,6 +2627,241 @@ __device__ void finalize_block(const Params& p) {
 
 __global__ void __launch_bounds__(256) k_finalize(Params p) { finalize_block(p); }
 
+// ---------------------------------------------------------------- multi-blank
+// Multi-blank transducer (ESPnet compute_multiblank_grad_kernel docs): besides
+// the one-frame blank, big blank i (output bb_id[i]) moves bb_dur[i] frames.
+// A path ends when a blank-type step reaches frame T with all U labels out.
+//
+// k_dp_mb: one CTA per (sample, direction), blockIdx.y = 0 forward (alpha),
+// 1 backward (beta).  Thread u owns lattice column u and walks the
+// anti-diagonals, one node per diagonal.  Only the label arc crosses columns:
+// its product goes through a double-buffered exchange in shared memory, one
+// barrier per diagonal.  Blank and big-blank arcs stay in the column: each
+// thread keeps its column's last kMbRing values in a private shared-memory
+// ring (slot t mod kMbRing), so a big blank of up to kMbRing frames needs no
+// extra barrier.  Extended-range arithmetic as in the standard recursions;
+// every transition probability is scaled by bb_c = e^-sigma.
+constexpr int kMbRing = RNNT_MAX_BIG_BLANK_DURATION;
+static_assert((kMbRing & (kMbRing - 1)) == 0, "ring slots are t mod a power of two");
+
+__device__ __forceinline__ void xf_mac(float& am, int& ae, float xm, int xe, float pm, int pe,
+                                       float c) {
+    // a += x * p * c
+    float m = xm * pm * c;
+    int e = xe + pe;
+    xf_norm(m, e);
+    xf_add(am, ae, m, e, am, ae);
+}
+
+__global__ void __launch_bounds__(1024) k_dp_mb(Params p) {
+    if (*p.err) return;
+    extern __shared__ float2 mb_smem[];
+    const int nthr = blockDim.x, u = threadIdx.x;
+    float2* ring = mb_smem;                          // [kMbRing][nthr]: {m, e bits}
+    float2* xch = mb_smem + (size_t)kMbRing * nthr;  // [2][nthr]
+    const int b = blockIdx.x;
+    const int T = __ldg(p.Tl + b), U = __ldg(p.Ul + b), W = U + 1, D = T + U;
+    const int64_t o = __ldcg(p.off + b);
+    const bool col = u < W;
+    const float c = p.bb_c;
+    const float2 zero = make_float2(0.0f, __int_as_float(kZeroExp));
+    if (blockIdx.y == 0) {
+        float bm = 0.0f;   // alpha(t-1,u) p_blank(t-1,u) c: this column's blank outflow
+        int be = kZeroExp;
+        for (int d = 0; d < D; ++d) {
+            const int t = d - u;
+            float2 out = zero;
+            if (col && t >= 0 && t < T) {
+                float am;
+                int ae;
+                if (t == 0 && u == 0) {
+                    am = 1.0f;
+                    ae = 0;
+                } else {
+                    am = bm;
+                    ae = be;
+                    if (u > 0) {
+                        const float2 v = xch[((d - 1) & 1) * nthr + u - 1];
+                        xf_add(am, ae, v.x, __float_as_int(v.y), am, ae);
+                    }
+                    for (int i = 0; i < p.K; ++i) {
+                        const int t0 = t - p.bb_dur[i];
+                        if (t0 < 0) continue;
+                        const float2 a = ring[(t0 & (kMbRing - 1)) * nthr + u];
+                        const int2 q = __ldcg(p.pbb + (int64_t)i * p.rows + o + node_index(t0, u, T, U));
+                        xf_mac(am, ae, a.x, __float_as_int(a.y), __int_as_float(q.x),
+                               q.y - kEdgeBias, c);
+                    }
+                }
+                const int64_t nd = o + node_index(t, u, T, U);
+                p.alpha[nd] = make_int2(__float_as_int(am), ae);
+                ring[(t & (kMbRing - 1)) * nthr + u] = make_float2(am, __int_as_float(ae));
+                const int4 ed = __ldcg(p.edge + nd);
+                bm = am * __int_as_float(ed.x) * c;
+                be = ae + ed.y - kEdgeBias;
+                xf_norm(bm, be);
+                float ym = am * __int_as_float(ed.z) * c;
+                int ye = ae + ed.w - kEdgeBias;
+                xf_norm(ym, ye);
+                out = make_float2(ym, __int_as_float(ye));
+            } else {
+                bm = 0.0f;
+                be = kZeroExp;
+            }
+            xch[(d & 1) * nthr + u] = out;
+            __syncthreads();
+        }
+        if (u == U) {
+            // P(y|x): the blank from (T-1,U) plus every big blank that ends at frame T.
+            float pm = bm;
+            int pe = be;
+            for (int i = 0; i < p.K; ++i) {
+                const int t0 = T - p.bb_dur[i];
+                if (t0 < 0) continue;
+                const float2 a = ring[(t0 & (kMbRing - 1)) * nthr + u];
+                const int2 q = __ldcg(p.pbb + (int64_t)i * p.rows + o + node_index(t0, u, T, U));
+                xf_mac(pm, pe, a.x, __float_as_int(a.y), __int_as_float(q.x), q.y - kEdgeBias, c);
+            }
+            p.pm[b] = pm;
+            p.pe[b] = pe;
+            const double ll2 = (double)pe + log2((double)pm);
+            p.lossa[b] = -ll2 * kLn2d;
+            p.loss[b] = (float)(-ll2 * kLn2d);
+        }
+    } else {
+        float qm = 0.0f;   // beta(t+1,u): this column's previous node
+        int qe = kZeroExp;
+        for (int d = D - 1; d >= 0; --d) {
+            const int t = d - u;
+            float2 out = zero;
+            if (col && t >= 0 && t < T) {
+                const int64_t nd = o + node_index(t, u, T, U);
+                const int4 ed = __ldcg(p.edge + nd);
+                float m = 0.0f;
+                int e = kZeroExp;
+                if (t + 1 < T) xf_mac(m, e, qm, qe, __int_as_float(ed.x), ed.y - kEdgeBias, c);
+                else if (u == U) xf_mac(m, e, 1.0f, 0, __int_as_float(ed.x), ed.y - kEdgeBias, c);
+                if (u < U) {
+                    const float2 v = xch[((d + 1) & 1) * nthr + u + 1];
+                    xf_mac(m, e, v.x, __float_as_int(v.y), __int_as_float(ed.z), ed.w - kEdgeBias, c);
+                }
+                for (int i = 0; i < p.K; ++i) {
+                    const int t1 = t + p.bb_dur[i];
+                    if (t1 > T || (t1 == T && u != U)) continue;
+                    const int2 q = __ldcg(p.pbb + (int64_t)i * p.rows + nd);
+                    if (t1 == T) {
+                        xf_mac(m, e, 1.0f, 0, __int_as_float(q.x), q.y - kEdgeBias, c);
+                    } else {
+                        const float2 a = ring[(t1 & (kMbRing - 1)) * nthr + u];
+                        xf_mac(m, e, a.x, __float_as_int(a.y), __int_as_float(q.x), q.y - kEdgeBias, c);
+                    }
+                }
+                p.beta[nd] = make_int2(__float_as_int(m), e);
+                out = make_float2(m, __int_as_float(e));
+                ring[(t & (kMbRing - 1)) * nthr + u] = out;
+                qm = m;
+                qe = e;
+            } else {
+                qm = 0.0f;
+                qe = kZeroExp;
+            }
+            xch[(d & 1) * nthr + u] = out;
+            __syncthreads();
+        }
+        if (u == 0) p.lossb[b] = -((double)qe + log2((double)qm)) * kLn2d;
+    }
+}
+
+// Gradient rows of the multi-blank loss, one warp per lattice row:
+// p_k * occ (fused) minus, at their outputs, the posteriors of the node's
+// arcs (blank, label, every big blank), clipped and scaled; FastEmit scales
+// the label arc.  Rows whose every element rounds to zero are written without
+// reading the logits.
+template <typename Tin>
+__global__ void __launch_bounds__(256) k_grad_mb(Params p) {
+    if (*p.err) return;
+    using E = Elt<Tin>;
+    const Tin* X = static_cast<const Tin*>(p.logits);
+    Tin* Y = static_cast<Tin*>(p.grad);
+    const int V = p.V, lane = threadIdx.x & 31;
+    const int64_t ng = (int64_t)gridDim.x * (blockDim.x / 32), nr = nodes(p);
+    const float cl = p.clamp * p.scale, c = p.bb_c;
+    const bool clip = p.clamp < INFINITY;
+    int b = 0;
+    for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32; r < nr; r += ng) {
+        b = find_sample(p.off, p.B, r);
+        const int T = __ldg(p.Tl + b), U = __ldg(p.Ul + b), W = U + 1;
+        const int64_t o = __ldcg(p.off + b);
+        const unsigned rr = (unsigned)(r - o);
+        const int t = (int)(rr / (unsigned)W), u = (int)(rr - (unsigned)t * W);
+        const int64_t nd = o + node_index(t, u, T, U);
+        const int2 A = __ldcg(p.alpha + nd), Bt = __ldcg(p.beta + nd);
+        const int4 Ed = __ldcg(p.edge + nd);
+        const float Pm = __ldcg(p.pm + b);
+        const int Pe = __ldcg(p.pe + b);
+        const float am = __int_as_float(A.x), bm = __int_as_float(Bt.x), inv = 1.0f / Pm;
+        const int y = (u < U) ? __ldg(p.targets + (int64_t)b * p.S + u) : -1;
+        float lc = -INFINITY;
+        if (am != 0.0f && bm != 0.0f) lc = (float)(A.y + Bt.y - Pe) + lg2(am * bm * inv);
+        // posterior of an arc with probability (qm, qe) into a node of beta (nm, ne)
+        auto post = [&](float qm, int qe, float nm, int ne) -> float {
+            if (am == 0.0f || qm == 0.0f || nm == 0.0f) return 0.0f;
+            return xf_to_float(am * qm * c * nm * inv, A.y + qe + ne - Pe);
+        };
+        float eb = 0.0f, ey = 0.0f;
+        if (t + 1 < T) {
+            const int2 Bn = __ldcg(p.beta + o + node_index(t + 1, u, T, U));
+            eb = post(__int_as_float(Ed.x), Ed.y - kEdgeBias, __int_as_float(Bn.x), Bn.y);
+        } else if (u == U) {
+            eb = post(__int_as_float(Ed.x), Ed.y - kEdgeBias, 1.0f, 0);
+        }
+        if (u < U) {
+            const int2 Bn = __ldcg(p.beta + o + node_index(t, u + 1, T, U));
+            ey = post(__int_as_float(Ed.z), Ed.w - kEdgeBias, __int_as_float(Bn.x), Bn.y);
+            if (p.fe > 0.0f && ey != 0.0f && bm != 0.0f) {
+                // FastEmit: occupancy occ (1 + fe post_label / occ)
+                const float ratio = xf_to_float(__int_as_float(Ed.z) * c * __int_as_float(Bn.x) / bm,
+                                                (Ed.w - kEdgeBias) + Bn.y - Bt.y);
+                lc += lg2(fmaf(p.fe, ratio, 1.0f));
+                ey *= 1.0f + p.fe;
+            }
+        }
+        float ebb[RNNT_MAX_BIG_BLANKS];
+#pragma unroll
+        for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) {
+            ebb[i] = 0.0f;
+            if (i >= p.K) continue;
+            const int t1 = t + p.bb_dur[i];
+            if (t1 > T || (t1 == T && u != U)) continue;
+            const int2 q = __ldcg(p.pbb + (int64_t)i * p.rows + nd);
+            if (t1 == T) {
+                ebb[i] = post(__int_as_float(q.x), q.y - kEdgeBias, 1.0f, 0);
+            } else {
+                const int2 Bn = __ldcg(p.beta + o + node_index(t1, u, T, U));
+                ebb[i] = post(__int_as_float(q.x), q.y - kEdgeBias, __int_as_float(Bn.x), Bn.y);
+            }
+        }
+        const bool zero = !(lc + p.fe_l2 >= p.skip2);
+        const float w2 = lc + p.lscale - __ldcg(p.lse2 + r);
+        const int64_t lr = lrow_s(p, r, b, o, W);
+        const Tin* row = X + lr * (int64_t)V;
+        Tin* out = Y + lr * (int64_t)V;
+        for (int k = lane; k < V; k += 32) {
+            float g = (p.fused && !zero) ? ex2(fmaf(E::get(row, k), kLog2e, w2)) : 0.0f;
+            if (!zero) {
+                if (k == p.blank) g -= eb * p.scale;
+                if (k == y) g -= ey * p.scale;
+#pragma unroll
+                for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i)
+                    if (i < p.K && k == p.bb_id[i]) g -= ebb[i] * p.scale;
+                if (clip) g = fminf(fmaxf(g, -cl), cl);
+            }
+            out[k] = E::from_f(g);
+        }
+    }
+    (void)b;
+}
+
 // ---------------------------------------------------------------- padding
 // Padded layout: zero gradient rows outside every lattice (t >= T_b or
 // u > U_b), one warp per row; rows inside a lattice are left to the gradient
@@ -2914,11 +3174,28 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
                         void* const* stage_events) {
     if (!logits || !targets || !logit_lengths || !target_lengths || !loss || !workspace)
         return RNNT_INVALID_VALUE;
-    float fe = 0.0f;
-    int padded = 0, maxT = 0, maxW = 0;
+    float fe = 0.0f, sigma = 0.0f;
+    int padded = 0, maxT = 0, maxW = 0, K = 0;
+    int bb_id[RNNT_MAX_BIG_BLANKS] = {}, bb_dur[RNNT_MAX_BIG_BLANKS] = {};
     if (opts) {
         fe = opts->fastemit_lambda;
         if (!(fe >= 0.0f) || !(fe < INFINITY)) return RNNT_INVALID_VALUE;
+        sigma = opts->sigma;
+        if (!(sigma >= 0.0f) || !(sigma < INFINITY)) return RNNT_INVALID_VALUE;
+        K = opts->num_big_blanks;
+        if (K < 0 || K > RNNT_MAX_BIG_BLANKS) return RNNT_INVALID_VALUE;
+        if (V < 1 || blank < -V || blank >= V) return RNNT_INVALID_VALUE;
+        const int bl = blank < 0 ? blank + V : blank;
+        for (int i = 0; i < K; ++i) {
+            const int id = opts->big_blank_ids[i], dur = opts->big_blank_durations[i];
+            if (id < -V || id >= V || dur < 2 || dur > RNNT_MAX_BIG_BLANK_DURATION)
+                return RNNT_INVALID_VALUE;
+            bb_id[i] = id < 0 ? id + V : id;
+            bb_dur[i] = dur;
+            if (bb_id[i] == bl) return RNNT_INVALID_VALUE;
+            for (int j = 0; j < i; ++j)
+                if (bb_id[j] == bb_id[i]) return RNNT_INVALID_VALUE;
+        }
         if (opts->padded) {
             padded = 1;
             maxT = opts->max_T;
@@ -2942,7 +3219,9 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
     const size_t nbytes = (size_t)rows * (size_t)V * es;
     if (grad && grad != logits && overlaps(grad, nbytes, logits, nbytes)) return RNNT_INVALID_VALUE;
     const Layout L = ws_layout(B, rows);
-    if (workspace_bytes < L.total) return RNNT_WORKSPACE_TOO_SMALL;
+    const bool multiblank = K > 0 || sigma > 0.0f;
+    if (workspace_bytes < (multiblank ? ws_total_mb(B, rows, K) : L.total))
+        return RNNT_WORKSPACE_TOO_SMALL;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return RNNT_LAUNCH_FAILED;
@@ -2977,6 +3256,13 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
     p.padded = padded;
     p.maxT = maxT;
     p.maxW = maxW;
+    p.K = K;
+    for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) {
+        p.bb_id[i] = bb_id[i];
+        p.bb_dur[i] = bb_dur[i];
+    }
+    p.bb_c = (float)exp(-(double)sigma);
+    p.pbb = multiblank ? reinterpret_cast<int2*>(static_cast<char*>(workspace) + L.total) : nullptr;
     p.stage_bytes = (int)(((size_t)V * es + 127) / 128 * 128);
     p.loss = loss;
     p.loss_red = loss_reduced;
@@ -3020,6 +3306,30 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
             return 0;
         });
     }
+    if (multiblank) {
+        // Multi-blank transducer: preparation, the row pass (also storing every
+        // big blank's probability), the recursions, the gradient rows, the check.
+        const int nthr = std::min(1024, (targets_stride + 1 + 31) / 32 * 32);
+        const size_t smem = (size_t)(kMbRing + 2) * nthr * sizeof(float2);
+        if (cudaFuncSetAttribute(k_dp_mb, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
+            return RNNT_LAUNCH_FAILED;
+        k_prepare<<<1, 1024, 0, st>>>(p);
+        with_type(dt, [&](auto tag) {
+            launch_rows<decltype(tag)>(p, st, sms);
+            return 0;
+        });
+        k_dp_mb<<<dim3(B, 2), nthr, smem, st>>>(p);
+        if (grad) {
+            with_type(dt, [&](auto tag) {
+                launch_gs(k_grad_mb<decltype(tag)>, rows * 32, sms, st, p);
+                return 0;
+            });
+        }
+        k_finalize<<<1, 256, 0, st>>>(p);
+        for (int i = 1; i <= 6; ++i) mark(i);
+        return cudaGetLastError() == cudaSuccess ? RNNT_OK : RNNT_LAUNCH_FAILED;
+    }
     if (grad) {
         // One cooperative kernel: preparation on its CTA 0, every task, and the
         // loss check / reduction on its last CTA.
@@ -3051,6 +3361,17 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
     k_finalize<<<1, 256, 0, st>>>(p);
     mark(6);
     return cudaGetLastError() == cudaSuccess ? RNNT_OK : RNNT_LAUNCH_FAILED;
+}
+
+extern "C" rnnt_status_t rnnt_workspace_size_ex(int32_t B, int64_t rows, int32_t V,
+                                                rnnt_dtype_t dt, const rnnt_options_t* options,
+                                                size_t* bytes) {
+    if (!bytes || B < 1 || rows < 1 || V < 1 || !valid_dtype(dt)) return RNNT_INVALID_VALUE;
+    const int K = options ? options->num_big_blanks : 0;
+    if (K < 0 || K > RNNT_MAX_BIG_BLANKS) return RNNT_INVALID_VALUE;
+    const bool mb = options && (K > 0 || options->sigma > 0.0f);
+    *bytes = mb ? ws_total_mb(B, rows, K) : ws_layout(B, rows).total;
+    return RNNT_OK;
 }
 
 extern "C" rnnt_status_t rnnt_loss_fused_staged(
@@ -3131,7 +3452,7 @@ extern "C" const char* rnnt_status_string(rnnt_status_t s) {
     return "unknown status";
 }
 
-extern "C" int32_t rnnt_abi_version(void) { return 101; }
+extern "C" int32_t rnnt_abi_version(void) { return 102; }
 
 // ---------------------------------------------------------------- no-alloc entry
 // rnnt_loss_fused_noalloc runs rnnt_loss_fused over a fixed scratch array of

@@ -44,14 +44,16 @@ def _check_inputs(logits, targets, logit_lengths, target_lengths):
 class Workspace:
     """Caller-owned scratch for one call (kept alive until backward)."""
 
-    def __init__(self, B, rows, V, dt, device):
-        self.nbytes = N.rnnt_workspace_size(B, rows, V, dt)
+    def __init__(self, B, rows, V, dt, device, **options):
+        self.nbytes = (N.rnnt_workspace_size_ex(B, rows, V, dt, **options) if options
+                       else N.rnnt_workspace_size(B, rows, V, dt))
         self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
 
 
 def rnnt_loss_forward(logits, targets, logit_lengths, target_lengths, blank=-1, clamp=-1.0,
                       reduction="mean", fused_log_softmax=True, want_grad=True,
-                      inplace_grad=False, check=True, fastemit_lambda=0.0):
+                      inplace_grad=False, check=True, fastemit_lambda=0.0, big_blanks=(),
+                      sigma=0.0):
     """One fused call.  Returns (loss[B] fp32, reduced fp32 scalar, grad or None, workspace).
 
     ``logits`` is the compact (sum_b T_b*(U_b+1), V) matrix or the padded
@@ -76,7 +78,14 @@ def rnnt_loss_forward(logits, targets, logit_lengths, target_lengths, blank=-1, 
     B = logit_lengths.shape[0]
     dt = _DT[logits.dtype]
     dev = logits.device
-    ws = Workspace(B, rows, V, dt, dev)
+    big_blanks = [(int(i), int(d)) for i, d in (big_blanks or ())]
+    if len(big_blanks) > N.MAX_BIG_BLANKS:
+        raise ValueError(f"at most {N.MAX_BIG_BLANKS} big blanks")
+    options = {}
+    if padded is not None or fastemit_lambda != 0.0 or big_blanks or sigma != 0.0:
+        options = dict(fastemit_lambda=fastemit_lambda, padded=padded, big_blanks=big_blanks,
+                       sigma=sigma)
+    ws = Workspace(B, rows, V, dt, dev, **options)
     loss = torch.empty(B, dtype=torch.float32, device=dev)
     reduced = torch.empty((), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -90,11 +99,10 @@ def rnnt_loss_forward(logits, targets, logit_lengths, target_lengths, blank=-1, 
             loss.data_ptr(), reduced.data_ptr(), grad.data_ptr() if grad is not None else None,
             ws.buf.data_ptr(), ws.nbytes, status.data_ptr(), stream)
     with torch.cuda.device(dev):
-        if padded is None and fastemit_lambda == 0.0:
+        if not options:
             rc, where = N.rnnt_loss_fused(*args), "rnnt_loss_fused"
         else:
-            rc = N.rnnt_loss_fused_ex(*args, fastemit_lambda=fastemit_lambda, padded=padded)
-            where = "rnnt_loss_fused_ex"
+            rc, where = N.rnnt_loss_fused_ex(*args, **options), "rnnt_loss_fused_ex"
     if rc != N.RNNT_OK:
         raise N.RNNTError(rc, where)
     if check:
@@ -112,11 +120,11 @@ def rnnt_loss_forward(logits, targets, logit_lengths, target_lengths, blank=-1, 
 class _RNNTLossFunction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, logits, targets, logit_lengths, target_lengths, blank, clamp, reduction,
-                fused_log_softmax, check, fastemit_lambda):
+                fused_log_softmax, check, fastemit_lambda, big_blanks, sigma):
         loss, reduced, grad, ws = rnnt_loss_forward(
             logits, targets, logit_lengths, target_lengths, blank, clamp, reduction,
             fused_log_softmax, want_grad=ctx.needs_input_grad[0], check=check,
-            fastemit_lambda=fastemit_lambda)
+            fastemit_lambda=fastemit_lambda, big_blanks=big_blanks, sigma=sigma)
         ctx.reduction = reduction
         ctx.ws = ws
         V = logits.shape[-1]
@@ -128,7 +136,7 @@ class _RNNTLossFunction(torch.autograd.Function):
     def backward(ctx, grad_out):
         grad = ctx.grad
         if grad is None:
-            return (None,) * 10
+            return (None,) * 12
         rows, V, B, dt = ctx.dims
         factors = grad_out.detach().to(torch.float32).contiguous()
         per_sample = 1 if ctx.reduction == "none" else 0
@@ -140,13 +148,14 @@ class _RNNTLossFunction(torch.autograd.Function):
             raise N.RNNTError(rc, "rnnt_grad_scale")
         ctx.grad = None
         ctx.ws = None
-        return grad, None, None, None, None, None, None, None, None, None
+        return grad, None, None, None, None, None, None, None, None, None, None, None
 
 
 def rnnt_loss(logits: torch.Tensor, targets: torch.Tensor, logit_lengths: torch.Tensor,
               target_lengths: torch.Tensor, blank: int = -1, clamp: float = -1.0,
               reduction: str = "mean", fused_log_softmax: bool = True,
-              check: bool = True, fastemit_lambda: float = 0.0) -> torch.Tensor:
+              check: bool = True, fastemit_lambda: float = 0.0, big_blanks=(),
+              sigma: float = 0.0) -> torch.Tensor:
     """RNN-T loss with the arguments of torchaudio.functional.rnnt_loss.
 
     ``logits`` is either the compact 2-D matrix of the rnnt-loss-ascend README
@@ -155,13 +164,17 @@ def rnnt_loss(logits: torch.Tensor, targets: torch.Tensor, logit_lengths: torch.
     GPURNNT docs; its gradient has the same layout (zero at padded
     positions).  ``fastemit_lambda`` (>= 0) scales the gradient of every
     label emission by 1 + lambda (FastEmit, GPURNNT docs); the loss is
-    unchanged.  Returns float32 per-sample losses (reduction="none") or a
+    unchanged.  ``big_blanks`` = [(output index, duration), ...] and ``sigma``
+    select the multi-blank transducer of the ESPnet compute_multiblank_grad_kernel
+    docs (big blanks advance `duration` frames; sigma is subtracted from every
+    log-probability).  Returns float32 per-sample losses (reduction="none") or a
     float32 scalar.  ``check`` reads the device status word after the call
     (one synchronisation) and raises on invalid lengths, labels or an
     alpha/beta loss mismatch.
     """
     return _RNNTLossFunction.apply(logits, targets, logit_lengths, target_lengths, blank, clamp,
-                                   reduction, fused_log_softmax, check, float(fastemit_lambda))
+                                   reduction, fused_log_softmax, check, float(fastemit_lambda),
+                                   tuple(big_blanks or ()), float(sigma))
 
 
 class RNNTLoss(torch.nn.Module):
@@ -169,13 +182,13 @@ class RNNTLoss(torch.nn.Module):
 
     def __init__(self, blank: int = -1, clamp: float = -1.0, reduction: str = "mean",
                  fused_log_softmax: bool = True, check: bool = True,
-                 fastemit_lambda: float = 0.0):
+                 fastemit_lambda: float = 0.0, big_blanks=(), sigma: float = 0.0):
         super().__init__()
         self.blank, self.clamp, self.reduction = blank, clamp, reduction
         self.fused_log_softmax, self.check = fused_log_softmax, check
-        self.fastemit_lambda = fastemit_lambda
+        self.fastemit_lambda, self.big_blanks, self.sigma = fastemit_lambda, big_blanks, sigma
 
     def forward(self, logits, targets, logit_lengths, target_lengths):
         return rnnt_loss(logits, targets, logit_lengths, target_lengths, self.blank, self.clamp,
                          self.reduction, self.fused_log_softmax, self.check,
-                         self.fastemit_lambda)
+                         self.fastemit_lambda, self.big_blanks, self.sigma)

@@ -40,7 +40,7 @@ def test_exports_every_declared_symbol(lib):
 def test_status_strings(lib):
     for code in range(6):
         assert N.status_string(code)
-    assert N.abi_version() == 101
+    assert N.abi_version() == 102
 
 
 def test_workspace_size(lib):
@@ -77,13 +77,14 @@ def test_host_validation_rejects(lib, bad):
     assert _call(**bad) == N.RNNT_INVALID_VALUE
 
 
-def _call_ex(fastemit_lambda=0.0, padded=None, **kw):
+def _call_ex(fastemit_lambda=0.0, padded=None, big_blanks=(), sigma=0.0, **kw):
     args = dict(logits=4096, dt=N.RNNT_F32, rows=50, V=16, targets=8192, targets_stride=3,
                 logit_lengths=8448, target_lengths=8704, B=2, blank=-1, clamp=-1.0,
                 fused_log_softmax=1, reduction=0, loss=8960, loss_reduced=None, grad=None,
                 workspace=1 << 20, workspace_bytes=1 << 30, status_dev=None, stream=None)
     args.update(kw)
-    return N.rnnt_loss_fused_ex(**args, fastemit_lambda=fastemit_lambda, padded=padded)
+    return N.rnnt_loss_fused_ex(**args, fastemit_lambda=fastemit_lambda, padded=padded,
+                                big_blanks=big_blanks, sigma=sigma)
 
 
 @pytest.mark.parametrize("bad", [
@@ -94,9 +95,30 @@ def _call_ex(fastemit_lambda=0.0, padded=None, **kw):
     dict(padded=(8, -1), rows=0),
     dict(padded=(8, 1024), rows=2 * 8 * 1025),
     dict(padded=(1 << 22, 1023), rows=2 * (1 << 22) * 1024),   # a slot of 2^32 rows
+    dict(sigma=-0.1), dict(sigma=float("nan")),
+    dict(big_blanks=[(3, 1)]),                 # duration below 2
+    dict(big_blanks=[(3, 17)]),                # duration above the maximum
+    dict(big_blanks=[(15, 2)]),                # the standard blank (-1 -> 15)
+    dict(big_blanks=[(-1, 2)]),                # the standard blank, counted from the end
+    dict(big_blanks=[(3, 2), (3, 4)]),         # repeated output
+    dict(big_blanks=[(16, 2)]),                # outside the vocabulary
+    dict(big_blanks=[(i, 2) for i in range(9)]),   # more than 8
 ])
 def test_ex_options_validation_rejects(lib, bad):
     assert _call_ex(**bad) == N.RNNT_INVALID_VALUE
+
+
+def test_workspace_size_ex(lib):
+    base = N.rnnt_workspace_size(2, 5000, 16, N.RNNT_F32)
+    assert N.rnnt_workspace_size_ex(2, 5000, 16, N.RNNT_F32) == base
+    assert N.rnnt_workspace_size_ex(2, 5000, 16, N.RNNT_F32, fastemit_lambda=0.5,
+                                    padded=(50, 49)) == base
+    two = N.rnnt_workspace_size_ex(2, 5000, 16, N.RNNT_F32, big_blanks=[(3, 2), (4, 4)])
+    assert two >= base + 2 * 8 * 5000
+    assert N.rnnt_workspace_size_ex(2, 5000, 16, N.RNNT_F32, sigma=0.1) >= base
+    # the multi-blank call wants the larger workspace (rejected before any launch)
+    base50 = N.rnnt_workspace_size(2, 50, 16, N.RNNT_F32)
+    assert _call_ex(big_blanks=[(3, 2)], workspace_bytes=base50) == N.RNNT_WORKSPACE_TOO_SMALL
 
 
 def test_workspace_too_small(lib):
