@@ -161,13 +161,13 @@ def oracle_sample_run(wl, n_samples: int):
     return r1 * wl.cfg.V, dt
 
 
-def cpu_baseline(wl, budget_s: float = 20.0):
+def cpu_baseline(wl, budget_s: float = 15.0):
     import oracle
     cores = oracle.num_threads()
     n = max(1, min(wl.cfg.B, cores))
     el, dt = oracle_sample_run(wl, n)
     total_el, total_t, reps = el, dt, 1
-    while total_t + dt < budget_s and reps < 10:
+    while total_t + dt < budget_s and reps < 40:
         e2, t2 = oracle_sample_run(wl, n)
         total_el += e2
         total_t += t2
@@ -219,6 +219,10 @@ def config_of(wl, args, l2):
                          f"{int(wl.U.max()) + 1}, {c.V})")
     if getattr(args, "fastemit", 0.0):
         out["fastemit_lambda"] = args.fastemit
+    if getattr(args, "big_blanks", ""):
+        out["big_blank_durations"] = [int(v) for v in args.big_blanks.split(",")]
+    if getattr(args, "sigma", 0.0):
+        out["sigma"] = args.sigma
     return out
 
 
@@ -260,11 +264,22 @@ def run_gpu(args, rank, world, local_rank):
         x_in = W.to_padded(wl)
         padded = (x_in.shape[1], x_in.shape[2] - 1)
     in_rows = x_in.numel() // V
-    use_ex = padded is not None or args.fastemit > 0
+    # Multi-blank: big blanks take the outputs below the standard blank (V-1);
+    # the workload's labels are folded below them.
+    durs = [int(v) for v in args.big_blanks.split(",")] if args.big_blanks else []
+    blank_id = cfg.blank + V if cfg.blank < 0 else cfg.blank
+    big = [(blank_id - 1 - i, d) for i, d in enumerate(durs)]
+    if big:
+        if blank_id != V - 1:
+            raise SystemExit("--big-blanks needs a workload whose blank is the last output")
+        wl.targets[:] = wl.targets % (V - 1 - len(big))
+    mb_opts = dict(big_blanks=big, sigma=args.sigma) if (big or args.sigma) else {}
+    use_ex = padded is not None or args.fastemit > 0 or bool(mb_opts)
     targets = torch.as_tensor(wl.targets, device=dev)
     Tl = torch.as_tensor(wl.T, device=dev)
     Ul = torch.as_tensor(wl.U, device=dev)
-    nbytes = N.rnnt_workspace_size(cfg.B, in_rows, V, dt)
+    nbytes = (N.rnnt_workspace_size_ex(cfg.B, in_rows, V, dt, **mb_opts) if mb_opts
+              else N.rnnt_workspace_size(cfg.B, in_rows, V, dt))
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     loss = torch.empty(cfg.B, dtype=torch.float32, device=dev)
     red = torch.empty((), dtype=torch.float32, device=dev)
@@ -298,7 +313,7 @@ def run_gpu(args, rank, world, local_rank):
                 Tl.data_ptr(), Ul.data_ptr(), cfg.B, cfg.blank, cfg.clamp, cfg.fused, red_code,
                 loss.data_ptr(), red.data_ptr(), grad.data_ptr(), ws.data_ptr(), nbytes,
                 status.data_ptr(), stream.cuda_stream, fastemit_lambda=args.fastemit,
-                padded=padded)
+                padded=padded, **mb_opts)
             for e in ev[1:]:
                 e.record(stream)
             if rc != N.RNNT_OK:
@@ -424,7 +439,7 @@ def run_gpu(args, rank, world, local_rank):
         d_U.copy_(h_U, non_blocking=True)
         l, r, g, _ = rnnt_loss_forward(d_logits, d_targets, d_T, d_U, cfg.blank, cfg.clamp,
                                        cfg.reduction, cfg.fused, check=False,
-                                       fastemit_lambda=args.fastemit)
+                                       fastemit_lambda=args.fastemit, **mb_opts)
         h_loss.copy_(l, non_blocking=True)
         h_red.copy_(r, non_blocking=True)
 
@@ -460,7 +475,8 @@ def run_gpu(args, rank, world, local_rank):
         "stages_ms": stage_ms,
         "e2e": {"value": job_throughput(wl.elements, e2e_t, world), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_t},
-        "gpu_launches": ((2 if padded else 1) if persistent else 6) * args.steps,
+        "gpu_launches": ((5 + (1 if padded else 0)) if mb_opts else
+                         ((2 if padded else 1) if persistent else 6)) * args.steps,
         "clocks": clk,
         "wall_ms_timed_region": wall * 1e3,
         "kernel_source_sha256_16": kernel_source_hash(),
@@ -488,6 +504,10 @@ def main(argv=None):
                     help="time the padded (B, max_T, max_U+1, V) layout (rnnt_loss_fused_ex)")
     ap.add_argument("--fastemit", type=float, default=0.0,
                     help="FastEmit weight (rnnt_loss_fused_ex)")
+    ap.add_argument("--big-blanks", default="",
+                    help="multi-blank durations, e.g. 2,4,8 (rnnt_loss_fused_ex)")
+    ap.add_argument("--sigma", type=float, default=0.0,
+                    help="multi-blank logit under-normalisation")
     ap.add_argument("--ref-samples", type=int, default=0,
                     help="samples per reference step (default: host core count)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
