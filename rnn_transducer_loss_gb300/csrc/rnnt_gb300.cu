@@ -2665,11 +2665,37 @@ __global__ void __launch_bounds__(1024) k_dp_mb(Params p) {
     const bool col = u < W;
     const float c = p.bb_c;
     const float2 zero = make_float2(0.0f, __int_as_float(kZeroExp));
-    if (blockIdx.y == 0) {
+    const bool fwd = blockIdx.y == 0;
+    // Records of this column's node at the next diagonal, loaded one diagonal
+    // ahead: its transition record and the big-blank probabilities it needs
+    // (forward: of the big blanks' source nodes (t - dur, u); backward: its own).
+    int4 ed_n = make_int4(0, 0, 0, 0);
+    int2 q_n[RNNT_MAX_BIG_BLANKS];
+#pragma unroll
+    for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) q_n[i] = make_int2(0, 0);
+    auto fetch = [&](int t) {
+        if (!(col && t >= 0 && t < T)) return;
+        const int64_t nd = o + node_index(t, u, T, U);
+        ed_n = __ldcg(p.edge + nd);
+#pragma unroll
+        for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) {
+            if (i >= p.K) break;
+            const int ts = fwd ? t - p.bb_dur[i] : t;
+            q_n[i] = ts >= 0 ? __ldcg(p.pbb + (int64_t)i * p.rows + o + node_index(ts, u, T, U))
+                             : make_int2(0, 0);
+        }
+    };
+    if (fwd) {
         float bm = 0.0f;   // alpha(t-1,u) p_blank(t-1,u) c: this column's blank outflow
         int be = kZeroExp;
+        fetch(-u);
         for (int d = 0; d < D; ++d) {
             const int t = d - u;
+            const int4 ed = ed_n;
+            int2 q[RNNT_MAX_BIG_BLANKS];
+#pragma unroll
+            for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) q[i] = q_n[i];
+            fetch(t + 1);
             float2 out = zero;
             if (col && t >= 0 && t < T) {
                 float am;
@@ -2684,19 +2710,18 @@ __global__ void __launch_bounds__(1024) k_dp_mb(Params p) {
                         const float2 v = xch[((d - 1) & 1) * nthr + u - 1];
                         xf_add(am, ae, v.x, __float_as_int(v.y), am, ae);
                     }
-                    for (int i = 0; i < p.K; ++i) {
+#pragma unroll
+                    for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) {
+                        if (i >= p.K) break;
                         const int t0 = t - p.bb_dur[i];
                         if (t0 < 0) continue;
                         const float2 a = ring[(t0 & (kMbRing - 1)) * nthr + u];
-                        const int2 q = __ldcg(p.pbb + (int64_t)i * p.rows + o + node_index(t0, u, T, U));
-                        xf_mac(am, ae, a.x, __float_as_int(a.y), __int_as_float(q.x),
-                               q.y - kEdgeBias, c);
+                        xf_mac(am, ae, a.x, __float_as_int(a.y), __int_as_float(q[i].x),
+                               q[i].y - kEdgeBias, c);
                     }
                 }
-                const int64_t nd = o + node_index(t, u, T, U);
-                p.alpha[nd] = make_int2(__float_as_int(am), ae);
+                p.alpha[o + node_index(t, u, T, U)] = make_int2(__float_as_int(am), ae);
                 ring[(t & (kMbRing - 1)) * nthr + u] = make_float2(am, __int_as_float(ae));
-                const int4 ed = __ldcg(p.edge + nd);
                 bm = am * __int_as_float(ed.x) * c;
                 be = ae + ed.y - kEdgeBias;
                 xf_norm(bm, be);
@@ -2731,12 +2756,16 @@ __global__ void __launch_bounds__(1024) k_dp_mb(Params p) {
     } else {
         float qm = 0.0f;   // beta(t+1,u): this column's previous node
         int qe = kZeroExp;
+        fetch(D - 1 - u);
         for (int d = D - 1; d >= 0; --d) {
             const int t = d - u;
+            const int4 ed = ed_n;
+            int2 q[RNNT_MAX_BIG_BLANKS];
+#pragma unroll
+            for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) q[i] = q_n[i];
+            fetch(t - 1);
             float2 out = zero;
             if (col && t >= 0 && t < T) {
-                const int64_t nd = o + node_index(t, u, T, U);
-                const int4 ed = __ldcg(p.edge + nd);
                 float m = 0.0f;
                 int e = kZeroExp;
                 if (t + 1 < T) xf_mac(m, e, qm, qe, __int_as_float(ed.x), ed.y - kEdgeBias, c);
@@ -2745,18 +2774,20 @@ __global__ void __launch_bounds__(1024) k_dp_mb(Params p) {
                     const float2 v = xch[((d + 1) & 1) * nthr + u + 1];
                     xf_mac(m, e, v.x, __float_as_int(v.y), __int_as_float(ed.z), ed.w - kEdgeBias, c);
                 }
-                for (int i = 0; i < p.K; ++i) {
+#pragma unroll
+                for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) {
+                    if (i >= p.K) break;
                     const int t1 = t + p.bb_dur[i];
                     if (t1 > T || (t1 == T && u != U)) continue;
-                    const int2 q = __ldcg(p.pbb + (int64_t)i * p.rows + nd);
                     if (t1 == T) {
-                        xf_mac(m, e, 1.0f, 0, __int_as_float(q.x), q.y - kEdgeBias, c);
+                        xf_mac(m, e, 1.0f, 0, __int_as_float(q[i].x), q[i].y - kEdgeBias, c);
                     } else {
                         const float2 a = ring[(t1 & (kMbRing - 1)) * nthr + u];
-                        xf_mac(m, e, a.x, __float_as_int(a.y), __int_as_float(q.x), q.y - kEdgeBias, c);
+                        xf_mac(m, e, a.x, __float_as_int(a.y), __int_as_float(q[i].x),
+                               q[i].y - kEdgeBias, c);
                     }
                 }
-                p.beta[nd] = make_int2(__float_as_int(m), e);
+                p.beta[o + node_index(t, u, T, U)] = make_int2(__float_as_int(m), e);
                 out = make_float2(m, __int_as_float(e));
                 ring[(t & (kMbRing - 1)) * nthr + u] = out;
                 qm = m;
@@ -2772,94 +2803,166 @@ __global__ void __launch_bounds__(1024) k_dp_mb(Params p) {
     }
 }
 
-// Gradient rows of the multi-blank loss, one warp per lattice row:
-// p_k * occ (fused) minus, at their outputs, the posteriors of the node's
-// arcs (blank, label, every big blank), clipped and scaled; FastEmit scales
-// the label arc.  Rows whose every element rounds to zero are written without
-// reading the logits.
-template <typename Tin>
+// Gradient rows of the multi-blank loss.  A warp takes 32 consecutive rows:
+// each lane first forms one row's record (occupancy and every arc's
+// posterior, all its loads issued together), then the warp writes the rows
+// one by one, p_k * occ (fused) minus the posteriors at their outputs,
+// clipped and scaled; FastEmit scales the label arc.  Rows whose every
+// element rounds to zero are written without reading the logits.
+struct MbRec {
+    float w2, eb, ey;
+    int y;
+    int64_t lr;   // logits / gradient row
+    bool zero;
+    float ebb[RNNT_MAX_BIG_BLANKS];
+};
+
+__device__ __forceinline__ MbRec mb_record(const Params& p, int64_t r, int b) {
+    MbRec q;
+    const float c = p.bb_c;
+    const int T = __ldg(p.Tl + b), U = __ldg(p.Ul + b), W = U + 1;
+    const int64_t o = __ldcg(p.off + b);
+    const unsigned rr = (unsigned)(r - o);
+    const int t = (int)(rr / (unsigned)W), u = (int)(rr - (unsigned)t * W);
+    const int64_t nd = o + node_index(t, u, T, U);
+    const int2 A = __ldcg(p.alpha + nd), Bt = __ldcg(p.beta + nd);
+    const int4 Ed = __ldcg(p.edge + nd);
+    const int2 Bb = (t + 1 < T) ? __ldcg(p.beta + o + node_index(t + 1, u, T, U)) : make_int2(0, 0);
+    const int2 By = (u < U) ? __ldcg(p.beta + o + node_index(t, u + 1, T, U)) : make_int2(0, 0);
+    int2 Qb[RNNT_MAX_BIG_BLANKS], Bq[RNNT_MAX_BIG_BLANKS];
+#pragma unroll
+    for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) {
+        Qb[i] = make_int2(0, 0);
+        Bq[i] = make_int2(0, 0);
+        if (i < p.K) {
+            const int t1 = t + p.bb_dur[i];
+            Qb[i] = __ldcg(p.pbb + (int64_t)i * p.rows + nd);
+            if (t1 < T) Bq[i] = __ldcg(p.beta + o + node_index(t1, u, T, U));
+        }
+    }
+    const float Pm = __ldcg(p.pm + b);
+    const int Pe = __ldcg(p.pe + b);
+    const float am = __int_as_float(A.x), bm = __int_as_float(Bt.x), inv = 1.0f / Pm;
+    q.y = (u < U) ? __ldg(p.targets + (int64_t)b * p.S + u) : -1;
+    float lc = -INFINITY;
+    if (am != 0.0f && bm != 0.0f) lc = (float)(A.y + Bt.y - Pe) + lg2(am * bm * inv);
+    // posterior of an arc with probability (qm, qe) into a node of beta (nm, ne)
+    auto post = [&](float qm, int qe, float nm, int ne) -> float {
+        if (am == 0.0f || qm == 0.0f || nm == 0.0f) return 0.0f;
+        return xf_to_float(am * qm * c * nm * inv, A.y + qe + ne - Pe);
+    };
+    q.eb = 0.0f;
+    q.ey = 0.0f;
+    if (t + 1 < T) q.eb = post(__int_as_float(Ed.x), Ed.y - kEdgeBias, __int_as_float(Bb.x), Bb.y);
+    else if (u == U) q.eb = post(__int_as_float(Ed.x), Ed.y - kEdgeBias, 1.0f, 0);
+    if (u < U) {
+        q.ey = post(__int_as_float(Ed.z), Ed.w - kEdgeBias, __int_as_float(By.x), By.y);
+        if (p.fe > 0.0f && q.ey != 0.0f && bm != 0.0f) {
+            // FastEmit: occupancy occ (1 + fe post_label / occ)
+            const float ratio = xf_to_float(__int_as_float(Ed.z) * c * __int_as_float(By.x) / bm,
+                                            (Ed.w - kEdgeBias) + By.y - Bt.y);
+            lc += lg2(fmaf(p.fe, ratio, 1.0f));
+            q.ey *= 1.0f + p.fe;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) {
+        q.ebb[i] = 0.0f;
+        if (i >= p.K) continue;
+        const int t1 = t + p.bb_dur[i];
+        const float qm = __int_as_float(Qb[i].x);
+        const int qe = Qb[i].y - kEdgeBias;
+        if (t1 == T && u == U) q.ebb[i] = post(qm, qe, 1.0f, 0);
+        else if (t1 < T) q.ebb[i] = post(qm, qe, __int_as_float(Bq[i].x), Bq[i].y);
+    }
+    q.zero = !(lc + p.fe_l2 >= p.skip2);
+    q.w2 = lc + p.lscale - __ldcg(p.lse2 + r);
+    q.lr = lrow_s(p, r, b, o, W);
+    return q;
+}
+
+template <typename Tin, bool VEC>
 __global__ void __launch_bounds__(256) k_grad_mb(Params p) {
     if (*p.err) return;
     using E = Elt<Tin>;
     const Tin* X = static_cast<const Tin*>(p.logits);
     Tin* Y = static_cast<Tin*>(p.grad);
-    const int V = p.V, lane = threadIdx.x & 31;
-    const int64_t ng = (int64_t)gridDim.x * (blockDim.x / 32), nr = nodes(p);
-    const float cl = p.clamp * p.scale, c = p.bb_c;
+    const int V = p.V, wl = threadIdx.x & 31;
+    const int64_t nr = nodes(p), nbatch = (nr + 31) / 32;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
+    const float cl = p.clamp * p.scale;
     const bool clip = p.clamp < INFINITY;
-    int b = 0;
-    for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32; r < nr; r += ng) {
-        b = find_sample(p.off, p.B, r);
-        const int T = __ldg(p.Tl + b), U = __ldg(p.Ul + b), W = U + 1;
-        const int64_t o = __ldcg(p.off + b);
-        const unsigned rr = (unsigned)(r - o);
-        const int t = (int)(rr / (unsigned)W), u = (int)(rr - (unsigned)t * W);
-        const int64_t nd = o + node_index(t, u, T, U);
-        const int2 A = __ldcg(p.alpha + nd), Bt = __ldcg(p.beta + nd);
-        const int4 Ed = __ldcg(p.edge + nd);
-        const float Pm = __ldcg(p.pm + b);
-        const int Pe = __ldcg(p.pe + b);
-        const float am = __int_as_float(A.x), bm = __int_as_float(Bt.x), inv = 1.0f / Pm;
-        const int y = (u < U) ? __ldg(p.targets + (int64_t)b * p.S + u) : -1;
-        float lc = -INFINITY;
-        if (am != 0.0f && bm != 0.0f) lc = (float)(A.y + Bt.y - Pe) + lg2(am * bm * inv);
-        // posterior of an arc with probability (qm, qe) into a node of beta (nm, ne)
-        auto post = [&](float qm, int qe, float nm, int ne) -> float {
-            if (am == 0.0f || qm == 0.0f || nm == 0.0f) return 0.0f;
-            return xf_to_float(am * qm * c * nm * inv, A.y + qe + ne - Pe);
-        };
-        float eb = 0.0f, ey = 0.0f;
-        if (t + 1 < T) {
-            const int2 Bn = __ldcg(p.beta + o + node_index(t + 1, u, T, U));
-            eb = post(__int_as_float(Ed.x), Ed.y - kEdgeBias, __int_as_float(Bn.x), Bn.y);
-        } else if (u == U) {
-            eb = post(__int_as_float(Ed.x), Ed.y - kEdgeBias, 1.0f, 0);
-        }
-        if (u < U) {
-            const int2 Bn = __ldcg(p.beta + o + node_index(t, u + 1, T, U));
-            ey = post(__int_as_float(Ed.z), Ed.w - kEdgeBias, __int_as_float(Bn.x), Bn.y);
-            if (p.fe > 0.0f && ey != 0.0f && bm != 0.0f) {
-                // FastEmit: occupancy occ (1 + fe post_label / occ)
-                const float ratio = xf_to_float(__int_as_float(Ed.z) * c * __int_as_float(Bn.x) / bm,
-                                                (Ed.w - kEdgeBias) + Bn.y - Bt.y);
-                lc += lg2(fmaf(p.fe, ratio, 1.0f));
-                ey *= 1.0f + p.fe;
-            }
-        }
-        float ebb[RNNT_MAX_BIG_BLANKS];
+    constexpr unsigned F = 0xffffffffu;
+    for (int64_t bt = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32; bt < nbatch;
+         bt += nwarps) {
+        const int64_t r0 = bt * 32;
+        const int n = (int)min((int64_t)32, nr - r0);
+        MbRec mine;
+        if (wl < n) mine = mb_record(p, r0 + wl, find_sample(p.off, p.B, r0 + wl));
+        for (int it = 0; it < n; ++it) {
+            const float w2 = __shfl_sync(F, mine.w2, it), eb = __shfl_sync(F, mine.eb, it);
+            const float ey = __shfl_sync(F, mine.ey, it);
+            const int y = __shfl_sync(F, mine.y, it);
+            const bool zero = __shfl_sync(F, (int)mine.zero, it) != 0;
+            const int64_t lr = __shfl_sync(F, mine.lr, it);
+            float ebb[RNNT_MAX_BIG_BLANKS];
 #pragma unroll
-        for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) {
-            ebb[i] = 0.0f;
-            if (i >= p.K) continue;
-            const int t1 = t + p.bb_dur[i];
-            if (t1 > T || (t1 == T && u != U)) continue;
-            const int2 q = __ldcg(p.pbb + (int64_t)i * p.rows + nd);
-            if (t1 == T) {
-                ebb[i] = post(__int_as_float(q.x), q.y - kEdgeBias, 1.0f, 0);
-            } else {
-                const int2 Bn = __ldcg(p.beta + o + node_index(t1, u, T, U));
-                ebb[i] = post(__int_as_float(q.x), q.y - kEdgeBias, __int_as_float(Bn.x), Bn.y);
-            }
-        }
-        const bool zero = !(lc + p.fe_l2 >= p.skip2);
-        const float w2 = lc + p.lscale - __ldcg(p.lse2 + r);
-        const int64_t lr = lrow_s(p, r, b, o, W);
-        const Tin* row = X + lr * (int64_t)V;
-        Tin* out = Y + lr * (int64_t)V;
-        for (int k = lane; k < V; k += 32) {
-            float g = (p.fused && !zero) ? ex2(fmaf(E::get(row, k), kLog2e, w2)) : 0.0f;
-            if (!zero) {
-                if (k == p.blank) g -= eb * p.scale;
-                if (k == y) g -= ey * p.scale;
+            for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i)
+                ebb[i] = i < p.K ? __shfl_sync(F, mine.ebb[i], it) : 0.0f;
+            const Tin* row = X + lr * (int64_t)V;
+            Tin* out = Y + lr * (int64_t)V;
+            // The element's gradient from its softmax term gk (0 when not fused).
+            auto finish = [&](int k, float gk) -> float {
+                if (zero) return 0.0f;
+                if (k == p.blank) gk -= eb * p.scale;
+                if (k == y) gk -= ey * p.scale;
 #pragma unroll
                 for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i)
-                    if (i < p.K && k == p.bb_id[i]) g -= ebb[i] * p.scale;
-                if (clip) g = fminf(fmaxf(g, -cl), cl);
+                    if (i < p.K && k == p.bb_id[i]) gk -= ebb[i] * p.scale;
+                return clip ? fminf(fmaxf(gk, -cl), cl) : gk;
+            };
+            if (VEC) {
+                constexpr int EPV = E::kPerVec;
+                const uint4* rv = reinterpret_cast<const uint4*>(row);
+                uint4* ov = reinterpret_cast<uint4*>(out);
+                for (int vi = wl; vi < V / EPV; vi += 32) {
+                    float g[EPV];
+                    if (p.fused && !zero) {
+                        float x[EPV];
+                        E::unpack(__ldcs(rv + vi), x);
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e) g[e] = ex2(fmaf(x[e], kLog2e, w2));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e) g[e] = 0.0f;
+                    }
+                    // Only a vector that holds an arc's output needs the subtractions.
+                    const int k0 = vi * EPV;
+                    bool special = (unsigned)(p.blank - k0) < (unsigned)EPV ||
+                                   (unsigned)(y - k0) < (unsigned)EPV;
+                    for (int i = 0; i < p.K; ++i)
+                        special |= (unsigned)(p.bb_id[i] - k0) < (unsigned)EPV;
+                    if (special) {
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e) g[e] = finish(k0 + e, g[e]);
+                    } else if (clip && !zero) {
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e) g[e] = fminf(fmaxf(g[e], -cl), cl);
+                    } else if (zero) {
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e) g[e] = 0.0f;
+                    }
+                    __stcs(ov + vi, E::pack(g));
+                }
+            } else {
+                for (int k = wl; k < V; k += 32) {
+                    const float gk =
+                        (p.fused && !zero) ? ex2(fmaf(E::get(row, k), kLog2e, w2)) : 0.0f;
+                    out[k] = E::from_f(finish(k, gk));
+                }
             }
-            out[k] = E::from_f(g);
         }
     }
-    (void)b;
 }
 
 // ---------------------------------------------------------------- padding
@@ -3322,7 +3425,11 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
         k_dp_mb<<<dim3(B, 2), nthr, smem, st>>>(p);
         if (grad) {
             with_type(dt, [&](auto tag) {
-                launch_gs(k_grad_mb<decltype(tag)>, rows * 32, sms, st, p);
+                using T = decltype(tag);
+                if (((size_t)V * sizeof(T)) % 16 == 0)
+                    launch_gs(k_grad_mb<T, true>, rows * 32, sms, st, p);
+                else
+                    launch_gs(k_grad_mb<T, false>, rows * 32, sms, st, p);
                 return 0;
             });
         }
