@@ -206,3 +206,37 @@ def test_bf16_schedules_agree_and_options(monkeypatch):
     ref = oracle.rnnt_loss_padded(to_np(xp), wl.targets, wl.T, wl.U, blank=-1, reduction="sum",
                                   fastemit_lambda=0.4)
     assert_grad_close(to_np(gp.float()), ref.grad, "bf16")
+
+
+# ------------------------------------------------------------------ degenerate shapes
+def test_padded_degenerate_lattices():
+    # T=1 and U=0 in every combination inside a padded tensor wider than all of them.
+    wl = make(4, [1, 1, 9, 5], [0, 4, 0, 2], 16, dtype="f32", blank=2, reduction="sum")
+    xp = W.to_padded(wl, max_T=10, max_U=6, fill=float("nan"))
+    loss, red, grad = run_padded(wl, xp, fastemit_lambda=0.5)
+    ref = oracle.rnnt_loss_padded(to_np(xp), wl.targets, wl.T, wl.U, blank=2, reduction="sum",
+                                  fastemit_lambda=0.5)
+    assert_loss_close(to_np(loss), ref.losses, "f32")
+    assert_grad_close(to_np(grad), ref.grad, "f32")
+
+
+def test_padded_single_slot_and_exact_fit():
+    # max_T = T and max_U = U for every sample: the padded layout is the compact one.
+    wl = make(2, [7, 7], [3, 3], 24, dtype="f16", blank=-1, reduction="mean")
+    xp = W.to_padded(wl)
+    assert xp.shape == (2, 7, 4, 24)
+    lp, rp, gp = run_padded(wl, xp)
+    lc, rc, gc = gpu_run(wl)
+    assert torch.equal(lp, lc) and torch.equal(gp.reshape(-1, 24), gc)
+
+
+def test_multiblank_degenerate_lattices():
+    # T shorter than every big blank, T equal to a duration, U=0 and T=1.
+    wl = make(5, [1, 2, 4, 3, 8], [0, 1, 0, 2, 0], 12, dtype="f32", blank=-1, reduction="sum")
+    wl.targets[:] = wl.targets % 9
+    big = [(10, 2), (9, 4)]
+    loss, red, grad = gpu_run(wl, big_blanks=big, sigma=0.1)
+    ref = oracle.rnnt_loss_multiblank(to_np(wl.logits), wl.targets, wl.T, wl.U, big, blank=-1,
+                                      sigma=0.1, reduction="sum")
+    assert_loss_close(to_np(loss), ref.losses, "f32")
+    assert_grad_close(to_np(grad), ref.grad, "f32")
