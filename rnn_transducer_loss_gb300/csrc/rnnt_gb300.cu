@@ -436,6 +436,9 @@ __device__ __forceinline__ float group_sum(float v, unsigned gm) {
 #define RNNT_KSTAGES 4
 #endif
 constexpr int kStages = RNNT_KSTAGES;
+// Ring depth of the persistent kernel's warps: rows of 8 vectors per lane
+// (4 KB) get 3 stages so that two CTAs still share an SM.
+__host__ __device__ constexpr int main_stages(int NV) { return NV >= 8 ? 3 : kStages; }
 constexpr int kWaitSpins = 1 << 22;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
@@ -2119,6 +2122,7 @@ template <typename Tin, int NV>
 __device__ bool row_batch_tma(const Params& p, int64_t r0, int n, unsigned char* buf,
                               uint64_t* bars, uint32_t& kk, int b, int T, int U, int64_t o) {
     using E = Elt<Tin>;
+    constexpr int ST = main_stages(NV);
     constexpr int EPV = E::kPerVec;
     const int wl = threadIdx.x & 31, sb = p.stage_bytes;
     const Tin* X = static_cast<const Tin*>(p.logits);
@@ -2132,8 +2136,8 @@ __device__ bool row_batch_tma(const Params& p, int64_t r0, int n, unsigned char*
     float myhb = 0.0f, myhy = 0.0f;
     if (wl == 0) {
         fence_proxy_async();
-        for (int i = 0; i < min(kStages, n); ++i) {
-            const uint32_t st = (kk + i) % kStages;
+        for (int i = 0; i < min(ST, n); ++i) {
+            const uint32_t st = (kk + i) % ST;
             tma_row_load(buf + st * sb, X + lrow_s(p, r0 + i, b, o, W) * (int64_t)V, rb,
                          &bars[st]);
         }
@@ -2148,8 +2152,8 @@ __device__ bool row_batch_tma(const Params& p, int64_t r0, int n, unsigned char*
             ls[j] = 0.0f;
             const int i = g0 + j;
             if (ifail < 0 && i < n) {
-                const uint32_t k = kk + i, st = k % kStages;
-                if (!mbar_wait(&bars[st], (k / kStages) & 1, p.err)) {
+                const uint32_t k = kk + i, st = k % ST;
+                if (!mbar_wait(&bars[st], (k / ST) & 1, p.err)) {
                     ifail = i;
                 } else {
                     const uint4* rv = reinterpret_cast<const uint4*>(buf + st * sb);
@@ -2163,10 +2167,10 @@ __device__ bool row_batch_tma(const Params& p, int64_t r0, int n, unsigned char*
                         myhy = y >= 0 ? E::to_f(rowp[y]) : 0.0f;
                     }
                     __syncwarp();
-                    if (wl == 0 && i + kStages < n) {
+                    if (wl == 0 && i + ST < n) {
                         fence_proxy_async();
                         tma_row_load(buf + st * sb,
-                                     X + lrow_s(p, r0 + i + kStages, b, o, W) * (int64_t)V, rb,
+                                     X + lrow_s(p, r0 + i + ST, b, o, W) * (int64_t)V, rb,
                                      &bars[st]);
                     }
                     row_partial<Tin, NV>(q, nvec, wl, lm[j], ls[j]);
@@ -2184,8 +2188,8 @@ __device__ bool row_batch_tma(const Params& p, int64_t r0, int n, unsigned char*
         }
     }
     if (ifail >= 0) {   // timeout: wait (bounded) for the copies still in flight
-        for (int q = ifail; q < min(ifail + kStages, n); ++q)
-            mbar_wait(&bars[(kk + q) % kStages], ((kk + q) / kStages) & 1, p.err);
+        for (int q = ifail; q < min(ifail + ST, n); ++q)
+            mbar_wait(&bars[(kk + q) % ST], ((kk + q) / ST) & 1, p.err);
         return false;
     }
     kk += n;
@@ -2206,6 +2210,7 @@ __device__ bool grad_batch_tma(const Params& p, int64_t r0, int s0, uint32_t zma
                                uint32_t& kk, const unsigned char* zbuf, int b, int64_t o,
                                int W) {
     using E = Elt<Tin>;
+    constexpr int ST = main_stages(NV);
     constexpr int EPV = E::kPerVec;
     const int wl = threadIdx.x & 31, sb = p.stage_bytes;
     const Tin* X = static_cast<const Tin*>(p.logits);
@@ -2235,8 +2240,8 @@ __device__ bool grad_batch_tma(const Params& p, int64_t r0, int s0, uint32_t zma
         }
         tma_store_commit();
         fence_proxy_async();
-        for (int i = 0; i < min(kStages, my); ++i) {
-            const uint32_t st = (kk + i) % kStages;
+        for (int i = 0; i < min(ST, my); ++i) {
+            const uint32_t st = (kk + i) % ST;
             tma_row_load(buf + st * sb,
                          X + lrow_s(p, r0 + list[first + i * stride], b, o, W) * (int64_t)V, rb,
                          &bars[st]);
@@ -2248,11 +2253,11 @@ __device__ bool grad_batch_tma(const Params& p, int64_t r0, int s0, uint32_t zma
         const float w2 = in.x, eb = in.y, ey = in.z;
         const int y = __float_as_int(in.w);
         const int vy = y >= 0 ? y / EPV : -1, ey_i = y >= 0 ? y % EPV : 0;
-        const uint32_t k = kk + i, st = k % kStages;
-        if (!mbar_wait(&bars[st], (k / kStages) & 1, p.err)) {
+        const uint32_t k = kk + i, st = k % ST;
+        if (!mbar_wait(&bars[st], (k / ST) & 1, p.err)) {
             // Timeout: wait (bounded) for the copies still in flight.
-            for (int q = i + 1; q < min(i + kStages, my); ++q)
-                mbar_wait(&bars[(kk + q) % kStages], ((kk + q) / kStages) & 1, p.err);
+            for (int q = i + 1; q < min(i + ST, my); ++q)
+                mbar_wait(&bars[(kk + q) % ST], ((kk + q) / ST) & 1, p.err);
             return false;
         }
         const uint4* rv = reinterpret_cast<const uint4*>(buf + st * sb);
@@ -2285,11 +2290,11 @@ __device__ bool grad_batch_tma(const Params& p, int64_t r0, int s0, uint32_t zma
             __stcs(ov + vi, E::pack(g));
         }
         __syncwarp();
-        if (wl == 0 && i + kStages < my) {
+        if (wl == 0 && i + ST < my) {
             fence_proxy_async();
             tma_row_load(
                 buf + st * sb,
-                X + lrow_s(p, r0 + list[first + (i + kStages) * stride], b, o, W) * (int64_t)V, rb,
+                X + lrow_s(p, r0 + list[first + (i + ST) * stride], b, o, W) * (int64_t)V, rb,
                 &bars[st]);
         }
     }
@@ -2398,8 +2403,9 @@ __device__ void finalize_block(const Params& p);
 
 template <typename Tin, int NV, int G, bool VEC>
 __device__ __forceinline__ void main_body(const Params& p) {
+    constexpr int ST = main_stages(NV > 0 ? NV : 1);
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    __shared__ uint64_t bars_all[8 * kStages];
+    __shared__ uint64_t bars_all[8 * ST];
     __shared__ float4 s_info[kTaskRows];
     __shared__ uint16_t s_nz[kTaskRows];
     __shared__ int s_cnt[8];
@@ -2448,8 +2454,8 @@ __device__ __forceinline__ void main_body(const Params& p) {
         return;
     }
 
-    unsigned char* buf = smem_raw + (size_t)wid * kStages * p.stage_bytes;
-    uint64_t* bars = bars_all + wid * kStages;
+    unsigned char* buf = smem_raw + (size_t)wid * ST * p.stage_bytes;
+    uint64_t* bars = bars_all + wid * ST;
     const unsigned char* zbuf = smem_raw + p.zero_off;
     if (NV > 0) {
         const int zn = p.zero_rows * p.V * (int)sizeof(Tin) / 16;
@@ -2460,7 +2466,7 @@ __device__ __forceinline__ void main_body(const Params& p) {
     }
     if (NV > 0 && wl == 0) {
 #pragma unroll
-        for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], 1);
+        for (int st = 0; st < ST; ++st) mbar_init(&bars[st], 1);
         fence_mbar_init();
     }
     uint32_t kk = 0;   // this warp's TMA ring position
@@ -3214,7 +3220,8 @@ bool launch_persistent(const Params& p, cudaStream_t st, int sms, int dev) {
     int zero_off = 0, zero_rows = 0;
     if (p.fused) {
         if (!(vec && nvec > 32 && nvec <= 256)) return false;
-        sm = std::max(sm, (size_t)8 * kStages * p.stage_bytes);
+        sm = std::max(sm, (size_t)8 * main_stages(nvec <= 64 ? 2 : nvec <= 128 ? 4 : 8) *
+                              p.stage_bytes);
         sm = (sm + 127) / 128 * 128;
         const int rb = V * (int)sizeof(Tin);
         // Zero-row buffer from what is left of the dynamic shared memory that

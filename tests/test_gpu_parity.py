@@ -254,6 +254,9 @@ SCHED_CASES = [
     dict(B=6, V=1024, dtype="f16", fused=True, blank=7, reduction="none", clamp=-1.0),
     dict(B=5, V=512, dtype="f16", fused=False, blank=-1, reduction="mean", clamp=0.5),
     dict(B=3, V=80, dtype="f32", fused=False, blank=2, reduction="sum", clamp=-1.0),
+    # 4 KB rows (8 vectors per lane): the persistent kernel's 3-stage rings
+    dict(B=4, V=1024, dtype="f32", fused=True, blank=-1, reduction="sum", clamp=-1.0),
+    dict(B=3, V=2048, dtype="f16", fused=True, blank=5, reduction="mean", clamp=0.2),
 ]
 
 
