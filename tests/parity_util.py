@@ -9,9 +9,9 @@ import oracle
 from rnn_transducer_loss_gb300 import workloads as W
 from rnn_transducer_loss_gb300.functional import rnnt_loss_forward
 
-# Tolerances of the benchmark spec: fp32 inputs loss rel 1e-5 / grad abs 1e-5,
-# fp16 inputs (fp32 accumulation) loss rel 1e-3 / grad abs 2e-3.  bf16 storage
-# (not in the statement): the same loss bound as fp16, and a gradient bound of
+# Parity tolerances against the float64 oracle: fp32 inputs loss rel 1e-5 /
+# grad abs 1e-5, fp16 inputs (fp32 accumulation) loss rel 1e-3 / grad abs
+# 2e-3.  bf16 storage: the same loss bound as fp16, and a gradient bound of
 # two bf16 half-ulps at magnitude 1 (the gradient is rounded once to 8
 # significant bits; |grad| <= 1): 2 * 2^-9 ~ 4e-3.
 TOL = {"f32": dict(loss_rel=1e-5, grad_abs=1e-5), "f16": dict(loss_rel=1e-3, grad_abs=2e-3),
