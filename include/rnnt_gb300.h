@@ -45,7 +45,7 @@ typedef enum {
     RNNT_WORKSPACE_TOO_SMALL = 2, /* workspace_bytes below rnnt_workspace_size()         */
     RNNT_LAUNCH_FAILED = 3,       /* a kernel launch returned a CUDA error               */
     RNNT_LOSS_MISMATCH = 4,       /* alpha-side and beta-side losses disagree (or NaN)   */
-    RNNT_TIMEOUT = 5              /* reserved: a bounded device wait gave up             */
+    RNNT_TIMEOUT = 5              /* a bounded device wait gave up                       */
 } rnnt_status_t;
 
 /* Storage type of the logits and the gradient (arithmetic is float32 for
@@ -293,6 +293,18 @@ rnnt_status_t rnnt_loss_fused_noalloc(const void *logits, rnnt_dtype_t dt, int64
                                       rnnt_reduction_t reduction, float *loss,
                                       float *loss_reduced, void *grad, int32_t *status_dev,
                                       rnnt_stream_t stream);
+
+/*
+ * rnnt_selftest_wait_timeout -- diagnostic of the bounded device waits (no
+ * counterpart on the pages).  Enqueues one kernel whose warp waits, with the
+ * same helper the loss kernels use for their shared-memory row copies, on a
+ * barrier that nothing completes; after `polls` (>= 1) polls the wait gives
+ * up, and status_dev (device int32) receives RNNT_TIMEOUT, as a loss call's
+ * status would.  Nothing faults, traps or stays in flight; the context stays
+ * usable.  Returns RNNT_INVALID_VALUE (NULL status_dev, polls < 1) or
+ * RNNT_LAUNCH_FAILED.
+ */
+rnnt_status_t rnnt_selftest_wait_timeout(int32_t *status_dev, int32_t polls, rnnt_stream_t stream);
 
 /* Static English description of a status code. */
 const char *rnnt_status_string(rnnt_status_t status);

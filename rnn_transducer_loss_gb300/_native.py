@@ -22,7 +22,8 @@ NOALLOC_SCRATCH_BYTES = 32 << 20     # RNNT_NOALLOC_SCRATCH_BYTES
 # Every symbol include/rnnt_gb300.h declares.
 EXPORTS = ("rnnt_workspace_size", "rnnt_workspace_size_ex", "rnnt_loss_fused", "rnnt_loss_fused_ex",
            "rnnt_loss_fused_staged", "rnnt_grad_scale", "rnnt_set_trace",
-           "rnnt_loss_fused_noalloc", "rnnt_status_string", "rnnt_abi_version")
+           "rnnt_loss_fused_noalloc", "rnnt_selftest_wait_timeout", "rnnt_status_string",
+           "rnnt_abi_version")
 
 
 MAX_BIG_BLANKS = 8                    # RNNT_MAX_BIG_BLANKS
@@ -89,6 +90,8 @@ def load() -> ctypes.CDLL:
     lib.rnnt_loss_fused_noalloc.restype = i32
     lib.rnnt_grad_scale.argtypes = [P, i32, i64, i32, i32, P, sz, P, i32, P]
     lib.rnnt_grad_scale.restype = i32
+    lib.rnnt_selftest_wait_timeout.argtypes = [P, i32, P]
+    lib.rnnt_selftest_wait_timeout.restype = i32
     lib.rnnt_set_trace.argtypes = [P, sz]
     lib.rnnt_set_trace.restype = i32
     lib.rnnt_status_string.argtypes = [i32]
@@ -180,3 +183,8 @@ def rnnt_grad_scale(grad, dt, rows, V, B, workspace, workspace_bytes, factors, p
 
 def rnnt_set_trace(buffer, nbytes) -> int:
     return int(load().rnnt_set_trace(buffer, nbytes))
+
+
+def rnnt_selftest_wait_timeout(status_dev, polls, stream) -> int:
+    """Runs the bounded-wait diagnostic; status_dev receives RNNT_TIMEOUT."""
+    return int(load().rnnt_selftest_wait_timeout(status_dev, int(polls), stream))

@@ -497,8 +497,9 @@ __device__ __forceinline__ void report_timeout(int32_t* err, int site, int arg) 
 }
 // Bounded wait for the copy of phase `parity`; false (error flag raised) on timeout.
 
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
-    for (int i = 0; i < kWaitSpins; ++i)
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err,
+                                          int limit = kWaitSpins) {
+    for (int i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     report_timeout(err, 1, (int)parity);
     return false;
@@ -2971,6 +2972,27 @@ __global__ void __launch_bounds__(256) k_grad_mb(Params p) {
     }
 }
 
+// ---------------------------------------------------------------- self-test
+// The bounded-wait path, exercised without any fault: one warp waits, through
+// the same helper as the row rings, on an mbarrier that nothing ever
+// completes; the wait gives up after `limit` polls, records the timeout in an
+// error word the way every kernel here does, and the kernel reports
+// RNNT_TIMEOUT in status.  Nothing is left in flight.
+__global__ void __launch_bounds__(32) k_selftest_wait(int32_t* status, int limit) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int32_t err[16];
+    const int wl = threadIdx.x;
+    if (wl < 16) err[wl] = 0;
+    if (wl == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    mbar_wait(&bar, 0, err, limit);
+    __syncwarp();
+    if (wl == 0) *status = (err[0] & ERR_TIMEOUT) ? RNNT_TIMEOUT : RNNT_OK;
+}
+
 // ---------------------------------------------------------------- padding
 // Padded layout: zero gradient rows outside every lattice (t >= T_b or
 // u > U_b), one warp per row; rows inside a lattice are left to the gradient
@@ -3546,6 +3568,13 @@ extern "C" rnnt_status_t rnnt_grad_scale(void* grad, rnnt_dtype_t dt, int64_t ro
                                                      per_sample);
         return 0;
     });
+    return cudaGetLastError() == cudaSuccess ? RNNT_OK : RNNT_LAUNCH_FAILED;
+}
+
+extern "C" rnnt_status_t rnnt_selftest_wait_timeout(int32_t* status_dev, int32_t polls,
+                                                    rnnt_stream_t stream) {
+    if (!status_dev || polls < 1) return RNNT_INVALID_VALUE;
+    k_selftest_wait<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(status_dev, polls);
     return cudaGetLastError() == cudaSuccess ? RNNT_OK : RNNT_LAUNCH_FAILED;
 }
 
