@@ -1,0 +1,85 @@
+"""Host-side pieces of bench.py that need no GPU: workload selection (dtype
+override, sub-batch), the config record of each option, and the traffic
+record that is reported only for the kernel source it was measured on."""
+import argparse
+import os
+import sys
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from rnn_transducer_loss_gb300 import workloads as W  # noqa: E402
+
+
+def _args(**kw):
+    a = dict(workload="tiny", dtype=None, samples=0, gpus=1, padded=False, fastemit=0.0,
+             big_blanks="", sigma=0.0)
+    a.update(kw)
+    return argparse.Namespace(**a)
+
+
+def test_dtype_override_keeps_the_values_distribution():
+    base = bench.make_workload(_args(), "cpu")
+    bf = bench.make_workload(_args(dtype="bf16"), "cpu")
+    assert bf.logits.dtype == torch.bfloat16 and bf.cfg.name == "tiny_bf16"
+    # same seeded draws, rounded to the other storage type
+    torch.testing.assert_close(bf.logits.float(), base.logits.to(torch.bfloat16).float())
+    np.testing.assert_array_equal(bf.T, base.T)
+    np.testing.assert_array_equal(bf.targets, base.targets)
+
+
+def test_subset_keeps_the_first_samples():
+    full = bench.make_workload(_args(workload="char_asr"), "cpu")
+    sub = bench.make_workload(_args(workload="char_asr", samples=5), "cpu")
+    assert sub.cfg.B == 5 and sub.rows == int(full.offsets[5])
+    assert torch.equal(sub.logits, full.logits[:sub.rows])
+
+
+def test_config_records_options():
+    wl = bench.make_workload(_args(), "cpu")
+    plain = bench.config_of(wl, _args(), l2="flushed")
+    assert plain["workload"] == "tiny" and plain["l2"] == "flushed"
+    assert "layout" not in plain and "fastemit_lambda" not in plain
+    cfg = bench.config_of(wl, _args(padded=True, fastemit=0.01, big_blanks="2,4", sigma=0.05),
+                          l2="flushed")
+    assert cfg["layout"].startswith("padded (B, max_T, max_U+1, V) = (2, 8, 4, 16)")
+    assert cfg["fastemit_lambda"] == 0.01
+    assert cfg["big_blank_durations"] == [2, 4] and cfg["sigma"] == 0.05
+
+
+def test_padded_layout_of_a_workload():
+    wl = W.make("tiny", "cpu")
+    xp = W.to_padded(wl, fill=float("nan"))
+    assert xp.shape == (2, 8, 4, 16)
+    for b in range(2):
+        T, U = int(wl.T[b]), int(wl.U[b])
+        assert torch.equal(xp[b, :T, :U + 1].reshape(-1, 16), wl.logits[wl.sample_rows(b)])
+        assert torch.isnan(xp[b, T:]).all() and torch.isnan(xp[b, :, U + 1:]).all()
+
+
+def test_traffic_record_matches_only_its_source(tmp_path, monkeypatch):
+    v = bench.recorded_traffic("persistent_main", "bpe_asr")
+    # a record is reported only for the kernel source it was taken on
+    assert v is None or v > 1.9e9
+    assert bench.recorded_traffic("persistent_main", "char_asr") is None
+    stale = tmp_path / "traffic.txt"
+    stale.write_text("source_sha256_16=0000000000000000\nworkload=bpe_asr\n"
+                     "persistent_main.dram_bytes_per_launch=123\n")
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(stale))
+    assert bench.recorded_traffic("persistent_main", "bpe_asr") is None
+    fresh = tmp_path / "fresh.txt"
+    fresh.write_text(f"source_sha256_16={bench.kernel_source_hash()}\nworkload=bpe_asr\n"
+                     "persistent_main.dram_bytes_per_launch=123\n")
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(fresh))
+    assert bench.recorded_traffic("persistent_main", "bpe_asr") == 123.0
+    assert bench.recorded_traffic("no_such_kernel", "bpe_asr") is None
+
+
+def test_peak_is_measured_or_the_stated_fallback():
+    peak, kind = bench.load_peak()
+    assert kind in ("measured", "fallback")
+    assert (peak == bench.FALLBACK_HBM_GBS) == (kind == "fallback")
