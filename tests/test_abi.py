@@ -137,3 +137,29 @@ def test_library_has_no_torch_dependency(lib):
     with open(N.LIB_PATH, "rb") as f:
         blob = f.read()
     assert b"libtorch" not in blob and b"libc10" not in blob
+
+
+def _declared_param_counts():
+    src = open(os.path.join(ROOT, "include", "rnnt_gb300.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(rnnt_[a-z_0-9]+)\s*\(([^)]*)\)\s*;", src):
+        args = m.group(2).strip()
+        out[m.group(1)] = 0 if args in ("", "void") else args.count(",") + 1
+    return out
+
+
+def test_binding_argument_counts_match_the_header(lib):
+    counts = _declared_param_counts()
+    assert set(counts) == set(N.EXPORTS)
+    for name, n in counts.items():
+        assert len(getattr(lib, name).argtypes) == n, name
+
+
+def test_options_struct_layout_matches_the_header():
+    # float, 4 int32, 8 int32 ids, 8 int32 durations, float: 22 four-byte fields
+    assert ctypes.sizeof(N.Options) == 4 * (1 + 4 + 2 * N.MAX_BIG_BLANKS + 1)
+    assert N.Options.sigma.offset == 4 * (1 + 4 + 2 * N.MAX_BIG_BLANKS)
+    hdr = open(os.path.join(ROOT, "include", "rnnt_gb300.h")).read()
+    assert f"#define RNNT_MAX_BIG_BLANKS {N.MAX_BIG_BLANKS}" in hdr
+    assert f"#define RNNT_MAX_BIG_BLANK_DURATION {N.MAX_BIG_BLANK_DURATION}" in hdr
