@@ -91,10 +91,64 @@ def recorded_traffic(kernel: str, workload: str):
     return float(v) if v else None
 
 
-class ClockSampler:
-    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+CLOCK_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+
+def parse_clock_lines(lines):
+    """Samples of `nvidia-smi --query-gpu=timestamp,index,clocks.sm,clocks.max.sm,
+    power.draw,clocks_event_reasons.active,<the four CLOCK_REASONS>` lines
+    (csv, noheader, nounits): [(datetime, sm MHz, max MHz, {active reasons})].
+    Lines that do not parse are skipped."""
+    import datetime as dt
+    out = []
+    for line in lines:
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 10:
+            continue
+        try:
+            sm, smax = float(f[2]), float(f[3])
+        except ValueError:
+            continue
+        ts = None   # a timestamp in another format leaves the sample untimed
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                ts = dt.datetime.strptime(f[0], fmt)
+                break
+            except ValueError:
+                pass
+        out.append((ts, sm, smax, {n for n, v in zip(CLOCK_REASONS, f[6:10])
+                                   if v.lower() == "active"}))
+    return out
+
+
+def summarize_clocks(samples, begin, end):
+    """The clocks line of the bench: samples taken inside [begin, end]; when the
+    timed region is shorter than the sampling period, the three samples
+    nearest to it, and the line says so."""
+    out = {}
+    if any(x[0] is None for x in samples):
+        inside = list(samples)
+        out["note"] = "samples without a readable timestamp: all samples"
+    else:
+        inside = [x for x in samples if begin <= x[0] <= end]
+    if not inside and samples:
+        mid = begin + (end - begin) / 2
+        inside = sorted(samples, key=lambda x: abs((x[0] - mid).total_seconds()))[:3]
+        out["note"] = "no sample inside the timed region; the 3 nearest samples"
+    if not inside:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+    reasons = set().union(*(x[3] for x in inside))
+    out.update({"sm_mhz": statistics.median(x[1] for x in inside),
+                "sm_max_mhz": max(x[2] for x in inside), "reasons": sorted(reasons),
+                "samples": len(inside)})
+    return out
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 20 ms around the timed region;
+    mark() records the region's start and end on the same wall clock."""
+
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -102,6 +156,7 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.window = {}
 
     def start(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -109,10 +164,14 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", str(self.gpu)],
+                 "-lms", "20", "-i", str(self.gpu)],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+
+    def mark(self, which: str):
+        import datetime as dt
+        self.window[which] = dt.datetime.now()
 
     def stop(self):
         if self.proc is None:
@@ -122,25 +181,13 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, reasons = [], [], set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in open(self.path):
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        os.unlink(self.path)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        try:
+            with open(self.path) as f:
+                samples = parse_clock_lines(f)
+            os.unlink(self.path)
+            return summarize_clocks(samples, self.window["begin"], self.window["end"])
+        except Exception as e:   # the clocks line must never stop the bench
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [f"sampler error: {e}"]}
 
 
 def oracle_sample_run(wl, n_samples: int):
@@ -368,12 +415,14 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
+    clocks.mark("begin")
     t0 = time.perf_counter()
     for k in range(args.steps):
         flush_l2()
         step(evs[k], stages=False)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
+    clocks.mark("end")
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
@@ -494,7 +543,7 @@ def run_gpu(args, rank, world, local_rank):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
     ap.add_argument("--workload", default="bpe_asr")

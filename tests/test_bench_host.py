@@ -83,3 +83,35 @@ def test_peak_is_measured_or_the_stated_fallback():
     peak, kind = bench.load_peak()
     assert kind in ("measured", "fallback")
     assert (peak == bench.FALLBACK_HBM_GBS) == (kind == "fallback")
+
+
+def test_clock_lines_parse_and_window_filter():
+    import datetime as dt
+    lines = [
+        "2026/12/02 15:49:01.000, 0, 1200, 2070, 150.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 15:49:01.020, 0, 2070, 2070, 900.5, 0x4, Not Active, Not Active, Not Active, Active",
+        "2026/12/02 15:49:01.040, 0, 2055, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+        "2026/12/02 15:49:01.200, 0, 1100, 2070, 120.0, 0x0, Not Active, Active, Not Active, Not Active",
+    ]
+    samples = bench.parse_clock_lines(lines)
+    assert len(samples) == 4
+    t = lambda ms: dt.datetime(2026, 12, 2, 15, 49, 1, ms * 1000)   # noqa: E731
+    inside = bench.summarize_clocks(samples, t(10), t(50))
+    assert inside["samples"] == 2 and inside["sm_mhz"] == (2070 + 2055) / 2
+    assert inside["reasons"] == ["sw_power_cap"] and "note" not in inside
+    # a window shorter than the sampling period: the nearest samples, said so
+    near = bench.summarize_clocks(samples, t(21), t(23))
+    assert near["samples"] == 3 and "note" in near
+    assert bench.summarize_clocks([], t(0), t(1))["reasons"] == ["no samples"]
+
+
+def test_clock_lines_without_readable_timestamps_use_all_samples():
+    import datetime as dt
+    lines = ["Tue Dec  2 15:49:01 2026, 0, 2070, 2070, 900, 0x0, Not Active, Not Active, "
+             "Not Active, Not Active"] * 3
+    samples = bench.parse_clock_lines(lines)
+    assert len(samples) == 3 and samples[0][0] is None
+    now = dt.datetime.now()
+    out = bench.summarize_clocks(samples, now, now)
+    assert out["samples"] == 3 and out["sm_mhz"] == 2070 and "note" in out
