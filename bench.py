@@ -35,6 +35,7 @@ if ROOT not in sys.path:
 METRIC = "RNN-T loss+grad logit elements/s (fwd+bwd, 1 GB300); % of HBM roofline"
 UNIT = "logit elements/s"
 FALLBACK_HBM_GBS = 6800.0
+REF_BUDGET_S = 120.0    # host time of the reference arm's warm-up and timed steps
 STAGES = ("prepare", "row_pass", "alpha_beta_dp", "combine", "grad_pass", "finalize")
 KERNEL_FILE = os.path.join(ROOT, "rnn_transducer_loss_gb300", "csrc", "rnnt_gb300.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
@@ -233,6 +234,13 @@ def run_reference(args, rank, world):
     wl = W.make(args.workload, "cpu")
     cores = oracle.num_threads()
     n = max(1, min(wl.cfg.B, args.ref_samples or cores))
+    # Bounded: size each step's sample so that the warm-up and timed steps
+    # together take about REF_BUDGET_S of host time (the rate does not depend
+    # on the sample's size).
+    _, t1 = oracle_sample_run(wl, n)
+    per_step = REF_BUDGET_S / max(1, args.steps + args.warmup)
+    if t1 > per_step and n > 1:
+        n = max(1, int(n * per_step / t1))
     for _ in range(args.warmup):
         oracle_sample_run(wl, n)
     times, el = [], 0

@@ -72,3 +72,13 @@ def test_reference_arm_under_torchrun_prints_one_line():
     assert line["n_gpus"] == 2 and line["steps"] == 2 and line["warmup"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["value"] > 0
+
+
+def test_reference_arm_sample_shrinks_to_the_host_budget(monkeypatch, capsys):
+    # With a budget far below one full step, each step times fewer samples.
+    monkeypatch.setattr(bench, "REF_BUDGET_S", 1e-6)
+    bench.main(["--impl", "reference", "--workload", "char_asr", "--steps", "2", "--warmup", "1",
+                "--ref-samples", "8"])
+    line = json.loads([l for l in capsys.readouterr().out.splitlines() if l.startswith("{")][-1])
+    assert line["cpu_baseline"]["sample"].startswith("first 1 of 32 samples")
+    assert line["value"] > 0
