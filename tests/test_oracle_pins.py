@@ -448,3 +448,38 @@ def test_multiblank_rows_sum_to_zero_and_finite_differences():
         lm_ = oracle.rnnt_loss_multiblank(xm, y, T, U, big, blank=blank, sigma=0.1,
                                           reduction="sum", want_grad=False).reduced
         assert (lp_ - lm_) / (2 * eps) == pytest.approx(r.grad[i, k], abs=1e-7)
+
+
+# ---------------------------------------------------------------- degenerate vocabularies
+def test_blank_only_vocabulary_has_zero_loss_and_gradient():
+    # V = 1: the blank is the only output, so p(blank) = 1 at every node, no
+    # label can exist (U = 0), the only alignment has probability 1.
+    x = np.random.default_rng(5).normal(size=(9, 1))
+    r = oracle.rnnt_loss(x, [[0]], [9], [0], blank=0, reduction="sum")
+    assert r.losses[0] == pytest.approx(0.0, abs=1e-15)
+    np.testing.assert_allclose(r.grad, 0.0, atol=1e-15)
+
+
+def test_certain_alignment_has_zero_loss_and_a_sharp_gradient():
+    # Log-probabilities that put probability 1 on one monotone path (labels at
+    # frame 0, then blanks): loss 0, and the non-fused gradient is -1 exactly on
+    # that path's arcs, 0 elsewhere.
+    T, U, V = 4, 2, 4
+    y = [1, 2]
+    lp = np.full((T * (U + 1), V), -np.inf)
+    W = U + 1
+    for t in range(T):
+        for u in range(W):
+            r = t * W + u
+            if t == 0 and u < U:
+                lp[r, y[u]] = 0.0           # emit the labels first
+            elif u == U:
+                lp[r, 0] = 0.0              # then only blanks
+    got = oracle.rnnt_loss(lp, [y], [T], [U], blank=0, reduction="sum",
+                           fused_log_softmax=False)
+    assert got.losses[0] == pytest.approx(0.0, abs=1e-15)
+    want = np.zeros_like(lp)
+    want[0 * W + 0, 1] = want[0 * W + 1, 2] = -1.0
+    for t in range(T):
+        want[t * W + U, 0] = -1.0
+    np.testing.assert_allclose(got.grad, want, atol=1e-15)
