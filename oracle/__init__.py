@@ -207,9 +207,10 @@ def rnnt_loss_padded(logits: np.ndarray, targets, logit_lengths, target_lengths,
 
     Node (t, u) of sample b is ``logits[b, t, u]``; entries with t >= T_b or
     u > U_b belong to no lattice, are never read and get a zero gradient.
-    The lattices are gathered into the compact layout, ``rnnt_loss`` runs on
-    it, and the gradient is scattered back into a zero (B, max_T, max_U+1, V)
-    array.  Keyword arguments are those of ``rnnt_loss``.
+    The lattices are gathered into the compact layout, ``rnnt_loss`` (or,
+    with ``big_blanks``, ``rnnt_loss_multiblank``) runs on it, and the
+    gradient is scattered back into a zero (B, max_T, max_U+1, V) array.
+    Keyword arguments are those of that function.
     """
     x = np.asarray(logits)
     if x.ndim != 4:
@@ -220,7 +221,14 @@ def rnnt_loss_padded(logits: np.ndarray, targets, logit_lengths, target_lengths,
     if T.shape[0] != B or (T > maxT).any() or (U + 1 > maxW).any():
         raise ValueError("lengths do not fit the padded tensor")
     compact = np.concatenate([x[b, :T[b], :U[b] + 1, :].reshape(-1, V) for b in range(B)])
-    res = rnnt_loss(compact, targets, T.astype(np.int32), U.astype(np.int32), **kw)
+    if kw.get("big_blanks") or kw.get("sigma"):
+        big = kw.pop("big_blanks", [])
+        res = rnnt_loss_multiblank(compact, targets, T.astype(np.int32), U.astype(np.int32), big,
+                                   **kw)
+    else:
+        kw.pop("big_blanks", None)
+        kw.pop("sigma", None)
+        res = rnnt_loss(compact, targets, T.astype(np.int32), U.astype(np.int32), **kw)
     if res.grad is not None:
         g = np.zeros((B, maxT, maxW, V))
         r = 0

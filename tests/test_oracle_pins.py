@@ -483,3 +483,25 @@ def test_certain_alignment_has_zero_loss_and_a_sharp_gradient():
     for t in range(T):
         want[t * W + U, 0] = -1.0
     np.testing.assert_allclose(got.grad, want, atol=1e-15)
+
+
+def test_padded_multiblank_matches_its_enumeration():
+    # Padded layout and big blanks together, against the enumerator that
+    # indexes the padded tensor (big blanks folded into the compact pass).
+    rng = np.random.default_rng(960)
+    x, y, T, U, blank = rand_padded(rng, B=2, maxT=6, maxU=2, V=6)
+    big = [(4, 2), (3, 3)]
+    y = (y % 3).astype(np.int32)
+    got = oracle.rnnt_loss_padded(x, y, T, U, blank=-1, reduction="sum", big_blanks=big,
+                                  sigma=0.1)
+    comp = np.concatenate([x[b, :T[b], :U[b] + 1].reshape(-1, 6) for b in range(2)])
+    wl, wr, wg = brute.rnnt_loss_multiblank(comp, y, T, U, big, blank=-1, sigma=0.1,
+                                            reduction="sum")
+    np.testing.assert_allclose(got.losses, wl, rtol=1e-12, atol=1e-12)
+    r = 0
+    for b in range(2):
+        n = int(T[b] * (U[b] + 1))
+        np.testing.assert_allclose(got.grad[b, :T[b], :U[b] + 1].reshape(-1, 6), wg[r:r + n],
+                                   rtol=1e-10, atol=1e-12)
+        assert not got.grad[b, T[b]:].any() and not got.grad[b, :, U[b] + 1:].any()
+        r += n
