@@ -115,6 +115,17 @@ int rnnt_oracle_normalize_blank(int blank, int V)
     return blank < 0 ? blank + V : blank;
 }
 
+/* Labels y[0..U) must be output indices other than blank (warp-transducer
+ * blog 4.4 / 5.2: a target equal to blank, or outside the vocabulary, is an
+ * invalid input).  Returns 0 when every label is valid, -1 otherwise. */
+static int labels_valid(const int32_t *y, int U, int V, int blank)
+{
+    for (int u = 0; u < U; ++u)
+        if (y[u] < 0 || y[u] >= V || y[u] == blank)
+            return -1;
+    return 0;
+}
+
 /* Exclusive prefix sum of T_b*(U_b+1): first row of each sample. off has B+1 entries. */
 void rnnt_oracle_offsets(int B, const int32_t *T, const int32_t *U, int64_t *off)
 {
@@ -140,7 +151,7 @@ int rnnt_oracle_forward(const void *x, int dtype, int V, int T, int U, const int
     if (T < 1 || U < 0 || V < 1)
         return -1;
     blank = rnnt_oracle_normalize_blank(blank, V);
-    if (blank < 0 || blank >= V)
+    if (blank < 0 || blank >= V || labels_valid(y, U, V, blank) != 0)
         return -1;
     const int W = U + 1;
     double *lp = (double *)malloc(sizeof(double) * (size_t)V);
@@ -208,6 +219,8 @@ int rnnt_oracle_grad(const void *x, int dtype, int V, int T, int U, const int32_
     if (T < 1 || U < 0 || V < 1)
         return -1;
     blank = rnnt_oracle_normalize_blank(blank, V);
+    if (blank < 0 || blank >= V || labels_valid(y, U, V, blank) != 0)
+        return -1;
     const int W = U + 1;
     const int64_t rows = (int64_t)T * W;
     if (r0 < 0 || r1 > rows || r0 > r1)
@@ -351,9 +364,15 @@ int rnnt_oracle_mb_sample(const void *x, int dtype, int V, int T, int U, const i
     if (T < 1 || U < 0 || V < 1 || K < 0 || K > 8)
         return -1;
     blank = rnnt_oracle_normalize_blank(blank, V);
-    for (int i = 0; i < K; ++i)
+    if (blank < 0 || blank >= V || labels_valid(y, U, V, blank) != 0)
+        return -1;
+    for (int i = 0; i < K; ++i) {
         if (bb_dur[i] < 2 || bb_id[i] < 0 || bb_id[i] >= V || bb_id[i] == blank)
             return -1;
+        for (int u = 0; u < U; ++u)   /* a big blank is never a label */
+            if (y[u] == bb_id[i])
+                return -1;
+    }
     const int W = U + 1;
     const int64_t n = (int64_t)T * W;
     /* per node: lp'(blank), lp'(label), lp'(big blank i); then alpha, beta */

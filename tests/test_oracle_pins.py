@@ -248,6 +248,40 @@ def test_rejects_bad_arguments():
         oracle.rnnt_loss(h.astype(np.float32), [[0]], [2], [2], blank=2)
 
 
+@pytest.mark.parametrize("bad", [-1, 5, 4, -3])
+def test_rejects_invalid_labels(bad):
+    # A label outside [0, V) or equal to blank is an invalid input (warp-transducer
+    # blog 4.4 / 5.2); the oracle refuses it in every entry point, as the CUDA path
+    # reports RNNT_INVALID_VALUE for it.  V = 5, blank = -1 -> 4; -3 stays invalid
+    # (labels are never counted from the end).
+    V, T, U = 5, 3, 2
+    rng = np.random.default_rng(0)
+    x = rng.normal(size=(T * (U + 1), V)).astype(np.float32)
+    good = [1, 2]
+    fw = oracle.sample_forward(x, T, U, good, -1, True)
+    y = [1, bad]
+    with pytest.raises(ValueError):
+        oracle.sample_forward(x, T, U, y, -1, True)
+    with pytest.raises(ValueError):
+        oracle.sample_grad(x, fw, y, -1, True, -1.0, 1.0)
+    with pytest.raises(ValueError):
+        oracle.rnnt_loss(x, [y], [T], [U], blank=-1)
+    with pytest.raises(ValueError):
+        oracle.rnnt_loss_multiblank(x, [y], [T], [U], [(3, 2)], blank=-1)
+    # Entries past the target length are padding and are never read.
+    r = oracle.rnnt_loss(x, [[1, 2, bad]], [T], [U], blank=-1)
+    assert np.isfinite(r.losses[0])
+
+
+def test_multiblank_rejects_a_label_equal_to_a_big_blank():
+    V, T, U = 6, 4, 2
+    x = np.random.default_rng(1).normal(size=(T * (U + 1), V))
+    with pytest.raises(ValueError):
+        oracle.rnnt_loss_multiblank(x, [[1, 3]], [T], [U], [(3, 2)], blank=-1)
+    r = oracle.rnnt_loss_multiblank(x, [[1, 2]], [T], [U], [(3, 2)], blank=-1)
+    assert np.isfinite(r.losses[0])
+
+
 # ---------------------------------------------------------------- FastEmit
 # The GPURNNT docs and compute_multiblank_grad_kernel take a FastEmit weight
 # lambda; the reading used here: the gradient term of every label-emission
