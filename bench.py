@@ -122,16 +122,24 @@ def parse_clock_lines(lines):
     return out
 
 
-def summarize_clocks(samples, begin, end):
-    """The clocks line of the bench: samples taken inside [begin, end]; when the
-    timed region is shorter than the sampling period, the three samples
-    nearest to it, and the line says so."""
+def summarize_clocks(samples, begin, end, loaded_begin=None):
+    """The clocks line of the bench: samples taken inside [begin, end] (the
+    timed region), or inside [loaded_begin, end] when the timed steps follow a
+    pre-roll of the same steps that keeps the GPU under the same load (a short
+    timed region holds few 20 ms samples); ``samples_timed`` counts the
+    samples inside the timed region itself.  With no sample in the window,
+    the three samples nearest to the timed region, and the line says so."""
     out = {}
+    w0 = loaded_begin if loaded_begin is not None else begin
     if any(x[0] is None for x in samples):
         inside = list(samples)
         out["note"] = "samples without a readable timestamp: all samples"
     else:
-        inside = [x for x in samples if begin <= x[0] <= end]
+        inside = [x for x in samples if w0 <= x[0] <= end]
+        out["samples_timed"] = sum(1 for x in samples if begin <= x[0] <= end)
+        if loaded_begin is not None:
+            out["window_s"] = round((end - w0).total_seconds(), 3)
+            out["window"] = "pre-roll of the same steps, then the timed steps"
     if not inside and samples:
         mid = begin + (end - begin) / 2
         inside = sorted(samples, key=lambda x: abs((x[0] - mid).total_seconds()))[:3]
@@ -186,7 +194,8 @@ class ClockSampler:
             with open(self.path) as f:
                 samples = parse_clock_lines(f)
             os.unlink(self.path)
-            return summarize_clocks(samples, self.window["begin"], self.window["end"])
+            return summarize_clocks(samples, self.window["begin"], self.window["end"],
+                                    self.window.get("loaded"))
         except Exception as e:   # the clocks line must never stop the bench
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [f"sampler error: {e}"]}
 
@@ -209,6 +218,53 @@ def oracle_sample_run(wl, n_samples: int):
     return r1 * wl.cfg.V, dt
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine() or "unknown"
+
+
+def oracle_rate(workload: str, budget_s: float) -> dict:
+    """Oracle loss+grad rate on a whole workload, repeated for about budget_s."""
+    from rnn_transducer_loss_gb300 import workloads as W
+    import oracle
+    wl = W.make(workload, "cpu")
+    el, dt = oracle_sample_run(wl, wl.cfg.B)
+    tot_el, tot_t, reps = el, dt, 1
+    while tot_t + dt < budget_s and reps < 50:
+        e2, t2 = oracle_sample_run(wl, wl.cfg.B)
+        tot_el, tot_t, reps = tot_el + e2, tot_t + t2, reps + 1
+    return {"value": tot_el / tot_t, "unit": UNIT, "cores": oracle.num_threads(),
+            "sample": f"whole {workload} workload ({el} logit elements) x {reps} runs, "
+                      f"{tot_t:.1f} s"}
+
+
+def oracle_one_thread(workload: str = "char_asr", budget_s: float = 3.0):
+    """The oracle on one host thread (OMP_NUM_THREADS=1 in a child process)."""
+    code = ("import json, bench; print(json.dumps(bench.oracle_rate(%r, %r)))"
+            % (workload, budget_s))
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    try:
+        out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env,
+                             capture_output=True, text=True, timeout=300)
+        return json.loads(out.stdout.strip().splitlines()[-1])
+    except Exception as e:   # the baseline must never stop the bench
+        return {"error": f"{type(e).__name__}: {e}"}
+
+
 def cpu_baseline(wl, budget_s: float = 15.0):
     import oracle
     cores = oracle.num_threads()
@@ -221,8 +277,10 @@ def cpu_baseline(wl, budget_s: float = 15.0):
         total_t += t2
         reps += 1
     return {"value": total_el / total_t, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": f"first {n} of {wl.cfg.B} samples ({el} logit elements) x {reps} runs, "
-                      f"float64 loss+grad, OpenMP over samples, {total_t:.1f} s"}
+                      f"float64 loss+grad, OpenMP over samples, {total_t:.1f} s",
+            "one_thread_char_asr": oracle_one_thread("char_asr")}
 
 
 def run_reference(args, rank, world):
@@ -255,6 +313,7 @@ def run_reference(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(wl, args, l2="host run"),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "cpu_model": cpu_model(),
                          "sample": f"first {n} of {wl.cfg.B} samples per step ({el} logit "
                                    f"elements), float64 loss+grad"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -278,6 +337,10 @@ def config_of(wl, args, l2):
         out["big_blank_durations"] = [int(v) for v in args.big_blanks.split(",")]
     if getattr(args, "sigma", 0.0):
         out["sigma"] = args.sigma
+    if getattr(args, "inplace", False):
+        out["inplace"] = True
+    if getattr(args, "logits", "normal") != "normal":
+        out["logits"] = "constant (every logit 0)"
     return out
 
 
@@ -292,11 +355,60 @@ def make_workload(args, device):
     return W.subset(wl, args.samples) if args.samples else wl
 
 
+def algorithmic_bytes(fused: bool, elements: int, rows: int, out_elements: int,
+                      esize: int) -> int:
+    """Bytes the method must move per call.  In-kernel log-softmax: one read
+    of every lattice logit and one write of every gradient element.  Without
+    it only the blank and label log-probabilities of a row are read (2
+    elements per row) and every gradient element is written."""
+    if fused:
+        return elements * esize + out_elements * esize
+    return out_elements * esize + 2 * rows * esize
+
+
+def kernel_roofline(kernel: str, bytes_per_launch: float, kernel_ms: float, step_ms: float,
+                    peak: float, peak_kind: str, traffic):
+    """Roofline record of the dominant kernel; refused (frac None) when its time
+    exceeds the whole step's, which no kernel of the step can do."""
+    rec = {"bound": "hbm", "kernel": kernel, "unit": "GB/s", "peak": peak,
+           "peak_kind": f"{peak_kind} (hbm_gbs, copy bandwidth)",
+           "algorithmic_bytes_per_launch": bytes_per_launch, "kernel_ms": kernel_ms,
+           "traffic": traffic}
+    if not (kernel_ms > 0) or kernel_ms > step_ms * 1.0001:
+        rec.update(achieved=None, frac=None,
+                   note=f"kernel time {kernel_ms:.4f} ms exceeds the step's {step_ms:.4f} ms: "
+                        "not reported")
+        return rec
+    ach = bytes_per_launch / (kernel_ms / 1e3) / 1e9
+    rec.update(achieved=ach, frac=ach / peak)
+    return rec
+
+
+def dp_latency(trace_rec, T, U):
+    """ns per anti-diagonal of the alpha/beta recursions from a task trace:
+    per sample, the recursion task's duration / (T_b + U_b)."""
+    import numpy as np
+    m = trace_rec["kind"] == 1
+    if not m.any():
+        return None
+    b = trace_rec["sample"][m]
+    dur_ns = (trace_rec["end_us"][m] - trace_rec["start_us"][m]) * 1e3
+    per = dur_ns / (T[b].astype(np.float64) + U[b])
+    longest = int(np.argmax(T[b].astype(np.int64) + U[b]))
+    return {"median_ns": float(np.median(per)), "max_ns": float(per.max()),
+            "min_ns": float(per.min()), "samples": int(m.sum()),
+            "longest_lattice": {"T": int(T[b[longest]]), "U": int(U[b[longest]]),
+                                "us": float(dur_ns[longest] / 1e3),
+                                "ns_per_diagonal": float(per[longest])}}
+
+
 def run_gpu(args, rank, world, local_rank):
+    import numpy as np
     import torch
     import torch.distributed as dist
     from rnn_transducer_loss_gb300 import _native as N
     from rnn_transducer_loss_gb300 import build as B
+    from rnn_transducer_loss_gb300 import trace as TR
     from rnn_transducer_loss_gb300 import workloads as W
     from rnn_transducer_loss_gb300.functional import _DT, rnnt_loss_forward
 
@@ -309,6 +421,8 @@ def run_gpu(args, rank, world, local_rank):
 
     wl = make_workload(args, dev)
     cfg = wl.cfg
+    if args.logits == "constant":
+        wl.logits.zero_()   # every alignment equally likely: the widest posterior band
     rows, V = wl.rows, cfg.V
     dt = _DT[wl.logits.dtype]
     esize = wl.logits.element_size()
@@ -329,6 +443,7 @@ def run_gpu(args, rank, world, local_rank):
             raise SystemExit("--big-blanks needs a workload whose blank is the last output")
         wl.targets[:] = wl.targets % (V - 1 - len(big))
     mb_opts = dict(big_blanks=big, sigma=args.sigma) if (big or args.sigma) else {}
+    ex_opts = dict(fastemit_lambda=args.fastemit, padded=padded, **mb_opts)
     use_ex = padded is not None or args.fastemit > 0 or bool(mb_opts)
     targets = torch.as_tensor(wl.targets, device=dev)
     Tl = torch.as_tensor(wl.T, device=dev)
@@ -339,11 +454,19 @@ def run_gpu(args, rank, world, local_rank):
     loss = torch.empty(cfg.B, dtype=torch.float32, device=dev)
     red = torch.empty((), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    grad = torch.empty_like(x_in)
+    # In place: the gradient overwrites the logits; every step first restores
+    # them from a pristine copy (a 1 GB copy, which also evicts L2).
+    pristine = x_in.clone() if args.inplace else None
+    grad = x_in if args.inplace else torch.empty_like(x_in)
+    plan = N.rnnt_plan(cfg.B, in_rows, V, dt, targets.shape[1], cfg.fused, True,
+                       **(ex_opts if use_ex else {}))
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     flush_rd = torch.ones(128 << 20, dtype=torch.float32, device=dev)
 
     def flush_l2():
+        if args.inplace:
+            x_in.copy_(pristine)
+            return
         # Write 512 MiB (evicts everything), then read 512 MiB of another buffer so
         # the dirty flush lines are written back here, outside the timed region.
         flush.zero_()
@@ -367,8 +490,7 @@ def run_gpu(args, rank, world, local_rank):
                 x_in.data_ptr(), dt, in_rows, V, targets.data_ptr(), targets.shape[1],
                 Tl.data_ptr(), Ul.data_ptr(), cfg.B, cfg.blank, cfg.clamp, cfg.fused, red_code,
                 loss.data_ptr(), red.data_ptr(), grad.data_ptr(), ws.data_ptr(), nbytes,
-                status.data_ptr(), stream.cuda_stream, fastemit_lambda=args.fastemit,
-                padded=padded, **mb_opts)
+                status.data_ptr(), stream.cuda_stream, **ex_opts)
             for e in ev[1:]:
                 e.record(stream)
             if rc != N.RNNT_OK:
@@ -376,7 +498,7 @@ def run_gpu(args, rank, world, local_rank):
             return
         handles = [e.cuda_event if (stages or i in (0, 6)) else None for i, e in enumerate(ev)]
         rc = N.rnnt_loss_fused_staged(
-            wl.logits.data_ptr(), dt, rows, V, targets.data_ptr(), targets.shape[1],
+            x_in.data_ptr(), dt, rows, V, targets.data_ptr(), targets.shape[1],
             Tl.data_ptr(), Ul.data_ptr(), cfg.B, cfg.blank, cfg.clamp, cfg.fused, red_code,
             loss.data_ptr(), red.data_ptr(), grad.data_ptr(), ws.data_ptr(), nbytes,
             status.data_ptr(), stream.cuda_stream, handles)
@@ -384,21 +506,22 @@ def run_gpu(args, rank, world, local_rank):
             raise N.RNNTError(rc, "rnnt_loss_fused_staged")
 
     if args.trace:
-        # Task timeline of the persistent kernel (after two warm calls).
-        from rnn_transducer_loss_gb300 import trace as TR
+        # Task timeline of the call (after two warm calls).
         ev = make_events()
         for _ in range(2):
             flush_l2()
             step(ev)
         flush_l2()
         rec = TR.traced(lambda: step(ev))
-        print(json.dumps({"trace": TR.summary(rec)}), flush=True)
+        print(json.dumps({"trace": TR.summary(rec),
+                          "dp_ns_per_diagonal": dp_latency(rec, wl.T, wl.U)}), flush=True)
         return
 
     if args.profile_steps:
         # Profiling mode (for ncu): run the path a fixed number of times, report nothing.
         ev = make_events()
         for _ in range(args.profile_steps):
+            flush_l2()
             step(ev)
         torch.cuda.synchronize()
         if int(status.item()) != N.RNNT_OK:
@@ -408,21 +531,33 @@ def run_gpu(args, rank, world, local_rank):
         return
 
     warm_ev = make_events()
-    for _ in range(max(3, args.warmup)):
+    warmup = max(3, args.warmup)
+    torch.cuda.synchronize()
+    tw = time.perf_counter()
+    for _ in range(warmup):
         flush_l2()
         step(warm_ev)
     torch.cuda.synchronize()
+    per_step_s = (time.perf_counter() - tw) / warmup
     if int(status.item()) != N.RNNT_OK:
         raise N.RNNTError(int(status.item()), "bench warm-up")
 
     evs = [make_events() for _ in range(args.steps)]
     torch.cuda.synchronize()
     clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    # Pre-roll: the same steps for about half a second right before the timed
+    # ones, so that the clock samples (every 20 ms) see the GPU under this load
+    # even when the timed region itself is short.  Not timed.
+    pre = min(20000, max(1, int(0.5 / max(per_step_s, 1e-6))))
+    clocks.mark("loaded")
+    for _ in range(pre):
+        flush_l2()
+        step(warm_ev, stages=False)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
     clocks.mark("begin")
     t0 = time.perf_counter()
     for k in range(args.steps):
@@ -435,53 +570,57 @@ def run_gpu(args, rank, world, local_rank):
         dist.barrier()
     clk = clocks.stop()
     step_ms = [ev[0].elapsed_time(ev[6]) for ev in evs]
-
-    # Stage breakdown from separate (untimed) steps that record every event.
-    bevs = [make_events() for _ in range(max(3, min(args.steps, 5)))]
-    for ev in bevs:
-        flush_l2()
-        step(ev)
-    torch.cuda.synchronize()
-    stage_ms = {s: statistics.mean(ev[i].elapsed_time(ev[i + 1]) for ev in bevs)
-                for i, s in enumerate(STAGES)}
     ms = max_over_ranks(statistics.mean(step_ms), world, dev)
     value = job_throughput(wl.elements, ms, world)
 
     peak, peak_kind = load_peak()
-    # Algorithmic bytes: one read of every lattice element and one write of
-    # every gradient element (padding rows included in the padded layout).
-    step_bytes = wl.elements * esize + x_in.numel() * esize
-    kernel_bytes = {"row_pass": wl.elements * esize if cfg.fused else 2 * rows * esize,
-                    "grad_pass": 2 * wl.elements * esize if cfg.fused
-                    else wl.elements * esize + 2 * rows * esize}
-    persistent = use_ex or sum(stage_ms[s] for s in STAGES[1:]) < 0.03
-    if use_ex:
-        # The whole call (padding zeroing, if any, and the persistent kernel).
-        stage_ms = {"call": statistics.mean(step_ms)}
-        kernel_bytes = {"call": step_bytes}
-        dom = "call"
-    elif persistent:
-        # One cooperative kernel ran everything: the preparation on its CTA 0, every
-        # row, DP and gradient task, and the loss check / reduction on its last CTA.
-        stage_ms = {"persistent_main": stage_ms["prepare"] + stage_ms["row_pass"]}
-        kernel_bytes = {"persistent_main": step_bytes}
-        dom = "persistent_main"
+    step_bytes = algorithmic_bytes(cfg.fused, wl.elements, rows, x_in.numel(), esize)
+    stage_ms = None
+    if use_ex or plan["persistent"]:
+        # The library reports that one kernel runs the whole call (or, for the
+        # options, the call is timed as a whole): its time is the timed steps'.
+        kname = ("persistent_main" if (plan["persistent"] and plan["launches"] == 1)
+                 else "call")
+        roof = kernel_roofline(kname, step_bytes, ms, ms, peak, peak_kind,
+                               recorded_traffic(kname, cfg.name))
     else:
-        dom = max(("row_pass", "alpha_beta_dp", "grad_pass"), key=lambda s: stage_ms[s])
-    if dom == "alpha_beta_dp":
-        roof = {"bound": "latency", "kernel": dom, "achieved": None, "peak": None,
-                "unit": "GB/s", "frac": None, "traffic": None,
-                "note": "the DP is bound by T+U dependent anti-diagonal steps"}
-    else:
-        ach = kernel_bytes[dom] / (stage_ms[dom] / 1e3) / 1e9
-        roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak, "unit": "GB/s",
-                "frac": ach / peak, "peak_kind": f"{peak_kind} (hbm_gbs, copy bandwidth)",
-                "algorithmic_bytes_per_launch": kernel_bytes[dom],
-                "traffic": recorded_traffic(dom, cfg.name)}
+        # Per-stage kernels: the median of 20 untimed steps that record every
+        # stage boundary, and the dominant stage.
+        bevs = [make_events() for _ in range(20)]
+        for ev in bevs:
+            flush_l2()
+            step(ev)
+        torch.cuda.synchronize()
+        stage_ms = {s_: statistics.median(ev[i].elapsed_time(ev[i + 1]) for ev in bevs)
+                    for i, s_ in enumerate(STAGES)}
+        kernel_bytes = {
+            "row_pass": wl.elements * esize if cfg.fused else 2 * rows * esize,
+            "grad_pass": (2 * wl.elements * esize if cfg.fused
+                          else wl.elements * esize + 2 * rows * esize)}
+        dom = max(("row_pass", "alpha_beta_dp", "grad_pass"), key=lambda k: stage_ms[k])
+        if dom == "alpha_beta_dp":
+            roof = {"bound": "latency", "kernel": dom, "achieved": None, "peak": None,
+                    "unit": "GB/s", "frac": None, "traffic": None,
+                    "kernel_ms": stage_ms[dom],
+                    "note": "the DP is bound by T+U dependent anti-diagonal steps"}
+        else:
+            roof = kernel_roofline(dom, kernel_bytes[dom], stage_ms[dom], ms, peak, peak_kind,
+                                   recorded_traffic(dom, cfg.name))
     step_ach = step_bytes / (ms / 1e3) / 1e9
 
+    # Recursion latency per anti-diagonal, from one traced call (not timed).
+    flush_l2()
+    rec = TR.traced(lambda: step(make_events()))
+    dpl = dp_latency(rec, wl.T, wl.U)
+    # Rows the gradient pass had to re-read: those whose gradient is not all zero.
+    if not args.inplace:
+        nz = int((grad.reshape(in_rows, V) != 0).any(dim=1).sum())
+        reread = {"rows_nonzero": nz, "rows": in_rows, "frac": nz / in_rows}
+    else:
+        reread = None
+
     # End to end through the public API: pinned host inputs -> device, loss -> host.
-    h_logits = x_in.cpu().pin_memory()
+    h_logits = (pristine if args.inplace else x_in).cpu().pin_memory()
     h_targets = targets.cpu().pin_memory()
     h_T, h_U = Tl.cpu().pin_memory(), Ul.cpu().pin_memory()
     d_logits = torch.empty_like(x_in)
@@ -496,6 +635,7 @@ def run_gpu(args, rank, world, local_rank):
         d_U.copy_(h_U, non_blocking=True)
         l, r, g, _ = rnnt_loss_forward(d_logits, d_targets, d_T, d_U, cfg.blank, cfg.clamp,
                                        cfg.reduction, cfg.fused, check=False,
+                                       inplace_grad=args.inplace,
                                        fastemit_lambda=args.fastemit, **mb_opts)
         h_loss.copy_(l, non_blocking=True)
         h_red.copy_(r, non_blocking=True)
@@ -517,27 +657,37 @@ def run_gpu(args, rank, world, local_rank):
            + h_T.numel() * 4 + h_U.numel() * 4)
     d2h = h_loss.numel() * 4 + 4
 
+    l2 = ("restored from a pristine copy before each step (1 GB copy, evicts L2)"
+          if args.inplace else
+          "flushed between steps (512 MiB write, then 512 MiB read of another buffer); "
+          "inputs 1 GB > L2")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+        "warmup": warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "storage_dtype": cfg.dtype,
-        "data": f"synthetic (seeded; shapes and value distribution of the {cfg.name} workload)",
-        "config": config_of(wl, args, l2="flushed between steps (512 MiB write, then "
-                                         "512 MiB read of another buffer); inputs 1 GB > L2"),
+        "data": f"synthetic (seeded; shapes and value distribution of the {cfg.name} workload"
+                + (", constant logits" if args.logits == "constant" else "") + ")",
+        "config": config_of(wl, args, l2=l2),
         "roofline": roof,
         "step_roofline": {"bound": "hbm", "achieved": step_ach, "peak": peak, "unit": "GB/s",
-                          "frac": step_ach / peak,
-                          "algorithmic_bytes": step_bytes,
-                          "note": "whole call: one logit read + one grad write per element"},
-        "stages_ms": stage_ms,
+                          "frac": step_ach / peak, "algorithmic_bytes": step_bytes,
+                          "note": ("whole call: one logit read + one grad write per element"
+                                   if cfg.fused else "whole call: one grad write per element "
+                                   "+ the blank and label log-probabilities of each row")},
+        "design_roofline_2r1w": {"frac_ceiling": 2 / 3,
+                                 "note": "if every row were re-read by the gradient pass"},
+        "grad_rows_reread": reread,
+        "dp_ns_per_diagonal": dpl,
+        "plan": plan,
         "e2e": {"value": job_throughput(wl.elements, e2e_t, world), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_t},
-        "gpu_launches": ((5 + (1 if padded else 0)) if mb_opts else
-                         ((2 if padded else 1) if persistent else 6)) * args.steps,
+        "gpu_launches": plan["launches"] * args.steps,
         "clocks": clk,
         "wall_ms_timed_region": wall * 1e3,
         "kernel_source_sha256_16": kernel_source_hash(),
     }
+    if stage_ms is not None:
+        line["stages_ms_median"] = stage_ms
     del h_logits, d_logits
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
@@ -574,6 +724,10 @@ def main(argv=None):
                     help="print the persistent kernel's task timeline and exit")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="run the path N times and exit without timing (for ncu)")
+    ap.add_argument("--inplace", action="store_true",
+                    help="gradient written over the logits (grad == logits)")
+    ap.add_argument("--logits", choices=("normal", "constant"), default="normal",
+                    help="constant: every logit 0 (all alignments equally likely)")
     args = ap.parse_args(argv)
     rank, world, local_rank = dist_info()
     if args.impl == "reference":

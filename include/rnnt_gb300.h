@@ -244,15 +244,43 @@ rnnt_status_t rnnt_grad_scale(void *grad, rnnt_dtype_t dt, int64_t rows, int32_t
                               const float *factors, int32_t per_sample, rnnt_stream_t stream);
 
 /*
- * rnnt_set_trace -- task tracing of the persistent kernel (a debugging aid;
- * process-wide setting, not thread-safe).  While a buffer is set, every
- * rnnt_loss_fused call that runs as one persistent kernel writes, for task t
- * (t < bytes/16), the record int4 {kind | sample << 2, SM id, start ns,
- * end ns} at index t (kind 0: row chunk, 1: DP, 2: gradient chunk);
- * times are relative to the start of the call's first kernel.  Task order:
- * for each sample (longest DP first) its row chunks and its DP task, then
- * every gradient chunk.  device_buffer must be 16-byte aligned device memory
- * that outlives the calls; NULL (or bytes < 16) turns tracing off.
+ * rnnt_plan -- how rnnt_loss_fused / rnnt_loss_fused_ex would run a call of
+ * this shape on the current device, without running it (a planning and
+ * measurement aid; no counterpart on the pages, whose README promises one
+ * kernel launch per call, 价值说明 "Kernel 启动次数").
+ *   B, rows, V, dt, targets_stride, fused_log_softmax   as for the call
+ *   want_grad   nonzero when the call will pass a gradient buffer
+ *   options     as for rnnt_loss_fused_ex, or NULL
+ *   plan        out: persistent = 1 when one cooperative kernel runs the
+ *               whole call (preparation, rows, recursions, gradient, check),
+ *               0 for one kernel per stage; launches = kernels the call
+ *               enqueues.
+ * The call itself takes the per-stage kernels instead if the device
+ * refuses the cooperative launch at that time.  Returns RNNT_INVALID_VALUE
+ * for bad sizes, RNNT_LAUNCH_FAILED when no device is current.
+ */
+typedef struct {
+    int32_t persistent;
+    int32_t launches;
+} rnnt_plan_t;
+
+rnnt_status_t rnnt_plan(int32_t B, int64_t rows, int32_t V, rnnt_dtype_t dt,
+                        int32_t targets_stride, int32_t fused_log_softmax, int32_t want_grad,
+                        const rnnt_options_t *options, rnnt_plan_t *plan);
+
+/*
+ * rnnt_set_trace -- task tracing (a debugging aid; process-wide setting, not
+ * thread-safe).  While a buffer is set, every rnnt_loss_fused call writes
+ * records int4 {kind | sample << 2, SM id, start ns, end ns} (kind 0: row
+ * chunk, 1: alpha/beta recursions of a sample, 2: gradient chunk; times
+ * relative to the start of the call's preparation) at indices below
+ * bytes/16.  A call that runs as one persistent kernel records every task:
+ * for each sample (longest DP first) its row chunks, then every gradient
+ * chunk (record = task index), and sample b's recursions at index
+ * (task count + b).  A call on the per-stage kernels records the recursions
+ * only, sample order[i] at index i.  device_buffer must be 16-byte aligned
+ * device memory that outlives the calls; NULL (or bytes < 16) turns tracing
+ * off.
  */
 rnnt_status_t rnnt_set_trace(void *device_buffer, size_t bytes);
 

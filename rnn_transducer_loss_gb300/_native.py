@@ -23,7 +23,7 @@ NOALLOC_SCRATCH_BYTES = 32 << 20     # RNNT_NOALLOC_SCRATCH_BYTES
 EXPORTS = ("rnnt_workspace_size", "rnnt_workspace_size_ex", "rnnt_loss_fused", "rnnt_loss_fused_ex",
            "rnnt_loss_fused_staged", "rnnt_grad_scale", "rnnt_set_trace",
            "rnnt_loss_fused_noalloc", "rnnt_selftest_wait_timeout", "rnnt_status_string",
-           "rnnt_abi_version")
+           "rnnt_abi_version", "rnnt_plan")
 
 
 MAX_BIG_BLANKS = 8                    # RNNT_MAX_BIG_BLANKS
@@ -53,6 +53,12 @@ def make_options(fastemit_lambda=0.0, padded=None, big_blanks=(), sigma=0.0) -> 
         o.big_blank_ids[i], o.big_blank_durations[i] = int(idx), int(dur)
     o.sigma = float(sigma)
     return o
+
+class Plan(ctypes.Structure):
+    """rnnt_plan_t: whether one persistent kernel runs the call, and how many
+    kernels the call enqueues."""
+    _fields_ = [("persistent", ctypes.c_int32), ("launches", ctypes.c_int32)]
+
 
 _lib = None
 
@@ -98,6 +104,9 @@ def load() -> ctypes.CDLL:
     lib.rnnt_status_string.restype = ctypes.c_char_p
     lib.rnnt_abi_version.argtypes = []
     lib.rnnt_abi_version.restype = i32
+    lib.rnnt_plan.argtypes = [i32, i64, i32, i32, i32, i32, i32, ctypes.POINTER(Options),
+                              ctypes.POINTER(Plan)]
+    lib.rnnt_plan.restype = i32
     _lib = lib
     return lib
 
@@ -188,3 +197,17 @@ def rnnt_set_trace(buffer, nbytes) -> int:
 def rnnt_selftest_wait_timeout(status_dev, polls, stream) -> int:
     """Runs the bounded-wait diagnostic; status_dev receives RNNT_TIMEOUT."""
     return int(load().rnnt_selftest_wait_timeout(status_dev, int(polls), stream))
+
+
+def rnnt_plan(B, rows, V, dt, targets_stride, fused_log_softmax, want_grad=True,
+              **options) -> dict:
+    """{'persistent': bool, 'launches': int} for a call of this shape on the
+    current device (options as make_options)."""
+    plan = Plan()
+    opt = make_options(**options) if options else None
+    rc = load().rnnt_plan(B, rows, V, dt, targets_stride, int(bool(fused_log_softmax)),
+                          int(bool(want_grad)), ctypes.byref(opt) if opt is not None else None,
+                          ctypes.byref(plan))
+    if rc != RNNT_OK:
+        raise RNNTError(rc, "rnnt_plan")
+    return {"persistent": bool(plan.persistent), "launches": int(plan.launches)}

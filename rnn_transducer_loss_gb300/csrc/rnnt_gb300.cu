@@ -537,6 +537,14 @@ __device__ __forceinline__ int smid() {
     return v;
 }
 
+// Trace record of task t: {kind | sample << 2, sm, start, end}, times in ns
+// since k_prepare started (err[4..5] hold that origin).
+__device__ __forceinline__ void trace_task(const Params& p, int t, int code, uint64_t t_start) {
+    if (t >= p.trace_cap) return;
+    const uint64_t origin = *reinterpret_cast<const uint64_t*>(p.err + 4);
+    p.trace[t] = make_int4(code, smid(), (int)(t_start - origin), (int)(global_ns() - origin));
+}
+
 // Log-softmax partials of one row held as NV 16-byte vectors per lane
 // (vector wl + 32 i of the row), for this lane's elements only: m = their
 // maximum and s = sum of 2^(h log2 e - m log2 e) over them (m = -inf, s = 0
@@ -1787,6 +1795,7 @@ __global__ void __launch_bounds__(256) k_dp(Params p) {
     c.W = c.U + 1;
     c.D = c.T + c.U;
     c.off = p.off[c.b];
+    const uint64_t t0 = (p.trace && threadIdx.x == 0) ? global_ns() : 0;
     const int J = dp_jclass(dp_slots(c.W));
     if (J == 1) dp_run<1>(p, c, smem, xch);
     else if (J == 2) dp_run<2>(p, c, smem, xch);
@@ -1794,6 +1803,10 @@ __global__ void __launch_bounds__(256) k_dp(Params p) {
     else if (J == 4) dp_run<4>(p, c, smem, xch);
     else if (J == 6) dp_run<6>(p, c, smem, xch);
     else dp_run<8>(p, c, smem, xch);
+    if (p.trace) {   // record b of the trace: this sample's recursions
+        __syncthreads();
+        if (threadIdx.x == 0) trace_task(p, blockIdx.x, TASK_DP | (c.b << 2), t0);
+    }
 }
 
 // ---------------------------------------------------------------- combine
@@ -2104,16 +2117,6 @@ __device__ __forceinline__ int ld_acquire(const int32_t* a) {
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(a) : "memory");
     return v;
 }
-__device__ __forceinline__ bool wait_at_least(const int32_t* a, int target, int32_t* err) {
-    for (int i = 0; i < kSpinLimit; ++i) {
-        if (ld_acquire(a) >= target) return true;
-        if (ld_acquire(err) & ERR_TIMEOUT) return false;
-        __nanosleep(128);
-    }
-    atomicOr(err, ERR_TIMEOUT);
-    return false;
-}
-
 // Warp: rows [r0, r0+n) (n <= 32) through the warp's TMA stage ring; kk counts
 // the ring's copies so far (stage kk % kStages, phase parity (kk / kStages) & 1).
 // Warp: rows [r0, r0+n) of sample b (T, U, first row o), one row per stage
@@ -2367,14 +2370,6 @@ __device__ __noinline__ void dp_task(const Params& p, int b, int4* smem, float2*
     if (J == 1) dp_run<1>(p, c, smem, xch);
     else if (J == 2) dp_run<2>(p, c, smem, xch);
     else if (threadIdx.x == 0) atomicOr(p.err, ERR_INTERNAL);
-}
-
-// Trace record of task t: {kind | sample << 2, sm, start, end}, times in ns
-// since k_prepare started (err[4..5] hold that origin).
-__device__ __forceinline__ void trace_task(const Params& p, int t, int code, uint64_t t_start) {
-    if (t >= p.trace_cap) return;
-    const uint64_t origin = *reinterpret_cast<const uint64_t*>(p.err + 4);
-    p.trace[t] = make_int4(code, smid(), (int)(t_start - origin), (int)(global_ns() - origin));
 }
 
 // Runs DP(b) on the calling CTA if nobody has claimed it yet (CTA-uniform).
@@ -3225,9 +3220,16 @@ bool coop_supported(int dev) {
 }
 
 // Persistent path: every row, DP and gradient task in one cooperative launch.
-// Returns false (nothing launched) when this shape is not covered.
+// persistent_setup decides whether a call's shape is covered and, if so, the
+// kernel, its shared memory and grid; launch_persistent then launches it.
+struct PersistentCfg {
+    const void* fn;
+    size_t smem;
+    int grid, zero_off, zero_rows, n_dp_sms;
+};
+
 template <typename Tin>
-bool launch_persistent(const Params& p, cudaStream_t st, int sms, int dev) {
+bool persistent_setup(const Params& p, int sms, int dev, PersistentCfg& c) {
     if (!coop_supported(dev)) return false;
     const char* env = getenv("RNNT_GB300_SCHEDULE");
     if (env && env[0] == 'k') return false;   // "kernels": one launch per stage
@@ -3267,14 +3269,30 @@ bool launch_persistent(const Params& p, cudaStream_t st, int sms, int dev) {
     if (sm > 110 * 1024) return false;
     const int occ = occupancy(fn, sm);
     if (occ < 1) return false;
-    Params q = p;
+    c.fn = fn;
+    c.smem = sm;
+    c.grid = occ * sms;
+    c.zero_off = zero_off;
+    c.zero_rows = zero_rows;
     // DP workers: up to 6 SMs (two DP CTAs each); measured on the BPE-ASR
     // workload, 6 beat 8 (the DP SMs idle most of the call) and 4.
-    q.n_dp_sms = std::min(std::min(6, (p.B + 1) / 2), sms / 8);
-    q.zero_off = zero_off;
-    q.zero_rows = zero_rows;
+    c.n_dp_sms = std::min(std::min(6, (p.B + 1) / 2), sms / 8);
+    return true;
+}
+
+// Returns false (nothing launched) when this shape is not covered or the
+// cooperative launch is refused.
+template <typename Tin>
+bool launch_persistent(const Params& p, cudaStream_t st, int sms, int dev) {
+    PersistentCfg c;
+    if (!persistent_setup<Tin>(p, sms, dev, c)) return false;
+    Params q = p;
+    q.n_dp_sms = c.n_dp_sms;
+    q.zero_off = c.zero_off;
+    q.zero_rows = c.zero_rows;
     void* args[] = {&q};
-    if (cudaLaunchCooperativeKernel(fn, dim3(occ * sms), dim3(256), args, sm, st) != cudaSuccess) {
+    if (cudaLaunchCooperativeKernel(c.fn, dim3(c.grid), dim3(256), args, c.smem, st) !=
+        cudaSuccess) {
         cudaGetLastError();   // not launched: the caller runs the staged kernels instead
         return false;
     }
@@ -3571,6 +3589,49 @@ extern "C" rnnt_status_t rnnt_grad_scale(void* grad, rnnt_dtype_t dt, int64_t ro
     return cudaGetLastError() == cudaSuccess ? RNNT_OK : RNNT_LAUNCH_FAILED;
 }
 
+extern "C" rnnt_status_t rnnt_plan(int32_t B, int64_t rows, int32_t V, rnnt_dtype_t dt,
+                                   int32_t targets_stride, int32_t fused_log_softmax,
+                                   int32_t want_grad, const rnnt_options_t* options,
+                                   rnnt_plan_t* plan) {
+    if (!plan || B < 1 || rows < 1 || V < 1 || !valid_dtype(dt)) return RNNT_INVALID_VALUE;
+    if (targets_stride < 1 || targets_stride > RNNT_MAX_TARGET_LENGTH) return RNNT_INVALID_VALUE;
+    const int K = options ? options->num_big_blanks : 0;
+    if (K < 0 || K > RNNT_MAX_BIG_BLANKS) return RNNT_INVALID_VALUE;
+    const bool multiblank = options && (K > 0 || options->sigma > 0.0f);
+    const int pad = (options && options->padded && want_grad) ? 1 : 0;
+    const int g = want_grad ? 1 : 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return RNNT_LAUNCH_FAILED;
+    }
+    plan->persistent = 0;
+    if (multiblank) {   // prepare, rows, recursions, gradient rows, check
+        plan->launches = pad + 4 + g;
+        return RNNT_OK;
+    }
+    if (want_grad) {
+        Params p{};
+        p.B = B;
+        p.V = V;
+        p.S = targets_stride;
+        p.fused = fused_log_softmax ? 1 : 0;
+        const size_t es = dt == RNNT_F32 ? 4 : 2;
+        p.stage_bytes = (int)(((size_t)V * es + 127) / 128 * 128);
+        PersistentCfg c;
+        const bool ok = with_type(dt, [&](auto tag) {
+            return persistent_setup<decltype(tag)>(p, num_sms(dev), dev, c);
+        });
+        if (ok) {
+            plan->persistent = 1;
+            plan->launches = pad + 1;
+            return RNNT_OK;
+        }
+    }
+    plan->launches = pad + 4 + 2 * g;   // prepare, rows, recursions, [records, gradient], check
+    return RNNT_OK;
+}
+
 extern "C" rnnt_status_t rnnt_selftest_wait_timeout(int32_t* status_dev, int32_t polls,
                                                     rnnt_stream_t stream) {
     if (!status_dev || polls < 1) return RNNT_INVALID_VALUE;
@@ -3597,7 +3658,7 @@ extern "C" const char* rnnt_status_string(rnnt_status_t s) {
     return "unknown status";
 }
 
-extern "C" int32_t rnnt_abi_version(void) { return 102; }
+extern "C" int32_t rnnt_abi_version(void) { return 103; }
 
 // ---------------------------------------------------------------- no-alloc entry
 // rnnt_loss_fused_noalloc runs rnnt_loss_fused over a fixed scratch array of

@@ -130,13 +130,20 @@ class _RNNTLossFunction(torch.autograd.Function):
         V = logits.shape[-1]
         ctx.dims = (logits.numel() // V, V, logit_lengths.shape[0], _DT[logits.dtype])
         ctx.grad = grad
+        ctx.used = False
         return loss if reduction == "none" else reduced
 
     @staticmethod
     def backward(ctx, grad_out):
         grad = ctx.grad
+        if ctx.used:
+            # The saved gradient was scaled in place by the first backward.
+            raise RuntimeError("rnnt_loss: backward can run only once per forward call "
+                               "(the gradient buffer is scaled in place); recompute the loss "
+                               "to differentiate again")
         if grad is None:
             return (None,) * 12
+        ctx.used = True
         rows, V, B, dt = ctx.dims
         factors = grad_out.detach().to(torch.float32).contiguous()
         per_sample = 1 if ctx.reduction == "none" else 0

@@ -40,7 +40,7 @@ def test_exports_every_declared_symbol(lib):
 def test_status_strings(lib):
     for code in range(6):
         assert N.status_string(code)
-    assert N.abi_version() == 102
+    assert N.abi_version() == 103
 
 
 def test_workspace_size(lib):
@@ -119,6 +119,16 @@ def test_workspace_size_ex(lib):
     # the multi-blank call wants the larger workspace (rejected before any launch)
     base50 = N.rnnt_workspace_size(2, 50, 16, N.RNNT_F32)
     assert _call_ex(big_blanks=[(3, 2)], workspace_bytes=base50) == N.RNNT_WORKSPACE_TOO_SMALL
+
+
+def test_plan_host_validation(lib):
+    bad = ctypes.c_void_p(None)
+    assert lib.rnnt_plan(2, 50, 16, 0, 3, 1, 1, None, None) == N.RNNT_INVALID_VALUE
+    p = N.Plan()
+    for args in [(0, 50, 16, 0, 3), (2, 0, 16, 0, 3), (2, 50, 0, 0, 3), (2, 50, 16, 9, 3),
+                 (2, 50, 16, 0, 0), (2, 50, 16, 0, 1024)]:
+        assert lib.rnnt_plan(*args, 1, 1, None, ctypes.byref(p)) == N.RNNT_INVALID_VALUE
+    del bad
 
 
 def test_workspace_too_small(lib):

@@ -115,3 +115,43 @@ def test_clock_lines_without_readable_timestamps_use_all_samples():
     now = dt.datetime.now()
     out = bench.summarize_clocks(samples, now, now)
     assert out["samples"] == 3 and out["sm_mhz"] == 2070 and "note" in out
+
+
+def test_roofline_uses_the_kernel_time_and_refuses_a_kernel_longer_than_the_step():
+    r = bench.kernel_roofline("persistent_main", 1.969e9, 0.4, 0.4, 6786.9, "measured", None)
+    assert abs(r["frac"] - 1.969e9 / 0.4e-3 / 1e9 / 6786.9) < 1e-12
+    # One outlier stage sample (2.83 ms against a 0.40 ms step) is refused.
+    r = bench.kernel_roofline("persistent_main", 1.969e9, 2.83, 0.40, 6786.9, "measured", None)
+    assert r["frac"] is None and r["achieved"] is None and "exceeds" in r["note"]
+
+
+def test_algorithmic_bytes_fused_and_not():
+    # fused: one read of every logit + one write of every gradient element
+    assert bench.algorithmic_bytes(True, 1000, 10, 1000, 2) == 4000
+    # not fused: the gradient write + the blank and label gathers of each row
+    assert bench.algorithmic_bytes(False, 811040 * 512, 811040, 811040 * 512, 2) == \
+        811040 * 512 * 2 + 2 * 2 * 811040
+
+
+def test_clock_summary_counts_the_timed_samples_inside_a_loaded_window():
+    import datetime as dt
+    t = dt.datetime(2026, 1, 1)
+    ms = lambda k: t + dt.timedelta(milliseconds=k)   # noqa: E731
+    samples = [(ms(k), 2070.0 - (k == 500), 2070.0, set()) for k in range(0, 700, 20)]
+    out = bench.summarize_clocks(samples, ms(600), ms(640), loaded_begin=ms(100))
+    assert out["samples"] == sum(1 for k in range(0, 700, 20) if 100 <= k <= 640)
+    assert out["samples_timed"] == 3 and out["sm_mhz"] == 2070.0 and out["reasons"] == []
+    out = bench.summarize_clocks(samples, ms(600), ms(640))
+    assert out["samples"] == 3
+
+
+def test_dp_latency_from_a_trace():
+    T = np.array([10, 20], dtype=np.int32)
+    U = np.array([5, 0], dtype=np.int32)
+    rec = {"kind": np.array([0, 1, 1]), "sample": np.array([0, 0, 1]),
+           "sm": np.array([0, 1, 2]), "start_us": np.array([0.0, 1.0, 2.0]),
+           "end_us": np.array([1.0, 4.0, 6.0])}
+    d = bench.dp_latency(rec, T, U)
+    assert d["samples"] == 2
+    assert abs(d["max_ns"] - 3000 / 15) < 1e-9 and abs(d["min_ns"] - 4000 / 20) < 1e-9
+    assert d["longest_lattice"]["T"] == 20

@@ -1,8 +1,8 @@
 """GPU parity: the CUDA path (called through the C ABI) against the float64
-oracle on identical seeded inputs.  Element-wise on every small and medium
-case; at full workload sizes, per-sample losses of all (or sampled) samples,
-sampled gradient rows recomputed by the oracle one by one, and properties that
-hold at any size (zero row sums, alpha/beta agreement via the status word)."""
+oracle on identical seeded inputs.  Element-wise everywhere: every loss and
+every gradient element of the small cases, and of the full-size workloads
+sample by sample in row blocks; plus properties that hold at any size (zero
+row sums, alpha/beta agreement via the status word)."""
 import numpy as np
 import pytest
 import torch
@@ -12,8 +12,8 @@ from rnn_transducer_loss_gb300 import workloads as W
 from rnn_transducer_loss_gb300 import _native as N
 from rnn_transducer_loss_gb300.functional import rnnt_loss, rnnt_loss_forward
 
-from parity_util import (TOL, assert_grad_close, assert_loss_close, gpu_run, oracle_full,
-                         sampled_rows, to_np)
+from parity_util import (TOL, assert_grad_close, assert_loss_close, every_row_compare,
+                         gpu_run, oracle_full, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -44,50 +44,66 @@ def test_char_asr_reductions(red):
     full_compare(W.make("char_asr", "cuda"), reduction=red, clamp=-1.0)
 
 
-def sampled_compare(wl, per_sample, samples=None, seed=0):
-    """Losses of `samples` and sampled gradient rows against the oracle, per sample."""
-    cfg = wl.cfg
-    loss, red, grad = gpu_run(wl)
-    gl = to_np(loss)
-    scale = 1.0 / cfg.B if cfg.reduction == "mean" else 1.0
-    rows = sampled_rows(wl, per_sample, seed)
-    samples = range(cfg.B) if samples is None else samples
-    for b in samples:
-        sl = wl.sample_rows(b)
-        x = to_np(wl.logits[sl])
-        T, U = int(wl.T[b]), int(wl.U[b])
-        fw = oracle.sample_forward(x, T, U, wl.targets[b], cfg.blank, cfg.fused)
-        assert_loss_close([gl[b]], [fw.loss_alpha], cfg.dtype)
-        ids = rows[b]
-        gsel = to_np(grad[sl][torch.as_tensor(ids, device=grad.device)].float())
-        for k, r in enumerate(ids):
-            want = oracle.sample_grad(x, fw, wl.targets[b], cfg.blank, cfg.fused, cfg.clamp,
-                                      scale, int(r), int(r) + 1)
-            assert_grad_close(gsel[k:k + 1], want, cfg.dtype, f"sample {b} row {r}")
-    return loss, red, grad
-
-
-def test_bpe_asr_full_size():
+# Full-size workloads: one call on the whole batch, in the configuration the
+# benchmark times, then every loss and every gradient element against the
+# oracle (sample by sample, in row blocks).
+def test_bpe_asr_every_row():
     wl = W.make("bpe_asr", "cuda")
-    loss, red, grad = sampled_compare(wl, per_sample=48)
+    loss, red, grad, ref = every_row_compare(wl)
     # Row sums of the fused, unclamped gradient vanish at any size.
     s = grad.float().sum(dim=1)
     assert float(s.abs().max()) < 0.05
-    assert abs(float(red) - float(loss.double().sum())) <= 1e-5 * abs(float(red))
 
 
-def test_skewed_full_size():
-    wl = W.make("skewed", "cuda")
-    sampled_compare(wl, per_sample=40)
+def test_skewed_every_row():
+    every_row_compare(W.make("skewed", "cuda"))
 
 
 @pytest.mark.slow
-def test_large_vocab_full_size():
+def test_large_vocab_every_row():
     wl = W.make("large_vocab", "cuda")
-    order = np.argsort(wl.T.astype(np.int64) * (wl.U + 1))
-    loss, red, grad = sampled_compare(wl, per_sample=24, samples=[int(order[0]), int(order[1])])
-    s = grad.sum(dim=1)
-    assert float(s.abs().max()) < 1e-5
+    loss, red, grad, ref = every_row_compare(wl)
+    assert float(grad.sum(dim=1).abs().max()) < 1e-5
+
+
+# The rnnt-loss-ascend README's accuracy table (精度测试: against a float64 CPU
+# reference, reduction "mean"): per row the dtype, batch, T and U ranges and V.
+# Lengths are drawn uniformly from the ranges; in the float32 B=4 row the first
+# sample is set to the range maxima (T=2000, U=500: 2500 anti-diagonals, above
+# the 2048-entry diagonal-base table, and 501 lattice columns), so the
+# recursions' table-free path runs.
+README_ACCURACY = [
+    ("f32", 2, (100, 1000), (100, 300), 50),
+    ("f32", 4, (200, 2000), (50, 500), 128),
+    ("f16", 2, (100, 500), (50, 200), 64),
+    ("f16", 4, (100, 1000), (50, 300), 128),
+]
+
+
+@pytest.mark.parametrize("row", range(len(README_ACCURACY)))
+def test_readme_accuracy_table_shapes(row):
+    dt, B, Tr, Ur, V = README_ACCURACY[row]
+    rng = np.random.default_rng(500 + row)
+    T = rng.integers(Tr[0], Tr[1] + 1, size=B)
+    U = rng.integers(Ur[0], Ur[1] + 1, size=B)
+    if row == 1:
+        T[0], U[0] = Tr[1], Ur[1]
+    wl = W.custom(B, T, U, V, dtype=dt, blank=-1, reduction="mean", seed=60 + row,
+                  device="cuda")
+    every_row_compare(wl)
+
+
+@pytest.mark.parametrize("case", ["persistent", "staged"])
+def test_more_than_2048_anti_diagonals(case):
+    # T+U > 2048 on both schedules: a 101-column lattice in the persistent
+    # kernel (fp16, V=1024) and a 21-column one on the per-stage kernels.
+    if case == "persistent":
+        wl = W.custom(2, [2100, 300], [100, 40], 1024, dtype="f16", sigma=1.5, blank=-1,
+                      reduction="sum", seed=71, device="cuda")
+    else:
+        wl = W.custom(2, [2200, 50], [20, 7], 64, dtype="f32", blank=0, reduction="mean",
+                      seed=72, device="cuda")
+    every_row_compare(wl)
 
 
 # ------------------------------------------------------------------ edge cases
@@ -241,6 +257,19 @@ def test_autograd_backward_scales(red):
     else:
         want *= float(w)
     assert_grad_close(to_np(x.grad), want, "f32")
+
+
+def test_second_backward_raises():
+    # The gradient is scaled in place by backward, so a second backward through
+    # the same forward (retain_graph=True) must fail loudly, not return None.
+    wl = make(2, [9, 5], [3, 2], 16, dtype="f32", blank=-1, reduction="sum")
+    x = wl.logits.clone().requires_grad_(True)
+    out = rnnt_loss(x, torch.as_tensor(wl.targets, device="cuda"),
+                    torch.as_tensor(wl.T, device="cuda"), torch.as_tensor(wl.U, device="cuda"),
+                    blank=-1, reduction="sum")
+    out.backward(retain_graph=True)
+    with pytest.raises(RuntimeError, match="only once"):
+        out.backward()
 
 
 # ------------------------------------------------------------------ schedules

@@ -70,6 +70,21 @@ def test_noalloc_matches_workspace_entry_point_two_calls():
         _compare(g, w, wl.cfg.dtype)
 
 
+@pytest.mark.gpu
+def test_noalloc_persistent_kernel_over_used_scratch():
+    # The first four BPE-ASR samples (about 120k rows) run as the one persistent
+    # kernel, whose task queue and per-sample counters live in the scratch; the
+    # call before it (a per-stage shape) and a repeat of it both leave their
+    # contents behind.
+    bpe = W.subset(W.make("bpe_asr", "cuda"), 4)
+    small = W.custom(B=3, T=[40, 17, 1], U=[12, 0, 5], V=64, dtype="f16", reduction="sum",
+                     seed=11, device="cuda")
+    want = _run(bpe, noalloc=False)
+    _run(small, noalloc=True)
+    for _ in range(2):
+        _compare(_run(bpe, noalloc=True), want, bpe.cfg.dtype)
+
+
 def test_noalloc_rejects_sizes_beyond_scratch():
     limit = N.NOALLOC_SCRATCH_BYTES
     rows = 10_000_000
