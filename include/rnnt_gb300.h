@@ -278,7 +278,8 @@ rnnt_status_t rnnt_plan(int32_t B, int64_t rows, int32_t V, rnnt_dtype_t dt,
  * for each sample (longest DP first) its row chunks, then every gradient
  * chunk (record = task index), and sample b's recursions at index
  * (task count + b).  A call on the per-stage kernels records the recursions
- * only, sample order[i] at index i.  device_buffer must be 16-byte aligned
+ * only: the forward and backward recursion of the i-th sample in DP order at
+ * indices 2i and 2i + 1.  device_buffer must be 16-byte aligned
  * device memory that outlives the calls; NULL (or bytes < 16) turns tracing
  * off.
  */

@@ -110,7 +110,7 @@ __host__ __device__ inline Layout ws_layout(int B, int64_t rows) {
     L.rdone = p;  p = al256(p + sizeof(int32_t) * (size_t)B);
     L.dpdone = p; p = al256(p + sizeof(int32_t) * (size_t)B);
     L.dpclaim = p; p = al256(p + sizeof(int32_t) * (size_t)B);
-    L.tasks = p;  p = al256(p + sizeof(int4) * (size_t)L.max_tasks);
+    L.tasks = p;  p = al256(p + 2 * sizeof(int4) * (size_t)L.max_tasks);
     L.total = p;
     return L;
 }
@@ -176,7 +176,8 @@ struct Params {
     int32_t* dpdone;  // DP finished flag per sample
     int32_t* dpclaim; // DP started (claimed) flag per sample
     int n_dp_sms;     // SMs whose CTAs only run DP tasks
-    int4* tasks;      // {kind | sample << 2, first row in sample, rows, 0}
+    int4* tasks;      // 2 per task: {kind | sample << 2, first row in sample, rows, T},
+                      // {U, 0, first row of the sample (int64, low, high)}
     int4* trace;      // optional per-task trace records (see rnnt_set_trace), or null
     int64_t trace_cap;
 };
@@ -710,7 +711,9 @@ __device__ __forceinline__ int64_t block_scan_excl(int64_t n, int64_t* wsum, int
 // Appends the chunk tasks of `kind` for every sample in DP order (p.order),
 // starting at task index t0, and returns how many it appended; chunks hold
 // kTaskRows rows (the last one of a sample fewer).  The row pass also resets
-// the per-sample scheduler counters.
+// the per-sample scheduler counters.  A task record (32 bytes) holds all a
+// CTA needs to start it: kind, sample, rows, the sample's lengths and first
+// row, so starting a task takes one round of loads.
 // The chunks of one sample are written by one warp, a chunk per lane.
 __device__ int64_t append_chunks(const Params& p, int64_t t0, int kind, int64_t* wsum,
                                  int64_t& carry, int64_t* s_before, int* s_nch) {
@@ -738,11 +741,14 @@ __device__ int64_t append_chunks(const Params& p, int64_t t0, int kind, int64_t*
         for (int j = wid; j < nb; j += nwarps) {
             const int ii = base + j;
             const int b = p.order[ii];
-            const int64_t nrows = (int64_t)p.Tl[b] * (p.Ul[b] + 1);
+            const int T = p.Tl[b], U = p.Ul[b];
+            const int64_t nrows = (int64_t)T * (U + 1);
+            const int64_t o = __ldcg(p.off + b);
             for (int k = lane; k < s_nch[j]; k += 32) {
                 const int r = k * kTaskRows;
-                p.tasks[t0 + s_before[j] + k] =
-                    make_int4(kind | (b << 2), r, (int)min((int64_t)kTaskRows, nrows - r), 0);
+                int4* rec = p.tasks + 2 * (t0 + s_before[j] + k);
+                rec[0] = make_int4(kind | (b << 2), r, (int)min((int64_t)kTaskRows, nrows - r), T);
+                rec[1] = make_int4(U, 0, (int)(uint32_t)o, (int)(o >> 32));
             }
         }
         __syncthreads();
@@ -1196,7 +1202,8 @@ template <> struct Ring<3> { static constexpr int R = 10; };
 template <> struct Ring<4> { static constexpr int R = 10; };
 template <> struct Ring<6> { static constexpr int R = 6; };
 template <> struct Ring<8> { static constexpr int R = 6; };
-constexpr int kDpWarps = 4;   // compute warps per direction, at most
+constexpr int kDpWarps = 4;         // compute warps per direction, at most (both directions on one CTA)
+constexpr int kDpWarpsStaged = 4;   // the same for the per-stage DP (one direction per CTA)
 
 // The DP's ring copies, waits and ring reads are all volatile asm without a
 // "memory" clobber: volatile asm statements keep their relative order (copy,
@@ -1306,11 +1313,11 @@ __device__ __forceinline__ void store_diag(int d, int bd, const Lanes<J>& L, con
 }
 
 // Forward variable: alpha(t,u) = alpha(t-1,u) p_blank(t-1,u) + alpha(t,u-1) p_label(t,u-1).
-// xch: [2][kDpWarps] (m, e) of the label arc leaving each warp's last column.
-template <int J>
+// xch: [2][kDpWarpsStaged] (m, e) of the label arc leaving each warp's last column.
+template <int J, int R = Ring<J>::R>
 __device__ void dp_alpha(const Params& p, const Samp& c, int u0, int w, int nwd, int4* ring,
                          float2* xch) {
-    constexpr int R = Ring<J>::R, PF = R - 2;
+    constexpr int PF = R - 2;
     const int lane = threadIdx.x & 31, nthreads = nwd * 32;
     Lanes<J> L;
     lanes_init<J>(c, u0, lane, p.edge + c.off, p.alpha + c.off, L);
@@ -1358,9 +1365,9 @@ __device__ void dp_alpha(const Params& p, const Samp& c, int u0, int w, int nwd,
         int edge_e = kZeroExp;
         if (nwd > 1) {
             if (lane == 31)
-                sts64(xch + (d & 1) * kDpWarps + w, make_float2(ym[J - 1], __int_as_float(ye[J - 1])));
+                sts64(xch + (d & 1) * kDpWarpsStaged + w, make_float2(ym[J - 1], __int_as_float(ye[J - 1])));
             named_barrier(1, nthreads);
-            const float2 v = lds64(xch + (d & 1) * kDpWarps + max(w - 1, 0));
+            const float2 v = lds64(xch + (d & 1) * kDpWarpsStaged + max(w - 1, 0));
             if (w > 0) {
                 edge_m = v.x;
                 edge_e = __float_as_int(v.y);
@@ -1409,11 +1416,11 @@ __device__ void dp_alpha(const Params& p, const Samp& c, int u0, int w, int nwd,
 
 // Backward variable: beta(t,u) = beta(t+1,u) p_blank(t,u) + beta(t,u+1) p_label(t,u),
 // started from a virtual node after the terminal blank with beta = 1.
-// xch: [2][kDpWarps] (m, e) of each warp's first column on the previous diagonal.
-template <int J>
+// xch: [2][kDpWarpsStaged] (m, e) of each warp's first column on the previous diagonal.
+template <int J, int R = Ring<J>::R>
 __device__ void dp_beta(const Params& p, const Samp& c, int u0, int w, int nwd, int4* ring,
                         float2* xch) {
-    constexpr int R = Ring<J>::R, PF = R - 2;
+    constexpr int PF = R - 2;
     const int lane = threadIdx.x & 31, nthreads = nwd * 32;
     Lanes<J> L;
     lanes_init<J>(c, u0, lane, p.edge + c.off, p.beta + c.off, L);
@@ -1450,9 +1457,9 @@ __device__ void dp_beta(const Params& p, const Samp& c, int u0, int w, int nwd, 
         float edge_m = 0.0f;
         int edge_e = kZeroExp;
         if (nwd > 1) {
-            if (lane == 0) sts64(xch + (d & 1) * kDpWarps + w, make_float2(vm[0], __int_as_float(ve[0])));
+            if (lane == 0) sts64(xch + (d & 1) * kDpWarpsStaged + w, make_float2(vm[0], __int_as_float(ve[0])));
             named_barrier(2, nthreads);
-            const float2 v = lds64(xch + (d & 1) * kDpWarps + min(w + 1, nwd - 1));
+            const float2 v = lds64(xch + (d & 1) * kDpWarpsStaged + min(w + 1, nwd - 1));
             if (w + 1 < nwd) {
                 edge_m = v.x;
                 edge_e = __float_as_int(v.y);
@@ -1525,10 +1532,10 @@ __device__ __forceinline__ void ring_issue_t(int4* slot, int e, int be, const La
 template <int R>
 __device__ __forceinline__ int ring_next(int i) { return i + 1 == R ? 0 : i + 1; }
 
-template <int J>
+template <int J, int R = Ring<J>::R>
 __device__ void dp_alpha_t(const Params& p, const Samp& c, int u0, int w, int nwd, int4* ring,
                            float2* xch, const int* tab) {
-    constexpr int R = Ring<J>::R, PF = R - 2;
+    constexpr int PF = R - 2;
     const int lane = threadIdx.x & 31, nthreads = nwd * 32;
     Lanes<J> L;
     lanes_init<J>(c, u0, lane, p.edge + c.off, p.alpha + c.off, L);
@@ -1634,10 +1641,10 @@ __device__ void dp_alpha_t(const Params& p, const Samp& c, int u0, int w, int nw
     }
 }
 
-template <int J>
+template <int J, int R = Ring<J>::R>
 __device__ void dp_beta_t(const Params& p, const Samp& c, int u0, int w, int nwd, int4* ring,
                           float2* xch, const int* tab) {
-    constexpr int R = Ring<J>::R, PF = R - 2;
+    constexpr int PF = R - 2;
     const int lane = threadIdx.x & 31, nthreads = nwd * 32;
     Lanes<J> L;
     lanes_init<J>(c, u0, lane, p.edge + c.off, p.beta + c.off, L);
@@ -1731,15 +1738,299 @@ __device__ void dp_beta_t(const Params& p, const Samp& c, int u0, int w, int nwd
     }
 }
 
+// ---- One warp per direction (lattices up to 32 * kWarpDpMaxJ columns) ----
+// The same recursions with a single warp per direction: lane l owns the J
+// consecutive columns u = J l + j, so the label arc crosses lanes only at a
+// lane's first column (alpha) or last column (beta): one shuffle pair per
+// anti-diagonal, and no other warp, barrier or shared exchange.  Alone on
+// their SM sub-partition the two warps issue the whole step without
+// contention.  The position of diagonal d in the sample's node arrays is a
+// running sum (no table, any number of diagonals): node (t, u) of diagonal d
+// is at base(d) - u, base(d) = N(d) + d - max(0, d - U), and
+// base(d + 1) = base(d) + min(d, T - 1) + 2 - max(0, d + 1 - U).
+// Transition records of future diagonals are prefetched with zero-filling
+// cp.async into a per-warp ring of R slots (slot layout [j][lane]: reads are
+// bank-conflict free); small J also keeps the next diagonal's records in
+// registers one step ahead.
+// Measured on GB300: faster than several warps per direction for lattices of
+// up to 64 columns (115 vs 146 ns per anti-diagonal on 21-41 columns), slower
+// above (one warp then issues the whole step alone).
+constexpr int kWarpDpMaxJ = 2;
+template <int J> struct WRing {
+    static constexpr int R = J <= 4 ? 16 : J <= 8 ? 8 : 4;   // ring slots (diagonals)
+    static constexpr bool kRegAhead = J <= 4;                 // records one step ahead in registers
+};
+__host__ __device__ inline int wdp_jclass(int W) { return W <= 32 ? 1 : 2; }
+__host__ __device__ inline int wdp_ring_depth(int Jc) { return Jc <= 4 ? 16 : Jc <= 8 ? 8 : 4; }
+// Shared memory of the two direction warps' rings for lattices up to W columns.
+__host__ __device__ inline size_t wdp_smem_bytes(int W) {
+    const int Jc = wdp_jclass(W);
+    return (size_t)2 * wdp_ring_depth(Jc) * Jc * 32 * sizeof(int4);
+}
+
+__device__ __forceinline__ int64_t wbase_next(int64_t b, int d, int T, int U) {
+    return b + min(d, T - 1) + 2 - max(0, d + 1 - U);
+}
+__device__ __forceinline__ int64_t wbase_prev(int64_t b, int d, int T, int U) {
+    return b - min(d - 1, T - 1) - 2 + max(0, d - U);
+}
+// Base of diagonal d from scratch (N(d) by inclusion-exclusion).
+__device__ __forceinline__ int64_t wbase_of(int d, int T, int U) {
+    return diag_start(d, T, U + 1) + d - max(0, d - U);
+}
+
+// Zero-filling copies of diagonal e's records (base be) into a ring slot:
+// lane l copies the records of its columns J l .. J l + J - 1.
+template <int J>
+__device__ __forceinline__ void wring_issue(int4* slot, const int4* es, int64_t be, int e, int lane,
+                                            int T, int U) {
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int u = J * lane + j;
+        const bool ok = u <= U && (unsigned)(e - u) < (unsigned)T;
+        cp16z(slot + j * 32 + lane, ok ? es + (be - u) : es, ok);
+    }
+}
+
+template <int J>
+__device__ __forceinline__ void wring_read(const int4* slot, int lane, int4 (&r)[J]) {
+#pragma unroll
+    for (int j = 0; j < J; ++j) r[j] = lds128(slot + j * 32 + lane);
+}
+
+// Forward variable on one warp: step e (e = 0..D-2) forms alpha on diagonal
+// e + 1 from alpha on diagonal e and the records of diagonal e.
+template <int J>
+__device__ void dp_alpha_w(const Params& p, const Samp& c, int4* ring) {
+    constexpr int R = WRing<J>::R, PF = R - 1;
+    constexpr bool AHEAD = WRing<J>::kRegAhead;
+    const int lane = threadIdx.x & 31;
+    const int T = c.T, U = c.U, D = c.D;
+    const int4* es = p.edge + c.off;
+    int2* out = p.alpha + c.off;
+    float am[J];
+    int ae[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const bool origin = lane == 0 && j == 0;
+        am[j] = origin ? 1.0f : 0.0f;
+        ae[j] = origin ? 0 : kZeroExp;
+    }
+    if (lane == 0) out[0] = make_int2(__float_as_int(1.0f), 0);   // alpha(0,0) = 1
+    // Prefetch diagonals 0 .. PF-1.
+    int64_t bi = 0;   // base of the next diagonal to issue
+    int ei = 0;
+    for (; ei < PF; ++ei) {
+        if (ei < D) wring_issue<J>(ring + (ei % R) * (J * 32), es, bi, ei, lane, T, U);
+        cp_commit();
+        bi = wbase_next(bi, ei, T, U);
+    }
+    int4 rc[J];
+    if (AHEAD) {
+        cp_wait<PF - 1>();
+        wring_read<J>(ring, lane, rc);
+    }
+    int64_t bs = wbase_next(0, 0, T, U);   // base of diagonal e + 1 (stores)
+    auto step = [&](int e, auto norm) {
+        if (ei < D) wring_issue<J>(ring + (ei % R) * (J * 32), es, bi, ei, lane, T, U);
+        cp_commit();
+        bi = wbase_next(bi, ei, T, U);
+        ++ei;
+        int4 rn[J];
+        // Without the register look-ahead the records are read from the ring as
+        // they are used (plain loads after a memory-clobbering wait, so that
+        // the compiler orders them after it but keeps few of them live).
+        const int4* cur = ring + (e % R) * (J * 32) + lane;
+        if (AHEAD) {
+            cp_wait<PF - 1>();   // diagonal e + 1 has landed
+            wring_read<J>(ring + ((e + 1) % R) * (J * 32), lane, rn);
+        } else {
+            cp_wait_mem<PF>();   // diagonal e has landed
+        }
+        auto rec = [&](int j) -> int4 { return AHEAD ? rc[j] : cur[j * 32]; };
+        // Label arc into this lane's first column: the last column of lane - 1.
+        float nm;
+        int ne;
+        {
+            float ym;
+            int ye;
+            const int4 rl = rec(J - 1);
+            xf_mul(am[J - 1], ae[J - 1], __int_as_float(rl.z), rl.w - kEdgeBias, ym, ye);
+            nm = __shfl_up_sync(0xffffffffu, ym, 1);
+            ne = __shfl_up_sync(0xffffffffu, ye, 1);
+            if (lane == 0) {
+                nm = 0.0f;
+                ne = kZeroExp;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            float bm, ym;
+            int be, ye;
+            const int4 r = rec(j);
+            xf_mul(am[j], ae[j], __int_as_float(r.x), r.y - kEdgeBias, bm, be);
+            xf_mul(am[j], ae[j], __int_as_float(r.z), r.w - kEdgeBias, ym, ye);
+            xf_add<decltype(norm)::value>(bm, be, nm, ne, am[j], ae[j]);
+            nm = ym;
+            ne = ye;
+        }
+        const int d = e + 1;
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const int u = J * lane + j;
+            if (u <= U && (unsigned)(d - u) < (unsigned)T)
+                out[bs - u] = make_int2(__float_as_int(am[j]), ae[j]);
+        }
+        bs = wbase_next(bs, d, T, U);
+        if (AHEAD) {
+#pragma unroll
+            for (int j = 0; j < J; ++j) rc[j] = rn[j];
+        }
+    };
+    int e = 0;
+    for (; e + 1 < D - 1; e += 2) {
+        step(e, std::false_type());
+        step(e + 1, std::true_type());
+    }
+    if (e < D - 1) step(e, std::false_type());
+    cp_wait<0>();
+    // P(y|x) = alpha(T-1,U) p_blank(T-1,U): the terminal blank (diagonal D-1).
+    const int jU = U % J;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        if (j == jU && lane == U / J) {
+            const int4 ed = __ldcg(es + node_index(T - 1, U, T, U));
+            float m;
+            int x;
+            xf_mul(am[j], ae[j], __int_as_float(ed.x), ed.y - kEdgeBias, m, x);
+            xf_norm(m, x);
+            p.pm[c.b] = m;
+            p.pe[c.b] = x;
+            const double ll2 = (double)x + log2((double)m);
+            p.lossa[c.b] = -ll2 * kLn2d;
+            p.loss[c.b] = (float)(-ll2 * kLn2d);
+        }
+    }
+}
+
+// Backward variable on one warp: step d (d = D-1..0) forms beta on diagonal d
+// from beta on diagonal d + 1 (a virtual node after the terminal blank holds
+// 1) and the records of diagonal d.
+template <int J>
+__device__ void dp_beta_w(const Params& p, const Samp& c, int4* ring) {
+    constexpr int R = WRing<J>::R, PF = R - 1;
+    constexpr bool AHEAD = WRing<J>::kRegAhead;
+    const int lane = threadIdx.x & 31;
+    const int T = c.T, U = c.U, D = c.D;
+    const int4* es = p.edge + c.off;
+    int2* out = p.beta + c.off;
+    float vm[J];
+    int ve[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const bool last = J * lane + j == U;
+        vm[j] = last ? 1.0f : 0.0f;
+        ve[j] = last ? 0 : kZeroExp;
+    }
+    // Prefetch diagonals D-1 down to D-PF.
+    int64_t bi = wbase_of(D - 1, T, U);   // base of the next diagonal to issue
+    int di = D - 1;
+    int k = 0;
+    for (; k < PF; ++k, --di) {
+        if (di >= 0) wring_issue<J>(ring + (k % R) * (J * 32), es, bi, di, lane, T, U);
+        cp_commit();
+        if (di > 0) bi = wbase_prev(bi, di, T, U);
+    }
+    int4 rc[J];
+    if (AHEAD) {
+        cp_wait<PF - 1>();
+        wring_read<J>(ring, lane, rc);
+    }
+    int64_t bs = wbase_of(D - 1, T, U);   // base of diagonal d (stores)
+    // Step number s = D-1-d uses ring slot s % R.
+    auto step = [&](int s, auto norm) {
+        const int d = D - 1 - s;
+        if (di >= 0) wring_issue<J>(ring + ((s + PF) % R) * (J * 32), es, bi, di, lane, T, U);
+        cp_commit();
+        if (di > 0) bi = wbase_prev(bi, di, T, U);
+        --di;
+        int4 rn[J];
+        const int4* cur = ring + (s % R) * (J * 32) + lane;
+        if (AHEAD) {
+            cp_wait<PF - 1>();   // diagonal d - 1 has landed
+            wring_read<J>(ring + ((s + 1) % R) * (J * 32), lane, rn);
+        } else {
+            cp_wait_mem<PF>();   // diagonal d has landed (records read as used)
+        }
+        auto rec = [&](int j) -> int4 { return AHEAD ? rc[j] : cur[j * 32]; };
+        // Label arc out of this lane's last column: the first column of lane + 1.
+        float nm = __shfl_down_sync(0xffffffffu, vm[0], 1);
+        int ne = __shfl_down_sync(0xffffffffu, ve[0], 1);
+        if (lane == 31) {
+            nm = 0.0f;
+            ne = kZeroExp;
+        }
+#pragma unroll
+        for (int j = J - 1; j >= 0; --j) {
+            float bm, ym;
+            int be, ye;
+            const int4 r = rec(j);
+            xf_mul(vm[j], ve[j], __int_as_float(r.x), r.y - kEdgeBias, bm, be);
+            const float cm = vm[j];
+            const int ce = ve[j];
+            xf_mul(nm, ne, __int_as_float(r.z), r.w - kEdgeBias, ym, ye);
+            xf_add<decltype(norm)::value>(bm, be, ym, ye, vm[j], ve[j]);
+            nm = cm;
+            ne = ce;
+        }
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const int u = J * lane + j;
+            if (u <= U && (unsigned)(d - u) < (unsigned)T)
+                out[bs - u] = make_int2(__float_as_int(vm[j]), ve[j]);
+        }
+        if (d > 0) bs = wbase_prev(bs, d, T, U);
+        if (AHEAD) {
+#pragma unroll
+            for (int j = 0; j < J; ++j) rc[j] = rn[j];
+        }
+    };
+    int s = 0;
+    for (; s + 1 < D; s += 2) {
+        step(s, std::false_type());
+        step(s + 1, std::true_type());
+    }
+    if (s < D) step(s, std::true_type());
+    cp_wait<0>();
+    if (lane == 0) {
+        float m = vm[0];
+        int x = ve[0];
+        xf_norm(m, x);
+        p.lossb[c.b] = -((double)x + log2((double)m)) * kLn2d;
+    }
+}
+
+// The recursion of direction dir (0 alpha, 1 beta) on the calling warp;
+// ring: that direction's ring (wdp_smem_bytes / 2).
+template <int J>
+__device__ __forceinline__ void dp_run_w(const Params& p, const Samp& c, int4* ring, int dir) {
+    if (dir == 0) dp_alpha_w<J>(p, c, ring);
+    else dp_beta_w<J>(p, c, ring);
+}
+__device__ __forceinline__ void dp_dispatch_w(const Params& p, const Samp& c, int4* ring, int dir) {
+    if (wdp_jclass(c.W) == 1) dp_run_w<1>(p, c, ring, dir);
+    else dp_run_w<2>(p, c, ring, dir);
+}
+
 // Target lattice columns per lane before another compute warp is added.
 #ifndef RNNT_DP_SLOTS
 #define RNNT_DP_SLOTS 1
 #endif
-__host__ __device__ inline int dp_warps(int W) {
-    return min(kDpWarps, (W + 32 * RNNT_DP_SLOTS - 1) / (32 * RNNT_DP_SLOTS));
+__host__ __device__ inline int dp_warps(int W, int maxw = kDpWarps) {
+    return min(maxw, (W + 32 * RNNT_DP_SLOTS - 1) / (32 * RNNT_DP_SLOTS));
 }
-__host__ __device__ inline int dp_slots(int W) {
-    const int n = dp_warps(W);
+__host__ __device__ inline int dp_slots(int W, int maxw = kDpWarps) {
+    const int n = dp_warps(W, maxw);
     return (W + 32 * n - 1) / (32 * n);
 }
 __host__ __device__ inline int dp_jclass(int J) {
@@ -1759,35 +2050,85 @@ __host__ __device__ inline size_t dp_smem_bytes(int W) {
     return dp_ring_bytes(W) + (size_t)kTabMax * sizeof(int);
 }
 
-// Called by every thread of the CTA.  xch: 2 * kDpWarps * kXch entries.
-template <int J>
-__device__ __forceinline__ void dp_run(const Params& p, const Samp& c, int4* smem, float2* xch) {
-    int* tab = reinterpret_cast<int*>(reinterpret_cast<char*>(smem) + dp_ring_bytes(c.W));
-    const bool use_tab = c.D <= kTabMax;
-    if (use_tab) {
-        for (int d = threadIdx.x; d < c.D; d += blockDim.x) tab[d] = diag_base(c, d);
-        __syncthreads();
-    }
-    // Direction warps interleave (alpha on even warp ids, beta on odd) so the
-    // two recursions of a sample run on different SM sub-partitions.
-    const int wid = threadIdx.x >> 5;
-    const int dir = wid & 1, w = wid >> 1;
-    const int nwd = dp_warps(c.W);
+// The recursion of direction dir on warps w = 0 .. dp_warps(W)-1 given by the
+// caller (other warps return at once); ring: the first of that direction's
+// rings, xch: its exchange area, tab: the diagonal base table (filled by the
+// caller when T+U <= kTabMax).
+template <int J, int R = Ring<J>::R, int MAXW = kDpWarps>
+__device__ __forceinline__ void dp_run_dir(const Params& p, const Samp& c, int dir, int w,
+                                           int4* ring, float2* xch, const int* tab) {
+    const int nwd = dp_warps(c.W, MAXW);
     if (w >= nwd) return;
-    int4* ring = smem + (size_t)(dir * nwd + w) * Ring<J>::R * J * 32;
-    if (use_tab) {
-        if (dir == 0) dp_alpha_t<J>(p, c, w * 32 * J, w, nwd, ring, xch, tab);
-        else dp_beta_t<J>(p, c, w * 32 * J, w, nwd, ring, xch + kDpWarps * kXch, tab);
+    ring += (size_t)w * R * J * 32;
+    if (c.D <= kTabMax) {
+        if (dir == 0) dp_alpha_t<J, R>(p, c, w * 32 * J, w, nwd, ring, xch, tab);
+        else dp_beta_t<J, R>(p, c, w * 32 * J, w, nwd, ring, xch, tab);
     } else {
-        if (dir == 0) dp_alpha<J>(p, c, w * 32 * J, w, nwd, ring, xch);
-        else dp_beta<J>(p, c, w * 32 * J, w, nwd, ring, xch + 2 * kDpWarps);
+        if (dir == 0) dp_alpha<J, R>(p, c, w * 32 * J, w, nwd, ring, xch);
+        else dp_beta<J, R>(p, c, w * 32 * J, w, nwd, ring, xch);
     }
 }
 
-__global__ void __launch_bounds__(256) k_dp(Params p) {
+__device__ __forceinline__ void dp_fill_tab(const Samp& c, int* tab) {
+    if (c.D <= kTabMax)
+        for (int d = threadIdx.x; d < c.D; d += blockDim.x) tab[d] = diag_base(c, d);
+}
+
+// Both directions of one sample on one CTA of 8 warps (the persistent
+// kernel's DP task): lattices of up to 64 columns on warps 0 (alpha) and 1
+// (beta) one warp each; wider ones alpha on even and beta on odd warp ids, so
+// that the two recursions run on different SM sub-partitions.  Called by
+// every thread of the CTA.  xch: 2 * kDpWarps * kXch entries.
+template <int J>
+__device__ __forceinline__ void dp_run(const Params& p, const Samp& c, int4* smem, float2* xch) {
+    const int wid = threadIdx.x >> 5;
+    if (c.W <= 32 * kWarpDpMaxJ) {
+        if (wid < 2)
+            dp_dispatch_w(p, c, smem + (size_t)wid * (wdp_smem_bytes(c.W) / 2 / sizeof(int4)), wid);
+        return;
+    }
+    int* tab = reinterpret_cast<int*>(reinterpret_cast<char*>(smem) + dp_ring_bytes(c.W));
+    dp_fill_tab(c, tab);
+    __syncthreads();
+    const int dir = wid & 1, w = wid >> 1;
+    int4* ring = smem + (size_t)dir * dp_warps(c.W) * Ring<J>::R * J * 32;
+    dp_run_dir<J>(p, c, dir, w, ring, xch + dir * kDpWarps * kXch, tab);
+}
+
+// Ring depth of the per-stage recursions (one direction per CTA, up to 4
+// warps): at most 96 KB of rings.
+__host__ __device__ constexpr int deep_ring(int J) {
+    return J <= 1 ? 24 : J <= 2 ? 16 : J <= 3 ? 12 : J <= 4 ? 10 : J <= 6 ? 8 : 6;
+}
+__host__ __device__ inline size_t dp_deep_ring_bytes(int W) {
+    const int Jc = dp_jclass(dp_slots(W, kDpWarpsStaged));
+    return (size_t)dp_warps(W, kDpWarpsStaged) * deep_ring(Jc) * Jc * 32 * sizeof(int4);
+}
+
+// Per-stage recursions: one CTA per (sample in DP order, direction =
+// blockIdx.y), so that the alpha and the beta recursion of a sample run on
+// different SMs (each SM's issue slots, not the recursion's dependent chain,
+// bound a step when both directions share one SM).  Lattices of up to 64
+// columns take one warp; wider ones dp_warps(W) warps (measured: 8 warps per
+// direction are slower than 4 on a 301-column lattice, 211 vs 176 ns per
+// anti-diagonal).
+template <int J>
+__device__ __forceinline__ void k_dp_body(const Params& p, const Samp& c, int4* smem, float2* xch) {
+    const int dir = blockIdx.y;
+    if (c.W <= 32 * kWarpDpMaxJ) {
+        if (threadIdx.x < 32) dp_dispatch_w(p, c, smem, dir);
+        return;
+    }
+    int* tab = reinterpret_cast<int*>(reinterpret_cast<char*>(smem) + dp_deep_ring_bytes(c.W));
+    dp_fill_tab(c, tab);
+    __syncthreads();
+    dp_run_dir<J, deep_ring(J), kDpWarpsStaged>(p, c, dir, threadIdx.x >> 5, smem, xch, tab);
+}
+
+__global__ void __launch_bounds__(32 * kDpWarpsStaged) k_dp(Params p) {
     if (*p.err) return;
     extern __shared__ int4 smem[];
-    __shared__ float2 xch[2 * kDpWarps * kXch];
+    __shared__ float2 xch[kDpWarpsStaged * kXch];
     Samp c;
     c.b = p.order[blockIdx.x];
     c.T = p.Tl[c.b];
@@ -1796,16 +2137,17 @@ __global__ void __launch_bounds__(256) k_dp(Params p) {
     c.D = c.T + c.U;
     c.off = p.off[c.b];
     const uint64_t t0 = (p.trace && threadIdx.x == 0) ? global_ns() : 0;
-    const int J = dp_jclass(dp_slots(c.W));
-    if (J == 1) dp_run<1>(p, c, smem, xch);
-    else if (J == 2) dp_run<2>(p, c, smem, xch);
-    else if (J == 3) dp_run<3>(p, c, smem, xch);
-    else if (J == 4) dp_run<4>(p, c, smem, xch);
-    else if (J == 6) dp_run<6>(p, c, smem, xch);
-    else dp_run<8>(p, c, smem, xch);
-    if (p.trace) {   // record b of the trace: this sample's recursions
+    const int J = dp_jclass(dp_slots(c.W, kDpWarpsStaged));
+    if (J == 1) k_dp_body<1>(p, c, smem, xch);
+    else if (J == 2) k_dp_body<2>(p, c, smem, xch);
+    else if (J == 3) k_dp_body<3>(p, c, smem, xch);
+    else if (J == 4) k_dp_body<4>(p, c, smem, xch);
+    else if (J == 6) k_dp_body<6>(p, c, smem, xch);
+    else k_dp_body<8>(p, c, smem, xch);
+    if (p.trace) {   // records 2b, 2b+1 of the trace: this sample's two recursions
         __syncthreads();
-        if (threadIdx.x == 0) trace_task(p, blockIdx.x, TASK_DP | (c.b << 2), t0);
+        if (threadIdx.x == 0)
+            trace_task(p, 2 * blockIdx.x + blockIdx.y, TASK_DP | (c.b << 2), t0);
     }
 }
 
@@ -2117,11 +2459,10 @@ __device__ __forceinline__ int ld_acquire(const int32_t* a) {
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(a) : "memory");
     return v;
 }
-// Warp: rows [r0, r0+n) (n <= 32) through the warp's TMA stage ring; kk counts
-// the ring's copies so far (stage kk % kStages, phase parity (kk / kStages) & 1).
-// Warp: rows [r0, r0+n) of sample b (T, U, first row o), one row per stage
-// of the warp's TMA ring; the lane that owns a row also takes the row's blank
-// and label logits from the staged copy.
+// Warp: rows [r0, r0+n) (n <= 32) of sample b (T, U, first row o), one row
+// per stage of the warp's TMA ring; the lane that owns a row also takes the
+// row's blank and label logits from the staged copy.  kk counts the ring's
+// copies so far (stage kk % ST, phase parity (kk / ST) & 1).
 template <typename Tin, int NV>
 __device__ bool row_batch_tma(const Params& p, int64_t r0, int n, unsigned char* buf,
                               uint64_t* bars, uint32_t& kk, int b, int T, int U, int64_t o) {
@@ -2478,10 +2819,10 @@ __device__ __forceinline__ void main_body(const Params& p) {
         const bool go = s_go;
         __syncthreads();
         if (t >= ntasks || !go) break;
-        const int4 tk = __ldcg(p.tasks + t);
+        const int4 tk = __ldcg(p.tasks + 2 * t), tc = __ldcg(p.tasks + 2 * t + 1);
         const int kind = tk.x & 3, b = tk.x >> 2, n = tk.z;
-        const int64_t o_b = __ldcg(p.off + b);
-        const int W_b = __ldg(p.Ul + b) + 1;
+        const int64_t o_b = (int64_t)(uint32_t)tc.z | ((int64_t)tc.w << 32);
+        const int W_b = tc.x + 1;
         const int64_t r0 = o_b + tk.y;
         const uint64_t t_start = (p.trace && tid == 0) ? global_ns() : 0;
         if (kind == TASK_ROW) {
@@ -2491,9 +2832,8 @@ __device__ __forceinline__ void main_body(const Params& p) {
             const int nw = min(per, n - per * wid);
             if (nw > 0) {
                 if (NV > 0) {
-                    row_batch_tma<Tin, (NV > 0 ? NV : 1)>(p, rw, nw, buf, bars, kk, b,
-                                                          __ldg(p.Tl + b), __ldg(p.Ul + b),
-                                                          __ldcg(p.off + b));
+                    row_batch_tma<Tin, (NV > 0 ? NV : 1)>(p, rw, nw, buf, bars, kk, b, tk.w,
+                                                          tc.x, o_b);
                 } else if (wl < nw) {
                     row_finish<Tin>(p, rw + wl, 0.0f, 1.0f);
                 }
@@ -3059,14 +3399,29 @@ int num_sms(int dev) {
     return g_num_sms[dev];
 }
 
-// k_dp shared memory covering every lattice width up to S+1.
+// DP shared memory of both directions for every lattice width up to S+1
+// (the persistent kernel's DP task: one-warp recursions up to 32 *
+// kWarpDpMaxJ columns, the multi-warp ones above).
 size_t dp_smem_for(int S) {
     size_t best = 0;
     for (int W = 1; W <= S + 1; ++W) {
-        const size_t b = dp_smem_bytes(W);
+        const size_t b = W <= 32 * kWarpDpMaxJ ? wdp_smem_bytes(W) : dp_smem_bytes(W);
         if (b > best) best = b;
     }
     return best;
+}
+// The per-stage DP (one direction per CTA): half the rings, and the table.
+size_t dp_smem_dir_for(int S) {
+    size_t best = 0;
+    for (int W = 1; W <= S + 1; ++W) {
+        const size_t b = W <= 32 * kWarpDpMaxJ ? wdp_smem_bytes(W) / 2
+                                               : dp_deep_ring_bytes(W) + (size_t)kTabMax * sizeof(int);
+        if (b > best) best = b;
+    }
+    return best;
+}
+int dp_threads_for(int S) {
+    return S + 1 <= 32 * kWarpDpMaxJ ? 32 : 32 * dp_warps(S + 1, kDpWarpsStaged);
 }
 
 int grid_for(int64_t work_threads, int sms, int per_sm) {
@@ -3439,7 +3794,7 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
     p.trace = static_cast<int4*>(g_trace);
     p.trace_cap = (int64_t)(g_trace_bytes / sizeof(int4));
 
-    const size_t dp_smem = dp_smem_for(targets_stride);
+    const size_t dp_smem = dp_smem_dir_for(targets_stride);
     if (dev >= 0 && dev < 64 && g_dp_smem_set[dev] < (int)dp_smem) {
         if (cudaFuncSetAttribute(k_dp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dp_smem) !=
             cudaSuccess)
@@ -3503,7 +3858,7 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
         return 0;
     });
     mark(2);
-    k_dp<<<B, 256, dp_smem, st>>>(p);
+    k_dp<<<dim3(B, 2), dp_threads_for(targets_stride), dp_smem, st>>>(p);
     mark(3);
     if (grad) launch_gs(k_combine, rows, sms, st, p);
     mark(4);
