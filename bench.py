@@ -532,13 +532,10 @@ def run_gpu(args, rank, world, local_rank):
 
     warm_ev = make_events()
     warmup = max(3, args.warmup)
-    torch.cuda.synchronize()
-    tw = time.perf_counter()
     for _ in range(warmup):
         flush_l2()
         step(warm_ev)
     torch.cuda.synchronize()
-    per_step_s = (time.perf_counter() - tw) / warmup
     if int(status.item()) != N.RNNT_OK:
         raise N.RNNTError(int(status.item()), "bench warm-up")
 
@@ -550,11 +547,13 @@ def run_gpu(args, rank, world, local_rank):
     # Pre-roll: the same steps for about half a second right before the timed
     # ones, so that the clock samples (every 20 ms) see the GPU under this load
     # even when the timed region itself is short.  Not timed.
-    pre = min(20000, max(1, int(0.5 / max(per_step_s, 1e-6))))
     clocks.mark("loaded")
-    for _ in range(pre):
-        flush_l2()
-        step(warm_ev, stages=False)
+    tp = time.perf_counter()
+    while time.perf_counter() - tp < 0.5:
+        for _ in range(10):
+            flush_l2()
+            step(warm_ev, stages=False)
+        torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()

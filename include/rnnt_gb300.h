@@ -66,7 +66,7 @@ typedef enum { RNNT_RED_NONE = 0, RNNT_RED_SUM = 1, RNNT_RED_MEAN = 2 } rnnt_red
  *   rows  number of logit rows, sum over b of T_b*(U_b+1) (>= 1)
  *   V     vocabulary size including blank (>= 1)
  *   dt    logit element type
- *   bytes out: required size; about 52 bytes per logit row plus O(B).
+ *   bytes out: required size; about 36 bytes per logit row plus O(B).
  * Returns RNNT_INVALID_VALUE for a NULL `bytes` or out-of-range sizes.
  */
 rnnt_status_t rnnt_workspace_size(int32_t B, int64_t rows, int32_t V, rnnt_dtype_t dt,
@@ -209,9 +209,11 @@ rnnt_status_t rnnt_loss_fused_ex(const void *logits, rnnt_dtype_t dt, int64_t ro
  * Same arguments, plus stage_events: NULL, or an array of 7 cudaEvent_t
  * handles (entries may be NULL) that the call records on `stream` at its
  * stage boundaries: [0] start, [1] after offsets/schedule, [2] after the
- * row pass, [3] after the alpha/beta DP, [4] after the per-row gradient
- * coefficients, [5] after the gradient pass, [6] after the loss
- * check/reduction.  The caller creates and owns the events.
+ * row pass, [3] after the alpha/beta DP, [4] = [3] (the per-row gradient
+ * coefficients are formed inside the gradient pass), [5] after the gradient
+ * pass (whose last CTA also runs the loss check/reduction), [6] at the end.
+ * A call that runs as one persistent kernel records [1]..[6] after it.
+ * The caller creates and owns the events.
  */
 rnnt_status_t rnnt_loss_fused_staged(const void *logits, rnnt_dtype_t dt, int64_t rows, int32_t V,
                                      const int32_t *targets, int32_t targets_stride,
@@ -286,7 +288,7 @@ rnnt_status_t rnnt_plan(int32_t B, int64_t rows, int32_t V, rnnt_dtype_t dt,
 rnnt_status_t rnnt_set_trace(void *device_buffer, size_t bytes);
 
 /* Size of the fixed device scratch array rnnt_loss_fused_noalloc uses: 32 MiB,
- * enough for rnnt_workspace_size() up to about 640,000 logit rows. */
+ * enough for rnnt_workspace_size() up to about 900,000 logit rows. */
 #define RNNT_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 
 /*

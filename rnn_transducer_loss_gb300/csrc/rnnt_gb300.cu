@@ -12,19 +12,22 @@
 //               step of the DP's anti-diagonal sweep (README 对角线遍历 α/β)
 //               reads and writes one contiguous run.  With the in-kernel log-softmax off only the two needed
 //               elements of a row are read.
-//   k_dp        one CTA of two warps per sample: warp 0 runs the forward
-//               (alpha) recursion over anti-diagonals d = 0..T+U-1, warp 1
-//               the backward (beta) recursion from the end; a lattice column
+//   k_dp        one CTA per (sample, direction): the forward (alpha)
+//               recursion over anti-diagonals d = 0..T+U-1, or the backward
+//               (beta) one from the end, on up to 4 warps; lattice columns
 //               per lane, the neighbouring column's value by warp shuffle.
-//   k_combine   per row: occupancy and the blank/label arc posteriors from
-//               alpha, beta and P(y|x) (README 核心梯度融合公式).
-//   k_grad      one read + one write of the logits: grad_k = p_k*occ -
+//   k_grad      per row the occupancy and the blank/label arc posteriors from
+//               alpha, beta and P(y|x) (README 核心梯度融合公式), then one
+//               read + one write of the logits: grad_k = p_k*occ -
 //               [k=blank]*post_blank - [k=y]*post_label, clip, reduction
 //               scale, store in the input dtype (may alias the logits).
 //               Rows whose occupancy is too small to change any output value
-//               are written as zeros without reading the logits.
-//   k_finalize  1 CTA: alpha/beta loss cross-check (README 精度保证 "双 loss
-//               互校验"), deterministic reduction, status word.
+//               are written as zeros without reading the logits.  Its last
+//               CTA runs the alpha/beta loss cross-check (README 精度保证
+//               "双 loss 互校验"), the deterministic reduction and the status
+//               word (k_finalize does so for a loss-only call).
+// One persistent cooperative kernel (k_main) runs all of this as tasks when
+// the shape allows; the kernels above are the per-stage schedule.
 //
 // Numerics.  The DP runs in the probability domain on extended-range
 // numbers m * 2^e (m in [1,2) as float, e as int32): a product is one
@@ -76,7 +79,7 @@ enum : int {
 constexpr int kTaskRows = 256;   // rows per row / gradient task of the persistent kernel
 
 struct Layout {
-    size_t err, off, order, lossa, lossb, pm, pe, lse2, edge, alpha, beta, info;
+    size_t err, off, order, lossa, lossb, pm, pe, lse2, edge, alpha, beta;
     size_t rtasks, rdone, dpdone, dpclaim, tasks, total;
     int64_t max_tasks;
 };
@@ -104,7 +107,6 @@ __host__ __device__ inline Layout ws_layout(int B, int64_t rows) {
     L.edge = p;  p = al256(p + sizeof(int4) * R);
     L.alpha = p; p = al256(p + sizeof(int2) * R);
     L.beta = p;  p = al256(p + sizeof(int2) * R);
-    L.info = p;  p = al256(p + sizeof(float4) * R);
     L.max_tasks = max_tasks_for(B, rows);
     L.rtasks = p; p = al256(p + sizeof(int32_t) * (size_t)B);
     L.rdone = p;  p = al256(p + sizeof(int32_t) * (size_t)B);
@@ -169,13 +171,13 @@ struct Params {
     int4* edge;       // per node (node_index order): {p_blank.m, p_blank.e, p_label.m, p_label.e}
     int2* alpha;      // per node (node_index order): {m, e}
     int2* beta;
-    float4* info;     // per row: gradient record (see k_combine)
     // persistent-kernel scheduler (err[1] = next task, err[2] = task count)
     int32_t* rtasks;  // row tasks per sample
     int32_t* rdone;   // finished row tasks per sample
     int32_t* dpdone;  // DP finished flag per sample
     int32_t* dpclaim; // DP started (claimed) flag per sample
     int n_dp_sms;     // SMs whose CTAs only run DP tasks
+    int build_tasks;  // the preparation builds the persistent kernel's task list
     int4* tasks;      // 2 per task: {kind | sample << 2, first row in sample, rows, T},
                       // {U, 0, first row of the sample (int64, low, high)}
     int4* trace;      // optional per-task trace records (see rnnt_set_trace), or null
@@ -857,7 +859,7 @@ __device__ void prepare_block(const Params& p, int64_t* s_before, int* s_nch) {
     // Task queue of the persistent kernel: the row chunks of every sample in DP
     // order, then the gradient chunks in the same order.  DP tasks are taken by
     // ticket (err[3]) in the same sample order.
-    if (errs == 0) {
+    if (errs == 0 && p.build_tasks) {
         const int64_t nrow = append_chunks(p, 0, TASK_ROW, wsum, carry, s_before, s_nch);
         const int64_t ngrad = append_chunks(p, nrow, TASK_GRAD, wsum, carry, s_before, s_nch);
         if (tid == 0) {
@@ -1198,10 +1200,6 @@ __global__ void __launch_bounds__(256) k_row_gather(Params p) {
 template <int J> struct Ring;
 template <> struct Ring<1> { static constexpr int R = 16; };
 template <> struct Ring<2> { static constexpr int R = 12; };
-template <> struct Ring<3> { static constexpr int R = 10; };
-template <> struct Ring<4> { static constexpr int R = 10; };
-template <> struct Ring<6> { static constexpr int R = 6; };
-template <> struct Ring<8> { static constexpr int R = 6; };
 constexpr int kDpWarps = 4;         // compute warps per direction, at most (both directions on one CTA)
 constexpr int kDpWarpsStaged = 4;   // the same for the per-stage DP (one direction per CTA)
 
@@ -2213,83 +2211,119 @@ __device__ __forceinline__ float4 combine_row(const Params& p, int64_t r, int b)
                        __int_as_float(y));
 }
 
-__global__ void __launch_bounds__(256) k_combine(Params p) {
-    if (*p.err) return;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    int b = (r < nodes(p)) ? find_sample(p.off, p.B, r) : 0;
-    for (; r < nodes(p); r += stride) {
-        b = advance_sample(p.off, p.B, b, r);
-        p.info[r] = combine_row(p, r, b);
+// The gradient record of row r for a lane that walks increasing rows (b: the
+// lane's current sample, -1 before its first row); a zero-row record for
+// lanes without a row.
+__device__ __forceinline__ float4 row_record(const Params& p, int64_t r, bool valid, int& b) {
+    if (!valid) return make_float4(-INFINITY, 0.0f, 0.0f, __int_as_float(-1));
+    b = b < 0 ? find_sample(p.off, p.B, r) : advance_sample(p.off, p.B, b, r);
+    return combine_row(p, r, b);
+}
+
+__device__ void finalize_block(const Params& p);
+
+// End of the last kernel of a per-stage call: every CTA publishes its writes
+// and counts itself out; the last one runs the loss check and reduction
+// (finalize_block, 256 threads), so no separate launch is needed.
+__device__ __forceinline__ void finalize_if_last(const Params& p) {
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&p.err[8], 1) == (int)gridDim.x - 1;
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        finalize_block(p);
     }
 }
 
 // ---------------------------------------------------------------- grad pass
 // grad_k * scale = 2^(h_k log2 e + log2(c scale) - lse2) - [k=blank] post_blank
 // scale - [k=y] post_label scale, clipped to +-clamp*scale (clip-then-scale).
+// Each warp takes batches of 32 consecutive rows: every lane forms one row's
+// record (occupancy, arc posteriors: combine_row), then groups of G lanes write
+// the rows, taking each row's record from its lane by shuffle.  The last CTA
+// finishes the call (loss check, reduction).
 template <typename Tin, int G, bool VEC, bool FUSED>
 __global__ void __launch_bounds__(256) k_grad(Params p) {
-    if (*p.err) return;
-    using E = Elt<Tin>;
-    constexpr int EPV = E::kPerVec;
-    const Tin* X = static_cast<const Tin*>(p.logits);
-    Tin* Y = static_cast<Tin*>(p.grad);
-    const int V = p.V;
-    const int lane = threadIdx.x & (G - 1);
-    const int64_t ng = (int64_t)gridDim.x * (blockDim.x / G);
-    const float cl = p.clamp * p.scale;
-    const bool clip = p.clamp < INFINITY;
-    const int vb = p.blank / EPV, eb_i = p.blank % EPV;
-    for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G; r < nodes(p); r += ng) {
-        const float4 in = p.info[r];
-        const bool zero = in.x == -INFINITY;
-        const float w2 = in.x, eb = in.y, ey = in.z;
-        const int y = __float_as_int(in.w);
-        const int64_t lr = lrow(p, r);
-        const Tin* row = X + lr * (int64_t)V;
-        Tin* out = Y + lr * (int64_t)V;
-        if (VEC) {
-            const int nvec = V / EPV;
-            const int vy = y >= 0 ? y / EPV : -1, ey_i = y >= 0 ? y % EPV : 0;
-            const uint4* rv = reinterpret_cast<const uint4*>(row);
-            uint4* ov = reinterpret_cast<uint4*>(out);
-            for (int vi = lane; vi < nvec; vi += G) {
-                float g[EPV];
-                if (FUSED && !zero) {
-                    float x[EPV];
-                    E::unpack(__ldcs(rv + vi), x);
+    if (*p.err == 0) {
+        using E = Elt<Tin>;
+        constexpr int EPV = E::kPerVec, NG = 32 / G;
+        constexpr unsigned F = 0xffffffffu;
+        const Tin* X = static_cast<const Tin*>(p.logits);
+        Tin* Y = static_cast<Tin*>(p.grad);
+        const int V = p.V;
+        const int wl = threadIdx.x & 31, lane = wl & (G - 1), grp = wl / G;
+        const float cl = p.clamp * p.scale;
+        const bool clip = p.clamp < INFINITY;
+        const int vb = p.blank / EPV, eb_i = p.blank % EPV;
+        const int64_t nr = nodes(p), nbatch = (nr + 31) / 32;
+        const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
+        int bs = -1;   // this lane's sample
+        for (int64_t bt = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32; bt < nbatch;
+             bt += nwarps) {
+            const int64_t r0 = bt * 32;
+            const int n = (int)min((int64_t)32, nr - r0);
+            const float4 rec = row_record(p, r0 + wl, wl < n, bs);
+            const int64_t lr_mine = wl < n ? (p.padded ? lrow_s(p, r0 + wl, bs, __ldcg(p.off + bs),
+                                                               __ldg(p.Ul + bs) + 1)
+                                                       : r0 + wl)
+                                           : 0;
+            for (int it = 0; it * NG < n; ++it) {
+                const int ri = it * NG + grp;
+                const float w2 = __shfl_sync(F, rec.x, ri), eb = __shfl_sync(F, rec.y, ri);
+                const float ey = __shfl_sync(F, rec.z, ri);
+                const int y = __shfl_sync(F, __float_as_int(rec.w), ri);
+                const int64_t lr = __shfl_sync(F, lr_mine, ri);
+                if (ri >= n) continue;
+                const bool zero = w2 == -INFINITY;
+                const Tin* row = X + lr * (int64_t)V;
+                Tin* out = Y + lr * (int64_t)V;
+                if (VEC) {
+                    const int nvec = V / EPV;
+                    const int vy = y >= 0 ? y / EPV : -1, ey_i = y >= 0 ? y % EPV : 0;
+                    const uint4* rv = reinterpret_cast<const uint4*>(row);
+                    uint4* ov = reinterpret_cast<uint4*>(out);
+                    for (int vi = lane; vi < nvec; vi += G) {
+                        float g[EPV];
+                        if (FUSED && !zero) {
+                            float x[EPV];
+                            E::unpack(__ldcs(rv + vi), x);
 #pragma unroll
-                    for (int e = 0; e < EPV; ++e) g[e] = ex2(fmaf(x[e], kLog2e, w2));
+                            for (int e = 0; e < EPV; ++e) g[e] = ex2(fmaf(x[e], kLog2e, w2));
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < EPV; ++e) g[e] = 0.0f;
+                        }
+                        if (vi == vb) {
+#pragma unroll
+                            for (int e = 0; e < EPV; ++e)
+                                if (e == eb_i) g[e] -= eb;
+                        }
+                        if (vi == vy) {
+#pragma unroll
+                            for (int e = 0; e < EPV; ++e)
+                                if (e == ey_i) g[e] -= ey;
+                        }
+                        if (clip) {
+#pragma unroll
+                            for (int e = 0; e < EPV; ++e) g[e] = fminf(fmaxf(g[e], -cl), cl);
+                        }
+                        __stcs(ov + vi, E::pack(g));
+                    }
                 } else {
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) g[e] = 0.0f;
+                    for (int k = lane; k < V; k += G) {
+                        float gv = (FUSED && !zero) ? ex2(fmaf(E::to_f(row[k]), kLog2e, w2)) : 0.0f;
+                        if (k == p.blank) gv -= eb;
+                        if (k == y) gv -= ey;
+                        if (clip) gv = fminf(fmaxf(gv, -cl), cl);
+                        out[k] = E::from_f(gv);
+                    }
                 }
-                if (vi == vb) {
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e)
-                        if (e == eb_i) g[e] -= eb;
-                }
-                if (vi == vy) {
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e)
-                        if (e == ey_i) g[e] -= ey;
-                }
-                if (clip) {
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) g[e] = fminf(fmaxf(g[e], -cl), cl);
-                }
-                __stcs(ov + vi, E::pack(g));
-            }
-        } else {
-            for (int k = lane; k < V; k += G) {
-                float gv = (FUSED && !zero) ? ex2(fmaf(E::to_f(row[k]), kLog2e, w2)) : 0.0f;
-                if (k == p.blank) gv -= eb;
-                if (k == y) gv -= ey;
-                if (clip) gv = fminf(fmaxf(gv, -cl), cl);
-                out[k] = E::from_f(gv);
             }
         }
     }
+    finalize_if_last(p);
 }
 
 // Gradient pass with TMA staging (16-byte aligned rows of <= 32*NV vectors).
@@ -2299,7 +2333,10 @@ __global__ void __launch_bounds__(256) k_grad(Params p) {
 // fetched into the warp's stage ring, up to kStages rows ahead.
 template <typename Tin, int NV>
 __global__ void __launch_bounds__(256) k_grad_tma(Params p) {
-    if (*p.err) return;
+    if (*p.err) {
+        finalize_if_last(p);
+        return;
+    }
     using E = Elt<Tin>;
     constexpr int EPV = E::kPerVec;
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -2324,10 +2361,11 @@ __global__ void __launch_bounds__(256) k_grad_tma(Params p) {
     seq.init(nodes(p), (int64_t)blockIdx.x * nw + wid, (int64_t)gridDim.x * nw);
     const int64_t nb = (seq.count + 31) / 32;   // batches of this warp
 
+    int bs = -1;   // this lane's sample (its rows increase along the sequence)
     auto load_info = [&](int64_t j) -> float4 {
         const int64_t k = j * 32 + wl;
-        return (j < nb && k < seq.count) ? p.info[seq.row(k)]
-                                         : make_float4(-INFINITY, 0.f, 0.f, __int_as_float(-1));
+        const bool valid = j < nb && k < seq.count;
+        return row_record(p, valid ? seq.row(k) : 0, valid, bs);
     };
     float4 cur = load_info(0), nxt = load_info(1);
     // Rows still to be fetched, as bit masks over the current and the next batch.
@@ -2440,6 +2478,7 @@ __global__ void __launch_bounds__(256) k_grad_tma(Params p) {
     if (!ok)
         for (int64_t k = consumed; k < issued; ++k)
             mbar_wait(&bars[k % kStages], (uint32_t)((k / kStages) & 1), p.err);
+    finalize_if_last(p);
 }
 
 // ---------------------------------------------------------------- persistent kernel
@@ -3496,6 +3535,7 @@ void launch_rows(const Params& p, cudaStream_t st, int sms) {
         launch_gs(k_row_gather<Tin>, p.rows, sms, st, p);
         return;
     }
+
     constexpr int EPV = Elt<Tin>::kPerVec;
     const bool vec = ((size_t)V * sizeof(Tin)) % 16 == 0;
     const int nvec = V / EPV;
@@ -3531,6 +3571,7 @@ void launch_rows(const Params& p, cudaStream_t st, int sms) {
 template <typename Tin>
 void launch_grad(const Params& p, cudaStream_t st, int sms) {
     const int V = p.V;
+
     const bool vec = ((size_t)V * sizeof(Tin)) % 16 == 0;
     const int nvec = V / Elt<Tin>::kPerVec;
     if (p.fused && vec && nvec > 32 && nvec <= 32 * 8) {
@@ -3643,6 +3684,7 @@ bool launch_persistent(const Params& p, cudaStream_t st, int sms, int dev) {
     if (!persistent_setup<Tin>(p, sms, dev, c)) return false;
     Params q = p;
     q.n_dp_sms = c.n_dp_sms;
+    q.build_tasks = 1;
     q.zero_off = c.zero_off;
     q.zero_rows = c.zero_rows;
     void* args[] = {&q};
@@ -3736,7 +3778,7 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
     char* w = static_cast<char*>(workspace);
-    Params p;
+    Params p{};
     p.logits = logits;
     p.grad = grad;
     p.rows = rows;
@@ -3785,7 +3827,6 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
     p.edge = reinterpret_cast<int4*>(w + L.edge);
     p.alpha = reinterpret_cast<int2*>(w + L.alpha);
     p.beta = reinterpret_cast<int2*>(w + L.beta);
-    p.info = reinterpret_cast<float4*>(w + L.info);
     p.rtasks = reinterpret_cast<int32_t*>(w + L.rtasks);
     p.rdone = reinterpret_cast<int32_t*>(w + L.rdone);
     p.dpdone = reinterpret_cast<int32_t*>(w + L.dpdone);
@@ -3860,16 +3901,18 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
     mark(2);
     k_dp<<<dim3(B, 2), dp_threads_for(targets_stride), dp_smem, st>>>(p);
     mark(3);
-    if (grad) launch_gs(k_combine, rows, sms, st, p);
-    mark(4);
+    mark(4);   // the gradient records are formed inside the gradient kernel
     if (grad) {
+        // The gradient kernel's last CTA also runs the loss check / reduction.
         with_type(dt, [&](auto tag) {
             launch_grad<decltype(tag)>(p, st, sms);
             return 0;
         });
+        mark(5);
+    } else {
+        mark(5);
+        k_finalize<<<1, 256, 0, st>>>(p);
     }
-    mark(5);
-    k_finalize<<<1, 256, 0, st>>>(p);
     mark(6);
     return cudaGetLastError() == cudaSuccess ? RNNT_OK : RNNT_LAUNCH_FAILED;
 }
@@ -3983,7 +4026,7 @@ extern "C" rnnt_status_t rnnt_plan(int32_t B, int64_t rows, int32_t V, rnnt_dtyp
             return RNNT_OK;
         }
     }
-    plan->launches = pad + 4 + 2 * g;   // prepare, rows, recursions, [records, gradient], check
+    plan->launches = pad + 4;   // prepare, rows, recursions, gradient (or loss check)
     return RNNT_OK;
 }
 
