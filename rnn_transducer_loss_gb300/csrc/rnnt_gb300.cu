@@ -2260,15 +2260,23 @@ __global__ void __launch_bounds__(256) k_grad(Params p) {
         const int64_t nr = nodes(p), nbatch = (nr + 31) / 32;
         const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
         int bs = -1;   // this lane's sample
-        for (int64_t bt = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32; bt < nbatch;
-             bt += nwarps) {
+        // The records of a batch are formed one batch ahead of its rows.
+        auto batch_rec = [&](int64_t bt, int64_t& lr) -> float4 {
+            const int64_t r = bt * 32 + wl;
+            const bool valid = bt < nbatch && r < nr;
+            const float4 rec = row_record(p, r, valid, bs);
+            lr = !valid ? 0 : p.padded ? lrow_s(p, r, bs, __ldcg(p.off + bs), __ldg(p.Ul + bs) + 1) : r;
+            return rec;
+        };
+        int64_t bt = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+        int64_t lr_next = 0;
+        float4 rec_next = batch_rec(bt, lr_next);
+        for (; bt < nbatch; bt += nwarps) {
             const int64_t r0 = bt * 32;
             const int n = (int)min((int64_t)32, nr - r0);
-            const float4 rec = row_record(p, r0 + wl, wl < n, bs);
-            const int64_t lr_mine = wl < n ? (p.padded ? lrow_s(p, r0 + wl, bs, __ldcg(p.off + bs),
-                                                               __ldg(p.Ul + bs) + 1)
-                                                       : r0 + wl)
-                                           : 0;
+            const float4 rec = rec_next;
+            const int64_t lr_mine = lr_next;
+            rec_next = batch_rec(bt + nwarps, lr_next);
             for (int it = 0; it * NG < n; ++it) {
                 const int ri = it * NG + grp;
                 const float w2 = __shfl_sync(F, rec.x, ri), eb = __shfl_sync(F, rec.y, ri);
@@ -2312,12 +2320,26 @@ __global__ void __launch_bounds__(256) k_grad(Params p) {
                         __stcs(ov + vi, E::pack(g));
                     }
                 } else {
-                    for (int k = lane; k < V; k += G) {
-                        float gv = (FUSED && !zero) ? ex2(fmaf(E::to_f(row[k]), kLog2e, w2)) : 0.0f;
-                        if (k == p.blank) gv -= eb;
-                        if (k == y) gv -= ey;
-                        if (clip) gv = fminf(fmaxf(gv, -cl), cl);
-                        out[k] = E::from_f(gv);
+                    // Rows that are not 16-byte vectors: elements k = lane + G q, the
+                    // loads of eight of them issued together.
+                    constexpr int KQ = 8;
+                    for (int k0 = lane; k0 < V; k0 += G * KQ) {
+                        float x[KQ];
+#pragma unroll
+                        for (int q = 0; q < KQ; ++q) {
+                            const int k = k0 + G * q;
+                            x[q] = (FUSED && !zero && k < V) ? E::to_f(row[k]) : 0.0f;
+                        }
+#pragma unroll
+                        for (int q = 0; q < KQ; ++q) {
+                            const int k = k0 + G * q;
+                            if (k >= V) break;
+                            float gv = (FUSED && !zero) ? ex2(fmaf(x[q], kLog2e, w2)) : 0.0f;
+                            if (k == p.blank) gv -= eb;
+                            if (k == y) gv -= ey;
+                            if (clip) gv = fminf(fmaxf(gv, -cl), cl);
+                            out[k] = E::from_f(gv);
+                        }
                     }
                 }
             }
