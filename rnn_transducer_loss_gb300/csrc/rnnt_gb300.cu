@@ -2348,12 +2348,93 @@ __global__ void __launch_bounds__(256) k_grad(Params p) {
     finalize_if_last(p);
 }
 
+// Gradient rows of the multi-blank loss.  A warp takes 32 consecutive rows:
+// each lane first forms one row's record (occupancy and every arc's
+// posterior, all its loads issued together), then the warp writes the rows
+// one by one, p_k * occ (fused) minus the posteriors at their outputs,
+// clipped and scaled; FastEmit scales the label arc.  Rows whose every
+// element rounds to zero are written without reading the logits.
+struct MbRec {
+    float w2, eb, ey;
+    int y;
+    int64_t lr;   // logits / gradient row
+    bool zero;
+    float ebb[RNNT_MAX_BIG_BLANKS];
+};
+
+__device__ __forceinline__ MbRec mb_record(const Params& p, int64_t r, int b) {
+    MbRec q;
+    const float c = p.bb_c;
+    const int T = __ldg(p.Tl + b), U = __ldg(p.Ul + b), W = U + 1;
+    const int64_t o = __ldcg(p.off + b);
+    const unsigned rr = (unsigned)(r - o);
+    const int t = (int)(rr / (unsigned)W), u = (int)(rr - (unsigned)t * W);
+    const int64_t nd = o + node_index(t, u, T, U);
+    const int2 A = __ldcg(p.alpha + nd), Bt = __ldcg(p.beta + nd);
+    const int4 Ed = __ldcg(p.edge + nd);
+    const int2 Bb = (t + 1 < T) ? __ldcg(p.beta + o + node_index(t + 1, u, T, U)) : make_int2(0, 0);
+    const int2 By = (u < U) ? __ldcg(p.beta + o + node_index(t, u + 1, T, U)) : make_int2(0, 0);
+    int2 Qb[RNNT_MAX_BIG_BLANKS], Bq[RNNT_MAX_BIG_BLANKS];
+#pragma unroll
+    for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) {
+        Qb[i] = make_int2(0, 0);
+        Bq[i] = make_int2(0, 0);
+        if (i < p.K) {
+            const int t1 = t + p.bb_dur[i];
+            Qb[i] = __ldcg(p.pbb + (int64_t)i * p.rows + nd);
+            if (t1 < T) Bq[i] = __ldcg(p.beta + o + node_index(t1, u, T, U));
+        }
+    }
+    const float Pm = __ldcg(p.pm + b);
+    const int Pe = __ldcg(p.pe + b);
+    const float am = __int_as_float(A.x), bm = __int_as_float(Bt.x), inv = 1.0f / Pm;
+    q.y = (u < U) ? __ldg(p.targets + (int64_t)b * p.S + u) : -1;
+    float lc = -INFINITY;
+    if (am != 0.0f && bm != 0.0f) lc = (float)(A.y + Bt.y - Pe) + lg2(am * bm * inv);
+    // posterior of an arc with probability (qm, qe) into a node of beta (nm, ne)
+    auto post = [&](float qm, int qe, float nm, int ne) -> float {
+        if (am == 0.0f || qm == 0.0f || nm == 0.0f) return 0.0f;
+        return xf_to_float(am * qm * c * nm * inv, A.y + qe + ne - Pe);
+    };
+    q.eb = 0.0f;
+    q.ey = 0.0f;
+    if (t + 1 < T) q.eb = post(__int_as_float(Ed.x), Ed.y - kEdgeBias, __int_as_float(Bb.x), Bb.y);
+    else if (u == U) q.eb = post(__int_as_float(Ed.x), Ed.y - kEdgeBias, 1.0f, 0);
+    if (u < U) {
+        q.ey = post(__int_as_float(Ed.z), Ed.w - kEdgeBias, __int_as_float(By.x), By.y);
+        if (p.fe > 0.0f && q.ey != 0.0f && bm != 0.0f) {
+            // FastEmit: occupancy occ (1 + fe post_label / occ)
+            const float ratio = xf_to_float(__int_as_float(Ed.z) * c * __int_as_float(By.x) / bm,
+                                            (Ed.w - kEdgeBias) + By.y - Bt.y);
+            lc += lg2(fmaf(p.fe, ratio, 1.0f));
+            q.ey *= 1.0f + p.fe;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) {
+        q.ebb[i] = 0.0f;
+        if (i >= p.K) continue;
+        const int t1 = t + p.bb_dur[i];
+        const float qm = __int_as_float(Qb[i].x);
+        const int qe = Qb[i].y - kEdgeBias;
+        if (t1 == T && u == U) q.ebb[i] = post(qm, qe, 1.0f, 0);
+        else if (t1 < T) q.ebb[i] = post(qm, qe, __int_as_float(Bq[i].x), Bq[i].y);
+    }
+    q.zero = !(lc + p.fe_l2 >= p.skip2);
+    q.w2 = q.zero ? -INFINITY : lc + p.lscale - __ldcg(p.lse2 + r);
+    q.lr = lrow_s(p, r, b, o, W);
+    return q;
+}
+
 // Gradient pass with TMA staging (16-byte aligned rows of <= 32*NV vectors).
 // Each warp walks its 32-row batches; the per-row records of a batch are
 // loaded one per lane (the next batch's one batch ahead), rows of exact zeros
 // are stored without reading the logits, and only the remaining rows are
-// fetched into the warp's stage ring, up to kStages rows ahead.
-template <typename Tin, int NV>
+// fetched into the warp's stage ring, up to kStages rows ahead.  MB: the
+// multi-blank loss (records from mb_record, and every big blank's arc
+// posterior subtracted at its output; the vectors holding a big-blank output
+// are known per lane up front, so the common vector pays one bit test).
+template <typename Tin, int NV, bool MB = false>
 __global__ void __launch_bounds__(256) k_grad_tma(Params p) {
     if (*p.err) {
         finalize_if_last(p);
@@ -2384,12 +2465,30 @@ __global__ void __launch_bounds__(256) k_grad_tma(Params p) {
     const int64_t nb = (seq.count + 31) / 32;   // batches of this warp
 
     int bs = -1;   // this lane's sample (its rows increase along the sequence)
-    auto load_info = [&](int64_t j) -> float4 {
+    // MB: per lane, the vectors (bit v: vector wl + 32 v) holding a big blank's output.
+    uint32_t bbmask = 0;
+    if (MB)
+        for (int i = 0; i < p.K; ++i) {
+            const int vi = p.bb_id[i] / EPV;
+            if ((vi & 31) == wl) bbmask |= 1u << (vi >> 5);
+        }
+    float ebb_cur[RNNT_MAX_BIG_BLANKS], ebb_nxt[RNNT_MAX_BIG_BLANKS];
+    auto load_info = [&](int64_t j, float (&ebb)[RNNT_MAX_BIG_BLANKS]) -> float4 {
         const int64_t k = j * 32 + wl;
         const bool valid = j < nb && k < seq.count;
-        return row_record(p, valid ? seq.row(k) : 0, valid, bs);
+        if (!MB) return row_record(p, valid ? seq.row(k) : 0, valid, bs);
+#pragma unroll
+        for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) ebb[i] = 0.0f;
+        if (!valid) return make_float4(-INFINITY, 0.f, 0.f, __int_as_float(-1));
+        const int64_t r = seq.row(k);
+        bs = bs < 0 ? find_sample(p.off, p.B, r) : advance_sample(p.off, p.B, bs, r);
+        const MbRec q = mb_record(p, r, bs);
+        const float sc = q.zero ? 0.0f : p.scale;   // a zero row stays exactly zero
+#pragma unroll
+        for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) ebb[i] = q.ebb[i] * sc;
+        return make_float4(q.w2, q.eb * sc, q.ey * sc, __int_as_float(q.y));
     };
-    float4 cur = load_info(0), nxt = load_info(1);
+    float4 cur = load_info(0, ebb_cur), nxt = load_info(1, ebb_nxt);
     // Rows still to be fetched, as bit masks over the current and the next batch.
     uint32_t pend_cur = __ballot_sync(0xffffffffu, cur.x != -INFINITY);
     uint32_t pend_nxt = 0;
@@ -2435,6 +2534,12 @@ __global__ void __launch_bounds__(256) k_grad_tma(Params p) {
             const float ey = __shfl_sync(0xffffffffu, cur.z, it);
             const int y = __shfl_sync(0xffffffffu, __float_as_int(cur.w), it);
             const int vy = y >= 0 ? y / EPV : -1, ey_i = y >= 0 ? y % EPV : 0;
+            float ebb[RNNT_MAX_BIG_BLANKS];
+            if (MB) {
+#pragma unroll
+                for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i)
+                    ebb[i] = i < p.K ? __shfl_sync(0xffffffffu, ebb_cur[i], it) : 0.0f;
+            }
             uint4* ov = reinterpret_cast<uint4*>(Y + lrow(p, r) * (int64_t)V);
             const bool zero = w2 == -INFINITY;
             const uint4* rv = nullptr;
@@ -2471,6 +2576,16 @@ __global__ void __launch_bounds__(256) k_grad_tma(Params p) {
                     for (int e = 0; e < EPV; ++e)
                         if (e == ey_i) g[e] -= ey;
                 }
+                if (MB && ((bbmask >> i) & 1u) && !zero) {
+#pragma unroll
+                    for (int q = 0; q < RNNT_MAX_BIG_BLANKS; ++q) {
+                        if (q >= p.K) break;
+                        const int k = p.bb_id[q] - vi * EPV;
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e)
+                            if (e == k) g[e] -= ebb[q];
+                    }
+                }
                 if (clip) {
 #pragma unroll
                     for (int e = 0; e < EPV; ++e) g[e] = fminf(fmaxf(g[e], -cl), cl);
@@ -2485,11 +2600,15 @@ __global__ void __launch_bounds__(256) k_grad_tma(Params p) {
         }
         // Advance to the next batch: its record is already loaded; fetch the one after.
         cur = nxt;
+        if (MB) {
+#pragma unroll
+            for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) ebb_cur[i] = ebb_nxt[i];
+        }
         if (!nxt_known) pend_nxt = __ballot_sync(0xffffffffu, cur.x != -INFINITY);
         pend_cur = pend_nxt;
         pend_nxt = 0;
         nxt_known = false;
-        nxt = load_info(j + 2);
+        nxt = load_info(j + 2, ebb_nxt);
         if (j + 1 < nb) {
             ++j;
             issue_more();
@@ -3206,84 +3325,6 @@ __global__ void __launch_bounds__(1024) k_dp_mb(Params p) {
     }
 }
 
-// Gradient rows of the multi-blank loss.  A warp takes 32 consecutive rows:
-// each lane first forms one row's record (occupancy and every arc's
-// posterior, all its loads issued together), then the warp writes the rows
-// one by one, p_k * occ (fused) minus the posteriors at their outputs,
-// clipped and scaled; FastEmit scales the label arc.  Rows whose every
-// element rounds to zero are written without reading the logits.
-struct MbRec {
-    float w2, eb, ey;
-    int y;
-    int64_t lr;   // logits / gradient row
-    bool zero;
-    float ebb[RNNT_MAX_BIG_BLANKS];
-};
-
-__device__ __forceinline__ MbRec mb_record(const Params& p, int64_t r, int b) {
-    MbRec q;
-    const float c = p.bb_c;
-    const int T = __ldg(p.Tl + b), U = __ldg(p.Ul + b), W = U + 1;
-    const int64_t o = __ldcg(p.off + b);
-    const unsigned rr = (unsigned)(r - o);
-    const int t = (int)(rr / (unsigned)W), u = (int)(rr - (unsigned)t * W);
-    const int64_t nd = o + node_index(t, u, T, U);
-    const int2 A = __ldcg(p.alpha + nd), Bt = __ldcg(p.beta + nd);
-    const int4 Ed = __ldcg(p.edge + nd);
-    const int2 Bb = (t + 1 < T) ? __ldcg(p.beta + o + node_index(t + 1, u, T, U)) : make_int2(0, 0);
-    const int2 By = (u < U) ? __ldcg(p.beta + o + node_index(t, u + 1, T, U)) : make_int2(0, 0);
-    int2 Qb[RNNT_MAX_BIG_BLANKS], Bq[RNNT_MAX_BIG_BLANKS];
-#pragma unroll
-    for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) {
-        Qb[i] = make_int2(0, 0);
-        Bq[i] = make_int2(0, 0);
-        if (i < p.K) {
-            const int t1 = t + p.bb_dur[i];
-            Qb[i] = __ldcg(p.pbb + (int64_t)i * p.rows + nd);
-            if (t1 < T) Bq[i] = __ldcg(p.beta + o + node_index(t1, u, T, U));
-        }
-    }
-    const float Pm = __ldcg(p.pm + b);
-    const int Pe = __ldcg(p.pe + b);
-    const float am = __int_as_float(A.x), bm = __int_as_float(Bt.x), inv = 1.0f / Pm;
-    q.y = (u < U) ? __ldg(p.targets + (int64_t)b * p.S + u) : -1;
-    float lc = -INFINITY;
-    if (am != 0.0f && bm != 0.0f) lc = (float)(A.y + Bt.y - Pe) + lg2(am * bm * inv);
-    // posterior of an arc with probability (qm, qe) into a node of beta (nm, ne)
-    auto post = [&](float qm, int qe, float nm, int ne) -> float {
-        if (am == 0.0f || qm == 0.0f || nm == 0.0f) return 0.0f;
-        return xf_to_float(am * qm * c * nm * inv, A.y + qe + ne - Pe);
-    };
-    q.eb = 0.0f;
-    q.ey = 0.0f;
-    if (t + 1 < T) q.eb = post(__int_as_float(Ed.x), Ed.y - kEdgeBias, __int_as_float(Bb.x), Bb.y);
-    else if (u == U) q.eb = post(__int_as_float(Ed.x), Ed.y - kEdgeBias, 1.0f, 0);
-    if (u < U) {
-        q.ey = post(__int_as_float(Ed.z), Ed.w - kEdgeBias, __int_as_float(By.x), By.y);
-        if (p.fe > 0.0f && q.ey != 0.0f && bm != 0.0f) {
-            // FastEmit: occupancy occ (1 + fe post_label / occ)
-            const float ratio = xf_to_float(__int_as_float(Ed.z) * c * __int_as_float(By.x) / bm,
-                                            (Ed.w - kEdgeBias) + By.y - Bt.y);
-            lc += lg2(fmaf(p.fe, ratio, 1.0f));
-            q.ey *= 1.0f + p.fe;
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) {
-        q.ebb[i] = 0.0f;
-        if (i >= p.K) continue;
-        const int t1 = t + p.bb_dur[i];
-        const float qm = __int_as_float(Qb[i].x);
-        const int qe = Qb[i].y - kEdgeBias;
-        if (t1 == T && u == U) q.ebb[i] = post(qm, qe, 1.0f, 0);
-        else if (t1 < T) q.ebb[i] = post(qm, qe, __int_as_float(Bq[i].x), Bq[i].y);
-    }
-    q.zero = !(lc + p.fe_l2 >= p.skip2);
-    q.w2 = lc + p.lscale - __ldcg(p.lse2 + r);
-    q.lr = lrow_s(p, r, b, o, W);
-    return q;
-}
-
 template <typename Tin, bool VEC>
 __global__ void __launch_bounds__(256) k_grad_mb(Params p) {
     if (*p.err) return;
@@ -3890,17 +3931,30 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
             return 0;
         });
         k_dp_mb<<<dim3(B, 2), nthr, smem, st>>>(p);
+        bool finalized = false;
         if (grad) {
-            with_type(dt, [&](auto tag) {
+            finalized = with_type(dt, [&](auto tag) {
                 using T = decltype(tag);
+                const int nv = V / Elt<T>::kPerVec;
+                if (fused_log_softmax && ((size_t)V * sizeof(T)) % 16 == 0 && nv > 32 &&
+                    nv <= 256) {
+                    // Rows staged by TMA (as the standard gradient pass); its last
+                    // CTA runs the loss check.
+                    const size_t sm = tma_smem(p);
+                    const int64_t wt = (rows + 31) / 32 * 32;
+                    if (nv <= 64) launch_gs(k_grad_tma<T, 2, true>, wt, sms, st, p, sm);
+                    else if (nv <= 128) launch_gs(k_grad_tma<T, 4, true>, wt, sms, st, p, sm);
+                    else launch_gs(k_grad_tma<T, 8, true>, wt, sms, st, p, sm);
+                    return true;
+                }
                 if (((size_t)V * sizeof(T)) % 16 == 0)
                     launch_gs(k_grad_mb<T, true>, rows * 32, sms, st, p);
                 else
                     launch_gs(k_grad_mb<T, false>, rows * 32, sms, st, p);
-                return 0;
+                return false;
             });
         }
-        k_finalize<<<1, 256, 0, st>>>(p);
+        if (!finalized) k_finalize<<<1, 256, 0, st>>>(p);
         for (int i = 1; i <= 6; ++i) mark(i);
         return cudaGetLastError() == cudaSuccess ? RNNT_OK : RNNT_LAUNCH_FAILED;
     }
