@@ -3166,6 +3166,13 @@ __global__ void __launch_bounds__(256) k_finalize(Params p) { finalize_block(p);
 constexpr int kMbRing = RNNT_MAX_BIG_BLANK_DURATION;
 static_assert((kMbRing & (kMbRing - 1)) == 0, "ring slots are t mod a power of two");
 
+// a += x * p * c without renormalising (the caller renormalises once per
+// step: xf_add aligns unnormalised mantissas exactly).
+__device__ __forceinline__ void xf_mac_raw(float& am, int& ae, float xm, int xe, float pm, int pe,
+                                           float c) {
+    xf_add<false>(am, ae, xm * (pm * c), xe + pe, am, ae);
+}
+
 __device__ __forceinline__ void xf_mac(float& am, int& ae, float xm, int xe, float pm, int pe,
                                        float c) {
     // a += x * p * c
@@ -3226,11 +3233,16 @@ __global__ void __launch_bounds__(1024) k_dp_mb(Params p) {
                     am = 1.0f;
                     ae = 0;
                 } else {
+                    // Two accumulators (blank + odd big blanks, label + even
+                    // ones) halve the dependent chain; one renormalisation.
                     am = bm;
                     ae = be;
+                    float a2 = 0.0f;
+                    int e2 = kZeroExp;
                     if (u > 0) {
                         const float2 v = xch[((d - 1) & 1) * nthr + u - 1];
-                        xf_add(am, ae, v.x, __float_as_int(v.y), am, ae);
+                        a2 = v.x;
+                        e2 = __float_as_int(v.y);
                     }
 #pragma unroll
                     for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) {
@@ -3238,18 +3250,23 @@ __global__ void __launch_bounds__(1024) k_dp_mb(Params p) {
                         const int t0 = t - p.bb_dur[i];
                         if (t0 < 0) continue;
                         const float2 a = ring[(t0 & (kMbRing - 1)) * nthr + u];
-                        xf_mac(am, ae, a.x, __float_as_int(a.y), __int_as_float(q[i].x),
-                               q[i].y - kEdgeBias, c);
+                        if (i & 1)
+                            xf_mac_raw(am, ae, a.x, __float_as_int(a.y), __int_as_float(q[i].x),
+                                       q[i].y - kEdgeBias, c);
+                        else
+                            xf_mac_raw(a2, e2, a.x, __float_as_int(a.y), __int_as_float(q[i].x),
+                                       q[i].y - kEdgeBias, c);
                     }
+                    xf_add<true>(am, ae, a2, e2, am, ae);
                 }
                 p.alpha[o + node_index(t, u, T, U)] = make_int2(__float_as_int(am), ae);
                 ring[(t & (kMbRing - 1)) * nthr + u] = make_float2(am, __int_as_float(ae));
-                bm = am * __int_as_float(ed.x) * c;
+                // Outflows (blank to (t+1,u), label to (t,u+1)); their mantissas
+                // stay below 4 and are renormalised by the adds they enter.
+                bm = am * (__int_as_float(ed.x) * c);
                 be = ae + ed.y - kEdgeBias;
-                xf_norm(bm, be);
-                float ym = am * __int_as_float(ed.z) * c;
-                int ye = ae + ed.w - kEdgeBias;
-                xf_norm(ym, ye);
+                const float ym = am * (__int_as_float(ed.z) * c);
+                const int ye = ae + ed.w - kEdgeBias;
                 out = make_float2(ym, __int_as_float(ye));
             } else {
                 bm = 0.0f;
@@ -3288,27 +3305,32 @@ __global__ void __launch_bounds__(1024) k_dp_mb(Params p) {
             fetch(t - 1);
             float2 out = zero;
             if (col && t >= 0 && t < T) {
-                float m = 0.0f;
-                int e = kZeroExp;
-                if (t + 1 < T) xf_mac(m, e, qm, qe, __int_as_float(ed.x), ed.y - kEdgeBias, c);
-                else if (u == U) xf_mac(m, e, 1.0f, 0, __int_as_float(ed.x), ed.y - kEdgeBias, c);
+                // Two accumulators (blank + odd big blanks, label + even ones).
+                float m = 0.0f, m2 = 0.0f;
+                int e = kZeroExp, e2 = kZeroExp;
+                if (t + 1 < T) xf_mac_raw(m, e, qm, qe, __int_as_float(ed.x), ed.y - kEdgeBias, c);
+                else if (u == U) xf_mac_raw(m, e, 1.0f, 0, __int_as_float(ed.x), ed.y - kEdgeBias, c);
                 if (u < U) {
                     const float2 v = xch[((d + 1) & 1) * nthr + u + 1];
-                    xf_mac(m, e, v.x, __float_as_int(v.y), __int_as_float(ed.z), ed.w - kEdgeBias, c);
+                    xf_mac_raw(m2, e2, v.x, __float_as_int(v.y), __int_as_float(ed.z),
+                               ed.w - kEdgeBias, c);
                 }
 #pragma unroll
                 for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) {
                     if (i >= p.K) break;
                     const int t1 = t + p.bb_dur[i];
                     if (t1 > T || (t1 == T && u != U)) continue;
-                    if (t1 == T) {
-                        xf_mac(m, e, 1.0f, 0, __int_as_float(q[i].x), q[i].y - kEdgeBias, c);
-                    } else {
+                    float am2 = 1.0f;
+                    int ae2 = 0;
+                    if (t1 < T) {
                         const float2 a = ring[(t1 & (kMbRing - 1)) * nthr + u];
-                        xf_mac(m, e, a.x, __float_as_int(a.y), __int_as_float(q[i].x),
-                               q[i].y - kEdgeBias, c);
+                        am2 = a.x;
+                        ae2 = __float_as_int(a.y);
                     }
+                    if (i & 1) xf_mac_raw(m, e, am2, ae2, __int_as_float(q[i].x), q[i].y - kEdgeBias, c);
+                    else xf_mac_raw(m2, e2, am2, ae2, __int_as_float(q[i].x), q[i].y - kEdgeBias, c);
                 }
+                xf_add<true>(m, e, m2, e2, m, e);
                 p.beta[o + node_index(t, u, T, U)] = make_int2(__float_as_int(m), e);
                 out = make_float2(m, __int_as_float(e));
                 ring[(t & (kMbRing - 1)) * nthr + u] = out;
