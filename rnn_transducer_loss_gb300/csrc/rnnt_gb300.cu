@@ -117,6 +117,19 @@ __host__ __device__ inline Layout ws_layout(int B, int64_t rows) {
     return L;
 }
 
+// Rows of at least this many bytes take a separate record pass before the
+// per-stage gradient kernel (measured on 20 KB rows: forming each row's record
+// inside the gradient kernel stalls its warp on a chain of dependent loads).
+constexpr size_t kLongRowBytes = 8192;
+__host__ __device__ inline bool long_rows(int V, int dt) {
+    return (size_t)V * (dt == RNNT_F32 ? 4 : 2) >= kLongRowBytes;
+}
+// Workspace: the common layout, plus for long rows one gradient record
+// (float4) per row after it.
+__host__ __device__ inline size_t ws_total(int B, int64_t rows, int V, int dt) {
+    return ws_layout(B, rows).total + (long_rows(V, dt) ? al256(sizeof(float4) * (size_t)rows) : 0);
+}
+
 // Workspace of the multi-blank kernels: the common layout plus one
 // extended-range probability per big blank and lattice node.
 __host__ __device__ inline size_t ws_total_mb(int B, int64_t rows, int K) {
@@ -168,6 +181,7 @@ struct Params {
     float* pm;        // P(y|x) of each sample, extended range
     int32_t* pe;
     float* lse2;      // per row (row order): log2 sum_k 2^(h_k log2 e)
+    float4* info;     // long rows only: per row the gradient record (k_combine)
     int4* edge;       // per node (node_index order): {p_blank.m, p_blank.e, p_label.m, p_label.e}
     int2* alpha;      // per node (node_index order): {m, e}
     int2* beta;
@@ -2211,6 +2225,18 @@ __device__ __forceinline__ float4 combine_row(const Params& p, int64_t r, int b)
                        __int_as_float(y));
 }
 
+// Long rows: every row's gradient record, ahead of the gradient kernel.
+__global__ void __launch_bounds__(256) k_combine(Params p) {
+    if (*p.err) return;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    int b = (r < nodes(p)) ? find_sample(p.off, p.B, r) : 0;
+    for (; r < nodes(p); r += stride) {
+        b = advance_sample(p.off, p.B, b, r);
+        p.info[r] = combine_row(p, r, b);
+    }
+}
+
 // The gradient record of row r for a lane that walks increasing rows (b: the
 // lane's current sample, -1 before its first row); a zero-row record for
 // lanes without a row.
@@ -2240,6 +2266,80 @@ __device__ __forceinline__ void finalize_if_last(const Params& p) {
 // ---------------------------------------------------------------- grad pass
 // grad_k * scale = 2^(h_k log2 e + log2(c scale) - lse2) - [k=blank] post_blank
 // scale - [k=y] post_label scale, clipped to +-clamp*scale (clip-then-scale).
+// Long rows (kLongRowBytes and more), a whole warp per row: rows
+// grid-strided over the warps so that the warps stream neighbouring rows;
+// each row's record comes from the record pass (k_combine), the next one's
+// loaded while the current row streams.  Few registers (the whole SM's
+// threads stream); k_finalize runs the loss check after it.
+template <typename Tin, bool VEC, bool FUSED>
+__global__ void __launch_bounds__(256) k_grad_long(Params p) {
+    if (*p.err) return;
+    using E = Elt<Tin>;
+    constexpr int EPV = E::kPerVec, G = 32;
+    const Tin* X = static_cast<const Tin*>(p.logits);
+    Tin* Y = static_cast<Tin*>(p.grad);
+    const int V = p.V;
+    const int lane = threadIdx.x & 31;
+    const float cl = p.clamp * p.scale;
+    const bool clip = p.clamp < INFINITY;
+    const int vb = p.blank / EPV, eb_i = p.blank % EPV;
+    const int64_t nr = nodes(p);
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+    float4 rec_next = gw < nr ? __ldcg(p.info + gw) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t r = gw; r < nr; r += nwarps) {
+        const float4 rec = rec_next;
+        if (r + nwarps < nr) rec_next = __ldcg(p.info + r + nwarps);
+        const float w2 = rec.x, eb = rec.y, ey = rec.z;
+        const int y = __float_as_int(rec.w);
+        const int64_t lr = lrow(p, r);
+        const bool zero = w2 == -INFINITY;
+        const Tin* row = X + lr * (int64_t)V;
+        Tin* out = Y + lr * (int64_t)V;
+        if (VEC) {
+            const int nvec = V / EPV;
+            const int vy = y >= 0 ? y / EPV : -1, ey_i = y >= 0 ? y % EPV : 0;
+            const uint4* rv = reinterpret_cast<const uint4*>(row);
+            uint4* ov = reinterpret_cast<uint4*>(out);
+            for (int vi = lane; vi < nvec; vi += G) {
+                float g[EPV];
+                if (FUSED && !zero) {
+                    float x[EPV];
+                    E::unpack(__ldcs(rv + vi), x);
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) g[e] = ex2(fmaf(x[e], kLog2e, w2));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) g[e] = 0.0f;
+                }
+                if (vi == vb) {
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e)
+                        if (e == eb_i) g[e] -= eb;
+                }
+                if (vi == vy) {
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e)
+                        if (e == ey_i) g[e] -= ey;
+                }
+                if (clip) {
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) g[e] = fminf(fmaxf(g[e], -cl), cl);
+                }
+                __stcs(ov + vi, E::pack(g));
+            }
+        } else {
+            for (int k = lane; k < V; k += G) {
+                float gv = (FUSED && !zero) ? ex2(fmaf(E::to_f(row[k]), kLog2e, w2)) : 0.0f;
+                if (k == p.blank) gv -= eb;
+                if (k == y) gv -= ey;
+                if (clip) gv = fminf(fmaxf(gv, -cl), cl);
+                out[k] = E::from_f(gv);
+            }
+        }
+    }
+}
+
 // Each warp takes batches of 32 consecutive rows: every lane forms one row's
 // record (occupancy, arc posteriors: combine_row), then groups of G lanes write
 // the rows, taking each row's record from its lane by shuffle.  The last CTA
@@ -3653,8 +3753,9 @@ void launch_rows(const Params& p, cudaStream_t st, int sms) {
 #undef ROWK
 }
 
+// Returns true when the launched kernel also ran the loss check.
 template <typename Tin>
-void launch_grad(const Params& p, cudaStream_t st, int sms) {
+bool launch_grad(const Params& p, cudaStream_t st, int sms) {
     const int V = p.V;
 
     const bool vec = ((size_t)V * sizeof(Tin)) % 16 == 0;
@@ -3665,7 +3766,18 @@ void launch_grad(const Params& p, cudaStream_t st, int sms) {
         if (nvec <= 64) launch_gs(k_grad_tma<Tin, 2>, wt, sms, st, p, sm);
         else if (nvec <= 128) launch_gs(k_grad_tma<Tin, 4>, wt, sms, st, p, sm);
         else launch_gs(k_grad_tma<Tin, 8>, wt, sms, st, p, sm);
-        return;
+        return true;
+    }
+    if (p.info) {   // long rows: records from k_combine
+        const int64_t wt = p.rows * 32;
+        if (p.fused) {
+            if (vec) launch_gs(k_grad_long<Tin, true, true>, wt, sms, st, p);
+            else launch_gs(k_grad_long<Tin, false, true>, wt, sms, st, p);
+        } else {
+            if (vec) launch_gs(k_grad_long<Tin, true, false>, wt, sms, st, p);
+            else launch_gs(k_grad_long<Tin, false, false>, wt, sms, st, p);
+        }
+        return false;
     }
 #define GRADK(G_)                                                                      \
     do {                                                                               \
@@ -3683,6 +3795,7 @@ void launch_grad(const Params& p, cudaStream_t st, int sms) {
     else if (V >= 32) GRADK(8);
     else GRADK(4);
 #undef GRADK
+    return true;
 }
 
 void* g_trace = nullptr;     // rnnt_set_trace: device buffer of int4 records
@@ -3792,7 +3905,7 @@ extern "C" rnnt_status_t rnnt_workspace_size(int32_t B, int64_t rows, int32_t V,
                                              size_t* bytes) {
     if (!bytes || B < 1 || rows < 1 || V < 1 || !valid_dtype(dt))
         return RNNT_INVALID_VALUE;
-    *bytes = ws_layout(B, rows).total;
+    *bytes = ws_total(B, rows, V, dt);
     return RNNT_OK;
 }
 
@@ -3854,7 +3967,7 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
     if (grad && grad != logits && overlaps(grad, nbytes, logits, nbytes)) return RNNT_INVALID_VALUE;
     const Layout L = ws_layout(B, rows);
     const bool multiblank = K > 0 || sigma > 0.0f;
-    if (workspace_bytes < (multiblank ? ws_total_mb(B, rows, K) : L.total))
+    if (workspace_bytes < (multiblank ? ws_total_mb(B, rows, K) : ws_total(B, rows, V, dt)))
         return RNNT_WORKSPACE_TOO_SMALL;
 
     int dev = 0;
@@ -3909,6 +4022,7 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
     p.pm = reinterpret_cast<float*>(w + L.pm);
     p.pe = reinterpret_cast<int32_t*>(w + L.pe);
     p.lse2 = reinterpret_cast<float*>(w + L.lse2);
+    p.info = (!multiblank && long_rows(V, dt)) ? reinterpret_cast<float4*>(w + L.total) : nullptr;
     p.edge = reinterpret_cast<int4*>(w + L.edge);
     p.alpha = reinterpret_cast<int2*>(w + L.alpha);
     p.beta = reinterpret_cast<int2*>(w + L.beta);
@@ -3999,14 +4113,16 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
     mark(2);
     k_dp<<<dim3(B, 2), dp_threads_for(targets_stride), dp_smem, st>>>(p);
     mark(3);
-    mark(4);   // the gradient records are formed inside the gradient kernel
+    if (grad && p.info) launch_gs(k_combine, rows, sms, st, p);   // long rows: the records first
+    mark(4);   // (otherwise the gradient records are formed inside the gradient kernel)
     if (grad) {
-        // The gradient kernel's last CTA also runs the loss check / reduction.
-        with_type(dt, [&](auto tag) {
-            launch_grad<decltype(tag)>(p, st, sms);
-            return 0;
+        // The gradient kernel's last CTA also runs the loss check / reduction
+        // (except the long-row kernel's: a check kernel follows it).
+        const bool checked = with_type(dt, [&](auto tag) {
+            return launch_grad<decltype(tag)>(p, st, sms);
         });
         mark(5);
+        if (!checked) k_finalize<<<1, 256, 0, st>>>(p);
     } else {
         mark(5);
         k_finalize<<<1, 256, 0, st>>>(p);
@@ -4022,7 +4138,7 @@ extern "C" rnnt_status_t rnnt_workspace_size_ex(int32_t B, int64_t rows, int32_t
     const int K = options ? options->num_big_blanks : 0;
     if (K < 0 || K > RNNT_MAX_BIG_BLANKS) return RNNT_INVALID_VALUE;
     const bool mb = options && (K > 0 || options->sigma > 0.0f);
-    *bytes = mb ? ws_total_mb(B, rows, K) : ws_layout(B, rows).total;
+    *bytes = mb ? ws_total_mb(B, rows, K) : ws_total(B, rows, V, dt);
     return RNNT_OK;
 }
 
@@ -4124,7 +4240,8 @@ extern "C" rnnt_status_t rnnt_plan(int32_t B, int64_t rows, int32_t V, rnnt_dtyp
             return RNNT_OK;
         }
     }
-    plan->launches = pad + 4;   // prepare, rows, recursions, gradient (or loss check)
+    // prepare, rows, recursions, [long rows: records], gradient, [long rows: check]
+    plan->launches = pad + 4 + ((want_grad && long_rows(V, dt)) ? 2 : 0);
     return RNNT_OK;
 }
 
@@ -4179,7 +4296,7 @@ extern "C" rnnt_status_t rnnt_loss_fused_noalloc(
     int32_t blank, float clamp, int32_t fused_log_softmax, rnnt_reduction_t reduction, float* loss,
     float* loss_reduced, void* grad, int32_t* status_dev, rnnt_stream_t stream) {
     if (B < 1 || rows < 1 || V < 1 || !valid_dtype(dt)) return RNNT_INVALID_VALUE;
-    const size_t need = ws_layout(B, rows).total;
+    const size_t need = ws_total(B, rows, V, dt);
     if (need > RNNT_NOALLOC_SCRATCH_BYTES) return RNNT_WORKSPACE_TOO_SMALL;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoallocMaxDevices)
