@@ -302,7 +302,10 @@ rnnt_status_t rnnt_set_trace(void *device_buffer, size_t bytes);
  * call allocates nothing (no cudaMalloc/cudaFree, no allocating library
  * routine).  The first call on a device, made with that device current,
  * looks up the array's device address (cudaGetSymbolAddress) once and
- * caches it; make that first call before any stream capture.
+ * caches it; make that first call before any stream capture.  The cached
+ * address is that of the device's primary context at the time: a process
+ * that destroys it (cudaDeviceReset) must not call this entry point on that
+ * device afterwards.
  *
  * Every call on a device shares the one array and leaves its contents
  * behind; each call rewrites everything it reads before reading it.  Calls

@@ -4219,7 +4219,12 @@ extern "C" rnnt_status_t rnnt_plan(int32_t B, int64_t rows, int32_t V, rnnt_dtyp
     }
     plan->persistent = 0;
     if (multiblank) {   // prepare, rows, recursions, gradient rows, check
-        plan->launches = pad + 4 + g;
+        // (the TMA-staged gradient kernel, for log-softmax on rows of 33 to 256
+        // 16-byte vectors, runs the check itself)
+        const int epv = dt == RNNT_F32 ? 4 : 8;
+        const int nv = V / epv;
+        const bool tma = want_grad && fused_log_softmax && V % epv == 0 && nv > 32 && nv <= 256;
+        plan->launches = pad + 4 + g - (tma ? 1 : 0);
         return RNNT_OK;
     }
     if (want_grad) {
