@@ -169,6 +169,12 @@ struct Params {
     int stage_bytes;  // per-stage shared-memory row buffer of the TMA-staged passes
     int zero_off;     // persistent kernel: shared-memory offset of a zeroed buffer ...
     int zero_rows;    // ... of zero_rows gradient rows, the source of zero-row bulk stores
+    // Calls without the in-kernel log-softmax: extra CTAs of the recursion
+    // launch zero the whole gradient buffer (zfill bytes; zcta CTAs at most,
+    // each with a zeroed shared buffer of zbuf bytes), and the gradient pass
+    // then writes only the blank and label elements.  zfill = 0: off.
+    int64_t zfill;
+    int zcta, zbuf;
     float* loss;
     float* loss_red;
     int32_t* status;
@@ -789,6 +795,9 @@ __device__ void prepare_block(const Params& p, int64_t* s_before, int* s_nch) {
         p.err[8] = 0;   // CTAs of the persistent kernel that have finished
         p.err[9] = 0;   // first timeout site (diagnosis)
         p.err[10] = 0;
+        p.err[13] = 0;    // next zero-fill chunk
+        p.err[14] = -1;   // SMs of the longest recursion's two CTAs (zero-fill CTAs skip them)
+        p.err[15] = -1;
         // Rows per sample slot of the padded layout (0: compact), for rnnt_grad_scale.
         p.err[12] = p.padded ? p.maxT * p.maxW : 0;
     }
@@ -1191,13 +1200,6 @@ __global__ void __launch_bounds__(256) k_row_stream(Params p) {
 }
 
 // In-kernel log-softmax off: the rows already hold log-probs; read 2 elements.
-template <typename Tin>
-__global__ void __launch_bounds__(256) k_row_gather(Params p) {
-    if (*p.err) return;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < nodes(p); r += stride)
-        row_finish<Tin>(p, r, 0.0f, 1.0f);
-}
 
 // ---------------------------------------------------------------- DP
 // One CTA per sample (8 warps).  Per direction, nwd compute warps (at most
@@ -2137,10 +2139,61 @@ __device__ __forceinline__ void k_dp_body(const Params& p, const Samp& c, int4* 
     dp_run_dir<J, deep_ring(J), kDpWarpsStaged>(p, c, dir, threadIdx.x >> 5, smem, xch, tab);
 }
 
+// Zero-fill of the gradient buffer by the CTAs of the recursion launch past
+// its two per sample (blockIdx.y >= 2): every CTA zeroes its shared buffer,
+// then one thread claims 1 MB chunks from a counter and writes each with bulk
+// (TMA) stores of that buffer, so the fill costs the SM few instructions
+// while recursions run beside it.  A CTA placed on an SM of the longest
+// recursion (its CTAs record their SMs first) leaves at once.  The bytes
+// past the last 16-byte boundary are stored by the thread that claims the
+// last chunk.
+//
+// Only as many CTAs take part as keep the fill within about the longest
+// recursion's duration: on GB300 a recursion step takes ~175 ns per
+// anti-diagonal and one CTA's bulk stores write ~60 GB/s, ~10 KB per step.
+// More CTAs saturate HBM, which slows the recursion (its transition records
+// stream from HBM) without ending the call sooner (measured on a 1500 x 301
+// lattice beside 830 MB of fill: 173 ns per step with 48 CTAs, 192 with 152).
+constexpr int64_t kZeroChunk = 1 << 20;
+constexpr int64_t kZeroBytesPerStep = 9500;
+__device__ __forceinline__ void zero_fill(const Params& p, int4* smem) {
+    const int z = blockIdx.x + gridDim.x * (blockIdx.y - 2);
+    const int bc = __ldcg(p.order);
+    const int64_t per = ((int64_t)__ldg(p.Tl + bc) + __ldg(p.Ul + bc)) * kZeroBytesPerStep;
+    const int64_t need = (p.zfill + per - 1) / per;
+    if (z >= min((int64_t)p.zcta, max((int64_t)8, need))) return;
+    const int sm = smid();
+    const volatile int32_t* ve = p.err;
+    if (sm == ve[14] || sm == ve[15]) return;
+    for (int i = threadIdx.x; i < p.zbuf / 16; i += blockDim.x) smem[i] = make_int4(0, 0, 0, 0);
+    fence_proxy_async();   // the zeros are read by the bulk-copy (async) proxy
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    char* g = static_cast<char*>(p.grad);
+    const int64_t body = p.zfill & ~int64_t(15);
+    for (;;) {
+        const int64_t a = (int64_t)atomicAdd(p.err + 13, 1) * kZeroChunk;
+        if (a >= p.zfill) break;
+        const int64_t e = min(a + kZeroChunk, p.zfill), eb = min(e, body);
+        for (int64_t x = a; x < eb; x += p.zbuf)
+            tma_store(g + x, smem, (uint32_t)min((int64_t)p.zbuf, eb - x));
+        tma_store_commit();
+        // At most 4 further chunks' stores in flight from this CTA.
+        asm volatile("cp.async.bulk.wait_group.read 4;\n" ::: "memory");
+        for (int64_t x = max(a, body); x < e; ++x) g[x] = 0;
+    }
+    tma_store_wait_all();
+}
+
 __global__ void __launch_bounds__(32 * kDpWarpsStaged) k_dp(Params p) {
     if (*p.err) return;
     extern __shared__ int4 smem[];
     __shared__ float2 xch[kDpWarpsStaged * kXch];
+    if (blockIdx.y >= 2) {
+        zero_fill(p, smem);
+        return;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0 && p.zfill) p.err[14 + blockIdx.y] = smid();
     Samp c;
     c.b = p.order[blockIdx.x];
     c.T = p.Tl[c.b];
@@ -2177,12 +2230,10 @@ __device__ __forceinline__ float xf_to_float(float m, int e) {
 // (alpha, beta, transition records, lse2, P) is loaded through L2 only
 // (ld.global.cg): in the persistent kernel other CTAs write these while this
 // SM may hold neighbouring lines in L1.
-__device__ __forceinline__ float4 combine_row(const Params& p, int64_t r, int b) {
-    const int T = __ldg(p.Tl + b), U = __ldg(p.Ul + b), W = U + 1;
-    const int64_t o = __ldcg(p.off + b);
-    const unsigned rr = (unsigned)(r - o);
-    const int t = (int)(rr / (unsigned)W), u = (int)(rr - (unsigned)t * W);
-    const int64_t i = o + node_index(t, u, T, U);
+// combine_at: node (t,u) of sample b (lengths T, U; first row / node o),
+// global node index i, compact row r.
+__device__ __forceinline__ float4 combine_at(const Params& p, int b, int T, int U, int64_t o,
+                                             int t, int u, int64_t i, int64_t r) {
     const int2 A = __ldcg(p.alpha + i), Bt = __ldcg(p.beta + i);
     const int4 Ed = __ldcg(p.edge + i);
     const float Pm = __ldcg(p.pm + b);
@@ -2221,8 +2272,16 @@ __device__ __forceinline__ float4 combine_row(const Params& p, int64_t r, int b)
             }
         }
     }
-    return make_float4(lc + p.lscale - __ldcg(p.lse2 + r), eb * p.scale, ey * p.scale,
-                       __int_as_float(y));
+    // (Without the log-softmax lse2 is 0 for every row.)
+    return make_float4(lc + p.lscale - (p.fused ? __ldcg(p.lse2 + r) : 0.0f), eb * p.scale,
+                       ey * p.scale, __int_as_float(y));
+}
+__device__ __forceinline__ float4 combine_row(const Params& p, int64_t r, int b) {
+    const int T = __ldg(p.Tl + b), U = __ldg(p.Ul + b), W = U + 1;
+    const int64_t o = __ldcg(p.off + b);
+    const unsigned rr = (unsigned)(r - o);
+    const int t = (int)(rr / (unsigned)W), u = (int)(rr - (unsigned)t * W);
+    return combine_at(p, b, T, U, o, t, u, o + node_index(t, u, T, U), r);
 }
 
 // Long rows: every row's gradient record, ahead of the gradient kernel.
@@ -2448,6 +2507,219 @@ __global__ void __launch_bounds__(256) k_grad(Params p) {
     finalize_if_last(p);
 }
 
+// Anti-diagonal of node k (0 <= k < T W) of a T x W lattice in the
+// anti-diagonal-packed order: a first guess from the lattice's three parts
+// (diagonal lengths rising 1 .. m-1, then m, then falling; m = min(T, W)),
+// corrected against diag_start.
+__device__ __forceinline__ int node_diag(int64_t k, int T, int W) {
+    const int m = min(T, W), M = max(T, W), D = T + W - 1;
+    const int64_t head = (int64_t)(m - 1) * m / 2;
+    int d;
+    if (k < head) {
+        d = (int)((sqrtf(8.0f * (float)k + 1.0f) - 1.0f) * 0.5f);
+    } else if (k < head + (int64_t)(M - m + 1) * m) {
+        d = m - 1 + (int)((k - head) / m);
+    } else {
+        const int64_t kr = (int64_t)T * W - 1 - k;
+        d = D - 1 - (int)((sqrtf(8.0f * (float)kr + 1.0f) - 1.0f) * 0.5f);
+    }
+    d = max(0, min(d, D - 1));
+    while (d > 0 && diag_start(d, T, W) > k) --d;
+    while (d + 1 < D && diag_start(d + 1, T, W) <= k) ++d;
+    return d;
+}
+
+template <typename Tin>
+__device__ __forceinline__ uint32_t elt_bits(Tin v) {
+    if constexpr (sizeof(Tin) == 4) {
+        uint32_t x;
+        memcpy(&x, &v, 4);
+        return x;
+    } else {
+        uint16_t x;
+        memcpy(&x, &v, 2);
+        return x;
+    }
+}
+
+// Stores elements k1 (bits v1, if w1) and k2 (bits v2, if w2) of a gradient
+// row whose other elements are already zero.  The aligned 32-byte sector
+// holding an element, when it lies inside the row, is written whole (zeros
+// around the value, both elements when they share it), so that no partial
+// sector is left for the memory system to merge; otherwise the element alone.
+template <typename Tin>
+__device__ __forceinline__ void put_sparse(Tin* row, int V, int k1, uint32_t v1, bool w1, int k2,
+                                           uint32_t v2, bool w2) {
+    constexpr int S = sizeof(Tin);
+    const uintptr_t base = reinterpret_cast<uintptr_t>(row), end = base + (uintptr_t)V * S;
+    const uintptr_t e1 = base + (uintptr_t)k1 * S, e2 = base + (uintptr_t)k2 * S;
+    const uintptr_t a1 = e1 & ~uintptr_t(31), a2 = e2 & ~uintptr_t(31);
+    const bool in1 = a1 >= base && a1 + 32 <= end, in2 = a2 >= base && a2 + 32 <= end;
+    // The sector at a with the value bits x1 at byte offset o1 and x2 at o2
+    // (an offset of -1: none).
+    auto sector = [](uintptr_t a, int o1, uint32_t x1, int o2, uint32_t x2) {
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint32_t v = 0;
+            if (o1 >= 0 && (o1 >> 2) == j) v |= S == 4 ? x1 : x1 << ((o1 & 2) * 8);
+            if (o2 >= 0 && (o2 >> 2) == j) v |= S == 4 ? x2 : x2 << ((o2 & 2) * 8);
+            w[j] = v;
+        }
+        uint4* q = reinterpret_cast<uint4*>(a);
+        q[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        q[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    };
+    auto single = [](uintptr_t e, uint32_t v) {
+        if constexpr (S == 4) *reinterpret_cast<uint32_t*>(e) = v;
+        else *reinterpret_cast<uint16_t*>(e) = (uint16_t)v;
+    };
+    if (w1 && w2 && in1 && a1 == a2) {
+        sector(a1, (int)(e1 - a1), v1, (int)(e2 - a1), v2);
+        return;
+    }
+    if (w1) {
+        if (in1) sector(a1, (int)(e1 - a1), v1, -1, 0u);
+        else single(e1, v1);
+    }
+    if (w2) {
+        if (in2) sector(a2, (int)(e2 - a2), v2, -1, 0u);
+        else single(e2, v2);
+    }
+}
+
+// Calls without the in-kernel log-softmax, the gradient buffer already
+// zeroed by the recursion launch: a row's only non-zero elements are at the
+// blank and the label, -post_blank and -post_label times the reduction scale,
+// clipped.  A CTA takes 1024 consecutive lattice nodes in the anti-diagonal
+// order of the node arrays (so that their reads coalesce), four per thread
+// with their loads issued together, the samples of its first and last node
+// looked up once.  An element is stored only where its value is not exactly
+// zero, so the buffer ends bit for bit as the full-row pass leaves it.  The
+// last CTA runs the loss check.
+constexpr int kSparseRows = 1024;
+template <typename Tin>
+__global__ void __launch_bounds__(256) k_grad_sparse(Params p) {
+    const int64_t nr = nodes(p);
+    const int64_t n0 = (int64_t)blockIdx.x * kSparseRows;
+    if (*p.err == 0 && n0 < nr) {
+        using E = Elt<Tin>;
+        constexpr int NR = kSparseRows / 256;
+        __shared__ int s_lo, s_hi;
+        if (threadIdx.x == 0) s_lo = find_sample(p.off, p.B, n0);
+        if (threadIdx.x == 32) s_hi = find_sample(p.off, p.B, min(n0 + kSparseRows - 1, nr - 1));
+        __syncthreads();
+        Tin* Y = static_cast<Tin*>(p.grad);
+        const float cl = p.clamp * p.scale;
+        const bool clip = p.clamp < INFINITY;
+        float4 rec[NR];
+        int64_t lr[NR];
+#pragma unroll
+        for (int k = 0; k < NR; ++k) {
+            const int64_t i = n0 + threadIdx.x + 256 * k;
+            rec[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            lr[k] = 0;
+            if (i < nr) {
+                int lo = s_lo, hi = s_hi + 1;
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (__ldcg(p.off + mid) <= i) lo = mid; else hi = mid;
+                }
+                const int T = __ldg(p.Tl + lo), U = __ldg(p.Ul + lo), W = U + 1;
+                const int64_t o = __ldcg(p.off + lo), kk = i - o;
+                const int d = node_diag(kk, T, W);
+                const int t = (int)(kk - diag_start(d, T, W)) + max(0, d - U), u = d - t;
+                const int64_t r = o + (int64_t)t * W + u;
+                rec[k] = combine_at(p, lo, T, U, o, t, u, i, r);
+                lr[k] = p.padded ? ((int64_t)lo * p.maxT + t) * p.maxW + u : r;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < NR; ++k) {
+            float gb = 0.0f - rec[k].y, gy = 0.0f - rec[k].z;
+            if (clip) {
+                gb = fminf(fmaxf(gb, -cl), cl);
+                gy = fminf(fmaxf(gy, -cl), cl);
+            }
+            const int y = __float_as_int(rec[k].w);
+            put_sparse<Tin>(Y + lr[k] * (int64_t)p.V, p.V, p.blank, elt_bits(E::from_f(gb)),
+                            rec[k].y != 0.0f, y < 0 ? 0 : y, elt_bits(E::from_f(gy)),
+                            rec[k].z != 0.0f);
+        }
+    }
+    finalize_if_last(p);
+}
+
+// Row pass without the log-softmax: each node's two transition
+// probabilities (and every big blank's) read straight from its row's
+// log-probabilities, the nodes taken in the anti-diagonal order of the node
+// arrays so that the records' stores coalesce: a CTA takes 1024 consecutive
+// nodes, four per thread with their loads issued together, the samples of its
+// first and last node looked up once.  (lse2, 0 for every such row, is never
+// read, so it is not stored.)
+constexpr int kGatherNodes = 1024;
+template <typename Tin>
+__global__ void __launch_bounds__(256) k_row_gather(Params p) {
+    const int64_t nr = nodes(p);
+    const int64_t n0 = (int64_t)blockIdx.x * kGatherNodes;
+    if (*p.err || n0 >= nr) return;
+    using E = Elt<Tin>;
+    constexpr int NR = kGatherNodes / 256;
+    __shared__ int s_lo, s_hi;
+    if (threadIdx.x == 0) s_lo = find_sample(p.off, p.B, n0);
+    if (threadIdx.x == 32) s_hi = find_sample(p.off, p.B, min(n0 + kGatherNodes - 1, nr - 1));
+    __syncthreads();
+    const Tin* X = static_cast<const Tin*>(p.logits);
+    const Tin* row[NR];
+    float hb[NR], hy[NR];
+    int tt[NR], uu[NR], TT[NR], UU[NR];
+#pragma unroll
+    for (int k = 0; k < NR; ++k) {
+        const int64_t i = n0 + threadIdx.x + 256 * k;
+        row[k] = nullptr;
+        hb[k] = hy[k] = 0.0f;
+        tt[k] = uu[k] = TT[k] = UU[k] = 0;
+        if (i < nr) {
+            int lo = s_lo, hi = s_hi + 1;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (__ldcg(p.off + mid) <= i) lo = mid; else hi = mid;
+            }
+            const int T = __ldg(p.Tl + lo), U = __ldg(p.Ul + lo), W = U + 1;
+            const int64_t o = __ldcg(p.off + lo), kk = i - o;
+            const int d = node_diag(kk, T, W);
+            const int t = (int)(kk - diag_start(d, T, W)) + max(0, d - U), u = d - t;
+            const int64_t lr = p.padded ? ((int64_t)lo * p.maxT + t) * p.maxW + u
+                                        : o + (int64_t)t * W + u;
+            row[k] = X + lr * (int64_t)p.V;
+            hb[k] = E::get(row[k], p.blank);
+            if (u < U) hy[k] = E::get(row[k], __ldg(p.targets + (int64_t)lo * p.S + u));
+            tt[k] = t;
+            uu[k] = u;
+            TT[k] = T;
+            UU[k] = U;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < NR; ++k) {
+        if (!row[k]) continue;
+        const int64_t i = n0 + threadIdx.x + 256 * k;
+        const int t = tt[k], u = uu[k], T = TT[k], U = UU[k];
+        if (!(hb[k] < INFINITY) || !(hy[k] < INFINITY)) atomicOr(p.err, ERR_NONFINITE);
+        float bm = 0.0f, ym = 0.0f;
+        int be = kZeroExp, ye = kZeroExp;
+        if (!(t == T - 1 && u < U)) xf_prob(hb[k], 0.0f, 1.0f, bm, be);
+        if (u < U) xf_prob(hy[k], 0.0f, 1.0f, ym, ye);
+        p.edge[i] = make_int4(__float_as_int(bm), be + kEdgeBias, __float_as_int(ym), ye + kEdgeBias);
+        for (int j = 0; j < p.K; ++j) {   // multi-blank: every big blank's probability
+            float m;
+            int e;
+            xf_prob(E::get(row[k], p.bb_id[j]), 0.0f, 1.0f, m, e);
+            p.pbb[(int64_t)j * p.rows + i] = make_int2(__float_as_int(m), e + kEdgeBias);
+        }
+    }
+}
+
 // Gradient rows of the multi-blank loss.  A warp takes 32 consecutive rows:
 // each lane first forms one row's record (occupancy and every arc's
 // posterior, all its loads issued together), then the warp writes the rows
@@ -2521,7 +2793,7 @@ __device__ __forceinline__ MbRec mb_record(const Params& p, int64_t r, int b) {
         else if (t1 < T) q.ebb[i] = post(qm, qe, __int_as_float(Bq[i].x), Bq[i].y);
     }
     q.zero = !(lc + p.fe_l2 >= p.skip2);
-    q.w2 = q.zero ? -INFINITY : lc + p.lscale - __ldcg(p.lse2 + r);
+    q.w2 = q.zero ? -INFINITY : lc + p.lscale - (p.fused ? __ldcg(p.lse2 + r) : 0.0f);
     q.lr = lrow_s(p, r, b, o, W);
     return q;
 }
@@ -3717,7 +3989,7 @@ template <typename Tin>
 void launch_rows(const Params& p, cudaStream_t st, int sms) {
     const int V = p.V;
     if (!p.fused) {
-        launch_gs(k_row_gather<Tin>, p.rows, sms, st, p);
+        k_row_gather<Tin><<<(unsigned)((p.rows + kGatherNodes - 1) / kGatherNodes), 256, 0, st>>>(p);
         return;
     }
 
@@ -4046,8 +4318,18 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
         if (stage_events && stage_events[i])
             cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), st);
     };
+    // Without the in-kernel log-softmax (single blank, per-stage kernels) the
+    // recursion launch also zeroes the whole gradient buffer, padding rows
+    // included, and the gradient pass writes only the blank and label
+    // elements.  (The persistent kernel, when it takes the call, writes every
+    // row itself.)
+    const bool persistent_shape = grad && !multiblank && with_type(dt, [&](auto tag) {
+        PersistentCfg c;
+        return persistent_setup<decltype(tag)>(p, sms, dev, c);
+    });
+    const bool sparse = grad && !multiblank && !fused_log_softmax && !persistent_shape;
     mark(0);
-    if (grad && padded) {   // zero gradient rows outside the lattices
+    if (grad && padded && !sparse) {   // zero gradient rows outside the lattices
         with_type(dt, [&](auto tag) {
             launch_gs(k_pad_zero<decltype(tag)>, rows * 32, sms, st, p);
             return 0;
@@ -4111,7 +4393,15 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
         return 0;
     });
     mark(2);
-    k_dp<<<dim3(B, 2), dp_threads_for(targets_stride), dp_smem, st>>>(p);
+    int zy = 0;   // rows of zero-fill CTAs in the recursion launch's grid
+    if (sparse) {
+        p.zfill = (int64_t)nbytes;
+        p.zcta = sms;
+        p.zbuf = (int)(std::min(dp_smem, (size_t)32768) & ~size_t(15));
+        p.info = nullptr;
+        zy = (sms + B - 1) / B;
+    }
+    k_dp<<<dim3(B, 2 + zy), dp_threads_for(targets_stride), dp_smem, st>>>(p);
     mark(3);
     if (grad && p.info) launch_gs(k_combine, rows, sms, st, p);   // long rows: the records first
     mark(4);   // (otherwise the gradient records are formed inside the gradient kernel)
@@ -4119,7 +4409,12 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
         // The gradient kernel's last CTA also runs the loss check / reduction
         // (except the long-row kernel's: a check kernel follows it).
         const bool checked = with_type(dt, [&](auto tag) {
-            return launch_grad<decltype(tag)>(p, st, sms);
+            using T = decltype(tag);
+            if (sparse) {
+                k_grad_sparse<T><<<(unsigned)((rows + kSparseRows - 1) / kSparseRows), 256, 0, st>>>(p);
+                return true;
+            }
+            return launch_grad<T>(p, st, sms);
         });
         mark(5);
         if (!checked) k_finalize<<<1, 256, 0, st>>>(p);
@@ -4245,8 +4540,11 @@ extern "C" rnnt_status_t rnnt_plan(int32_t B, int64_t rows, int32_t V, rnnt_dtyp
             return RNNT_OK;
         }
     }
-    // prepare, rows, recursions, [long rows: records], gradient, [long rows: check]
-    plan->launches = pad + 4 + ((want_grad && long_rows(V, dt)) ? 2 : 0);
+    // prepare, rows, recursions, [long rows: records], gradient, [long rows: check];
+    // without the log-softmax: prepare, rows, recursions (and zero-fill), the
+    // blank / label elements (and check)
+    if (want_grad && !fused_log_softmax) plan->launches = 4;
+    else plan->launches = pad + 4 + ((want_grad && long_rows(V, dt)) ? 2 : 0);
     return RNNT_OK;
 }
 

@@ -240,3 +240,44 @@ def test_multiblank_degenerate_lattices():
                                       sigma=0.1, reduction="sum")
     assert_loss_close(to_np(loss), ref.losses, "f32")
     assert_grad_close(to_np(grad), ref.grad, "f32")
+
+
+# ------------------------------------------------------------------ log-probability inputs, per-stage
+# Without the in-kernel log-softmax, a call the persistent kernel does not take
+# (here a lattice of 301 columns) zeroes the whole gradient buffer from extra
+# CTAs of the recursion launch and then stores only the blank and label
+# elements.  Every element must match the oracle whatever the buffer held
+# before (in place: the log-probabilities themselves), with a byte count that
+# is no multiple of 16 (74-byte rows), long rows, and padding rows.
+LOGPROB_CASES = [
+    dict(V=37, dtype="f16", blank=5, clamp=-1.0, reduction="sum"),
+    dict(V=512, dtype="f16", blank=-1, clamp=0.5, reduction="mean"),
+    dict(V=80, dtype="f32", blank=2, clamp=0.3, reduction="none"),
+    dict(V=2500, dtype="bf16", blank=0, clamp=-1.0, reduction="mean"),
+    dict(V=2200, dtype="f32", blank=-1, clamp=-1.0, reduction="sum"),   # 8.8 KB rows
+]
+
+
+@pytest.mark.parametrize("case", range(len(LOGPROB_CASES)))
+def test_log_prob_inputs_zero_filled_buffer(case):
+    kw = LOGPROB_CASES[case]
+    wl = make(3, [7, 25, 4], [300, 9, 0], fused=False, sigma=1.0, seed=150 + case, **kw)
+    dt = {"f32": 0, "f16": 1, "bf16": 2}[kw["dtype"]]
+    plan = N.rnnt_plan(3, wl.logits.shape[0], kw["V"], dt, wl.targets.shape[1], False, True)
+    assert plan == {"persistent": False, "launches": 4}
+    ref = oracle_full(wl)
+    loss, red, grad = gpu_run(wl, inplace=True)
+    assert_loss_close(to_np(loss), ref.losses, kw["dtype"])
+    assert_grad_close(to_np(grad.float()), ref.grad, kw["dtype"])
+    # Exact zeros wherever the oracle's gradient is zero (every element but
+    # the blank and label ones).
+    assert not grad.float()[torch.as_tensor(ref.grad == 0.0, device="cuda")].any()
+    lc, rc, gc = gpu_run(wl)
+    assert torch.equal(lc, loss) and torch.equal(gc, grad)
+    xp = W.to_padded(wl, max_T=27, max_U=302, fill=float("nan"))
+    lp, rp, gp = run_padded(wl, xp)
+    assert torch.equal(lp, lc) and torch.equal(rp, rc)
+    for b in range(3):
+        T, U = int(wl.T[b]), int(wl.U[b])
+        assert torch.equal(gp[b, :T, :U + 1].reshape(-1, kw["V"]), gc[wl.sample_rows(b)])
+        assert not gp[b, T:].any() and not gp[b, :, U + 1:].any()
