@@ -1143,6 +1143,10 @@ __device__ __forceinline__ void row_stats_stream(const Tin* row, int V, int lane
 #pragma unroll
                 for (int e = 0; e < UNR * EPV; ++e) s += ex2(fmaf(x[e], kLog2e, -nmL));
                 m = nm;
+            } else {   // nothing but -inf and NaN so far: a NaN still reaches the sum
+#pragma unroll
+                for (int e = 0; e < UNR * EPV; ++e)
+                    if (x[e] != x[e]) s = x[e];
             }
         }
     } else {
@@ -1164,6 +1168,10 @@ __device__ __forceinline__ void row_stats_stream(const Tin* row, int V, int lane
 #pragma unroll
                 for (int e = 0; e < UNR; ++e) s += ex2(fmaf(x[e], kLog2e, -nmL));
                 m = nm;
+            } else {   // nothing but -inf and NaN so far: a NaN still reaches the sum
+#pragma unroll
+                for (int e = 0; e < UNR; ++e)
+                    if (x[e] != x[e]) s = x[e];
             }
         }
     }
@@ -1171,6 +1179,120 @@ __device__ __forceinline__ void row_stats_stream(const Tin* row, int V, int lane
     s = (M == -INFINITY) ? 0.0f : s * ex2((m - M) * kLog2e);
     Mo = M;
     so = group_sum<G>(s, gm);
+}
+
+// ---- Short rows that are not 16-byte vectors (compact layout) ----
+// Up to kFlatRowBytes bytes per row.  A warp stages up to 32 consecutive
+// rows into shared memory: coalesced 16-byte loads of the 16-byte aligned
+// span that holds them (its first chunk may start inside the previous row;
+// the bytes past its last full chunk are loaded element by element, so
+// nothing past the tensor is read); lane l then reduces row l there, the
+// maximum and then the sum of 2^((x - max) log2 e) in element order.  Both
+// schedules use these functions, so they give the same bits.
+constexpr int kFlatRowBytes = 256;
+__host__ __device__ inline size_t flat_warp_bytes(int V, int es) {
+    return (size_t)32 * V * es + 32;
+}
+// (The padded layout reduces such rows the same way, each lane reading its
+// row from global memory: padded and compact calls agree bit for bit.)
+__host__ __device__ inline bool flat_rows(int V, int es, int fused) {
+    return fused && ((size_t)V * es) % 16 != 0 && (size_t)V * es <= kFlatRowBytes;
+}
+
+template <typename Tin>
+__device__ __forceinline__ const Tin* flat_stage(const Tin* X, int64_t r0, int n, int V,
+                                                 unsigned char* sbuf, int lane) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(X + r0 * (int64_t)V);
+    const uintptr_t e = reinterpret_cast<uintptr_t>(X + (r0 + n) * (int64_t)V);
+    const uintptr_t a0 = a & ~uintptr_t(15), e0 = e & ~uintptr_t(15);
+    const int nv = (int)((e0 - a0) / 16);
+    const uint4* src = reinterpret_cast<const uint4*>(a0);
+    uint4* dst = reinterpret_cast<uint4*>(sbuf);
+    for (int i = lane; i < nv; i += 32) dst[i] = __ldcs(src + i);
+    const int nt = (int)((e - e0) / sizeof(Tin));
+    if (lane < nt)
+        reinterpret_cast<Tin*>(sbuf + (e0 - a0))[lane] = reinterpret_cast<const Tin*>(e0)[lane];
+    __syncwarp();
+    return reinterpret_cast<const Tin*>(sbuf + (a - a0));
+}
+
+template <typename Tin>
+__device__ __forceinline__ void flat_row_stats(const Tin* row, int V, float& M, float& s) {
+    using E = Elt<Tin>;
+    float m = -INFINITY;
+    for (int k = 0; k < V; ++k) m = fmaxf(m, E::to_f(row[k]));
+    const float mL = m == -INFINITY ? 0.0f : m * kLog2e;
+    float acc = 0.0f;   // a NaN element makes it NaN (fmaxf above skips it)
+    for (int k = 0; k < V; ++k) acc += ex2(fmaf(E::to_f(row[k]), kLog2e, -mL));
+    M = m;
+    s = acc;
+}
+
+// Gradient of n <= 32 consecutive compact rows from r0 (log-softmax on) in
+// flat element order: lane l takes elements l, l + 32, ... of the rows'
+// contiguous span, four at a time with their loads issued together; rec(i)
+// gives row i's record (called by every lane, same trip count).  Rows of exact
+// zeros are not read.
+template <typename Tin, typename Rec>
+__device__ __forceinline__ void flat_grad(const Params& p, int64_t r0, int n, int lane, Rec rec) {
+    using E = Elt<Tin>;
+    constexpr int UF = 4;
+    const int V = p.V;
+    const Tin* X = static_cast<const Tin*>(p.logits) + r0 * (int64_t)V;
+    Tin* Y = static_cast<Tin*>(p.grad) + r0 * (int64_t)V;
+    const float invV = 1.0f / (float)V;   // (f + 1/2) / V floors exactly for f < 32 V <= 2^13
+    const float cl = p.clamp * p.scale;
+    const bool clip = p.clamp < INFINITY;
+    const int nel = n * V;
+    for (int f0 = 0; f0 < nel; f0 += 32 * UF) {
+        float x[UF];
+        float4 rc[UF];
+        int kk[UF];
+#pragma unroll
+        for (int u = 0; u < UF; ++u) {
+            const int f = f0 + 32 * u + lane;
+            const int rw = f < nel ? (int)(((float)f + 0.5f) * invV) : 0;
+            kk[u] = f - rw * V;
+            rc[u] = rec(rw);
+            x[u] = (f < nel && rc[u].x != -INFINITY) ? E::to_f(__ldcs(X + f)) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < UF; ++u) {
+            const int f = f0 + 32 * u + lane;
+            if (f >= nel) break;
+            float gv = rc[u].x != -INFINITY ? ex2(fmaf(x[u], kLog2e, rc[u].x)) : 0.0f;
+            if (kk[u] == p.blank) gv -= rc[u].y;
+            if (kk[u] == __float_as_int(rc[u].w)) gv -= rc[u].z;
+            if (clip) gv = fminf(fmaxf(gv, -cl), cl);
+            __stcs(Y + f, E::from_f(gv));
+        }
+    }
+}
+
+// Per-stage row pass for such rows: a warp per 32-row chunk (grid-stride).
+template <typename Tin>
+__global__ void __launch_bounds__(256) k_row_flat(Params p) {
+    if (*p.err) return;
+    extern __shared__ __align__(16) unsigned char flat_smem[];
+    const int wl = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    unsigned char* sbuf = flat_smem + (size_t)wid * flat_warp_bytes(p.V, sizeof(Tin));
+    const Tin* X = static_cast<const Tin*>(p.logits);
+    const int64_t nr = nodes(p), nbatch = (nr + 31) / 32;
+    const int64_t wstride = (int64_t)gridDim.x * (blockDim.x / 32);
+    for (int64_t bt = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32; bt < nbatch;
+         bt += wstride) {
+        const int64_t r0 = bt * 32;
+        const int n = (int)min((int64_t)32, nr - r0);
+        float M = 0.0f, s = 0.0f;
+        if (p.padded) {
+            if (wl < n) flat_row_stats<Tin>(X + lrow(p, r0 + wl) * (int64_t)p.V, p.V, M, s);
+        } else {
+            const Tin* rows = flat_stage<Tin>(X, r0, n, p.V, sbuf, wl);
+            if (wl < n) flat_row_stats<Tin>(rows + (int64_t)wl * p.V, p.V, M, s);
+            __syncwarp();   // the buffer is reused by the next chunk
+        }
+        if (wl < n) row_finish<Tin>(p, r0 + wl, M, s);
+    }
 }
 
 template <typename Tin, int G, bool VEC>
@@ -2097,8 +2219,12 @@ template <int J>
 __device__ __forceinline__ void dp_run(const Params& p, const Samp& c, int4* smem, float2* xch) {
     const int wid = threadIdx.x >> 5;
     if (c.W <= 32 * kWarpDpMaxJ) {
-        if (wid < 2)
-            dp_dispatch_w(p, c, smem + (size_t)wid * (wdp_smem_bytes(c.W) / 2 / sizeof(int4)), wid);
+        // Warps 0/1, or 2/3 in the second half of a two-CTA-per-SM grid, so
+        // that two CTAs on one SM (blocks i and i + gridDim/2 in the usual
+        // placement) put their four recursion warps on four sub-partitions.
+        const int w = wid - ((blockIdx.x >= gridDim.x / 2) ? 2 : 0);
+        if (w == 0 || w == 1)
+            dp_dispatch_w(p, c, smem + (size_t)w * (wdp_smem_bytes(c.W) / 2 / sizeof(int4)), w);
         return;
     }
     int* tab = reinterpret_cast<int*>(reinterpret_cast<char*>(smem) + dp_ring_bytes(c.W));
@@ -2418,6 +2544,7 @@ __global__ void __launch_bounds__(256) k_grad(Params p) {
         const int vb = p.blank / EPV, eb_i = p.blank % EPV;
         const int64_t nr = nodes(p), nbatch = (nr + 31) / 32;
         const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
+        const bool flat = flat_rows(V, sizeof(Tin), p.fused) && !p.padded;
         int bs = -1;   // this lane's sample
         // The records of a batch are formed one batch ahead of its rows.
         auto batch_rec = [&](int64_t bt, int64_t& lr) -> float4 {
@@ -2436,6 +2563,13 @@ __global__ void __launch_bounds__(256) k_grad(Params p) {
             const float4 rec = rec_next;
             const int64_t lr_mine = lr_next;
             rec_next = batch_rec(bt + nwarps, lr_next);
+            if (!VEC && FUSED && flat) {   // short rows: flat element order
+                flat_grad<Tin>(p, r0, n, wl, [&](int i) {
+                    return make_float4(__shfl_sync(F, rec.x, i), __shfl_sync(F, rec.y, i),
+                                       __shfl_sync(F, rec.z, i), __shfl_sync(F, rec.w, i));
+                });
+                continue;
+            }
             for (int it = 0; it * NG < n; ++it) {
                 const int ri = it * NG + grp;
                 const float w2 = __shfl_sync(F, rec.x, ri), eb = __shfl_sync(F, rec.y, ri);
@@ -3386,6 +3520,55 @@ __device__ __forceinline__ void main_body(const Params& p) {
                 if (NV > 0) {
                     row_batch_tma<Tin, (NV > 0 ? NV : 1)>(p, rw, nw, buf, bars, kk, b, tk.w,
                                                           tc.x, o_b);
+                } else if (flat_rows(p.V, sizeof(Tin), p.fused)) {
+                    const Tin* X = static_cast<const Tin*>(p.logits);
+                    if (p.padded) {
+                        float M = 0.0f, s = 0.0f;
+                        if (wl < nw) {
+                            flat_row_stats<Tin>(X + lrow_s(p, rw + wl, b, o_b, W_b) * (int64_t)p.V,
+                                                p.V, M, s);
+                            row_finish<Tin>(p, rw + wl, M, s);
+                        }
+                    } else {
+                        const Tin* rows = flat_stage<Tin>(
+                            X, rw, nw, p.V,
+                            smem_raw + (size_t)wid * flat_warp_bytes(p.V, sizeof(Tin)), wl);
+                        if (wl < nw) {
+                            // The sample is the task's, and the blank and label
+                            // log-probabilities are in the staged row.
+                            const Tin* row = rows + (int64_t)wl * p.V;
+                            float M, s;
+                            flat_row_stats<Tin>(row, p.V, M, s);
+                            const int64_t r = rw + wl;
+                            const unsigned rr = (unsigned)(r - o_b);
+                            const int t = (int)(rr / (unsigned)W_b), u = (int)(rr - (unsigned)t * W_b);
+                            const int U = W_b - 1;
+                            const float hb = Elt<Tin>::to_f(row[p.blank]);
+                            const float hy =
+                                u < U ? Elt<Tin>::to_f(row[__ldg(p.targets + (int64_t)b * p.S + u)])
+                                      : 0.0f;
+                            row_finish_at<Tin>(p, r, M, s, hb, hy, t, u, tk.w, U, o_b);
+                        }
+                    }
+                } else if (p.fused) {
+                    // Rows that are not 16-byte vectors: G-lane groups reduce
+                    // the rows (as the per-stage row kernel does), each row's
+                    // statistics handed to its lane.
+                    constexpr int NG = 32 / G;
+                    const int lane = wl & (G - 1), grp = wl / G;
+                    const unsigned gm = group_mask<G>();
+                    float myM = 0.0f, mys = 0.0f;
+                    for (int it = 0; it < G; ++it) {
+                        const int ri = it * NG + grp;
+                        float M = -INFINITY, s = 0.0f;
+                        if (ri < nw)
+                            row_stats_stream<Tin, G, VEC>(
+                                static_cast<const Tin*>(p.logits) +
+                                    lrow_s(p, rw + ri, b, o_b, W_b) * (int64_t)p.V,
+                                p.V, lane, gm, M, s);
+                        hand_over<G>(it, wl, M, s, myM, mys);
+                    }
+                    if (wl < nw) row_finish<Tin>(p, rw + wl, myM, mys);
                 } else if (wl < nw) {
                     row_finish<Tin>(p, rw + wl, 0.0f, 1.0f);
                 }
@@ -3447,8 +3630,14 @@ __device__ __forceinline__ void main_body(const Params& p) {
             grad_batch_tma<Tin, (NV > 0 ? NV : 1)>(p, r0, 32 * wid, zmask, s_nz, cnt, wid, 8,
                                                   s_info, buf, bars, kk, zbuf, b, o_b, W_b);
         } else if (nw > 0) {
-            grad_batch_plain<Tin, G, VEC, false>(p, r0 + 32 * wid, nw, s_info + 32 * wid, b, o_b,
-                                                 W_b);
+            if (flat_rows(p.V, sizeof(Tin), p.fused) && !p.padded)
+                flat_grad<Tin>(p, r0 + 32 * wid, nw, wl, [&](int i) { return s_info[32 * wid + i]; });
+            else if (p.fused)
+                grad_batch_plain<Tin, G, VEC, true>(p, r0 + 32 * wid, nw, s_info + 32 * wid, b, o_b,
+                                                    W_b);
+            else
+                grad_batch_plain<Tin, G, VEC, false>(p, r0 + 32 * wid, nw, s_info + 32 * wid, b,
+                                                     o_b, W_b);
         }
         if (p.trace) {
             __syncthreads();
@@ -3985,6 +4174,11 @@ size_t tma_smem(const Params& p) {
     return (size_t)8 * kStages * p.stage_bytes + (size_t)8 * kStages * sizeof(uint64_t);
 }
 
+// Lanes per row of the log-softmax statistics for rows that are not 16-byte
+// vectors and at most 1 KB long, on either schedule (the same reduction order,
+// so that both give the same bits).
+inline int plain_group(int V) { return V >= 256 ? 32 : 8; }
+
 template <typename Tin>
 void launch_rows(const Params& p, cudaStream_t st, int sms) {
     const int V = p.V;
@@ -4011,6 +4205,15 @@ void launch_rows(const Params& p, cudaStream_t st, int sms) {
         else if (nvec <= 64) launch_gs(k_row_regs<Tin, 32, 2>, wt, sms, st, p);
         else if (nvec <= 128) launch_gs(k_row_regs<Tin, 32, 4>, wt, sms, st, p);
         else launch_gs(k_row_regs<Tin, 32, 8>, wt, sms, st, p);
+        return;
+    }
+    if (flat_rows(V, sizeof(Tin), p.fused)) {
+        launch_gs(k_row_flat<Tin>, wt, sms, st, p, 8 * flat_warp_bytes(V, sizeof(Tin)));
+        return;
+    }
+    if (!vec && (size_t)V * sizeof(Tin) <= 1024) {
+        if (plain_group(V) == 32) launch_gs(k_row_stream<Tin, 32, false>, wt, sms, st, p);
+        else launch_gs(k_row_stream<Tin, 8, false>, wt, sms, st, p);
         return;
     }
 #define ROWK(G_)                                                                 \
@@ -4108,7 +4311,10 @@ bool persistent_setup(const Params& p, int sms, int dev, PersistentCfg& c) {
     const void* fn = nullptr;
     size_t sm = dps;
     int zero_off = 0, zero_rows = 0;
-    if (p.fused) {
+    // Log-softmax on short rows that are not 16-byte vectors (at most 1 KB):
+    // plain loads, G-lane groups of plain_group(V) lanes per row.
+    const bool plain = p.fused && !vec && (size_t)V * sizeof(Tin) <= 1024;
+    if (p.fused && !plain) {
         if (!(vec && nvec > 32 && nvec <= 256)) return false;
         sm = std::max(sm, (size_t)8 * main_stages(nvec <= 64 ? 2 : nvec <= 128 ? 4 : 8) *
                               p.stage_bytes);
@@ -4126,7 +4332,9 @@ bool persistent_setup(const Params& p, int sms, int dev, PersistentCfg& c) {
              : nvec <= 128 ? reinterpret_cast<const void*>(k_main<Tin, 4, 32, true>)
                            : reinterpret_cast<const void*>(k_main<Tin, 8, 32, true>);
     } else {
-        const bool wide = V >= 256;
+        if (flat_rows(V, sizeof(Tin), p.fused))   // shared staging of short rows
+            sm = std::max(sm, (size_t)8 * flat_warp_bytes(V, sizeof(Tin)));
+        const bool wide = plain ? plain_group(V) == 32 : V >= 256;
         fn = vec ? (wide ? reinterpret_cast<const void*>(k_main<Tin, 0, 32, true>)
                          : reinterpret_cast<const void*>(k_main<Tin, 0, 8, true>))
                  : (wide ? reinterpret_cast<const void*>(k_main<Tin, 0, 32, false>)
@@ -4141,8 +4349,13 @@ bool persistent_setup(const Params& p, int sms, int dev, PersistentCfg& c) {
     c.zero_off = zero_off;
     c.zero_rows = zero_rows;
     // DP workers: up to 6 SMs (two DP CTAs each); measured on the BPE-ASR
-    // workload, 6 beat 8 (the DP SMs idle most of the call) and 4.
-    c.n_dp_sms = std::min(std::min(6, (p.B + 1) / 2), sms / 8);
+    // workload, 6 beat 8 (the DP SMs idle most of the call) and 4.  A call of
+    // short rows (under 64 MB of logits) is bound by its recursions, not by
+    // HBM: there every sample's recursion gets a worker CTA, up to a quarter
+    // of the SMs.
+    const bool small = (double)p.rows * V * sizeof(Tin) < 64.0 * (1 << 20);
+    c.n_dp_sms = small ? std::min((p.B + 1) / 2, sms / 4)
+                       : std::min(std::min(6, (p.B + 1) / 2), sms / 8);
     return true;
 }
 

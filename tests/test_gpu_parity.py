@@ -36,7 +36,11 @@ def test_tiny_elementwise():
 
 
 def test_char_asr_elementwise():
-    full_compare(W.make("char_asr", "cuda"))
+    wl = W.make("char_asr", "cuda")
+    # 116-byte rows take the persistent kernel: one launch
+    plan = N.rnnt_plan(wl.cfg.B, wl.logits.shape[0], wl.cfg.V, 0, wl.targets.shape[1], True, True)
+    assert plan == {"persistent": True, "launches": 1}
+    full_compare(wl)
 
 
 @pytest.mark.parametrize("red", ["none", "sum", "mean"])
@@ -229,9 +233,15 @@ def test_device_detects_bad_inputs():
     full_compare(wl)
 
 
-def test_non_finite_input_reports_mismatch():
+@pytest.mark.parametrize("sched", ["persistent", "kernels"])
+@pytest.mark.parametrize("k", [2, 6])
+def test_non_finite_input_reports_mismatch(k, sched, monkeypatch):
+    # A NaN that is the only element some lane of the row reduction sees (7
+    # elements over 8-lane groups) must still reach the non-finite check.
+    if sched == "kernels":
+        monkeypatch.setenv("RNNT_GB300_SCHEDULE", "kernels")
     wl = make(2, [5, 4], [2, 3], 7, dtype="f32", blank=0, reduction="sum")
-    wl.logits[3, 2] = float("nan")
+    wl.logits[3, k] = float("nan")
     e = _status_of(wl)
     assert isinstance(e, N.RNNTError) and e.code == N.RNNT_LOSS_MISMATCH
 
@@ -286,6 +296,11 @@ SCHED_CASES = [
     # 4 KB rows (8 vectors per lane): the persistent kernel's 3-stage rings
     dict(B=4, V=1024, dtype="f32", fused=True, blank=-1, reduction="sum", clamp=-1.0),
     dict(B=3, V=2048, dtype="f16", fused=True, blank=5, reduction="mean", clamp=0.2),
+    # log-softmax on rows that are not 16-byte vectors (116-byte fp32 rows of
+    # the character vocabulary, 74-byte fp16, 502-byte bf16 rows): plain loads
+    dict(B=6, V=29, dtype="f32", fused=True, blank=0, reduction="mean", clamp=0.1),
+    dict(B=4, V=37, dtype="f16", fused=True, blank=3, reduction="sum", clamp=-1.0),
+    dict(B=3, V=251, dtype="bf16", fused=True, blank=-1, reduction="none", clamp=-1.0),
 ]
 
 
