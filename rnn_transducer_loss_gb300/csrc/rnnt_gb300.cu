@@ -240,6 +240,23 @@ __device__ __forceinline__ int find_sample(const int64_t* off, int B, int64_t r)
     return lo;
 }
 
+// The same by a whole warp (every lane calls it, same r): a 32-way search, one
+// round of loads per factor of 32 in B, all lanes return the sample.
+__device__ __forceinline__ int find_sample_warp(const int64_t* off, int B, int64_t r) {
+    const int lane = threadIdx.x & 31;
+    int lo = 0, n = B;   // off[lo] <= r < off[lo + n]
+    while (n > 1) {
+        const int step = (n + 31) / 32;
+        const int idx = lo + lane * step;
+        const bool le = idx < lo + n && __ldcg(off + idx) <= r;
+        const unsigned bal = __ballot_sync(0xffffffffu, le);
+        const int k = 31 - __clz(bal);
+        lo += k * step;
+        n = min(step, n - k * step);
+    }
+    return lo;
+}
+
 // Logits / gradient row holding lattice row r (compact numbering) of sample b,
 // whose compact rows start at o and whose lattice is W nodes wide: r itself in
 // the compact layout, (b*maxT + t)*maxW + u in the padded one.
@@ -2740,8 +2757,13 @@ __global__ void __launch_bounds__(256) k_grad_sparse(Params p) {
         using E = Elt<Tin>;
         constexpr int NR = kSparseRows / 256;
         __shared__ int s_lo, s_hi;
-        if (threadIdx.x == 0) s_lo = find_sample(p.off, p.B, n0);
-        if (threadIdx.x == 32) s_hi = find_sample(p.off, p.B, min(n0 + kSparseRows - 1, nr - 1));
+        if (threadIdx.x < 32) {
+            const int v = find_sample_warp(p.off, p.B, n0);
+            if (threadIdx.x == 0) s_lo = v;
+        } else if (threadIdx.x < 64) {
+            const int v = find_sample_warp(p.off, p.B, min(n0 + kSparseRows - 1, nr - 1));
+            if (threadIdx.x == 32) s_hi = v;
+        }
         __syncthreads();
         Tin* Y = static_cast<Tin*>(p.grad);
         const float cl = p.clamp * p.scale;
@@ -2800,8 +2822,13 @@ __global__ void __launch_bounds__(256) k_row_gather(Params p) {
     using E = Elt<Tin>;
     constexpr int NR = kGatherNodes / 256;
     __shared__ int s_lo, s_hi;
-    if (threadIdx.x == 0) s_lo = find_sample(p.off, p.B, n0);
-    if (threadIdx.x == 32) s_hi = find_sample(p.off, p.B, min(n0 + kGatherNodes - 1, nr - 1));
+    if (threadIdx.x < 32) {
+        const int v = find_sample_warp(p.off, p.B, n0);
+        if (threadIdx.x == 0) s_lo = v;
+    } else if (threadIdx.x < 64) {
+        const int v = find_sample_warp(p.off, p.B, min(n0 + kGatherNodes - 1, nr - 1));
+        if (threadIdx.x == 32) s_hi = v;
+    }
     __syncthreads();
     const Tin* X = static_cast<const Tin*>(p.logits);
     const Tin* row[NR];
@@ -3743,14 +3770,18 @@ __device__ __forceinline__ void xf_mac(float& am, int& ae, float xm, int xe, flo
     xf_add(am, ae, m, e, am, ae);
 }
 
-__global__ void __launch_bounds__(1024) k_dp_mb(Params p) {
+template <int NT>   // block size bound: 256 (lattices of up to 256 columns) or 1024
+__global__ void __launch_bounds__(NT) k_dp_mb(Params p) {
     if (*p.err) return;
     extern __shared__ float2 mb_smem[];
     const int nthr = blockDim.x, u = threadIdx.x;
     float2* ring = mb_smem;                          // [kMbRing][nthr]: {m, e bits}
     float2* xch = mb_smem + (size_t)kMbRing * nthr;  // [2][nthr]
+    // [kMbRing][nthr]: node index of this column's node at frame t (slot t mod
+    // kMbRing), for the big blanks' source nodes.
+    int* iring = reinterpret_cast<int*>(mb_smem + (size_t)(kMbRing + 2) * nthr);
     const int b = blockIdx.x;
-    const int T = __ldg(p.Tl + b), U = __ldg(p.Ul + b), W = U + 1, D = T + U;
+    const int T = __ldg(p.Tl + b), U = __ldg(p.Ul + b), W = U + 1, D = T + U, mTW = min(T, W);
     const int64_t o = __ldcg(p.off + b);
     const bool col = u < W;
     const float c = p.bb_c;
@@ -3763,17 +3794,24 @@ __global__ void __launch_bounds__(1024) k_dp_mb(Params p) {
     int2 q_n[RNNT_MAX_BIG_BLANKS];
 #pragma unroll
     for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) q_n[i] = make_int2(0, 0);
+    // Node index (in the sample) of this column's node at the fetched frame,
+    // stepped from frame to frame: idx(t+1,u) = idx(t,u) + len(d) + 1 - [d >= U]
+    // (d = t + u, len(d) the length of anti-diagonal d).
+    int fi = 0;
+    auto step_len = [&](int dd) { return min(min(dd + 1, mTW), D - dd) + 1 - (dd >= U ? 1 : 0); };
     auto fetch = [&](int t) {
         if (!(col && t >= 0 && t < T)) return;
-        const int64_t nd = o + node_index(t, u, T, U);
-        ed_n = __ldcg(p.edge + nd);
+        if (fwd) fi = t == 0 ? (int)node_index(0, u, T, U) : fi + step_len(t - 1 + u);
+        else fi = t == T - 1 ? (int)node_index(T - 1, u, T, U) : fi - step_len(t + u);
+        ed_n = __ldcg(p.edge + o + fi);
 #pragma unroll
         for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) {
             if (i >= p.K) break;
             const int ts = fwd ? t - p.bb_dur[i] : t;
-            q_n[i] = ts >= 0 ? __ldcg(p.pbb + (int64_t)i * p.rows + o + node_index(ts, u, T, U))
-                             : make_int2(0, 0);
+            const int si = fwd ? iring[(ts & (kMbRing - 1)) * nthr + u] : fi;
+            q_n[i] = ts >= 0 ? __ldcg(p.pbb + (int64_t)i * p.rows + o + si) : make_int2(0, 0);
         }
+        if (fwd) iring[(t & (kMbRing - 1)) * nthr + u] = fi;
     };
     if (fwd) {
         float bm = 0.0f;   // alpha(t-1,u) p_blank(t-1,u) c: this column's blank outflow
@@ -3782,6 +3820,7 @@ __global__ void __launch_bounds__(1024) k_dp_mb(Params p) {
         for (int d = 0; d < D; ++d) {
             const int t = d - u;
             const int4 ed = ed_n;
+            const int ni = fi;   // node index of (t, u)
             int2 q[RNNT_MAX_BIG_BLANKS];
 #pragma unroll
             for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) q[i] = q_n[i];
@@ -3820,7 +3859,7 @@ __global__ void __launch_bounds__(1024) k_dp_mb(Params p) {
                     }
                     xf_add<true>(am, ae, a2, e2, am, ae);
                 }
-                p.alpha[o + node_index(t, u, T, U)] = make_int2(__float_as_int(am), ae);
+                p.alpha[o + ni] = make_int2(__float_as_int(am), ae);
                 ring[(t & (kMbRing - 1)) * nthr + u] = make_float2(am, __int_as_float(ae));
                 // Outflows (blank to (t+1,u), label to (t,u+1)); their mantissas
                 // stay below 4 and are renormalised by the adds they enter.
@@ -3860,6 +3899,7 @@ __global__ void __launch_bounds__(1024) k_dp_mb(Params p) {
         for (int d = D - 1; d >= 0; --d) {
             const int t = d - u;
             const int4 ed = ed_n;
+            const int ni = fi;   // node index of (t, u)
             int2 q[RNNT_MAX_BIG_BLANKS];
 #pragma unroll
             for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) q[i] = q_n[i];
@@ -3892,7 +3932,7 @@ __global__ void __launch_bounds__(1024) k_dp_mb(Params p) {
                     else xf_mac_raw(m2, e2, am2, ae2, __int_as_float(q[i].x), q[i].y - kEdgeBias, c);
                 }
                 xf_add<true>(m, e, m2, e2, m, e);
-                p.beta[o + node_index(t, u, T, U)] = make_int2(__float_as_int(m), e);
+                p.beta[o + ni] = make_int2(__float_as_int(m), e);
                 out = make_float2(m, __int_as_float(e));
                 ring[(t & (kMbRing - 1)) * nthr + u] = out;
                 qm = m;
@@ -4552,16 +4592,20 @@ static rnnt_status_t loss_impl(const void* logits, rnnt_dtype_t dt, int64_t rows
         // Multi-blank transducer: preparation, the row pass (also storing every
         // big blank's probability), the recursions, the gradient rows, the check.
         const int nthr = std::min(1024, (targets_stride + 1 + 31) / 32 * 32);
-        const size_t smem = (size_t)(kMbRing + 2) * nthr * sizeof(float2);
-        if (cudaFuncSetAttribute(k_dp_mb, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
+        const size_t smem = (size_t)(kMbRing + 2) * nthr * sizeof(float2) +
+                            (size_t)kMbRing * nthr * sizeof(int);
+        const void* kmb = nthr <= 256 ? reinterpret_cast<const void*>(k_dp_mb<256>)
+                                      : reinterpret_cast<const void*>(k_dp_mb<1024>);
+        if (cudaFuncSetAttribute(kmb, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
             return RNNT_LAUNCH_FAILED;
         k_prepare<<<1, 1024, 0, st>>>(p);
         with_type(dt, [&](auto tag) {
             launch_rows<decltype(tag)>(p, st, sms);
             return 0;
         });
-        k_dp_mb<<<dim3(B, 2), nthr, smem, st>>>(p);
+        if (nthr <= 256) k_dp_mb<256><<<dim3(B, 2), nthr, smem, st>>>(p);
+        else k_dp_mb<1024><<<dim3(B, 2), nthr, smem, st>>>(p);
         bool finalized = false;
         if (grad) {
             finalized = with_type(dt, [&](auto tag) {
