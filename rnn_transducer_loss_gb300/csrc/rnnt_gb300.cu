@@ -226,8 +226,18 @@ __device__ __forceinline__ int64_t diag_start(int d, int T, int W) {
 // Index of node (t,u) relative to its sample's first record in the per-node
 // arrays (transition records, alpha, beta): anti-diagonal-packed, so each
 // diagonal d = t+u is one contiguous run ordered by t.
+// When T + W <= 65536 every triangular number involved is below 2^32 and the
+// index below 2^31, so 32-bit unsigned arithmetic gives it exactly.
+__device__ __forceinline__ unsigned tri32(int n) {
+    return n > 0 ? ((unsigned)n * (unsigned)(n + 1)) >> 1 : 0u;
+}
 __device__ __forceinline__ int64_t node_index(int t, int u, int T, int U) {
     const int d = t + u;
+    if (T + U < 65536) {
+        const int W = U + 1;
+        const unsigned ds = tri32(d) - tri32(d - T) - tri32(d - W) + tri32(d - T - W);
+        return (int64_t)(int)(ds + (unsigned)(t - max(0, d - U)));
+    }
     return diag_start(d, T, U + 1) + (t - max(0, d - U));
 }
 
@@ -2903,10 +2913,19 @@ __device__ __forceinline__ MbRec mb_record(const Params& p, int64_t r, int b) {
     const unsigned rr = (unsigned)(r - o);
     const int t = (int)(rr / (unsigned)W), u = (int)(rr - (unsigned)t * W);
     const int64_t nd = o + node_index(t, u, T, U);
+    // Inside the band of full-length anti-diagonals (U <= t + u, the node k
+    // frames later still before frame T - u), node (t + k, u) is k W nodes
+    // further and (t, u + 1) W - 1 further.
+    const int d = t + u;
+    auto down = [&](int k) { return (d >= U && d + k <= T - 1) ? nd + (int64_t)k * W
+                                                                : o + node_index(t + k, u, T, U); };
     const int2 A = __ldcg(p.alpha + nd), Bt = __ldcg(p.beta + nd);
     const int4 Ed = __ldcg(p.edge + nd);
-    const int2 Bb = (t + 1 < T) ? __ldcg(p.beta + o + node_index(t + 1, u, T, U)) : make_int2(0, 0);
-    const int2 By = (u < U) ? __ldcg(p.beta + o + node_index(t, u + 1, T, U)) : make_int2(0, 0);
+    const int2 Bb = (t + 1 < T) ? __ldcg(p.beta + down(1)) : make_int2(0, 0);
+    const int2 By = (u < U) ? __ldcg(p.beta + ((d >= U && d + 1 <= T - 1)
+                                                   ? nd + W - 1
+                                                   : o + node_index(t, u + 1, T, U)))
+                            : make_int2(0, 0);
     int2 Qb[RNNT_MAX_BIG_BLANKS], Bq[RNNT_MAX_BIG_BLANKS];
 #pragma unroll
     for (int i = 0; i < RNNT_MAX_BIG_BLANKS; ++i) {
@@ -2915,7 +2934,7 @@ __device__ __forceinline__ MbRec mb_record(const Params& p, int64_t r, int b) {
         if (i < p.K) {
             const int t1 = t + p.bb_dur[i];
             Qb[i] = __ldcg(p.pbb + (int64_t)i * p.rows + nd);
-            if (t1 < T) Bq[i] = __ldcg(p.beta + o + node_index(t1, u, T, U));
+            if (t1 < T) Bq[i] = __ldcg(p.beta + down(p.bb_dur[i]));
         }
     }
     const float Pm = __ldcg(p.pm + b);
